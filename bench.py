@@ -1,0 +1,495 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused-chain hot path on one GB300 (or N, one process per GPU, weak scaling).
+
+Metric: fused-chain HBM GB/s (and % of the GB300 peak) with the fused/unfused speedup as a
+function of K, on the pointwise chain x, y fp32 [16,777,216], K in {2, 3, 4, 6, 8}, stage
+y = a_s y + b_s (a_s ~ U[0.9,1.1], b_s ~ U[-0.1,0.1]), ReLU on even s.
+
+One step = one pass over every row of the hot path on its own synthetic batch:
+  chain fused (K = 2,3,4,6,8) | chain unfused (same K) | fat probe (same K) |
+  RMSNorm [2048,4096] fused + unfused | causal softmax [8,16,2048,2048] fused (skip 0/64/128) +
+  unfused.
+Each row runs as a group: one untimed launch of the same kernels first, then the timed launches
+back to back over rotating buffers (4 input/output pairs, 512 MiB for the chain: larger than the
+126 MiB L2), so every timed launch pays for the dirty lines its predecessor of the same kind left
+in L2, as in a steady stream.  Every launch is bracketed by CUDA events on the launching stream.
+
+``value`` = fused-chain algorithmic bytes (2 N b per launch, N b read + N b written) / summed
+fused-chain device time.  ``e2e`` = the same bytes / time of pinned-host -> device copy, the
+C-ABI call and the device -> host copy of y, per K.
+
+``--impl reference`` times the plain CPU oracle (the only other place this script runs it) on
+the same workload on the host cores, rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+NOMINAL_HBM_GBS = 7900.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rows", choices=["all", "chain"], default="all",
+                    help="'chain' restricts a step to the metric's own row (the chain sweep)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS if k in d}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"t": _smi_time(f[0]), "sm": float(f[2]), "sm_max": float(f[3]),
+                             "power": f[4], "active": f[5], "hw": f[6], "hw_thermal": f[7],
+                             "sw_thermal": f[8], "sw_power": f[9]})
+            except ValueError:
+                continue
+        return rows
+
+
+def _smi_time(stamp: str) -> float:
+    """nvidia-smi timestamp 'YYYY/MM/DD HH:MM:SS.mmm' (local time) -> seconds since the epoch."""
+    whole, _, frac = stamp.partition(".")
+    return time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
+
+
+def summarize_clocks(rows, t0, t1):
+    if not rows:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"]}
+    inside = [r for r in rows if t0 - 0.05 <= r["t"] <= t1 + 0.05] or rows
+    reasons = set()
+    for r in inside:
+        for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                          ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+            if r[key].lower() == "active":
+                reasons.add(name)
+    return {"sm_mhz": statistics.median(r["sm"] for r in inside),
+            "sm_max_mhz": max(r["sm_max"] for r in inside), "reasons": sorted(reasons),
+            "samples": len(inside)}
+
+
+# ------------------------------------------------------------------------------ traffic
+def committed_traffic(kernel_src: str):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was
+    captured from the current kernel source (sha256 recorded in the summary), else None."""
+    path = os.path.join(ROOT, "profiles", "chain_fused_f32_n16M.txt")
+    if not os.path.exists(path):
+        return None
+    with open(kernel_src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and not line.startswith("#"):
+                k, v = line.split(":", 1)
+                vals[k.strip()] = v.strip()
+    if vals.get("source_sha256") != sha:
+        return None
+    try:
+        return int(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------------------ our arm
+def run_ours(args, rank, world, local):
+    import torch
+    import epilogue_chains_gb300 as fc
+    from epilogue_chains_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = stream.cuda_stream
+    lib = fc._load()
+    peaks, peak_src = load_peaks()
+
+    N = wl.CHAIN_N
+    KS = wl.CHAIN_KS
+    R = 4
+    with torch.cuda.stream(stream):
+        xs = [wl.chain_input(N, device=dev, salt=r + 100 * rank) for r in range(R)]
+        ys = [torch.empty_like(xs[0]) for _ in range(R)]
+    stage_sets = {}
+    for K in KS:
+        relu, a, b = wl.chain_stages(K)
+        stage_sets[K] = fc._stages([(fc.FUSE_OP_AFFINE_RELU if r_ else fc.FUSE_OP_AFFINE, p, q)
+                                    for r_, p, q in zip(relu, a, b)])
+    chain_bytes = fc.fuse_chain_bytes(1, N, fc.FUSE_F32, fc.FUSE_FUSED)  # 2 N b, any K
+
+    launches = {"n": 0}
+    rot = {"i": 0}
+
+    def chain_call(K, mode):
+        i = rot["i"] % R
+        rot["i"] += 1
+        st = stage_sets[K]
+        rc = lib.fuse_chain_run(st, K, xs[i].data_ptr(), ys[i].data_ptr(), N, fc.FUSE_F32, mode, sh)
+        if rc != 0:
+            raise fc.FuseError(rc, "fuse_chain_run")
+        launches["n"] += K if mode == fc.FUSE_UNFUSED else 1
+
+    rows_all = args.rows == "all"
+    if rows_all:
+        with torch.cuda.stream(stream):
+            rx, rw = wl.rmsnorm_input(device=dev, salt=rank)
+            rys = [torch.empty_like(rx) for _ in range(2)]
+            rxs = [rx, rx.clone()]
+            rws = torch.empty(fc.fuse_rmsnorm_workspace_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN,
+                                                              fc.FUSE_UNFUSED),
+                              dtype=torch.uint8, device=dev)
+            bh, S = wl.SM_B * wl.SM_H, wl.SM_S
+            ss = wl.softmax_input(bh, S, device=dev, salt=rank)
+            sps = [torch.empty_like(ss) for _ in range(2)]
+            sws = torch.empty(fc.fuse_causal_softmax_workspace_bytes(bh, S, fc.FUSE_UNFUSED),
+                              dtype=torch.uint8, device=dev)
+    rrot = {"i": 0}
+
+    def rms_call(mode):
+        i = rrot["i"] % 2
+        rrot["i"] += 1
+        rc = lib.fuse_rmsnorm(rxs[i].data_ptr(), rw.data_ptr(), rys[i].data_ptr(), wl.RMS_ROWS,
+                              wl.RMS_HIDDEN, wl.RMS_EPS, mode, rws.data_ptr(), rws.numel(), sh)
+        if rc != 0:
+            raise fc.FuseError(rc, "fuse_rmsnorm")
+        launches["n"] += 1 if mode == fc.FUSE_FUSED else 4
+
+    srot = {"i": 0}
+
+    def sm_call(tile, mode):
+        i = srot["i"] % 2
+        srot["i"] += 1
+        rc = lib.fuse_causal_softmax(ss.data_ptr(), sps[i].data_ptr(), bh, S, wl.SM_SCALE, tile,
+                                     fc.FUSE_BF16, mode, sws.data_ptr(), sws.numel(), sh)
+        if rc != 0:
+            raise fc.FuseError(rc, "fuse_causal_softmax")
+        launches["n"] += 1 if mode == fc.FUSE_FUSED else 5
+
+    # one step = the groups below; every timed call gets its own event pair
+    groups = [("chain_fused", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_FUSED)) for K in KS],
+               lambda: chain_call(KS[0], fc.FUSE_FUSED)),
+              ("chain_unfused", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_UNFUSED)) for K in KS],
+               lambda: chain_call(KS[0], fc.FUSE_UNFUSED)),
+              ("chain_fat", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_FAT)) for K in KS],
+               lambda: chain_call(KS[0], fc.FUSE_FAT))]
+    if rows_all:
+        groups += [
+            ("rmsnorm_fused", [("r", lambda: rms_call(fc.FUSE_FUSED))] * 2, lambda: rms_call(fc.FUSE_FUSED)),
+            ("rmsnorm_unfused", [("r", lambda: rms_call(fc.FUSE_UNFUSED))] * 2,
+             lambda: rms_call(fc.FUSE_UNFUSED)),
+            ("softmax_fused", [(f"T{t}", lambda t=t: sm_call(t, fc.FUSE_FUSED)) for t in (0, 64, 128)],
+             lambda: sm_call(0, fc.FUSE_FUSED)),
+            ("softmax_unfused", [("T0", lambda: sm_call(0, fc.FUSE_UNFUSED))],
+             lambda: sm_call(0, fc.FUSE_UNFUSED)),
+        ]
+
+    def make_events():
+        return {g: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                    for _ in calls] for g, calls, _ in groups}
+
+    def step(evs):
+        # each group: its untimed leading call, then the timed calls back to back
+        with torch.cuda.stream(stream):
+            for g, calls, pre in groups:
+                pre()
+                for (tag, fn), (e0, e1) in zip(calls, evs[g]):
+                    e0.record(stream)
+                    fn()
+                    e1.record(stream)
+
+    for _ in range(max(3, args.warmup)):      # warm-up steps (untimed)
+        step(make_events())
+    torch.cuda.synchronize()
+
+    all_evs = [make_events() for _ in range(args.steps)]
+    sampler = ClockSampler(local)
+    time.sleep(0.3)  # let nvidia-smi start sampling
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    launches["n"] = 0
+    t0 = time.time()
+    for s in range(args.steps):
+        step(all_evs[s])
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    t1 = time.time()
+    clocks = summarize_clocks(sampler.stop(), t0, t1)
+    timed_launches = launches["n"]   # every kernel of ours launched inside the timed region
+
+    # collect
+    times = {g: [[e0.elapsed_time(e1) for e0, e1 in evs[g]] for evs in all_evs]
+             for g, _, _ in groups}   # ms, [step][call]
+    def mean_ms(g, idx):
+        return float(np.mean([st[idx] for st in times[g]]))
+
+    fused_ms_total = sum(sum(st) for st in times["chain_fused"])
+    n_fused = args.steps * len(KS)
+    my_bytes = n_fused * chain_bytes
+    elapsed_s = fused_ms_total / 1e3
+    step_ms = float(np.mean([sum(sum(times[g][s]) for g in times) for s in range(args.steps)]))
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_s, step_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_s, step_ms = float(t[0]), float(t[1])
+    value = my_bytes * world / elapsed_s / 1e9
+
+    per_k = {}
+    for j, K in enumerate(KS):
+        f = mean_ms("chain_fused", j)
+        u = mean_ms("chain_unfused", j)
+        fat = mean_ms("chain_fat", j)
+        per_k[str(K)] = {
+            "fused_us": round(f * 1e3, 2), "unfused_us": round(u * 1e3, 2),
+            "fat_us": round(fat * 1e3, 2), "speedup_fused_vs_unfused": round(u / f, 3),
+            "fat_over_fused": round(fat / f, 3),
+            "fused_GBs": round(chain_bytes / (f / 1e3) / 1e9, 1),
+            "unfused_GBs": round(fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED) / (u / 1e3) / 1e9, 1),
+        }
+    fused_avg_ms = fused_ms_total / n_fused
+    achieved = chain_bytes / (fused_avg_ms / 1e3) / 1e9
+    kernel_src = os.path.join(ROOT, "epilogue_chains_gb300", "csrc", "chain.cu")
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "traffic": committed_traffic(kernel_src), "peak_source": peak_src,
+                "kernel": "chain_fused_kernel<f32>", "algorithmic_bytes_per_launch": chain_bytes,
+                "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4)}
+
+    rows = {"chain": per_k}
+    if rows_all:
+        hbm = peaks["hbm_gbs"]
+        rb_f = fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_FUSED)
+        rb_u = fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_UNFUSED)
+        rf = float(np.mean([np.mean(st) for st in times["rmsnorm_fused"]]))
+        ru = float(np.mean([np.mean(st) for st in times["rmsnorm_unfused"]]))
+        rows["rmsnorm"] = {"fused_us": round(rf * 1e3, 2), "unfused_us": round(ru * 1e3, 2),
+                           "fused_GBs": round(rb_f / rf / 1e6, 1),
+                           "fused_frac_hbm": round(rb_f / rf / 1e6 / hbm, 4),
+                           "unfused_GBs": round(rb_u / ru / 1e6, 1),
+                           "speedup": round(ru / rf, 3)}
+        sm = {}
+        for j, t in enumerate((0, 64, 128)):
+            ms_ = mean_ms("softmax_fused", j)
+            b_ = fc.fuse_causal_softmax_bytes(bh, S, t, fc.FUSE_BF16, fc.FUSE_FUSED)
+            sm[f"fused_T{t}"] = {"us": round(ms_ * 1e3, 1), "bytes": b_,
+                                 "GBs": round(b_ / ms_ / 1e6, 1),
+                                 "frac_hbm": round(b_ / ms_ / 1e6 / hbm, 4)}
+        mu = mean_ms("softmax_unfused", 0)
+        bu = fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED)
+        sm["unfused"] = {"us": round(mu * 1e3, 1), "bytes": bu, "GBs": round(bu / mu / 1e6, 1)}
+        sm["speedup_fused_T0"] = round(mu / mean_ms("softmax_fused", 0), 3)
+        rows["causal_softmax"] = sm
+
+    # ---------------------------------------------------------------- e2e through host buffers
+    e2e = run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e["_elapsed"]], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e["_elapsed"] = float(t[0])
+    e2e_value = e2e["_bytes"] * world / e2e["_elapsed"] / 1e9
+
+    report = None
+    if rank == 0:
+        cpu = None
+        if not args.no_cpu_baseline and world == 1:
+            cpu = cpu_baseline(wl, seconds=10.0)
+        report = {
+            "metric": "fused-chain HBM GB/s and % of GB300 peak; fused/unfused speedup vs K",
+            "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(step_ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "pointwise chain fp32 N=16,777,216, K in {2,3,4,6,8}, "
+                                   "a_s~U[0.9,1.1], b_s~U[-0.1,0.1], ReLU on even s",
+                       "N": N, "K": list(KS), "step": "all rows" if rows_all else "chain sweep",
+                       "l2": "4 rotating x/y pairs (512 MiB) > L2; each group led by an untimed "
+                             "same-kind launch", "parallelism": f"replicas x{world}"},
+            "frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
+            "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+            "gpu_launches": timed_launches,
+            "clocks": clocks,
+            "rows": rows,
+            "cpu_baseline": cpu,
+        }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return report
+
+
+def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world):
+    """Per K: pinned host x -> device, the fused chain through the C ABI, device y -> pinned host."""
+    import torch
+    hx = torch.from_numpy(wl.chain_input(N, salt=7)).pin_memory()
+    hy = torch.empty(N, dtype=torch.float32).pin_memory()
+    dx = torch.empty(N, dtype=torch.float32, device=dev)
+    dy = torch.empty(N, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+
+    def one_step():
+        with torch.cuda.stream(stream):
+            for K in KS:
+                dx.copy_(hx, non_blocking=True)
+                rc = lib.fuse_chain_run(stage_sets[K], K, dx.data_ptr(), dy.data_ptr(), N,
+                                        fc.FUSE_F32, fc.FUSE_FUSED, sh)
+                if rc != 0:
+                    raise fc.FuseError(rc, "fuse_chain_run")
+                hy.copy_(dy, non_blocking=True)
+
+    for _ in range(2):
+        one_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    steps = max(3, min(args.steps, 10))
+    e0.record(stream)
+    for _ in range(steps):
+        one_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    elapsed = e0.elapsed_time(e1) / 1e3
+    return {"_elapsed": elapsed, "_bytes": steps * len(KS) * chain_bytes,
+            "h2d": len(KS) * N * 4, "d2h": len(KS) * N * 4}
+
+
+# ------------------------------------------------------------------------------ oracle arms
+def cpu_baseline(wl, seconds=10.0):
+    """The plain CPU oracle (single thread), as it stands, on the same chain workload: whole K
+    sweeps over the full N = 16,777,216 elements, repeated until ~`seconds` of CPU time."""
+    import oracle
+    x = wl.chain_input(wl.CHAIN_N, salt=0)
+    stages = {K: wl.chain_stages(K) for K in wl.CHAIN_KS}
+    nbytes, t_total, sweeps = 0, 0.0, 0
+    while t_total < seconds or sweeps == 0:
+        for K in wl.CHAIN_KS:
+            relu, a, b = stages[K]
+            t0 = time.perf_counter()
+            oracle.chain(relu, a, b, x)
+            t_total += time.perf_counter() - t0
+            nbytes += 2 * wl.CHAIN_N * 4
+        sweeps += 1
+    return {"value": round(nbytes / t_total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{sweeps} full K-sweeps (K=2,3,4,6,8) over N=16,777,216 fp32, single thread, "
+                      f"{t_total:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle timed on the host cores, rank 0 only."""
+    if rank != 0:
+        return None
+    from epilogue_chains_gb300 import workloads as wl
+    import oracle
+    N = wl.CHAIN_N
+    x = wl.chain_input(N, salt=0)
+    stages = {K: wl.chain_stages(K) for K in wl.CHAIN_KS}
+
+    def sweep():
+        for K in wl.CHAIN_KS:
+            relu, a, b = stages[K]
+            oracle.chain(relu, a, b, x)
+
+    for _ in range(args.warmup):
+        sweep()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        sweep()
+    dt = time.perf_counter() - t0
+    nbytes = args.steps * len(wl.CHAIN_KS) * 2 * N * 4
+    value = nbytes / dt / 1e9
+    return {"impl": "reference",
+            "metric": "fused-chain HBM GB/s and % of GB300 peak; fused/unfused speedup vs K",
+            "value": round(value, 3), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic",
+            "config": {"workload": "pointwise chain fp32 N=16,777,216, K in {2,3,4,6,8}, "
+                                   "a_s~U[0.9,1.1], b_s~U[-0.1,0.1], ReLU on even s",
+                       "N": N, "K": list(wl.CHAIN_KS), "step": "one K sweep"},
+            "cpu_baseline": {"value": round(value, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{args.steps} full K-sweeps over N=16,777,216, single thread"},
+            "e2e": {"value": round(value, 3), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        out = run_reference(args, rank, world)
+    else:
+        out = run_ours(args, rank, world, local)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

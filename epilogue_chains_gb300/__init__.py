@@ -1,1 +1,246 @@
-"""epilogue_chains_gb300: vertical fusion of dependent operator chains on one GB300 (sm_103a)."""
+"""epilogue_chains_gb300 -- vertical fusion of dependent operator chains on one GB300 (sm_103a).
+
+Thin Python binding of the C ABI in ``include/fusechain.h`` (``libfusechain.so``): the functions
+below have the C names and only marshal arguments (torch tensors -> device pointers, the current
+torch stream -> ``cudaStream_t``, status codes -> ``FuseError``).  Every step of every chain runs
+in the library's CUDA kernels; there is no fallback: if the library cannot be built or loaded, the
+first call raises.
+
+PyTorch is used for device memory and streams only.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+FUSE_OK, FUSE_EINVAL, FUSE_EALIGN, FUSE_EUNSUPPORTED = 0, -1, -2, -3
+FUSE_ECUDA, FUSE_ETIMEOUT, FUSE_EWORKSPACE = -4, -5, -6
+FUSE_F32, FUSE_F16, FUSE_BF16 = 0, 1, 2
+FUSE_FUSED, FUSE_UNFUSED, FUSE_FAT = 0, 1, 2
+FUSE_OP_AFFINE, FUSE_OP_AFFINE_RELU = 0, 1
+FUSE_MAX_STAGES = 32
+FUSE_FAT_TEMPS = 48
+
+
+class FuseError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        lib = _load()
+        msg = lib.fuse_strerror(status).decode()
+        extra = lib.fuse_last_cuda_error().decode() if status == FUSE_ECUDA else ""
+        super().__init__(f"{where}: {msg} ({status}) {extra}".strip())
+        self.status = status
+
+
+class fuse_stage(ctypes.Structure):
+    _fields_ = [("op", ctypes.c_int32), ("a", ctypes.c_float), ("b", ctypes.c_float),
+                ("writes", ctypes.c_int64), ("ext_reads", ctypes.c_int64),
+                ("flops", ctypes.c_int64), ("live_regs", ctypes.c_int32)]
+
+
+class fuse_ledger_t(ctypes.Structure):
+    _fields_ = [("bytes", ctypes.c_int64), ("launches", ctypes.c_int64),
+                ("reg_peak", ctypes.c_int64), ("flops", ctypes.c_int64)]
+
+
+class fuse_kernel_record(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 64), ("regs_per_thread", ctypes.c_int32),
+                ("local_bytes_per_thread", ctypes.c_int32), ("static_smem_bytes", ctypes.c_int32),
+                ("dynamic_smem_bytes", ctypes.c_int32), ("block_threads", ctypes.c_int32),
+                ("blocks_per_sm", ctypes.c_int32), ("max_threads_per_block", ctypes.c_int32)]
+
+
+_P, _I32, _I64, _U32, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
+                                   ctypes.c_float, ctypes.c_size_t)
+# every symbol the header declares, with its C signature
+SIGNATURES = {
+    "fuse_chain_run": ([ctypes.POINTER(fuse_stage), _I32, _P, _P, _I64, _I32, _I32, _P], _I32),
+    "fuse_rmsnorm": ([_P, _P, _P, _I64, _I64, _F32, _I32, _P, _SZ, _P], _I32),
+    "fuse_rmsnorm_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "fuse_causal_softmax": ([_P, _P, _I64, _I64, _F32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
+    "fuse_causal_softmax_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "fuse_ledger": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_ledger_t)], _I32),
+    "fuse_chain_bytes": ([_I32, _I64, _I32, _I32], _I64),
+    "fuse_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
+    "fuse_causal_softmax_bytes": ([_I64, _I64, _I32, _I32, _I32], _I64),
+    "fuse_kernel_count": ([], _I32),
+    "fuse_kernel_report": ([_I32, ctypes.POINTER(fuse_kernel_record)], _I32),
+    "fuse_strerror": ([_I32], ctypes.c_char_p),
+    "fuse_last_cuda_error": ([], ctypes.c_char_p),
+    "fuse_check": ([_P], _I32),
+    "fuse_debug_expire_wait": ([_I64, _P], _I32),
+    "fuse_version": ([], _I32),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+def _load():
+    """Build (if needed) and load libfusechain.so; raises if either fails."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is None:
+            from . import _build
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = lib
+    return _lib
+
+
+def library_path() -> str:
+    from . import _build
+    return _build.LIB
+
+
+def _check(status: int, where: str) -> None:
+    if status != FUSE_OK:
+        raise FuseError(status, where)
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    return {torch.float32: FUSE_F32, torch.float16: FUSE_F16, torch.bfloat16: FUSE_BF16}[t.dtype]
+
+
+def _stages(stages) -> ctypes.Array:
+    """Accept fuse_stage objects, (op, a, b) tuples or dicts with the struct's field names."""
+    arr = (fuse_stage * len(stages))()
+    for i, s in enumerate(stages):
+        if isinstance(s, fuse_stage):
+            arr[i] = s
+        elif isinstance(s, dict):
+            arr[i] = fuse_stage(**s)
+        else:
+            op, a, b = s
+            arr[i] = fuse_stage(int(op), float(a), float(b), 0, 0, 0, 0)
+    return arr
+
+
+def _need_device(*ts):
+    for t in ts:
+        if t is not None and not isinstance(t, int):
+            if not t.is_cuda or not t.is_contiguous():
+                raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+# ------------------------------------------------------------------------------- chains
+def fuse_chain_run(stages, x, y, mode: int = FUSE_FUSED, stream=None) -> None:
+    """y <- f_{K-1}(...f_0(x)) with f_s(v) = [ReLU](a_s v + b_s); see fusechain.h."""
+    _need_device(x, y)
+    if x.dtype != y.dtype or x.numel() != y.numel():
+        raise ValueError("x and y must have the same dtype and element count")
+    st = _stages(stages)
+    _check(_load().fuse_chain_run(st, len(st), _ptr(x), _ptr(y), x.numel(), _dtype_code(x), mode,
+                                  _stream(stream)), "fuse_chain_run")
+
+
+def fuse_rmsnorm(x, w, y, eps: float, mode: int = FUSE_FUSED, workspace=None, stream=None) -> None:
+    """y = x * rsqrt(mean(x^2, -1) + eps) * w over rows of a [rows, hidden] fp32 tensor."""
+    import torch
+    _need_device(x, w, y)
+    rows, hidden = x.shape
+    lib = _load()
+    ws_bytes = lib.fuse_rmsnorm_workspace_bytes(rows, hidden, mode)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.fuse_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(eps), mode,
+                            _ptr(workspace), ws_size, _stream(stream)), "fuse_rmsnorm")
+
+
+def fuse_causal_softmax(s, p, scale: float, skip_tile: int = 0, mode: int = FUSE_FUSED,
+                        workspace=None, stream=None) -> None:
+    """p = causal softmax(scale * s) over the last axis of a bf16 [..., S, S] tensor."""
+    import torch
+    _need_device(s, p)
+    S = s.shape[-1]
+    bh = s.numel() // (S * S)
+    lib = _load()
+    ws_bytes = lib.fuse_causal_softmax_workspace_bytes(bh, S, mode)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=s.device)
+    ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.fuse_causal_softmax(_ptr(s), _ptr(p), bh, S, float(scale), int(skip_tile),
+                                   _dtype_code(p), mode, _ptr(workspace), ws_size,
+                                   _stream(stream)), "fuse_causal_softmax")
+
+
+# ------------------------------------------------------------------------------- ledgers
+def fuse_ledger(stages, cut_mask: int, elem_bytes: int) -> dict:
+    st = _stages(stages)
+    out = fuse_ledger_t()
+    _check(_load().fuse_ledger(st, len(st), cut_mask, elem_bytes, ctypes.byref(out)), "fuse_ledger")
+    return {"bytes": out.bytes, "launches": out.launches, "reg_peak": out.reg_peak,
+            "flops": out.flops}
+
+
+def fuse_chain_bytes(K: int, n: int, dtype: int, mode: int) -> int:
+    return _load().fuse_chain_bytes(K, n, dtype, mode)
+
+
+def fuse_rmsnorm_bytes(rows: int, hidden: int, mode: int) -> int:
+    return _load().fuse_rmsnorm_bytes(rows, hidden, mode)
+
+
+def fuse_causal_softmax_bytes(bh: int, S: int, skip_tile: int, out_dtype: int, mode: int) -> int:
+    return _load().fuse_causal_softmax_bytes(bh, S, skip_tile, out_dtype, mode)
+
+
+def fuse_rmsnorm_workspace_bytes(rows: int, hidden: int, mode: int) -> int:
+    return _load().fuse_rmsnorm_workspace_bytes(rows, hidden, mode)
+
+
+def fuse_causal_softmax_workspace_bytes(bh: int, S: int, mode: int) -> int:
+    return _load().fuse_causal_softmax_workspace_bytes(bh, S, mode)
+
+
+# ------------------------------------------------------------------------------- status
+def fuse_kernel_count() -> int:
+    return _load().fuse_kernel_count()
+
+
+def fuse_kernel_report(index: int) -> dict:
+    rec = fuse_kernel_record()
+    _check(_load().fuse_kernel_report(index, ctypes.byref(rec)), "fuse_kernel_report")
+    return {f: (getattr(rec, f).decode() if f == "name" else getattr(rec, f))
+            for f, _ in fuse_kernel_record._fields_}
+
+
+def fuse_check(stream=None) -> int:
+    return _load().fuse_check(_stream(stream))
+
+
+def fuse_debug_expire_wait(budget_cycles: int, stream=None) -> None:
+    _check(_load().fuse_debug_expire_wait(int(budget_cycles), _stream(stream)),
+           "fuse_debug_expire_wait")
+
+
+def fuse_strerror(status: int) -> str:
+    return _load().fuse_strerror(status).decode()
+
+
+def fuse_version() -> int:
+    return _load().fuse_version()

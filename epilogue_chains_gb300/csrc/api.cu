@@ -1,0 +1,127 @@
+// api.cu -- status, error strings, device queries and the kernel report of the C ABI.
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "fc_internal.cuh"
+
+namespace fc {
+
+// per-translation-unit report tables (defined next to their kernels)
+int chain_report_count();
+int chain_report(int i, fuse_kernel_record* out);
+int rmsnorm_report_count();
+int rmsnorm_report(int i, fuse_kernel_record* out);
+int softmax_report_count();
+int softmax_report(int i, fuse_kernel_record* out);
+int gemm_report_count();
+int gemm_report(int i, fuse_kernel_record* out);
+int watchdog_take();  // 1 if a bounded device wait expired since the last call (and clears it)
+
+namespace {
+thread_local char t_last_error[256] = "";
+}
+
+int record_cuda_error(cudaError_t e) {
+    snprintf(t_last_error, sizeof(t_last_error), "%s: %s", cudaGetErrorName(e),
+             cudaGetErrorString(e));
+    return FUSE_ECUDA;
+}
+
+int sm_count() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 1;
+    }
+    if (dev < 0 || dev >= 64) return 1;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            n = 1;
+        }
+        cached[dev] = n > 0 ? n : 1;
+    }
+    return cached[dev];
+}
+
+int describe_kernel(const void* kernel, const char* name, int block, int dyn_smem,
+                    fuse_kernel_record* out) {
+    if (!out) return FUSE_EINVAL;
+    memset(out, 0, sizeof(*out));
+    snprintf(out->name, sizeof(out->name), "%s", name);
+    cudaFuncAttributes a;
+    cudaError_t e = cudaFuncGetAttributes(&a, kernel);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    out->regs_per_thread = a.numRegs;
+    out->local_bytes_per_thread = static_cast<int32_t>(a.localSizeBytes);
+    out->static_smem_bytes = static_cast<int32_t>(a.sharedSizeBytes);
+    out->dynamic_smem_bytes = dyn_smem;
+    out->block_threads = block;
+    out->max_threads_per_block = a.maxThreadsPerBlock;
+    int b = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, dyn_smem);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    out->blocks_per_sm = b;
+    return FUSE_OK;
+}
+
+}  // namespace fc
+
+namespace {
+struct ReportTable {
+    int (*count)();
+    int (*get)(int, fuse_kernel_record*);
+};
+const ReportTable kTables[] = {
+    {fc::chain_report_count, fc::chain_report},
+    {fc::rmsnorm_report_count, fc::rmsnorm_report},
+    {fc::softmax_report_count, fc::softmax_report},
+    {fc::gemm_report_count, fc::gemm_report},
+};
+}  // namespace
+
+extern "C" int fuse_kernel_count(void) {
+    int n = 0;
+    for (const auto& t : kTables) n += t.count();
+    return n;
+}
+
+extern "C" int fuse_kernel_report(int index, fuse_kernel_record* out) {
+    if (!out || index < 0) return FUSE_EINVAL;
+    for (const auto& t : kTables) {
+        const int c = t.count();
+        if (index < c) return t.get(index, out);
+        index -= c;
+    }
+    return FUSE_EINVAL;
+}
+
+extern "C" const char* fuse_strerror(int status) {
+    switch (status) {
+        case FUSE_OK: return "ok";
+        case FUSE_EINVAL: return "invalid argument";
+        case FUSE_EALIGN: return "alignment or leading-dimension rule not met";
+        case FUSE_EUNSUPPORTED: return "unsupported size or combination";
+        case FUSE_ECUDA: return "CUDA launch or runtime error";
+        case FUSE_ETIMEOUT: return "bounded device wait expired (watchdog)";
+        case FUSE_EWORKSPACE: return "workspace missing or too small";
+        default: return "unknown status";
+    }
+}
+
+extern "C" const char* fuse_last_cuda_error(void) { return fc::t_last_error; }
+
+extern "C" int fuse_check(fuse_stream_t stream) {
+    cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fc::record_cuda_error(e);
+    if (fc::watchdog_take()) return FUSE_ETIMEOUT;
+    return FUSE_OK;
+}
+
+extern "C" int fuse_version(void) { return (1 << 16) | 0; }

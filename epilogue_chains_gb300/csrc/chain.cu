@@ -1,0 +1,313 @@
+// chain.cu -- the pointwise chain y = f_{K-1}(...f_0(x)), f_s(v) = [ReLU](a_s*v + b_s).
+//
+// [C05] §3 "API / experiment shape" names the three forms built here:
+//   naive  -- one stage kernel per s, the intermediate passes through global memory;
+//   fused  -- one kernel that loops s = 0..K-1 in registers and writes once;
+//   fat    -- the fused kernel plus C05_FAT_TEMPS (48) live temporaries summed into a sink, a
+//             probe of the register-pressure cliff ([C05] §6.2: blocks/SM 6 -> 1 on sm_120).
+// [OFCG] §3.2 gives their byte ledgers: 2*K*N*b unfused, 2*N*b fused.
+//
+// GB300 design: the work is pure HBM streaming (8 B/element for fp32, 2 flops per stage), so the
+// kernels are sized for bytes in flight, not ALU: 16-byte streaming loads/stores (ld/st .cs),
+// U independent vectors per thread issued before any arithmetic, and a grid of exactly one
+// resident wave (SM count x occupancy) that strides over the tensor.  Stage coefficients are a
+// __grid_constant__ parameter, read from the constant bank with no local copy.
+#include "fc_internal.cuh"
+
+namespace fc {
+namespace {
+
+constexpr int kBlock = 256;
+constexpr int kUnroll = 4;
+
+struct ChainParams {
+    const void* x;
+    void* y;
+    int64_t n;      // elements
+    int64_t head;   // scalar elements before the 16-byte-aligned body
+    int64_t nvec;   // 16-byte vectors in the body
+    int K;
+    uint32_t relu_mask;
+    float a[FUSE_MAX_STAGES];
+    float b[FUSE_MAX_STAGES];
+};
+
+__device__ float g_fat_sink;  // written only on an impossible bit pattern: keeps the fat sum live
+
+// One stage, rounded twice (fl32(fl32(a*v) + b)), then ReLU(t) = t > 0 ? t : +0.
+__device__ __forceinline__ float stage_apply(float v, float a, float b, bool relu) {
+    float t = __fadd_rn(__fmul_rn(a, v), b);
+    return relu ? (t > 0.0f ? t : 0.0f) : t;
+}
+
+template <int E, bool kOneStage>
+__device__ __forceinline__ void run_chain(float (&f)[E], const ChainParams& p) {
+    const int K = kOneStage ? 1 : p.K;
+    for (int s = 0; s < K; ++s) {
+        const float a = p.a[s];
+        const float b = p.b[s];
+        const bool relu = (p.relu_mask >> s) & 1u;
+#pragma unroll
+        for (int e = 0; e < E; ++e) f[e] = stage_apply(f[e], a, b, relu);
+    }
+}
+
+template <typename T, int U, bool kOneStage>
+__device__ __forceinline__ void chain_body(const ChainParams& p) {
+    using V = Vec16<T>;
+    constexpr int E = V::N;
+    const T* x = static_cast<const T*>(p.x);
+    T* y = static_cast<T*>(p.y);
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+
+    // unaligned head and tail (fewer than 16 bytes each when x and y share their alignment;
+    // the whole tensor when they do not)
+    const int64_t tail0 = p.head + p.nvec * E;
+    for (int64_t i = tid; i < p.head; i += nthr) {
+        float f[1] = {to_f32(x[i])};
+        run_chain<1, kOneStage>(f, p);
+        y[i] = from_f32<T>(f[0]);
+    }
+    for (int64_t i = tail0 + tid; i < p.n; i += nthr) {
+        float f[1] = {to_f32(x[i])};
+        run_chain<1, kOneStage>(f, p);
+        y[i] = from_f32<T>(f[0]);
+    }
+
+    const uint4* xv = reinterpret_cast<const uint4*>(x + p.head);
+    uint4* yv = reinterpret_cast<uint4*>(y + p.head);
+    int64_t i = tid;
+    for (; i + (U - 1) * nthr < p.nvec; i += U * nthr) {
+        uint4 r[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) r[u] = ld_stream(xv + i + u * nthr);
+        float f[U * E];
+#pragma unroll
+        for (int u = 0; u < U; ++u) V::unpack(r[u], f + u * E);
+        run_chain<U * E, kOneStage>(f, p);
+#pragma unroll
+        for (int u = 0; u < U; ++u) st_stream(yv + i + u * nthr, V::pack(f + u * E));
+    }
+    for (; i < p.nvec; i += nthr) {
+        float f[E];
+        V::unpack(ld_stream(xv + i), f);
+        run_chain<E, kOneStage>(f, p);
+        st_stream(yv + i, V::pack(f));
+    }
+}
+
+template <typename T, int U>
+__global__ void __launch_bounds__(kBlock) chain_fused_kernel(const __grid_constant__ ChainParams p) {
+    chain_body<T, U, false>(p);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kBlock) chain_stage_kernel(const __grid_constant__ ChainParams p) {
+    chain_body<T, kUnroll, true>(p);
+}
+
+// ---------------------------------------------------------------------------------- fat probe
+// Each element carries FUSE_FAT_TEMPS temporaries t_j, updated every stage as t_j <- t_j*a_s + v
+// and summed into a sink at the end.  The stage loop has a run-time trip count, so all
+// temporaries of the 4 elements a thread holds (4 x 48 = 192 fp32) are live across it.
+template <int E>
+__device__ __forceinline__ float fat_group(float (&v)[E], const ChainParams& p) {
+    float t[E][FUSE_FAT_TEMPS];
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+#pragma unroll
+        for (int j = 0; j < FUSE_FAT_TEMPS; ++j) t[e][j] = v[e] * (1.0f + j * (1.0f / 64.0f));
+    for (int s = 0; s < p.K; ++s) {
+        const float a = p.a[s];
+        const float b = p.b[s];
+        const bool relu = (p.relu_mask >> s) & 1u;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            v[e] = stage_apply(v[e], a, b, relu);
+#pragma unroll
+            for (int j = 0; j < FUSE_FAT_TEMPS; ++j) t[e][j] = __fmaf_rn(t[e][j], a, v[e]);
+        }
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int e = 0; e < E; ++e)
+#pragma unroll
+        for (int j = 0; j < FUSE_FAT_TEMPS; ++j) acc += t[e][j];
+    return acc;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kBlock, 1) chain_fat_kernel(const __grid_constant__ ChainParams p) {
+    const T* x = static_cast<const T*>(p.x);
+    T* y = static_cast<T*>(p.y);
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    float sink = 0.0f;
+
+    // groups of 4 consecutive elements (the body is 16-byte aligned, so 4 elements are aligned
+    // to 4*sizeof(T)); head and tail one element at a time
+    const int64_t body = p.nvec * Vec16<T>::N;
+    const int64_t groups = body / 4;
+    const int64_t tail0 = p.head + groups * 4;
+    for (int64_t i = tid; i < p.head; i += nthr) {
+        float v[1] = {to_f32(x[i])};
+        sink += fat_group<1>(v, p);
+        y[i] = from_f32<T>(v[0]);
+    }
+    for (int64_t i = tail0 + tid; i < p.n; i += nthr) {
+        float v[1] = {to_f32(x[i])};
+        sink += fat_group<1>(v, p);
+        y[i] = from_f32<T>(v[0]);
+    }
+    const T* xb = x + p.head;
+    T* yb = y + p.head;
+    for (int64_t g = tid; g < groups; g += nthr) {
+        float v[4];
+        if constexpr (sizeof(T) == 4) {
+            uint4 r = ld_stream(reinterpret_cast<const uint4*>(xb) + g);
+            Vec16<float>::unpack(r, v);
+        } else {
+            uint2 r = __ldcs(reinterpret_cast<const uint2*>(xb) + g);
+            const T* h = reinterpret_cast<const T*>(&r);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = to_f32(h[e]);
+        }
+        sink += fat_group<4>(v, p);
+        if constexpr (sizeof(T) == 4) {
+            st_stream(reinterpret_cast<uint4*>(yb) + g, Vec16<float>::pack(v));
+        } else {
+            T h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = from_f32<T>(v[e]);
+            __stcs(reinterpret_cast<uint2*>(yb) + g, *reinterpret_cast<uint2*>(h));
+        }
+    }
+    if (__float_as_uint(sink) == 0x7fbadbadu) g_fat_sink = sink;
+}
+
+// ---------------------------------------------------------------------------------- host side
+template <typename T>
+int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
+    const int sms = sm_count();
+    ChainParams p = base;
+    const int64_t work = p.nvec > 0 ? p.nvec : p.n;  // units a thread strides over
+    auto grid_for = [&](int occ, int per_thread) {
+        int64_t want = ceil_div(ceil_div(work, per_thread), kBlock);
+        int64_t cap = static_cast<int64_t>(sms) * occ;
+        return static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
+    };
+    if (mode == FUSE_FUSED) {
+        static int occ = blocks_per_sm(chain_fused_kernel<T, kUnroll>, kBlock);
+        chain_fused_kernel<T, kUnroll><<<grid_for(occ, kUnroll), kBlock, 0, stream>>>(p);
+        return check_launch();
+    }
+    if (mode == FUSE_FAT) {
+        static int occ = blocks_per_sm(chain_fat_kernel<T>, kBlock);
+        chain_fat_kernel<T><<<grid_for(occ, 1), kBlock, 0, stream>>>(p);
+        return check_launch();
+    }
+    // FUSE_UNFUSED: stage s is its own launch; stage 0 reads x, every later stage reads and
+    // rewrites y in place, so each intermediate makes a full round trip through HBM.
+    static int occ = blocks_per_sm(chain_stage_kernel<T>, kBlock);
+    for (int s = 0; s < base.K; ++s) {
+        ChainParams q = base;
+        q.K = 1;
+        q.a[0] = base.a[s];
+        q.b[0] = base.b[s];
+        q.relu_mask = (base.relu_mask >> s) & 1u;
+        if (s > 0) {
+            q.x = base.y;  // y is 16-byte partitioned the same way for both operands now
+            const uintptr_t off = reinterpret_cast<uintptr_t>(base.y) % 16;
+            int64_t head = off ? static_cast<int64_t>((16 - off) / sizeof(T)) : 0;
+            if (head > base.n) head = base.n;
+            q.head = head;
+            q.nvec = (base.n - head) / Vec16<T>::N;
+        }
+        const int64_t w = q.nvec > 0 ? q.nvec : q.n;
+        int64_t want = ceil_div(ceil_div(w, kUnroll), kBlock);
+        int64_t cap = static_cast<int64_t>(sms) * occ;
+        unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
+        chain_stage_kernel<T><<<grid, kBlock, 0, stream>>>(q);
+        int rc = check_launch();
+        if (rc != FUSE_OK) return rc;
+    }
+    return FUSE_OK;
+}
+
+}  // namespace
+
+// report entries of this translation unit
+int chain_report_count() { return 5; }
+int chain_report(int i, fuse_kernel_record* out) {
+    switch (i) {
+        case 0: return describe_kernel((const void*)chain_fused_kernel<float, kUnroll>,
+                                       "chain_fused_kernel<f32>", kBlock, 0, out);
+        case 1: return describe_kernel((const void*)chain_stage_kernel<float>,
+                                       "chain_stage_kernel<f32> (unfused stage)", kBlock, 0, out);
+        case 2: return describe_kernel((const void*)chain_fat_kernel<float>,
+                                       "chain_fat_kernel<f32> (48 live temps)", kBlock, 0, out);
+        case 3: return describe_kernel((const void*)chain_fused_kernel<__nv_bfloat16, kUnroll>,
+                                       "chain_fused_kernel<bf16>", kBlock, 0, out);
+        case 4: return describe_kernel((const void*)chain_fat_kernel<__nv_bfloat16>,
+                                       "chain_fat_kernel<bf16> (48 live temps)", kBlock, 0, out);
+        default: return FUSE_EINVAL;
+    }
+}
+
+}  // namespace fc
+
+extern "C" int fuse_chain_run(const fuse_stage* stages, int K, const void* x, void* y, int64_t n,
+                              int dtype, int mode, fuse_stream_t stream) {
+    using namespace fc;
+    if (!stages || K < 1 || K > FUSE_MAX_STAGES || n < 0) return FUSE_EINVAL;
+    if (dtype != FUSE_F32 && dtype != FUSE_F16 && dtype != FUSE_BF16) return FUSE_EINVAL;
+    if (mode != FUSE_FUSED && mode != FUSE_UNFUSED && mode != FUSE_FAT) return FUSE_EINVAL;
+    for (int s = 0; s < K; ++s)
+        if (stages[s].op != FUSE_OP_AFFINE && stages[s].op != FUSE_OP_AFFINE_RELU) return FUSE_EINVAL;
+    if (n == 0) return FUSE_OK;
+    if (!x || !y) return FUSE_EINVAL;
+    const size_t eb = dtype == FUSE_F32 ? 4 : 2;
+    if (!is_aligned(x, eb) || !is_aligned(y, eb)) return FUSE_EALIGN;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x), ya = reinterpret_cast<uintptr_t>(y);
+    const uintptr_t bytes = static_cast<uintptr_t>(n) * eb;
+    if (xa != ya && xa < ya + bytes && ya < xa + bytes) return FUSE_EINVAL;  // partial overlap
+
+    ChainParams p{};
+    p.x = x;
+    p.y = y;
+    p.n = n;
+    p.K = K;
+    for (int s = 0; s < K; ++s) {
+        p.a[s] = stages[s].a;
+        p.b[s] = stages[s].b;
+        if (stages[s].op == FUSE_OP_AFFINE_RELU) p.relu_mask |= 1u << s;
+    }
+    const uintptr_t xo = xa % 16, yo = ya % 16;
+    const int64_t vecN = dtype == FUSE_F32 ? 4 : 8;
+    if (xo == yo) {
+        int64_t head = xo ? static_cast<int64_t>((16 - xo) / eb) : 0;
+        if (head > n) head = n;
+        p.head = head;
+        p.nvec = (n - head) / vecN;
+    } else {
+        p.head = n;  // operands misaligned against each other: element-wise path only
+        p.nvec = 0;
+    }
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    switch (dtype) {
+        case FUSE_F32: return launch_chain<float>(p, mode, st);
+        case FUSE_F16: return launch_chain<__half>(p, mode, st);
+        default: return launch_chain<__nv_bfloat16>(p, mode, st);
+    }
+}
+
+extern "C" int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode) {
+    if (K < 1 || K > FUSE_MAX_STAGES || n < 0) return FUSE_EINVAL;
+    if (dtype != FUSE_F32 && dtype != FUSE_F16 && dtype != FUSE_BF16) return FUSE_EINVAL;
+    const int64_t b = dtype == FUSE_F32 ? 4 : 2;
+    // [OFCG] §3.2: every kernel reads N*b and writes N*b.
+    if (mode == FUSE_UNFUSED) return 2 * static_cast<int64_t>(K) * n * b;
+    if (mode == FUSE_FUSED || mode == FUSE_FAT) return 2 * n * b;
+    return FUSE_EINVAL;
+}

@@ -1,0 +1,66 @@
+// fc_ptx.cuh -- inline-PTX building blocks for sm_103a: mbarriers with bounded waits.
+// (TMA and tcgen05 wrappers live in gemm.cu, their only user.)
+#pragma once
+
+#include <stdint.h>
+
+namespace fc {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the async proxy (TMA, tcgen05.commit).
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Default budget of one bounded wait, in SM clock cycles (~1 s at 2 GHz).
+constexpr long long kWaitBudget = 2000000000LL;
+
+// Wait for phase `parity` of an mbarrier to complete, for at most `budget` SM cycles.  On expiry
+// (or when another thread already raised the watchdog flag) the flag is set and false is
+// returned; the caller must then unwind without issuing new asynchronous work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* flag,
+                                                  long long budget = kWaitBudget) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (++spins % 64u == 0u) {
+            if (*reinterpret_cast<volatile int*>(flag) != 0) return false;
+            if (clock64() - t0 > budget) {
+                atomicExch(flag, 1);
+                return false;
+            }
+        }
+    }
+    return true;
+}
+
+}  // namespace fc

@@ -1,0 +1,273 @@
+// rmsnorm.cu -- RMSNorm, fused (one pass) and unfused (four kernels).
+//
+// [OFCG] §3.2 and fusion_lab [A2]: unfused RMSNorm is x*x -> reduce-mean -> x*r -> *g, each step
+// a kernel that reads and writes HBM; fused it is one pass.  Per row i:
+//     r_i = 1/sqrt(mean_j x_ij^2 + eps),   y_ij = (x_ij * r_i) * w_j.
+//
+// GB300 design (fused): one CTA per row with the whole row held in registers (16 B vector loads,
+// VPT vectors per thread, all issued before the reduction), a warp-shuffle reduction followed by
+// a shared-memory reduction across the CTA's warps, then the scaled row is written with 16 B
+// streaming stores.  x is read from HBM exactly once; w (16 KB at hidden 4096) stays in L2.
+#include "fc_internal.cuh"
+
+namespace fc {
+namespace {
+
+constexpr int kRowThreads = 128;     // vector path: 128 threads x VPT float4 per row
+constexpr int kRowThreadsScalar = 512;
+constexpr int kEwBlock = 256;
+
+template <int THREADS>
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    constexpr int W = THREADS / 32;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k) t += red[k];
+    return t;
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
+    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int hidden,
+    float eps) {
+    __shared__ float red[kRowThreads / 32];
+    const int64_t row = blockIdx.x;
+    const int nv = hidden / 4;
+    const float4* xr = reinterpret_cast<const float4*>(x + row * hidden);
+    float4* yr = reinterpret_cast<float4*>(y + row * hidden);
+    const float4* wv = reinterpret_cast<const float4*>(w);
+    float4 v[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int idx = threadIdx.x + k * kRowThreads;
+        v[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    const float total = block_sum<kRowThreads>(ss, red);
+    const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int idx = threadIdx.x + k * kRowThreads;
+        if (idx < nv) {
+            const float4 g = __ldg(wv + idx);
+            float4 o;
+            o.x = __fmul_rn(__fmul_rn(v[k].x, r), g.x);
+            o.y = __fmul_rn(__fmul_rn(v[k].y, r), g.y);
+            o.z = __fmul_rn(__fmul_rn(v[k].z, r), g.z);
+            o.w = __fmul_rn(__fmul_rn(v[k].w, r), g.w);
+            __stcs(yr + idx, o);
+        }
+    }
+}
+
+// Element-wise variant for rows that are not whole 16-byte vectors (odd hidden or offsets).
+template <int EPT>
+__global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel(
+    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int hidden,
+    float eps) {
+    __shared__ float red[kRowThreadsScalar / 32];
+    const int64_t row = blockIdx.x;
+    const float* xr = x + row * hidden;
+    float* yr = y + row * hidden;
+    float v[EPT];
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        const int j = threadIdx.x + k * kRowThreadsScalar;
+        v[k] = j < hidden ? xr[j] : 0.0f;
+        ss += v[k] * v[k];
+    }
+    const float total = block_sum<kRowThreadsScalar>(ss, red);
+    const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
+#pragma unroll
+    for (int k = 0; k < EPT; ++k) {
+        const int j = threadIdx.x + k * kRowThreadsScalar;
+        if (j < hidden) yr[j] = __fmul_rn(__fmul_rn(v[k], r), w[j]);
+    }
+}
+
+// ------------------------------------------------------------------------- unfused kernels
+// (1) sq = x*x   (2) ms = rowmean(sq)   (3) t = x * rsqrt(ms + eps)   (4) y = t * w
+__global__ void __launch_bounds__(kEwBlock) rms_square_kernel(const float* __restrict__ x,
+                                                              float* __restrict__ y, int64_t n,
+                                                              bool vec) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = n / 4;
+        for (int64_t i = tid; i < nv; i += nthr) {
+            float4 a = __ldcs(reinterpret_cast<const float4*>(x) + i);
+            a.x = __fmul_rn(a.x, a.x); a.y = __fmul_rn(a.y, a.y);
+            a.z = __fmul_rn(a.z, a.z); a.w = __fmul_rn(a.w, a.w);
+            __stcs(reinterpret_cast<float4*>(y) + i, a);
+        }
+        done = nv * 4;
+    }
+    for (int64_t i = done + tid; i < n; i += nthr) y[i] = __fmul_rn(x[i], x[i]);
+}
+
+__global__ void __launch_bounds__(kRowThreadsScalar) rms_rowmean_kernel(
+    const float* __restrict__ sq, float* __restrict__ ms, int hidden) {
+    __shared__ float red[kRowThreadsScalar / 32];
+    const int64_t row = blockIdx.x;
+    const float* r = sq + row * hidden;
+    float acc = 0.0f;
+    for (int j = threadIdx.x; j < hidden; j += kRowThreadsScalar) acc += __ldcs(r + j);
+    const float total = block_sum<kRowThreadsScalar>(acc, red);
+    if (threadIdx.x == 0) ms[row] = __fdiv_rn(total, static_cast<float>(hidden));
+}
+
+__global__ void __launch_bounds__(kEwBlock) rms_scale_kernel(const float* __restrict__ x,
+                                                             const float* __restrict__ ms,
+                                                             float* __restrict__ y, int64_t n,
+                                                             int hidden, float eps, bool vec) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (vec) {  // hidden % 4 == 0: a vector never straddles two rows
+        const int64_t nv = n / 4;
+        const int vpr = hidden / 4;
+        for (int64_t i = tid; i < nv; i += nthr) {
+            const float r = rsqrtf(__ldg(ms + i / vpr) + eps);
+            float4 a = __ldcs(reinterpret_cast<const float4*>(x) + i);
+            a.x = __fmul_rn(a.x, r); a.y = __fmul_rn(a.y, r);
+            a.z = __fmul_rn(a.z, r); a.w = __fmul_rn(a.w, r);
+            __stcs(reinterpret_cast<float4*>(y) + i, a);
+        }
+        return;
+    }
+    for (int64_t i = tid; i < n; i += nthr) y[i] = __fmul_rn(x[i], rsqrtf(ms[i / hidden] + eps));
+}
+
+__global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict__ y,
+                                                              const float* __restrict__ w,
+                                                              int64_t n, int hidden, bool vec) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    if (vec) {
+        const int64_t nv = n / 4;
+        const int vpr = hidden / 4;
+        for (int64_t i = tid; i < nv; i += nthr) {
+            const float4 g = __ldg(reinterpret_cast<const float4*>(w) + i % vpr);
+            float4 a = __ldcs(reinterpret_cast<const float4*>(y) + i);
+            a.x = __fmul_rn(a.x, g.x); a.y = __fmul_rn(a.y, g.y);
+            a.z = __fmul_rn(a.z, g.z); a.w = __fmul_rn(a.w, g.w);
+            __stcs(reinterpret_cast<float4*>(y) + i, a);
+        }
+        return;
+    }
+    for (int64_t i = tid; i < n; i += nthr) y[i] = __fmul_rn(y[i], w[i % hidden]);
+}
+
+template <int VPT>
+int launch_fused_vec(const float* x, const float* w, float* y, int64_t rows, int hidden, float eps,
+                     cudaStream_t st) {
+    rmsnorm_fused_kernel<VPT><<<static_cast<unsigned>(rows), kRowThreads, 0, st>>>(x, w, y, hidden, eps);
+    return check_launch();
+}
+
+template <int EPT>
+int launch_fused_scalar(const float* x, const float* w, float* y, int64_t rows, int hidden,
+                        float eps, cudaStream_t st) {
+    rmsnorm_fused_scalar_kernel<EPT><<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(
+        x, w, y, hidden, eps);
+    return check_launch();
+}
+
+unsigned ew_grid(int64_t units) {
+    const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kEwBlock);
+    int64_t g = ceil_div(units, kEwBlock);
+    if (g > cap) g = cap;
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
+}  // namespace
+
+int rmsnorm_report_count() { return 3; }
+int rmsnorm_report(int i, fuse_kernel_record* out) {
+    switch (i) {
+        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<8>,
+                                       "rmsnorm_fused_kernel<VPT=8> (hidden 4096)", kRowThreads, 0, out);
+        case 1: return describe_kernel((const void*)rms_rowmean_kernel,
+                                       "rms_rowmean_kernel (unfused step 2)", kRowThreadsScalar, 0, out);
+        case 2: return describe_kernel((const void*)rms_scale_kernel,
+                                       "rms_scale_kernel (unfused step 3)", kEwBlock, 0, out);
+        default: return FUSE_EINVAL;
+    }
+}
+
+}  // namespace fc
+
+extern "C" size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode) {
+    (void)hidden;
+    if (rows < 0) return 0;
+    return mode == FUSE_UNFUSED ? static_cast<size_t>(rows) * sizeof(float) : 0;
+}
+
+extern "C" int fuse_rmsnorm(const float* x, const float* w, float* y, int64_t rows, int64_t hidden,
+                            float eps, int mode, void* workspace, size_t ws_bytes,
+                            fuse_stream_t stream) {
+    using namespace fc;
+    if (rows < 0 || hidden < 1 || hidden > 65536 || !(eps >= 0.0f)) return FUSE_EINVAL;
+    if (mode != FUSE_FUSED && mode != FUSE_UNFUSED) return FUSE_EINVAL;
+    if (rows > 2147483647LL) return FUSE_EUNSUPPORTED;
+    if (rows == 0) return FUSE_OK;
+    if (!x || !w || !y) return FUSE_EINVAL;
+    if (!is_aligned(x, 4) || !is_aligned(w, 4) || !is_aligned(y, 4)) return FUSE_EALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int H = static_cast<int>(hidden);
+    const bool vec = (H % 4 == 0) && is_aligned(x, 16) && is_aligned(y, 16) && is_aligned(w, 16);
+
+    if (mode == FUSE_FUSED) {
+        if (H > 16384) return FUSE_EUNSUPPORTED;
+        if (vec) {
+            const int nv = H / 4;
+            if (nv <= 1 * kRowThreads) return launch_fused_vec<1>(x, w, y, rows, H, eps, st);
+            if (nv <= 2 * kRowThreads) return launch_fused_vec<2>(x, w, y, rows, H, eps, st);
+            if (nv <= 4 * kRowThreads) return launch_fused_vec<4>(x, w, y, rows, H, eps, st);
+            if (nv <= 8 * kRowThreads) return launch_fused_vec<8>(x, w, y, rows, H, eps, st);
+            if (nv <= 16 * kRowThreads) return launch_fused_vec<16>(x, w, y, rows, H, eps, st);
+            return launch_fused_vec<32>(x, w, y, rows, H, eps, st);
+        }
+        if (H <= 1 * kRowThreadsScalar) return launch_fused_scalar<1>(x, w, y, rows, H, eps, st);
+        if (H <= 2 * kRowThreadsScalar) return launch_fused_scalar<2>(x, w, y, rows, H, eps, st);
+        if (H <= 4 * kRowThreadsScalar) return launch_fused_scalar<4>(x, w, y, rows, H, eps, st);
+        if (H <= 8 * kRowThreadsScalar) return launch_fused_scalar<8>(x, w, y, rows, H, eps, st);
+        if (H <= 16 * kRowThreadsScalar) return launch_fused_scalar<16>(x, w, y, rows, H, eps, st);
+        return launch_fused_scalar<32>(x, w, y, rows, H, eps, st);
+    }
+
+    // FUSE_UNFUSED: four kernels; the N-sized intermediates live in y, the row means in workspace.
+    if (!workspace || ws_bytes < fuse_rmsnorm_workspace_bytes(rows, hidden, mode)) return FUSE_EWORKSPACE;
+    if (!is_aligned(workspace, 4)) return FUSE_EALIGN;
+    if (x == y) return FUSE_EINVAL;  // step 3 re-reads x after step 1 overwrote y
+    float* ms = static_cast<float*>(workspace);
+    const int64_t n = rows * hidden;
+    const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
+    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
+    int rc = check_launch();
+    if (rc) return rc;
+    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
+    if ((rc = check_launch())) return rc;
+    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
+    if ((rc = check_launch())) return rc;
+    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
+    return check_launch();
+}
+
+extern "C" int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode) {
+    if (rows < 0 || hidden < 1) return FUSE_EINVAL;
+    const int64_t n = rows * hidden, b = 4;
+    // fused: read x, write y, read w once
+    if (mode == FUSE_FUSED) return 2 * n * b + hidden * b;
+    // unfused: sq (r x, w y) + mean (r y, w ms) + scale (r x, r ms, w y) + weight (r y, r w, w y)
+    if (mode == FUSE_UNFUSED) return 7 * n * b + 2 * rows * b + hidden * b;
+    return FUSE_EINVAL;
+}

@@ -1,0 +1,216 @@
+/*
+ * fusechain.h -- C ABI of the vertical-fusion library for one NVIDIA GB300 (sm_103a).
+ *
+ * A chain of K dependent operators runs as ONE kernel that reads its inputs from HBM once, keeps
+ * every intermediate in registers or shared memory and writes only the final output.  Each chain
+ * also has an explicit unfused mode (one kernel per stage, intermediates through global memory)
+ * so that the byte ledgers of the pages can be checked against measured DRAM traffic.
+ *
+ * Sources (web pages; cited by title and section):
+ *   [K4]   "K4 walkthrough: the three ledgers of fusion -- bytes, launches, registers"
+ *   [C05]  "C-05 Kernel Fusion cost boundary: less write-back vs register pressure and occupancy"
+ *   [OFCG] "AIGC fundamentals | operator fusion and CUDA Graph"
+ *
+ * Conventions for every entry point below:
+ *   - Compute calls are stream-ordered and asynchronous: they validate their arguments on the
+ *     host, enqueue kernels on `stream` (NULL = the legacy default stream) and return.  None of
+ *     them synchronizes.
+ *   - Pointers named as device pointers must be device (or managed) memory that stays valid until
+ *     the enqueued work finishes; the caller owns all of it.  Host pointers (stage arrays, output
+ *     records) are read or written before the call returns.
+ *   - No compute entry point allocates memory.  Unfused modes that need row statistics take a
+ *     caller workspace whose size the matching *_workspace_bytes() call returns.
+ *   - All tensors are dense, row-major and contiguous.
+ *   - Return value: FUSE_OK (0) or a negative fuse_status.  FUSE_ECUDA means the launch itself
+ *     failed (cudaGetLastError() after the launch); the CUDA error string is then available from
+ *     fuse_last_cuda_error().  No C++ exception crosses this boundary.
+ *   - The library is thread-compatible: concurrent calls on different streams are allowed.
+ */
+#ifndef FUSECHAIN_H
+#define FUSECHAIN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t / CUstream. */
+typedef struct CUstream_st* fuse_stream_t;
+
+typedef enum {
+    FUSE_OK = 0,
+    FUSE_EINVAL = -1,         /* null pointer, size <= 0, K out of range, bad enum value     */
+    FUSE_EALIGN = -2,         /* alignment / leading-dimension rule of the call not met       */
+    FUSE_EUNSUPPORTED = -3,   /* a size or combination this build does not implement          */
+    FUSE_ECUDA = -4,          /* a CUDA launch or runtime call failed                         */
+    FUSE_ETIMEOUT = -5,       /* a bounded device-side wait ran out (watchdog)                */
+    FUSE_EWORKSPACE = -6      /* workspace pointer missing or smaller than required           */
+} fuse_status;
+
+typedef enum { FUSE_F32 = 0, FUSE_F16 = 1, FUSE_BF16 = 2 } fuse_dtype;
+
+typedef enum {
+    FUSE_FUSED = 0,           /* one kernel for the whole chain                                */
+    FUSE_UNFUSED = 1,         /* one kernel per stage, intermediates through global memory     */
+    FUSE_FAT = 2              /* fused + a deliberately register-heavy live-temporary probe    */
+} fuse_mode;
+
+typedef enum {
+    FUSE_OP_AFFINE = 0,       /* v <- a*v + b                                                  */
+    FUSE_OP_AFFINE_RELU = 1   /* v <- max(a*v + b, +0)  (t > 0 ? t : +0)                       */
+} fuse_op;
+
+#define FUSE_MAX_STAGES 32
+#define FUSE_FAT_TEMPS 48     /* live fp32 temporaries per element in FUSE_FAT mode ([C05] §3) */
+
+/*
+ * One operator of a chain.  [K4] introduction and §③: a Stage states how many elements it
+ * writes, how many elements it reads from outside the chain (weights, bias, residual, or the
+ * chain input for the first stage), its FLOPs and the registers it keeps live when fused.
+ * fuse_chain_run() executes `op`, `a`, `b`; fuse_ledger() reads the other fields.
+ */
+typedef struct {
+    int32_t op;               /* fuse_op                                                       */
+    float a;                  /* multiplier (fp32)                                             */
+    float b;                  /* addend (fp32)                                                 */
+    int64_t writes;           /* elements written                                              */
+    int64_t ext_reads;        /* elements read from outside the chain                          */
+    int64_t flops;            /* floating-point operations                                     */
+    int32_t live_regs;        /* registers live per thread when fused                          */
+} fuse_stage;
+
+/* ===================================================================== pointwise chain
+ * [C05] §3 (API / experiment shape): stage s computes y = a_s*y + b_s (ReLU on the even stages
+ * in the pages' sweep); the fused kernel loops s = 0..K-1 in registers and writes once; the
+ * naive form launches one stage kernel per s and passes the intermediate through global memory;
+ * the fat form is the fused kernel plus FUSE_FAT_TEMPS live temporaries summed into a sink.
+ * [OFCG] §3.2 gives the byte ledger: unfused 2*K*N*b, fused 2*N*b.
+ *
+ * Arithmetic: every stage rounds twice in fp32, t = fl32(fl32(a*v) + b) (no FMA contraction),
+ * then ReLU if op == FUSE_OP_AFFINE_RELU.  Values are loaded from `dtype` exactly and the result
+ * is rounded once (nearest-even) to `dtype`.  FUSED, UNFUSED and FAT give bit-identical y.
+ *
+ *   stages  host array of K stages (1 <= K <= FUSE_MAX_STAGES)
+ *   x       device pointer, n elements of `dtype` (input; may equal y, may not partially overlap)
+ *   y       device pointer, n elements of `dtype` (output)
+ *   n       element count, n >= 0 (n == 0 enqueues nothing)
+ *   dtype   FUSE_F32, FUSE_F16 or FUSE_BF16 (storage type; math is fp32)
+ *   mode    FUSE_FUSED: 1 launch, reads x once, writes y once.
+ *           FUSE_UNFUSED: K launches; stage 0 reads x and writes y, stage s > 0 reads y and
+ *             writes y in place (the intermediate round-trips through global memory each stage).
+ *           FUSE_FAT: 1 launch of the register-heavy probe; y identical to FUSED.
+ * Alignment: any element-aligned pointers work; the 16-byte vector path is used where x and y
+ * share their offset modulo 16 bytes.
+ */
+int fuse_chain_run(const fuse_stage* stages, int K, const void* x, void* y, int64_t n,
+                   int dtype, int mode, fuse_stream_t stream);
+
+/* ===================================================================== RMSNorm
+ * [OFCG] §3.2 and fusion_lab [A2]: RMSNorm unfused is four passes (x*x, reduce-mean, x*r, *g),
+ * fused is one.  Computes, per row i,
+ *     r_i = 1 / sqrt(mean_j x_ij^2 + eps),   y_ij = (x_ij * r_i) * w_j
+ * with fp32 storage and fp32 accumulation.
+ *
+ *   x, y    device fp32 [rows, hidden];  w  device fp32 [hidden]
+ *   rows >= 0, 1 <= hidden <= 65536, eps >= 0
+ *   mode    FUSE_FUSED: one kernel, one CTA per row with the row kept in registers
+ *           (hidden <= 16384 in this build; larger -> FUSE_EUNSUPPORTED).
+ *           FUSE_UNFUSED: four kernels: sq = x^2 -> y;  ms = rowmean(y) -> workspace;
+ *             t = x * rsqrt(ms + eps) -> y;  y = y * w  (in place).
+ *   workspace / ws_bytes: device scratch for the unfused row statistics; at least
+ *           fuse_rmsnorm_workspace_bytes(rows, hidden, mode) bytes; may be NULL for FUSED.
+ */
+int fuse_rmsnorm(const float* x, const float* w, float* y, int64_t rows, int64_t hidden,
+                 float eps, int mode, void* workspace, size_t ws_bytes, fuse_stream_t stream);
+size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode);
+
+/* ===================================================================== causal softmax
+ * [OFCG] fusion_lab [E] (max -> subtract -> exp -> sum -> divide over the last axis), §3.5
+ * (causal mask: query i sees keys j <= i; block-granular skipping) and [A3] (8 copies of the
+ * score tensor unfused vs 2 fused).  For every row i of every (batch*head):
+ *     z_j = scale * s_ij (j <= i),  p_ij = exp(z_j - max z) / sum exp(z - max z),  p_ij = +0 (j > i)
+ * fp32 math, bf16 input, bf16 (nearest-even) or fp32 output.
+ *
+ *   s          device bf16 [batch_heads, S, S]
+ *   p          device [batch_heads, S, S] of out_dtype (FUSE_BF16 or FUSE_F32)
+ *   S          1 <= S <= 8192
+ *   skip_tile  0: every row reads all S scores (masked ones are ignored);
+ *              T > 0 (a multiple of 8): row i reads only the columns < (floor(i/T)+1)*T, i.e.
+ *              the key blocks of a T x T block-causal tiling that are not fully masked.
+ *              Output values do not depend on skip_tile.  FUSED mode only.
+ *   mode       FUSE_FUSED: one kernel, one warp per row, row kept in registers.
+ *              FUSE_UNFUSED: five kernels over whole rows; the three elementwise intermediates
+ *              (scaled-and-shifted scores, exponentials) are bf16 and live in p; the row max
+ *              and row sum (fp32) live in the workspace.  skip_tile must be 0.
+ */
+int fuse_causal_softmax(const void* s, void* p, int64_t batch_heads, int64_t S, float scale,
+                        int skip_tile, int out_dtype, int mode, void* workspace,
+                        size_t ws_bytes, fuse_stream_t stream);
+size_t fuse_causal_softmax_workspace_bytes(int64_t batch_heads, int64_t S, int mode);
+
+/* ===================================================================== ledgers
+ * [K4] §① traffic(): a cut plan splits the K stages into consecutive kernels (cut_mask bit i =
+ * a kernel boundary after stage i).  Each kernel reads the previous kernel's output (the
+ * `writes` of the stage just before it, if any) plus the ext_reads of its stages, and writes
+ * the `writes` of its last stage.  Bytes = elements * elem_bytes.  reg_peak is the largest sum
+ * of live_regs over the stages of one kernel; flops is the plain sum.
+ */
+typedef struct {
+    int64_t bytes;
+    int64_t launches;
+    int64_t reg_peak;
+    int64_t flops;
+} fuse_ledger_t;
+
+int fuse_ledger(const fuse_stage* stages, int K, uint32_t cut_mask, int elem_bytes,
+                fuse_ledger_t* out);
+
+/* Algorithmic DRAM bytes of one call of the entry points above (what the kernel must move at
+ * minimum; the unfused forms count every intermediate round trip).  Negative = fuse_status. */
+int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode);
+int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode);
+int64_t fuse_causal_softmax_bytes(int64_t batch_heads, int64_t S, int skip_tile, int out_dtype,
+                                  int mode);
+
+/* ===================================================================== reports and status
+ * [K4] §③ and [C05] §6.2: registers per thread, spills and blocks per SM decide when fusion
+ * loses.  fuse_kernel_report() describes one kernel variant as launched by this library.
+ */
+typedef struct {
+    char name[64];
+    int32_t regs_per_thread;
+    int32_t local_bytes_per_thread;   /* local memory (spills + local arrays)                   */
+    int32_t static_smem_bytes;
+    int32_t dynamic_smem_bytes;       /* as launched                                            */
+    int32_t block_threads;            /* as launched                                            */
+    int32_t blocks_per_sm;            /* occupancy API at that block size and smem              */
+    int32_t max_threads_per_block;
+} fuse_kernel_record;
+
+/* Number of kernel variants fuse_kernel_report() knows (index 0 .. count-1). */
+int fuse_kernel_count(void);
+/* Fill *out for variant `index` (needs a CUDA device; the current device is used). */
+int fuse_kernel_report(int index, fuse_kernel_record* out);
+
+const char* fuse_strerror(int status);
+/* Message of the last CUDA error seen by this library on this thread ("" if none). */
+const char* fuse_last_cuda_error(void);
+/* Synchronize `stream`, then return FUSE_ETIMEOUT if a device watchdog fired since the last
+ * check (and clear it), FUSE_ECUDA if the stream reported an error, else FUSE_OK. */
+int fuse_check(fuse_stream_t stream);
+/* Test hook of the watchdog: one thread waits on an mbarrier that nothing arrives on, for
+ * budget_cycles SM clock cycles (0 <= budget_cycles < 2^31), then records the timeout and
+ * returns normally; the next fuse_check() returns FUSE_ETIMEOUT.  It faults and traps nothing
+ * and leaves the context usable (the same bounded wait guards every mbarrier wait of the GEMM). */
+int fuse_debug_expire_wait(int64_t budget_cycles, fuse_stream_t stream);
+
+/* Library version, (major << 16) | minor. */
+int fuse_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FUSECHAIN_H */

@@ -1,0 +1,113 @@
+"""Parity of the causal softmax (fused with and without block skip, five-kernel unfused) against
+the CPU oracle through the C ABI.
+
+Bars: masked outputs (j > i) are exactly +0 (bit-exact); bf16 outputs are within 1 bf16 ulp of
+the oracle's nearest-even result (fused) and within 2 ulps of the oracle that rounds at the same
+four points (unfused); fp32 outputs within 1e-5 relative per element."""
+import numpy as np
+import pytest
+
+import epilogue_chains_gb300 as fc
+import oracle
+from epilogue_chains_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(s_bits, scale, tile, mode, out="bf16", p_off=0):
+    import torch
+    s = torch.from_numpy(s_bits.view(np.int16)).cuda().view(torch.bfloat16)
+    tdt = torch.bfloat16 if out == "bf16" else torch.float32
+    n = s.numel()
+    pb = torch.full((n + 16,), float("nan"), dtype=tdt, device="cuda")
+    p = pb[p_off:p_off + n].view(s.shape)
+    fc.fuse_causal_softmax(s, p, scale, tile, mode)
+    torch.cuda.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    guard = torch.cat([pb[:p_off], pb[p_off + n:]]).float().cpu().numpy()
+    assert np.all(np.isnan(guard))
+    if out == "bf16":
+        return p.cpu().view(torch.int16).numpy().view(np.uint16)
+    return p.cpu().numpy()
+
+
+def _check_bf16(p, ref, S, ulps):
+    iu = np.triu_indices(S, 1)
+    assert np.all(p[..., iu[0], iu[1]] == 0), "masked outputs must be +0"
+    d = np.abs(p.astype(np.int32) - ref.astype(np.int32))   # outputs are >= 0: bit distance = ulps
+    assert d.max() <= ulps, int(d.max())
+
+
+@pytest.mark.parametrize("S", [1, 2, 7, 8, 16, 63, 64, 65, 128, 200, 256, 520, 1024, 2048])
+@pytest.mark.parametrize("tile", [0, 8, 64, 128])
+def test_fused_bf16(cuda_device, S, tile):
+    s = wl.softmax_input(3, S, salt=S)
+    p = _run(s, wl.SM_SCALE, tile, fc.FUSE_FUSED)
+    _check_bf16(p, oracle.causal_softmax(s, wl.SM_SCALE), S, 1)
+
+
+@pytest.mark.parametrize("S", [5, 64, 100, 2048, 3000, 4096])
+@pytest.mark.parametrize("tile", [0, 64])
+def test_fused_fp32(cuda_device, S, tile):
+    s = wl.softmax_input(2 if S <= 2048 else 1, S, salt=S + 1)
+    p = _run(s, wl.SM_SCALE, tile, fc.FUSE_FUSED, out="f32")
+    ref = oracle.causal_softmax(s, wl.SM_SCALE, out="f32")
+    iu = np.triu_indices(S, 1)
+    assert np.all(p[..., iu[0], iu[1]].view(np.uint32) == 0)
+    err = np.abs(p.astype(np.float64) - ref)
+    assert np.all(err <= 1e-5 * np.abs(ref) + 1e-30), float((err / (ref + 1e-30)).max())
+
+
+@pytest.mark.parametrize("S", [1, 7, 64, 65, 640, 2048])
+def test_unfused_five_kernels(cuda_device, S):
+    s = wl.softmax_input(2, S, salt=S + 2)
+    p = _run(s, wl.SM_SCALE, 0, fc.FUSE_UNFUSED)
+    _check_bf16(p, oracle.causal_softmax(s, wl.SM_SCALE, unfused=True), S, 2)
+    _check_bf16(p, oracle.causal_softmax(s, wl.SM_SCALE), S, 4)
+
+
+def test_generic_path_misaligned_output(cuda_device):
+    s = wl.softmax_input(2, 96, salt=3)
+    p = _run(s, wl.SM_SCALE, 0, fc.FUSE_FUSED, p_off=1)   # p not 16-byte aligned
+    _check_bf16(p, oracle.causal_softmax(s, wl.SM_SCALE), 96, 1)
+
+
+def test_masked_region_is_never_read(cuda_device):
+    """Scores above the diagonal (huge values, NaN) change nothing: the mask is applied before use."""
+    S = 256
+    s = wl.softmax_input(2, S, salt=4)
+    ref = oracle.causal_softmax(s, wl.SM_SCALE)
+    s2 = s.copy()
+    iu = np.triu_indices(S, 1)
+    s2[:, iu[0], iu[1]] = 0x7FC0                              # NaN
+    s2[:, 5, 200] = 0x4700
+    for tile in (0, 64):
+        for mode in (fc.FUSE_FUSED,):
+            _check_bf16(_run(s2, wl.SM_SCALE, tile, mode), ref, S, 1)
+
+
+def test_full_size_sampled_heads(cuda_device):
+    """[8, 16, 2048, 2048] as benchmarked: the GPU runs the whole tensor (every skip tile); four
+    heads are compared element by element with the oracle, and the causal nonzero count of every
+    head is checked (S(S+1)/2 = 2,098,176)."""
+    import torch
+    bh, S = wl.SM_B * wl.SM_H, wl.SM_S
+    s = wl.softmax_input(bh, S, device="cuda")
+    heads = [0, 37, 90, bh - 1]
+    s_h = s[heads].cpu().view(torch.int16).numpy().view(np.uint16)
+    ref = oracle.causal_softmax(s_h, wl.SM_SCALE)
+    for tile in (0, 64, 128):
+        p = torch.empty_like(s)
+        fc.fuse_causal_softmax(s, p, wl.SM_SCALE, tile, fc.FUSE_FUSED)
+        torch.cuda.synchronize()
+        got = p[heads].cpu().view(torch.int16).numpy().view(np.uint16)
+        _check_bf16(got, ref, S, 1)
+        nz = torch.count_nonzero(p.view(torch.int16).view(bh, -1), dim=1)
+        assert torch.all(nz == S * (S + 1) // 2)
+    ws = torch.empty(fc.fuse_causal_softmax_workspace_bytes(bh, S, fc.FUSE_UNFUSED),
+                     dtype=torch.uint8, device="cuda")
+    p = torch.empty_like(s)
+    fc.fuse_causal_softmax(s, p, wl.SM_SCALE, 0, fc.FUSE_UNFUSED, workspace=ws)
+    torch.cuda.synchronize()
+    got = p[heads].cpu().view(torch.int16).numpy().view(np.uint16)
+    _check_bf16(got, ref, S, 4)

@@ -1,0 +1,38 @@
+"""Watchdog and kernel report on the GPU.
+
+The watchdog test makes a bounded wait run out on purpose: one thread waits on an mbarrier that
+nothing arrives on, gives up after a short budget, records the timeout and returns.  Nothing
+faults or traps; the context stays usable, which the follow-up chain call checks."""
+import numpy as np
+import pytest
+
+import epilogue_chains_gb300 as fc
+import oracle
+from epilogue_chains_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(cuda_device):
+    import torch
+    assert fc.fuse_check() == fc.FUSE_OK
+    fc.fuse_debug_expire_wait(2_000_000)          # ~1 ms of SM clocks
+    assert fc.fuse_check() == fc.FUSE_ETIMEOUT
+    assert fc.fuse_check() == fc.FUSE_OK          # the flag is cleared once reported
+    relu, a, b = wl.chain_stages(4)
+    x = wl.chain_input(4096, salt=1)
+    y = torch.empty(4096, device="cuda")
+    fc.fuse_chain_run([(int(r), float(p), float(q)) for r, p, q in zip(relu, a, b)],
+                      torch.from_numpy(x).cuda(), y)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), oracle.chain(relu, a, b, x))
+
+
+def test_kernel_report_covers_every_variant(cuda_device):
+    n = fc.fuse_kernel_count()
+    assert n >= 10
+    for i in range(n):
+        r = fc.fuse_kernel_report(i)
+        assert r["regs_per_thread"] > 0 and r["blocks_per_sm"] >= 1, r
+    with pytest.raises(fc.FuseError):
+        fc.fuse_kernel_report(n)
