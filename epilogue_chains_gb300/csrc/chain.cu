@@ -8,24 +8,24 @@
 // [OFCG] §3.2 gives their byte ledgers: 2*K*N*b unfused, 2*N*b fused.
 //
 // GB300 design: the work is pure HBM streaming (8 B/element for fp32, 2 flops per stage), so the
-// kernels are sized for bytes in flight, not ALU: 16-byte streaming loads/stores (ld/st .cs),
-// U independent vectors per thread issued before any arithmetic, and a grid of exactly one
-// resident wave (SM count x occupancy) that strides over the tensor.  Stage coefficients are a
-// __grid_constant__ parameter, read from the constant bank with no local copy.
+// kernels are shaped for DRAM efficiency, not ALU: one 32-byte vector per thread (256-bit
+// ld/st.global.cs, sm_100+), an exact grid of many short CTAs (measured on GB300 to match
+// cudaMemcpy at this size, where persistent grid-stride loops and TMA bulk-copy pipelines were
+// slower), and stage coefficients in a __grid_constant__ parameter read from the constant bank.
 #include "fc_internal.cuh"
 
 namespace fc {
 namespace {
 
 constexpr int kBlock = 256;
-constexpr int kUnroll = 4;
 
 struct ChainParams {
     const void* x;
     void* y;
     int64_t n;      // elements
-    int64_t head;   // scalar elements before the 16-byte-aligned body
-    int64_t nvec;   // 16-byte vectors in the body
+    int64_t head;   // scalar elements before the 32-byte-aligned body
+    int64_t nvec;   // 32-byte vectors in the body (fused/unfused); the fat probe reads the same
+                    // body in groups of 4 elements
     int K;
     uint32_t relu_mask;
     float a[FUSE_MAX_STAGES];
@@ -52,59 +52,61 @@ __device__ __forceinline__ void run_chain(float (&f)[E], const ChainParams& p) {
     }
 }
 
-template <typename T, int U, bool kOneStage>
+// 32-byte vectors: 8 fp32 or 16 fp16/bf16 values
+template <typename T> struct Vec32 {
+    static constexpr int N = 32 / sizeof(T);
+    __device__ __forceinline__ static void load(const T* p, float* f) {
+        uint32_t w[8];
+        asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                       "=r"(w[6]), "=r"(w[7])
+                     : "l"(p));
+        Vec16<T>::unpack(make_uint4(w[0], w[1], w[2], w[3]), f);
+        Vec16<T>::unpack(make_uint4(w[4], w[5], w[6], w[7]), f + N / 2);
+    }
+    __device__ __forceinline__ static void store(T* p, const float* f) {
+        const uint4 lo = Vec16<T>::pack(f), hi = Vec16<T>::pack(f + N / 2);
+        asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(lo.x),
+                     "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                     : "memory");
+    }
+};
+
+// Thread g handles: head element g (if g < head), vector g (if g < nvec), tail element g.
+template <typename T, bool kOneStage>
 __device__ __forceinline__ void chain_body(const ChainParams& p) {
-    using V = Vec16<T>;
+    using V = Vec32<T>;
     constexpr int E = V::N;
     const T* x = static_cast<const T*>(p.x);
     T* y = static_cast<T*>(p.y);
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-
-    // unaligned head and tail (fewer than 16 bytes each when x and y share their alignment;
-    // the whole tensor when they do not)
-    const int64_t tail0 = p.head + p.nvec * E;
-    for (int64_t i = tid; i < p.head; i += nthr) {
-        float f[1] = {to_f32(x[i])};
-        run_chain<1, kOneStage>(f, p);
-        y[i] = from_f32<T>(f[0]);
-    }
-    for (int64_t i = tail0 + tid; i < p.n; i += nthr) {
-        float f[1] = {to_f32(x[i])};
-        run_chain<1, kOneStage>(f, p);
-        y[i] = from_f32<T>(f[0]);
-    }
-
-    const uint4* xv = reinterpret_cast<const uint4*>(x + p.head);
-    uint4* yv = reinterpret_cast<uint4*>(y + p.head);
-    int64_t i = tid;
-    for (; i + (U - 1) * nthr < p.nvec; i += U * nthr) {
-        uint4 r[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) r[u] = ld_stream(xv + i + u * nthr);
-        float f[U * E];
-#pragma unroll
-        for (int u = 0; u < U; ++u) V::unpack(r[u], f + u * E);
-        run_chain<U * E, kOneStage>(f, p);
-#pragma unroll
-        for (int u = 0; u < U; ++u) st_stream(yv + i + u * nthr, V::pack(f + u * E));
-    }
-    for (; i < p.nvec; i += nthr) {
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (g < p.nvec) {
         float f[E];
-        V::unpack(ld_stream(xv + i), f);
+        V::load(x + p.head + g * E, f);
         run_chain<E, kOneStage>(f, p);
-        st_stream(yv + i, V::pack(f));
+        V::store(y + p.head + g * E, f);
+    }
+    if (g < p.head) {
+        float f[1] = {to_f32(x[g])};
+        run_chain<1, kOneStage>(f, p);
+        y[g] = from_f32<T>(f[0]);
+    }
+    const int64_t t = p.head + p.nvec * E + g;
+    if (t < p.n) {
+        float f[1] = {to_f32(x[t])};
+        run_chain<1, kOneStage>(f, p);
+        y[t] = from_f32<T>(f[0]);
     }
 }
 
-template <typename T, int U>
+template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_fused_kernel(const __grid_constant__ ChainParams p) {
-    chain_body<T, U, false>(p);
+    chain_body<T, false>(p);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_stage_kernel(const __grid_constant__ ChainParams p) {
-    chain_body<T, kUnroll, true>(p);
+    chain_body<T, true>(p);
 }
 
 // ---------------------------------------------------------------------------------- fat probe
@@ -145,9 +147,9 @@ __global__ void __launch_bounds__(kBlock, 1) chain_fat_kernel(const __grid_const
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     float sink = 0.0f;
 
-    // groups of 4 consecutive elements (the body is 16-byte aligned, so 4 elements are aligned
+    // groups of 4 consecutive elements (the body is 32-byte aligned, so 4 elements are aligned
     // to 4*sizeof(T)); head and tail one element at a time
-    const int64_t body = p.nvec * Vec16<T>::N;
+    const int64_t body = p.nvec * Vec32<T>::N;
     const int64_t groups = body / 4;
     const int64_t tail0 = p.head + groups * 4;
     for (int64_t i = tid; i < p.head; i += nthr) {
@@ -187,49 +189,60 @@ __global__ void __launch_bounds__(kBlock, 1) chain_fat_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------------- host side
+// Split [0, n) into a scalar head up to the first 32-byte boundary, 32-byte vectors, and a scalar
+// tail, when x and y sit at the same offset modulo 32 bytes; otherwise all elements are scalar.
+template <typename T>
+void partition(ChainParams& p, const void* x, const void* y) {
+    const uintptr_t xo = reinterpret_cast<uintptr_t>(x) % 32, yo = reinterpret_cast<uintptr_t>(y) % 32;
+    if (xo == yo) {
+        int64_t head = xo ? static_cast<int64_t>((32 - xo) / sizeof(T)) : 0;
+        if (head > p.n) head = p.n;
+        p.head = head;
+        p.nvec = (p.n - head) / Vec32<T>::N;
+    } else {
+        p.head = p.n;
+        p.nvec = 0;
+    }
+}
+
+template <typename T>
+unsigned exact_grid(const ChainParams& p) {
+    int64_t units = p.nvec;
+    const int64_t tail = p.n - p.head - p.nvec * Vec32<T>::N;
+    if (p.head > units) units = p.head;
+    if (tail > units) units = tail;
+    const int64_t g = ceil_div(units, kBlock);
+    return static_cast<unsigned>(g < 1 ? 1 : g);
+}
+
 template <typename T>
 int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
-    const int sms = sm_count();
     ChainParams p = base;
-    const int64_t work = p.nvec > 0 ? p.nvec : p.n;  // units a thread strides over
-    auto grid_for = [&](int occ, int per_thread) {
-        int64_t want = ceil_div(ceil_div(work, per_thread), kBlock);
-        int64_t cap = static_cast<int64_t>(sms) * occ;
-        return static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
-    };
+    partition<T>(p, p.x, p.y);
     if (mode == FUSE_FUSED) {
-        static int occ = blocks_per_sm(chain_fused_kernel<T, kUnroll>, kBlock);
-        chain_fused_kernel<T, kUnroll><<<grid_for(occ, kUnroll), kBlock, 0, stream>>>(p);
+        chain_fused_kernel<T><<<exact_grid<T>(p), kBlock, 0, stream>>>(p);
         return check_launch();
     }
     if (mode == FUSE_FAT) {
-        static int occ = blocks_per_sm(chain_fat_kernel<T>, kBlock);
-        chain_fat_kernel<T><<<grid_for(occ, 1), kBlock, 0, stream>>>(p);
+        static const int occ = blocks_per_sm(chain_fat_kernel<T>, kBlock);
+        const int64_t want = ceil_div(ceil_div(p.n, 4), kBlock);
+        const int64_t cap = static_cast<int64_t>(sm_count()) * occ;
+        const unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
+        chain_fat_kernel<T><<<grid, kBlock, 0, stream>>>(p);
         return check_launch();
     }
     // FUSE_UNFUSED: stage s is its own launch; stage 0 reads x, every later stage reads and
-    // rewrites y in place, so each intermediate makes a full round trip through HBM.
-    static int occ = blocks_per_sm(chain_stage_kernel<T>, kBlock);
+    // rewrites y in place, so each intermediate makes a full round trip through global memory.
     for (int s = 0; s < base.K; ++s) {
         ChainParams q = base;
         q.K = 1;
         q.a[0] = base.a[s];
         q.b[0] = base.b[s];
         q.relu_mask = (base.relu_mask >> s) & 1u;
-        if (s > 0) {
-            q.x = base.y;  // y is 16-byte partitioned the same way for both operands now
-            const uintptr_t off = reinterpret_cast<uintptr_t>(base.y) % 16;
-            int64_t head = off ? static_cast<int64_t>((16 - off) / sizeof(T)) : 0;
-            if (head > base.n) head = base.n;
-            q.head = head;
-            q.nvec = (base.n - head) / Vec16<T>::N;
-        }
-        const int64_t w = q.nvec > 0 ? q.nvec : q.n;
-        int64_t want = ceil_div(ceil_div(w, kUnroll), kBlock);
-        int64_t cap = static_cast<int64_t>(sms) * occ;
-        unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
-        chain_stage_kernel<T><<<grid, kBlock, 0, stream>>>(q);
-        int rc = check_launch();
+        if (s > 0) q.x = base.y;
+        partition<T>(q, q.x, q.y);
+        chain_stage_kernel<T><<<exact_grid<T>(q), kBlock, 0, stream>>>(q);
+        const int rc = check_launch();
         if (rc != FUSE_OK) return rc;
     }
     return FUSE_OK;
@@ -241,13 +254,13 @@ int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
 int chain_report_count() { return 5; }
 int chain_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)chain_fused_kernel<float, kUnroll>,
+        case 0: return describe_kernel((const void*)chain_fused_kernel<float>,
                                        "chain_fused_kernel<f32>", kBlock, 0, out);
         case 1: return describe_kernel((const void*)chain_stage_kernel<float>,
                                        "chain_stage_kernel<f32> (unfused stage)", kBlock, 0, out);
         case 2: return describe_kernel((const void*)chain_fat_kernel<float>,
                                        "chain_fat_kernel<f32> (48 live temps)", kBlock, 0, out);
-        case 3: return describe_kernel((const void*)chain_fused_kernel<__nv_bfloat16, kUnroll>,
+        case 3: return describe_kernel((const void*)chain_fused_kernel<__nv_bfloat16>,
                                        "chain_fused_kernel<bf16>", kBlock, 0, out);
         case 4: return describe_kernel((const void*)chain_fat_kernel<__nv_bfloat16>,
                                        "chain_fat_kernel<bf16> (48 live temps)", kBlock, 0, out);
@@ -282,17 +295,6 @@ extern "C" int fuse_chain_run(const fuse_stage* stages, int K, const void* x, vo
         p.a[s] = stages[s].a;
         p.b[s] = stages[s].b;
         if (stages[s].op == FUSE_OP_AFFINE_RELU) p.relu_mask |= 1u << s;
-    }
-    const uintptr_t xo = xa % 16, yo = ya % 16;
-    const int64_t vecN = dtype == FUSE_F32 ? 4 : 8;
-    if (xo == yo) {
-        int64_t head = xo ? static_cast<int64_t>((16 - xo) / eb) : 0;
-        if (head > n) head = n;
-        p.head = head;
-        p.nvec = (n - head) / vecN;
-    } else {
-        p.head = n;  // operands misaligned against each other: element-wise path only
-        p.nvec = 0;
     }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     switch (dtype) {

@@ -23,6 +23,10 @@ inline int check_launch() {
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// Device address of the watchdog word on the current device (nullptr on failure).  Kernels with
+// bounded waits take it as a parameter and set it when a wait runs out.
+int* watchdog_flag();
+
 // Occupancy-derived blocks per SM for a kernel at a block size (cached by caller as needed).
 template <typename K>
 int blocks_per_sm(K kernel, int block, size_t dyn_smem = 0) {

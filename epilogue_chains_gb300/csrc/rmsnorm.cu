@@ -4,16 +4,17 @@
 // a kernel that reads and writes HBM; fused it is one pass.  Per row i:
 //     r_i = 1/sqrt(mean_j x_ij^2 + eps),   y_ij = (x_ij * r_i) * w_j.
 //
-// GB300 design (fused): one CTA per row with the whole row held in registers (16 B vector loads,
-// VPT vectors per thread, all issued before the reduction), a warp-shuffle reduction followed by
-// a shared-memory reduction across the CTA's warps, then the scaled row is written with 16 B
-// streaming stores.  x is read from HBM exactly once; w (16 KB at hidden 4096) stays in L2.
+// GB300 design (fused): persistent CTAs (one wave: SM count x occupancy), each holding a whole row
+// in registers (16 B vector loads, VPT vectors per thread) while the next row's loads are already
+// in flight; a warp-shuffle reduction followed by a shared-memory reduction across the CTA's
+// warps, then the scaled row is written with 16 B streaming stores.  x is read from HBM exactly
+// once; w (16 KB at hidden 4096) stays in L1/L2.
 #include "fc_internal.cuh"
 
 namespace fc {
 namespace {
 
-constexpr int kRowThreads = 128;     // vector path: 128 threads x VPT float4 per row
+constexpr int kRowThreads = 256;     // vector path: 256 threads x VPT float4 per row
 constexpr int kRowThreadsScalar = 512;
 constexpr int kEwBlock = 256;
 
@@ -31,39 +32,62 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-template <int VPT>
+// Persistent: CTA b handles rows b, b + gridDim.x, ...; while it reduces and writes one row, the
+// next row's loads are already in flight (PREFETCH).  The per-warp partial sums are double
+// buffered, so one barrier per row suffices: a warp that runs ahead writes the other buffer.
+template <int VPT, bool PREFETCH>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
-    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int hidden,
-    float eps) {
-    __shared__ float red[kRowThreads / 32];
-    const int64_t row = blockIdx.x;
+    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int64_t rows,
+    int hidden, float eps) {
+    __shared__ float red[2][kRowThreads / 32];
     const int nv = hidden / 4;
-    const float4* xr = reinterpret_cast<const float4*>(x + row * hidden);
-    float4* yr = reinterpret_cast<float4*>(y + row * hidden);
     const float4* wv = reinterpret_cast<const float4*>(w);
-    float4 v[VPT];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    float4 nxt[VPT];
+    auto load_row = [&](int64_t r) {
+        const float4* xr = reinterpret_cast<const float4*>(x + r * hidden);
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int idx = threadIdx.x + k * kRowThreads;
-        v[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-    float ss = 0.0f;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
-    const float total = block_sum<kRowThreads>(ss, red);
-    const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int idx = threadIdx.x + k * kRowThreads;
-        if (idx < nv) {
-            const float4 g = __ldg(wv + idx);
-            float4 o;
-            o.x = __fmul_rn(__fmul_rn(v[k].x, r), g.x);
-            o.y = __fmul_rn(__fmul_rn(v[k].y, r), g.y);
-            o.z = __fmul_rn(__fmul_rn(v[k].z, r), g.z);
-            o.w = __fmul_rn(__fmul_rn(v[k].w, r), g.w);
-            __stcs(yr + idx, o);
+        for (int k = 0; k < VPT; ++k) {
+            const int idx = threadIdx.x + k * kRowThreads;
+            nxt[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+    };
+    int64_t row = blockIdx.x;
+    if (row < rows) load_row(row);
+    int buf = 0;
+    for (; row < rows; row += gridDim.x) {
+        float4 v[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) v[k] = nxt[k];
+        if (PREFETCH && row + gridDim.x < rows) load_row(row + gridDim.x);
+        float ss = 0.0f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+            ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) red[buf][warp] = ss;
+        __syncthreads();
+        float total = 0.0f;
+#pragma unroll
+        for (int k = 0; k < kRowThreads / 32; ++k) total += red[buf][k];
+        buf ^= 1;
+        const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
+        float4* yr = reinterpret_cast<float4*>(y + row * hidden);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int idx = threadIdx.x + k * kRowThreads;
+            if (idx < nv) {
+                const float4 g = __ldg(wv + idx);
+                float4 o;
+                o.x = __fmul_rn(__fmul_rn(v[k].x, r), g.x);
+                o.y = __fmul_rn(__fmul_rn(v[k].y, r), g.y);
+                o.z = __fmul_rn(__fmul_rn(v[k].z, r), g.z);
+                o.w = __fmul_rn(__fmul_rn(v[k].w, r), g.w);
+                __stcs(yr + idx, o);
+            }
+        }
+        if (!PREFETCH && row + gridDim.x < rows) load_row(row + gridDim.x);
     }
 }
 
@@ -169,7 +193,12 @@ __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict_
 template <int VPT>
 int launch_fused_vec(const float* x, const float* w, float* y, int64_t rows, int hidden, float eps,
                      cudaStream_t st) {
-    rmsnorm_fused_kernel<VPT><<<static_cast<unsigned>(rows), kRowThreads, 0, st>>>(x, w, y, hidden, eps);
+    constexpr bool kPrefetch = VPT <= 8;  // two rows in registers up to hidden 8192
+    static const int occ = blocks_per_sm(rmsnorm_fused_kernel<VPT, kPrefetch>, kRowThreads);
+    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
+    if (grid > rows) grid = rows;
+    rmsnorm_fused_kernel<VPT, kPrefetch><<<static_cast<unsigned>(grid), kRowThreads, 0, st>>>(
+        x, w, y, rows, hidden, eps);
     return check_launch();
 }
 
@@ -193,8 +222,8 @@ unsigned ew_grid(int64_t units) {
 int rmsnorm_report_count() { return 3; }
 int rmsnorm_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<8>,
-                                       "rmsnorm_fused_kernel<VPT=8> (hidden 4096)", kRowThreads, 0, out);
+        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true>,
+                                       "rmsnorm_fused_kernel<VPT=4> (hidden 4096)", kRowThreads, 0, out);
         case 1: return describe_kernel((const void*)rms_rowmean_kernel,
                                        "rms_rowmean_kernel (unfused step 2)", kRowThreadsScalar, 0, out);
         case 2: return describe_kernel((const void*)rms_scale_kernel,
@@ -233,8 +262,7 @@ extern "C" int fuse_rmsnorm(const float* x, const float* w, float* y, int64_t ro
             if (nv <= 2 * kRowThreads) return launch_fused_vec<2>(x, w, y, rows, H, eps, st);
             if (nv <= 4 * kRowThreads) return launch_fused_vec<4>(x, w, y, rows, H, eps, st);
             if (nv <= 8 * kRowThreads) return launch_fused_vec<8>(x, w, y, rows, H, eps, st);
-            if (nv <= 16 * kRowThreads) return launch_fused_vec<16>(x, w, y, rows, H, eps, st);
-            return launch_fused_vec<32>(x, w, y, rows, H, eps, st);
+            return launch_fused_vec<16>(x, w, y, rows, H, eps, st);
         }
         if (H <= 1 * kRowThreadsScalar) return launch_fused_scalar<1>(x, w, y, rows, H, eps, st);
         if (H <= 2 * kRowThreadsScalar) return launch_fused_scalar<2>(x, w, y, rows, H, eps, st);

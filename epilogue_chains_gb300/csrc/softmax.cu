@@ -3,15 +3,21 @@
 // [OFCG] fusion_lab [E]: softmax is max -> subtract -> exp -> sum -> divide over a row; unfused,
 // each step reads (and the elementwise ones write) the whole score tensor: 8 copies of it,
 // against 2 fused ([A3]).  §3.5: query i sees keys j <= i; skipping whole key blocks of a T x T
-// tiling leaves the fraction (n_b + 1)/(2 n_b) of the blocks to read.
+// tiling leaves the fraction (n_b + 1)/(2 n_b) of the scores to read.
 //
-// GB300 design (fused): one warp per row, the row's kept columns loaded as 16 B vectors (8 bf16)
-// straight into registers, a warp-shuffle max and sum (no shared memory, no block barrier), the
-// exponentials kept in registers, one 16 B streaming store per 8 outputs.  With skip tile T,
-// row i loads only the columns < (floor(i/T)+1)*T and writes zeros past them without reading.
+// GB300 design (fused): persistent warps, one row per warp at a time.  The bulk-copy engine (TMA,
+// cp.async.bulk) streams each row's kept columns into a per-warp two-stage shared-memory ring, so
+// a warp computes row r while its next two rows land, at no register cost; the row is then held
+// in registers as 32-byte vectors (16 bf16).  Each lane's vectors are classified against the diagonal:
+// fully kept vectors run an unmasked path, the one diagonal vector a masked path, and masked
+// vectors do no arithmetic (and, with skip tile T, are not even read).  exp(z - m) is computed as
+// 2^(t - m') with t = s * (scale * log2 e) -- one multiply, one subtract, one ex2 per element.
+// Max and sum are warp-shuffle reductions: a row never leaves its warp, so no shared memory or
+// block barrier is needed.
 #include <math.h>
 
 #include "fc_internal.cuh"
+#include "fc_ptx.cuh"
 
 namespace fc {
 namespace {
@@ -19,6 +25,7 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 constexpr int kSmBlock = 32 * kWarpsPerBlock;
 constexpr int kEwBlock = 256;
+constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -30,95 +37,219 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+// 2^x, the MUFU instruction (relative error ~2^-22; ftz: subnormal results flush to +0)
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-template <typename OutT> struct OutVec;
-template <> struct OutVec<__nv_bfloat16> {  // 8 outputs = one 16 B store
+__device__ __forceinline__ void ld32(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                   "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st32(void* p, const uint32_t (&w)[8]) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+// 16 bf16 (8 words) -> 16 fp32 (exact)
+__device__ __forceinline__ void unpack16(const uint32_t (&w)[8], float* f) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        f[2 * k] = __uint_as_float(w[k] << 16);
+        f[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+
+// 16 outputs of one 32-byte input vector
+template <typename OutT> struct Out16;
+template <> struct Out16<__nv_bfloat16> {  // one 32-byte store
     __device__ __forceinline__ static void store(__nv_bfloat16* row, int v, const float* f) {
-        __stcs(reinterpret_cast<uint4*>(row) + v, Vec16<__nv_bfloat16>::pack(f));
+        uint32_t w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st32(row + 16 * v, w);
     }
     __device__ __forceinline__ static void zero(__nv_bfloat16* row, int v) {
-        __stcs(reinterpret_cast<uint4*>(row) + v, make_uint4(0, 0, 0, 0));
+        const uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        st32(row + 16 * v, w);
     }
 };
-template <> struct OutVec<float> {  // 8 outputs = two 16 B stores
+template <> struct Out16<float> {  // two 32-byte stores
     __device__ __forceinline__ static void store(float* row, int v, const float* f) {
-        __stcs(reinterpret_cast<float4*>(row) + 2 * v, make_float4(f[0], f[1], f[2], f[3]));
-        __stcs(reinterpret_cast<float4*>(row) + 2 * v + 1, make_float4(f[4], f[5], f[6], f[7]));
+        uint32_t w[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = __float_as_uint(f[8 * h + k]);
+            st32(row + 16 * v + 8 * h, w);
+        }
     }
     __device__ __forceinline__ static void zero(float* row, int v) {
-        __stcs(reinterpret_cast<float4*>(row) + 2 * v, make_float4(0.f, 0.f, 0.f, 0.f));
-        __stcs(reinterpret_cast<float4*>(row) + 2 * v + 1, make_float4(0.f, 0.f, 0.f, 0.f));
+        const uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        st32(row + 16 * v, w);
+        st32(row + 16 * v + 8, w);
     }
 };
 
-// Fused, register-resident: S % 8 == 0 and S <= 256 * VPL.
-template <int VPL, typename OutT>
-__global__ void __launch_bounds__(kSmBlock) softmax_fused_kernel(
-    const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float scale,
-    int skip_tile) {
-    const int lane = threadIdx.x % 32;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
-    if (row >= rows) return;
-    const int i = static_cast<int>(row % S);  // query index inside its (batch, head)
+__device__ __forceinline__ int load_vectors(int i, int S, int skip_tile) {
     const int ncols = skip_tile > 0 ? min(S, (i / skip_tile + 1) * skip_tile) : S;
-    const int nvec_load = ncols / 8;
-    const int nvec = S / 8;
-    const uint4* srow = reinterpret_cast<const uint4*>(s + row * S);
-    OutT* prow = p + row * S;
+    return ncols / 16;  // S and skip_tile are multiples of 16 on this path
+}
 
-    float f[VPL][8];
+// Fused, persistent, TMA-fed: S % 16 == 0, S <= 512 * VPL, 32-byte aligned rows.
+// Warp w owns a ring of kStages row buffers in shared memory; lane 0 asks the bulk-copy engine for
+// the kept columns of each row it will process next (one cp.async.bulk per row, completion counted
+// on the stage's mbarrier), so the warp computes row r while rows r + nw and r + 2 nw are landing.
+constexpr int kStages = 2;
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ void lds32(uint32_t addr, uint32_t (&w)[8]) {
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]) : "r"(addr));
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7]) : "r"(addr + 16));
+}
+
+size_t fused_smem_bytes(int S) {
+    return static_cast<size_t>(kWarpsPerBlock) * kStages * (static_cast<size_t>(S) * 2 + 8);
+}
+
+template <int VPL, typename OutT>
+__global__ void __launch_bounds__(kSmBlock, 2) softmax_fused_kernel(
+    const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float c,
+    int skip_tile, int* flag) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t rowbytes = static_cast<uint32_t>(S) * 2;
+    const uint32_t wbuf = smem_addr(smem) + warp * kStages * rowbytes;
+    const uint32_t bars = smem_addr(smem) + kWarpsPerBlock * kStages * rowbytes + warp * kStages * 8;
+    const int64_t nw = static_cast<int64_t>(gridDim.x) * kWarpsPerBlock;
+    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + warp;
+    const int nvec = S / 16;
+
+    if (lane == 0) {
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        const int v = lane + 32 * u;
-        uint4 r = make_uint4(0, 0, 0, 0);
-        if (v < nvec_load) r = __ldcs(srow + v);
-        Vec16<__nv_bfloat16>::unpack(r, f[u]);
+        for (int st = 0; st < kStages; ++st) mbar_init(bars + 8 * st, 1);
+        fence_mbar_init();
     }
-    float mx = -INFINITY;
+    __syncwarp();
+    auto issue = [&](int64_t r, int st) {  // lane 0
+        const uint32_t bytes = 32u * load_vectors(static_cast<int>(r % S), S, skip_tile);
+        mbar_arrive_expect_tx(bars + 8 * st, bytes);
+        bulk_g2s(wbuf + st * rowbytes, s + r * S, bytes, bars + 8 * st);
+    };
+    uint32_t pending = 0, phase = 0;  // per stage: a copy is in flight / parity of its next phase
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int col = 8 * (lane + 32 * u) + e;
-            const float z = f[u][e] * scale;
-            f[u][e] = z;
-            if (col <= i) mx = fmaxf(mx, z);
+    for (int st = 0; st < kStages; ++st) {
+        const int64_t r = r0 + st * nw;
+        if (r < rows) {
+            if (lane == 0) issue(r, st);
+            pending |= 1u << st;
         }
     }
-    mx = warp_max(mx);
-    float sum = 0.0f;
-#pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int col = 8 * (lane + 32 * u) + e;
-            const float ev = col <= i ? __expf(f[u][e] - mx) : 0.0f;
-            f[u][e] = ev;
-            sum += ev;
+
+    int st = 0;
+    for (int64_t row = r0; row < rows; row += nw, st = (st + 1) % kStages) {
+        if (!mbar_wait_bounded(bars + 8 * st, (phase >> st) & 1u, flag)) {
+            // give up: let the copies still in flight land (bounded) before the CTA exits
+            for (int k = 0; k < kStages; ++k)
+                if ((pending >> k) & 1u) (void)mbar_wait_bounded(bars + 8 * k, (phase >> k) & 1u, flag, kWaitBudget / 8);
+            return;
         }
-    }
-    sum = warp_sum(sum);
-    const float inv = __frcp_rn(sum);
+        phase ^= 1u << st;
+        pending &= ~(1u << st);
+
+        const int i = static_cast<int>(row % S);
+        const int kv = i / 16;  // vectors < kv are fully kept, kv holds the diagonal
+        uint32_t cur[VPL][8];
 #pragma unroll
-    for (int u = 0; u < VPL; ++u) {
-        const int v = lane + 32 * u;
-        if (v < nvec) {
-            if (v < nvec_load) {
+        for (int u = 0; u < VPL; ++u) {
+            const int v = lane + 32 * u;
+            if (v <= kv) lds32(wbuf + st * rowbytes + 32 * v, cur[u]);
+        }
+        __syncwarp();  // every lane has read the stage: it may be refilled
+        if (row + kStages * nw < rows) {
+            if (lane == 0) issue(row + kStages * nw, st);
+            pending |= 1u << st;
+        }
+
+        float m = -INFINITY;
 #pragma unroll
-                for (int e = 0; e < 8; ++e) f[u][e] = __fmul_rn(f[u][e], inv);
-                OutVec<OutT>::store(prow, v, f[u]);
-            } else {
-                OutVec<OutT>::zero(prow, v);
+        for (int u = 0; u < VPL; ++u) {
+            const int v = lane + 32 * u;
+            if (v <= kv) {
+                float f[16];
+                unpack16(cur[u], f);
+                if (v < kv) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) m = fmaxf(m, f[e] * c);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e)
+                        if (16 * v + e <= i) m = fmaxf(m, f[e] * c);
+                }
+            }
+        }
+        m = warp_max(m);
+
+        float ev[VPL][16];
+        float sum = 0.0f;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            const int v = lane + 32 * u;
+            if (v <= kv) {
+                unpack16(cur[u], ev[u]);
+                if (v < kv) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        ev[u][e] = ex2(ev[u][e] * c - m);
+                        sum += ev[u][e];
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) {
+                        ev[u][e] = (16 * v + e <= i) ? ex2(ev[u][e] * c - m) : 0.0f;
+                        sum += ev[u][e];
+                    }
+                }
+            }
+        }
+        sum = warp_sum(sum);
+        const float inv = __frcp_rn(sum);
+
+        OutT* prow = p + row * S;
+#pragma unroll
+        for (int u = 0; u < VPL; ++u) {
+            const int v = lane + 32 * u;
+            if (v < nvec) {
+                if (v <= kv) {
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) ev[u][e] = __fmul_rn(ev[u][e], inv);
+                    Out16<OutT>::store(prow, v, ev[u]);
+                } else {
+                    Out16<OutT>::zero(prow, v);
+                }
             }
         }
     }
 }
 
-// Fused, any S (<= 8192) and any alignment: pass 1 folds the row into a running (max, sum) per
-// lane and merges the lanes; pass 2 re-reads the kept scores and writes every output.
+// Fused, any S (<= 8192) and any alignment: pass 1 folds the kept scores into a running
+// (max, sum) per lane and merges the lanes; pass 2 re-reads them and writes every output.
 template <typename OutT>
 __global__ void __launch_bounds__(kSmBlock) softmax_fused_generic_kernel(
-    const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float scale,
+    const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float c,
     int skip_tile) {
     const int lane = threadIdx.x % 32;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
@@ -129,17 +260,17 @@ __global__ void __launch_bounds__(kSmBlock) softmax_fused_generic_kernel(
     OutT* prow = p + row * S;
     float m = -INFINITY, l = 0.0f;
     for (int j = lane; j < ncols && j <= i; j += 32) {
-        const float z = __bfloat162float(srow[j]) * scale;
-        const float mn = fmaxf(m, z);
-        l = l * __expf(m - mn) + __expf(z - mn);
+        const float t = __bfloat162float(srow[j]) * c;
+        const float mn = fmaxf(m, t);
+        l = l * ex2(m - mn) + ex2(t - mn);
         m = mn;
     }
     const float M = warp_max(m);
-    l = (m == -INFINITY) ? 0.0f : l * __expf(m - M);
+    l = (m == -INFINITY) ? 0.0f : l * ex2(m - M);
     const float inv = __frcp_rn(warp_sum(l));
     for (int j = lane; j < S; j += 32) {
         float v = 0.0f;
-        if (j <= i) v = __fmul_rn(__expf(__bfloat162float(srow[j]) * scale - M), inv);
+        if (j <= i) v = __fmul_rn(ex2(__bfloat162float(srow[j]) * c - M), inv);
         prow[j] = from_f32<OutT>(v);
     }
 }
@@ -148,7 +279,9 @@ __global__ void __launch_bounds__(kSmBlock) softmax_fused_generic_kernel(
 // (1) m = rowmax(scale*s)  (2) d = bf16(scale*s - m), -inf where j > i  (3) e = bf16(exp d)
 // (4) l = rowsum(e)        (5) p = bf16(e / l)
 // Step 2 folds scale and mask into the subtraction, so no mask tensor exists ([OFCG] [A3] notes
-// that a materialised mask would add another full copy of the score tensor).
+// that a materialised mask would add another full copy of the score tensor).  Every step streams
+// whole rows with 32-byte vectors when S % 16 == 0 and the tensors are 32-byte aligned.
+template <bool VEC>
 __global__ void __launch_bounds__(kSmBlock) sm_rowmax_kernel(const __nv_bfloat16* __restrict__ s,
                                                              float* __restrict__ m, int64_t rows,
                                                              int S, float scale) {
@@ -158,35 +291,82 @@ __global__ void __launch_bounds__(kSmBlock) sm_rowmax_kernel(const __nv_bfloat16
     const int i = static_cast<int>(row % S);
     const __nv_bfloat16* r = s + row * S;
     float mx = -INFINITY;
-    for (int j = lane; j < S; j += 32) {
-        const float z = __bfloat162float(__ldcs(r + j)) * scale;  // whole row read, as unfused
-        if (j <= i) mx = fmaxf(mx, z);
+    if (VEC) {
+        for (int v = lane; v < S / 16; v += 32) {
+            uint32_t w[8];
+            ld32(r + 16 * v, w);
+            float f[16];
+            unpack16(w, f);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                if (16 * v + e <= i) mx = fmaxf(mx, f[e] * scale);
+        }
+    } else {
+        for (int j = lane; j < S; j += 32) {
+            const float z = __bfloat162float(r[j]) * scale;
+            if (j <= i) mx = fmaxf(mx, z);
+        }
     }
     mx = warp_max(mx);
     if (lane == 0) m[row] = mx;
 }
 
+template <bool VEC>
 __global__ void __launch_bounds__(kEwBlock) sm_sub_kernel(const __nv_bfloat16* __restrict__ s,
                                                           const float* __restrict__ m,
                                                           __nv_bfloat16* __restrict__ d,
                                                           int64_t n, int S, float scale) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t k = tid; k < n; k += nthr) {
-        const int64_t row = k / S;
-        const int j = static_cast<int>(k - row * S);
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (VEC) {
+        const int64_t vpr = S / 16;
+        if (g >= n / 16) return;
+        const int64_t row = g / vpr;
+        const int j0 = static_cast<int>(g - row * vpr) * 16;
         const int i = static_cast<int>(row % S);
-        const float z = __bfloat162float(__ldcs(s + k)) * scale;
-        d[k] = j <= i ? __float2bfloat16_rn(z - __ldg(m + row)) : __float2bfloat16_rn(-INFINITY);
+        const float mr = __ldg(m + row);
+        uint32_t w[8];
+        ld32(s + 16 * g, w);
+        float f[16];
+        unpack16(w, f);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) f[e] = (j0 + e <= i) ? f[e] * scale - mr : -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * k], f[2 * k + 1]);
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st32(d + 16 * g, w);
+        return;
     }
+    if (g >= n) return;
+    const int64_t row = g / S;
+    const int j = static_cast<int>(g - row * S);
+    const int i = static_cast<int>(row % S);
+    const float z = __bfloat162float(s[g]) * scale;
+    d[g] = __float2bfloat16_rn(j <= i ? z - __ldg(m + row) : -INFINITY);
 }
 
+template <bool VEC>
 __global__ void __launch_bounds__(kEwBlock) sm_exp_kernel(__nv_bfloat16* __restrict__ d, int64_t n) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t k = tid; k < n; k += nthr) d[k] = __float2bfloat16_rn(expf(__bfloat162float(d[k])));
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (VEC) {
+        if (g >= n / 16) return;
+        uint32_t w[8];
+        ld32(d + 16 * g, w);
+        float f[16];
+        unpack16(w, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(expf(f[2 * k]), expf(f[2 * k + 1]));
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st32(d + 16 * g, w);
+        return;
+    }
+    if (g < n) d[g] = __float2bfloat16_rn(expf(__bfloat162float(d[g])));
 }
 
+template <bool VEC>
 __global__ void __launch_bounds__(kSmBlock) sm_rowsum_kernel(const __nv_bfloat16* __restrict__ e,
                                                              float* __restrict__ l, int64_t rows,
                                                              int S) {
@@ -195,40 +375,98 @@ __global__ void __launch_bounds__(kSmBlock) sm_rowsum_kernel(const __nv_bfloat16
     if (row >= rows) return;
     const __nv_bfloat16* r = e + row * S;
     float acc = 0.0f;
-    for (int j = lane; j < S; j += 32) acc += __bfloat162float(__ldcs(r + j));
+    if (VEC) {
+        for (int v = lane; v < S / 16; v += 32) {
+            uint32_t w[8];
+            ld32(r + 16 * v, w);
+            float f[16];
+            unpack16(w, f);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc += f[k];
+        }
+    } else {
+        for (int j = lane; j < S; j += 32) acc += __bfloat162float(r[j]);
+    }
     acc = warp_sum(acc);
     if (lane == 0) l[row] = acc;
 }
 
+template <bool VEC>
 __global__ void __launch_bounds__(kEwBlock) sm_div_kernel(__nv_bfloat16* __restrict__ e,
                                                           const float* __restrict__ l, int64_t n,
                                                           int S) {
-    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t k = tid; k < n; k += nthr)
-        e[k] = __float2bfloat16_rn(__fdiv_rn(__bfloat162float(e[k]), __ldg(l + k / S)));
+    const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (VEC) {
+        if (g >= n / 16) return;
+        const float lr = __ldg(l + g / (S / 16));
+        uint32_t w[8];
+        ld32(e + 16 * g, w);
+        float f[16];
+        unpack16(w, f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(__fdiv_rn(f[2 * k], lr), __fdiv_rn(f[2 * k + 1], lr));
+            w[k] = *reinterpret_cast<uint32_t*>(&h);
+        }
+        st32(e + 16 * g, w);
+        return;
+    }
+    if (g < n) e[g] = __float2bfloat16_rn(__fdiv_rn(__bfloat162float(e[g]), __ldg(l + g / S)));
 }
 
-unsigned ew_grid(int64_t units) {
-    const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kEwBlock);
-    int64_t g = ceil_div(units, kEwBlock);
-    if (g > cap) g = cap;
+unsigned grid_for(int64_t units, int block) {
+    const int64_t g = ceil_div(units, block);
     return static_cast<unsigned>(g < 1 ? 1 : g);
 }
 
+template <int VPL, typename OutT>
+int launch_vec(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float c, int tile,
+               cudaStream_t st) {
+    const size_t smem = fused_smem_bytes(S);
+    static const bool attr_ok = cudaFuncSetAttribute(softmax_fused_kernel<VPL, OutT>,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                     static_cast<int>(fused_smem_bytes(512 * VPL))) == cudaSuccess;
+    if (!attr_ok) return check_launch();
+    int* flag = watchdog_flag();
+    if (!flag) return FUSE_ECUDA;
+    const int occ = blocks_per_sm(softmax_fused_kernel<VPL, OutT>, kSmBlock, smem);
+    int64_t grid = ceil_div(rows, kWarpsPerBlock);
+    const int64_t cap = static_cast<int64_t>(sm_count()) * occ;
+    if (grid > cap) grid = cap;
+    softmax_fused_kernel<VPL, OutT><<<static_cast<unsigned>(grid), kSmBlock, smem, st>>>(
+        s, p, rows, S, c, tile, flag);
+    return check_launch();
+}
+
 template <typename OutT>
-int launch_fused(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float scale, int tile,
-                 bool vec, cudaStream_t st) {
-    const unsigned grid = static_cast<unsigned>(ceil_div(rows, kWarpsPerBlock));
+int launch_fused(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float c, int tile, bool vec,
+                 cudaStream_t st) {
     if (vec) {
-        const int vpl = static_cast<int>(ceil_div(S / 8, 32));
-        if (vpl <= 1) softmax_fused_kernel<1, OutT><<<grid, kSmBlock, 0, st>>>(s, p, rows, S, scale, tile);
-        else if (vpl <= 2) softmax_fused_kernel<2, OutT><<<grid, kSmBlock, 0, st>>>(s, p, rows, S, scale, tile);
-        else if (vpl <= 4) softmax_fused_kernel<4, OutT><<<grid, kSmBlock, 0, st>>>(s, p, rows, S, scale, tile);
-        else softmax_fused_kernel<8, OutT><<<grid, kSmBlock, 0, st>>>(s, p, rows, S, scale, tile);
-    } else {
-        softmax_fused_generic_kernel<OutT><<<grid, kSmBlock, 0, st>>>(s, p, rows, S, scale, tile);
+        const int vpl = static_cast<int>(ceil_div(S / 16, 32));
+        if (vpl <= 1) return launch_vec<1, OutT>(s, p, rows, S, c, tile, st);
+        if (vpl <= 2) return launch_vec<2, OutT>(s, p, rows, S, c, tile, st);
+        return launch_vec<4, OutT>(s, p, rows, S, c, tile, st);
     }
+    softmax_fused_generic_kernel<OutT><<<grid_for(rows, kWarpsPerBlock), kSmBlock, 0, st>>>(s, p, rows, S, c, tile);
+    return check_launch();
+}
+
+template <bool VEC>
+int launch_unfused(const __nv_bfloat16* s, __nv_bfloat16* d, float* m, float* l, int64_t rows,
+                   int S, float scale, cudaStream_t st) {
+    const int64_t n = rows * S;
+    const int64_t units = VEC ? n / 16 : n;
+    const unsigned rgrid = grid_for(rows, kWarpsPerBlock);
+    int rc;
+    sm_rowmax_kernel<VEC><<<rgrid, kSmBlock, 0, st>>>(s, m, rows, S, scale);
+    if ((rc = check_launch())) return rc;
+    sm_sub_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(s, m, d, n, S, scale);
+    if ((rc = check_launch())) return rc;
+    sm_exp_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(d, n);
+    if ((rc = check_launch())) return rc;
+    sm_rowsum_kernel<VEC><<<rgrid, kSmBlock, 0, st>>>(d, l, rows, S);
+    if ((rc = check_launch())) return rc;
+    sm_div_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(d, l, n, S);
     return check_launch();
 }
 
@@ -237,13 +475,14 @@ int launch_fused(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float sca
 int softmax_report_count() { return 4; }
 int softmax_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)softmax_fused_kernel<8, __nv_bfloat16>,
-                                       "softmax_fused_kernel<VPL=8,bf16> (S 2048)", kSmBlock, 0, out);
+        case 0: return describe_kernel((const void*)softmax_fused_kernel<4, __nv_bfloat16>,
+                                       "softmax_fused_kernel<VPL=4,bf16> (S 2048)", kSmBlock,
+                                       static_cast<int>(fused_smem_bytes(2048)), out);
         case 1: return describe_kernel((const void*)softmax_fused_generic_kernel<__nv_bfloat16>,
                                        "softmax_fused_generic_kernel<bf16>", kSmBlock, 0, out);
-        case 2: return describe_kernel((const void*)sm_sub_kernel,
+        case 2: return describe_kernel((const void*)sm_sub_kernel<true>,
                                        "sm_sub_kernel (unfused step 2)", kEwBlock, 0, out);
-        case 3: return describe_kernel((const void*)sm_rowmax_kernel,
+        case 3: return describe_kernel((const void*)sm_rowmax_kernel<true>,
                                        "sm_rowmax_kernel (unfused step 1)", kSmBlock, 0, out);
         default: return FUSE_EINVAL;
     }
@@ -261,11 +500,11 @@ extern "C" int fuse_causal_softmax(const void* s, void* p, int64_t batch_heads, 
                                    void* workspace, size_t ws_bytes, fuse_stream_t stream) {
     using namespace fc;
     if (batch_heads < 0 || S < 1 || S > 8192 || !isfinite(scale)) return FUSE_EINVAL;
-    if (skip_tile < 0 || (skip_tile > 0 && skip_tile % 8 != 0)) return FUSE_EINVAL;
+    if (skip_tile < 0 || (skip_tile > 0 && skip_tile % 16 != 0)) return FUSE_EINVAL;
     if (out_dtype != FUSE_BF16 && out_dtype != FUSE_F32) return FUSE_EINVAL;
     if (mode != FUSE_FUSED && mode != FUSE_UNFUSED) return FUSE_EINVAL;
     const int64_t rows = batch_heads * S;
-    if (ceil_div(rows, kWarpsPerBlock) > 2147483647LL) return FUSE_EUNSUPPORTED;
+    if (ceil_div(rows * S, kEwBlock) > 2147483647LL) return FUSE_EUNSUPPORTED;
     if (rows == 0) return FUSE_OK;
     if (!s || !p) return FUSE_EINVAL;
     if (!is_aligned(s, 2) || !is_aligned(p, out_dtype == FUSE_F32 ? 4 : 2)) return FUSE_EALIGN;
@@ -277,12 +516,14 @@ extern "C" int fuse_causal_softmax(const void* s, void* p, int64_t batch_heads, 
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int Si = static_cast<int>(S);
     const __nv_bfloat16* sp = static_cast<const __nv_bfloat16*>(s);
+    const bool vec = (Si % 16 == 0) && is_aligned(s, 32) && is_aligned(p, 32);
 
     if (mode == FUSE_FUSED) {
-        const bool vec = (Si % 8 == 0) && Si <= 2048 && is_aligned(s, 16) && is_aligned(p, 16);
+        const float c = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+        const bool reg = vec && Si <= 2048;
         if (out_dtype == FUSE_BF16)
-            return launch_fused(sp, static_cast<__nv_bfloat16*>(p), rows, Si, scale, skip_tile, vec, st);
-        return launch_fused(sp, static_cast<float*>(p), rows, Si, scale, skip_tile, vec, st);
+            return launch_fused(sp, static_cast<__nv_bfloat16*>(p), rows, Si, c, skip_tile, reg, st);
+        return launch_fused(sp, static_cast<float*>(p), rows, Si, c, skip_tile, reg, st);
     }
 
     // FUSE_UNFUSED: five kernels over whole rows; intermediates are bf16 in p.
@@ -293,18 +534,8 @@ extern "C" int fuse_causal_softmax(const void* s, void* p, int64_t batch_heads, 
     float* m = static_cast<float*>(workspace);
     float* l = m + rows;
     __nv_bfloat16* d = static_cast<__nv_bfloat16*>(p);
-    const unsigned rgrid = static_cast<unsigned>(ceil_div(rows, kWarpsPerBlock));
-    int rc;
-    sm_rowmax_kernel<<<rgrid, kSmBlock, 0, st>>>(sp, m, rows, Si, scale);
-    if ((rc = check_launch())) return rc;
-    sm_sub_kernel<<<ew_grid(n), kEwBlock, 0, st>>>(sp, m, d, n, Si, scale);
-    if ((rc = check_launch())) return rc;
-    sm_exp_kernel<<<ew_grid(n), kEwBlock, 0, st>>>(d, n);
-    if ((rc = check_launch())) return rc;
-    sm_rowsum_kernel<<<rgrid, kSmBlock, 0, st>>>(d, l, rows, Si);
-    if ((rc = check_launch())) return rc;
-    sm_div_kernel<<<ew_grid(n), kEwBlock, 0, st>>>(d, l, n, Si);
-    return check_launch();
+    if (vec) return launch_unfused<true>(sp, d, m, l, rows, Si, scale, st);
+    return launch_unfused<false>(sp, d, m, l, rows, Si, scale, st);
 }
 
 extern "C" int64_t fuse_causal_softmax_bytes(int64_t batch_heads, int64_t S, int skip_tile,

@@ -89,8 +89,10 @@ typedef struct {
  * [OFCG] §3.2 gives the byte ledger: unfused 2*K*N*b, fused 2*N*b.
  *
  * Arithmetic: every stage rounds twice in fp32, t = fl32(fl32(a*v) + b) (no FMA contraction),
- * then ReLU if op == FUSE_OP_AFFINE_RELU.  Values are loaded from `dtype` exactly and the result
- * is rounded once (nearest-even) to `dtype`.  FUSED, UNFUSED and FAT give bit-identical y.
+ * then ReLU if op == FUSE_OP_AFFINE_RELU.  Values are loaded from `dtype` exactly and every value
+ * stored to global memory is rounded (nearest-even) to `dtype`: FUSED and FAT store once, so
+ * they give bit-identical y; UNFUSED stores after every stage, so it equals them for FUSE_F32
+ * and, for 16-bit storage, equals the chain applied one stage at a time.
  *
  *   stages  host array of K stages (1 <= K <= FUSE_MAX_STAGES)
  *   x       device pointer, n elements of `dtype` (input; may equal y, may not partially overlap)
@@ -101,8 +103,8 @@ typedef struct {
  *           FUSE_UNFUSED: K launches; stage 0 reads x and writes y, stage s > 0 reads y and
  *             writes y in place (the intermediate round-trips through global memory each stage).
  *           FUSE_FAT: 1 launch of the register-heavy probe; y identical to FUSED.
- * Alignment: any element-aligned pointers work; the 16-byte vector path is used where x and y
- * share their offset modulo 16 bytes.
+ * Alignment: any element-aligned pointers work; the 32-byte vector path is used where x and y
+ * share their offset modulo 32 bytes.
  */
 int fuse_chain_run(const fuse_stage* stages, int K, const void* x, void* y, int64_t n,
                    int dtype, int mode, fuse_stream_t stream);
@@ -118,7 +120,7 @@ int fuse_chain_run(const fuse_stage* stages, int K, const void* x, void* y, int6
  *   mode    FUSE_FUSED: one kernel, one CTA per row with the row kept in registers
  *           (hidden <= 16384 in this build; larger -> FUSE_EUNSUPPORTED).
  *           FUSE_UNFUSED: four kernels: sq = x^2 -> y;  ms = rowmean(y) -> workspace;
- *             t = x * rsqrt(ms + eps) -> y;  y = y * w  (in place).
+ *             t = x * rsqrt(ms + eps) -> y;  y = y * w  (in place).  Requires y != x.
  *   workspace / ws_bytes: device scratch for the unfused row statistics; at least
  *           fuse_rmsnorm_workspace_bytes(rows, hidden, mode) bytes; may be NULL for FUSED.
  */
@@ -137,10 +139,13 @@ size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode);
  *   p          device [batch_heads, S, S] of out_dtype (FUSE_BF16 or FUSE_F32)
  *   S          1 <= S <= 8192
  *   skip_tile  0: every row reads all S scores (masked ones are ignored);
- *              T > 0 (a multiple of 8): row i reads only the columns < (floor(i/T)+1)*T, i.e.
+ *              T > 0 (a multiple of 16): row i reads only the columns < (floor(i/T)+1)*T, i.e.
  *              the key blocks of a T x T block-causal tiling that are not fully masked.
  *              Output values do not depend on skip_tile.  FUSED mode only.
- *   mode       FUSE_FUSED: one kernel, one warp per row, row kept in registers.
+ *   scale      any finite value
+ *   mode       FUSE_FUSED: one kernel, one warp per row, row kept in registers (32-byte vectors
+ *              when S % 16 == 0, S <= 2048 and s, p are 32-byte aligned; otherwise a two-pass
+ *              element-wise kernel that re-reads the kept scores).
  *              FUSE_UNFUSED: five kernels over whole rows; the three elementwise intermediates
  *              (scaled-and-shifted scores, exponentials) are bf16 and live in p; the row max
  *              and row sum (fp32) live in the workspace.  skip_tile must be 0.

@@ -55,7 +55,7 @@ def test_host_side_validation_needs_no_gpu():
     assert lib.fuse_rmsnorm(0x1000, 0x2000, 0x3000, 4, 64, 1e-6, fc.FUSE_UNFUSED, None, 0,
                             None) == fc.FUSE_EWORKSPACE
     assert lib.fuse_causal_softmax(0x1000, 0x100000, 1, 16, 0.5, 12, fc.FUSE_BF16, 0, None, 0,
-                                   None) == fc.FUSE_EINVAL           # tile not a multiple of 8
+                                   None) == fc.FUSE_EINVAL           # tile not a multiple of 16
     assert lib.fuse_causal_softmax(0x1000, 0x100000, 1, 16, 0.5, 64, fc.FUSE_BF16,
                                    fc.FUSE_UNFUSED, None, 0, None) == fc.FUSE_EUNSUPPORTED
     assert lib.fuse_causal_softmax(0x1000, 0x1000, 1, 16, 0.5, 0, fc.FUSE_BF16, fc.FUSE_FUSED,
