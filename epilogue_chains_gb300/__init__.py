@@ -56,6 +56,7 @@ SIGNATURES = {
     "fuse_chain_run": ([ctypes.POINTER(fuse_stage), _I32, _P, _P, _I64, _I32, _I32, _P], _I32),
     "fuse_rmsnorm": ([_P, _P, _P, _I64, _I64, _F32, _I32, _P, _SZ, _P], _I32),
     "fuse_rmsnorm_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "fuse_rmsnorm_unfused_static": ([_P, _P, _P, _I64, _I64, _F32, _P], _I32),
     "fuse_causal_softmax": ([_P, _P, _I64, _I64, _F32, _I32, _I32, _I32, _P, _SZ, _P], _I32),
     "fuse_causal_softmax_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "fuse_ledger": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_ledger_t)], _I32),
@@ -169,6 +170,18 @@ def fuse_rmsnorm(x, w, y, eps: float, mode: int = FUSE_FUSED, workspace=None, st
     ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(lib.fuse_rmsnorm(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(eps), mode,
                             _ptr(workspace), ws_size, _stream(stream)), "fuse_rmsnorm")
+
+
+def fuse_rmsnorm_unfused_static(x, w, y, eps: float, stream=None) -> None:
+    """Unfused RMSNorm with its row statistics in the library's own fixed device array (no
+    workspace, no allocation; rows <= FUSE_RMSNORM_STATIC_MAX_ROWS)."""
+    _need_device(x, w, y)
+    rows, hidden = x.shape
+    _check(_load().fuse_rmsnorm_unfused_static(_ptr(x), _ptr(w), _ptr(y), rows, hidden, float(eps),
+                                               _stream(stream)), "fuse_rmsnorm_unfused_static")
+
+
+FUSE_RMSNORM_STATIC_MAX_ROWS = 65536
 
 
 def fuse_causal_softmax(s, p, scale: float, skip_tile: int = 0, mode: int = FUSE_FUSED,

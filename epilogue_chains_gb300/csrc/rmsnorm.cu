@@ -9,6 +9,8 @@
 // in flight; a warp-shuffle reduction followed by a shared-memory reduction across the CTA's
 // warps, then the scaled row is written with 16 B streaming stores.  x is read from HBM exactly
 // once; w (16 KB at hidden 4096) stays in L1/L2.
+#include <mutex>
+
 #include "fc_internal.cuh"
 
 namespace fc {
@@ -298,4 +300,60 @@ extern "C" int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode) {
     // unfused: sq (r x, w y) + mean (r y, w ms) + scale (r x, r ms, w y) + weight (r y, r w, w y)
     if (mode == FUSE_UNFUSED) return 7 * n * b + 2 * rows * b + hidden * b;
     return FUSE_EINVAL;
+}
+
+// ------------------------------------------------------------------------- allocation-free entry
+// The four-kernel unfused RMSNorm with its row statistics in a fixed, library-owned device array
+// instead of a caller workspace, for callers that cannot allocate device memory.  The array lives
+// for the life of the process on every device that loads this library.
+namespace {
+constexpr int64_t kStaticMaxRows = 65536;  // 256 KiB of fp32 row statistics
+__device__ __align__(256) float g_rms_static_ms[kStaticMaxRows];
+}  // namespace
+
+extern "C" int fuse_rmsnorm_unfused_static(const float* x, const float* w, float* y, int64_t rows,
+                                           int64_t hidden, float eps, fuse_stream_t stream) {
+    using namespace fc;
+    if (rows < 0 || hidden < 1 || hidden > 65536 || !(eps >= 0.0f)) return FUSE_EINVAL;
+    if (rows > kStaticMaxRows) return FUSE_EUNSUPPORTED;
+    if (rows == 0) return FUSE_OK;
+    if (!x || !w || !y || x == y) return FUSE_EINVAL;
+    if (!is_aligned(x, 4) || !is_aligned(w, 4) || !is_aligned(y, 4)) return FUSE_EALIGN;
+
+    // Host code cannot use the array's name as a device address: look the address up once per
+    // device, with that device current.
+    static std::mutex mu;
+    static float* dev_ms[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
+    float* ms = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!dev_ms[dev]) {
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_rms_static_ms);
+            if (e != cudaSuccess) return record_cuda_error(e);
+            dev_ms[dev] = static_cast<float*>(p);
+        }
+        ms = dev_ms[dev];
+    }
+
+    // Same four kernels as the unfused mode of fuse_rmsnorm().  Every row statistic the later
+    // kernels read is written by the row-mean kernel of the same call, so nothing is cleared.
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int H = static_cast<int>(hidden);
+    const int64_t n = rows * hidden;
+    const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
+    const bool vec = (H % 4 == 0) && fvec && is_aligned(w, 16);
+    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
+    int rc = check_launch();
+    if (rc) return rc;
+    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
+    if ((rc = check_launch())) return rc;
+    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
+    if ((rc = check_launch())) return rc;
+    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
+    return check_launch();
 }

@@ -128,6 +128,24 @@ int fuse_rmsnorm(const float* x, const float* w, float* y, int64_t rows, int64_t
                  float eps, int mode, void* workspace, size_t ws_bytes, fuse_stream_t stream);
 size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode);
 
+/* Allocation-free variant of the unfused RMSNorm (the pages have no counterpart: this entry point
+ * exists for callers, not for the method).  Some callers cannot allocate device memory at the
+ * point where they call: a host that hands this library a fixed memory budget and owns every
+ * allocation in it, or a latency-critical loop where cudaMalloc (which can synchronize the device
+ * and take unbounded time) is not allowed.  This call takes no workspace and allocates nothing:
+ * its row statistics live in one library-owned __device__ array of FUSE_RMSNORM_STATIC_MAX_ROWS
+ * floats (256 KiB), which every GPU that loads the library keeps until the process exits.
+ * Same arithmetic, kernels and output as fuse_rmsnorm(..., FUSE_UNFUSED, ...).
+ *   rows > FUSE_RMSNORM_STATIC_MAX_ROWS -> FUSE_EUNSUPPORTED (nothing launched); y != x.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current; make that first call before any stream capture.  All calls share the
+ * array and it keeps the last call's contents, so calls that may overlap on the GPU (different
+ * streams, or different host threads on one device) race; serialize them.
+ */
+#define FUSE_RMSNORM_STATIC_MAX_ROWS 65536
+int fuse_rmsnorm_unfused_static(const float* x, const float* w, float* y, int64_t rows,
+                                int64_t hidden, float eps, fuse_stream_t stream);
+
 /* ===================================================================== causal softmax
  * [OFCG] fusion_lab [E] (max -> subtract -> exp -> sum -> divide over the last axis), §3.5
  * (causal mask: query i sees keys j <= i; block-granular skipping) and [A3] (8 copies of the
