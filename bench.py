@@ -50,6 +50,15 @@ def parse_args():
     ap.add_argument("--rows", choices=["all", "chain"], default="all",
                     help="'chain' restricts a step to the metric's own row (the chain sweep)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", default=None,
+                    choices=["chain_fused", "chain_unfused", "chain_fat", "rmsnorm_fused",
+                             "rmsnorm_unfused", "softmax_fused", "softmax_unfused"],
+                    help="run only `--launches` calls of one row (for ncu), print a short line")
+    ap.add_argument("--size", type=int, default=None,
+                    help="profile size: chain elements, RMSNorm rows or softmax batch*heads")
+    ap.add_argument("--launches", type=int, default=3)
+    ap.add_argument("--K", type=int, default=8, help="chain stages for --profile")
+    ap.add_argument("--tile", type=int, default=64, help="softmax skip tile for --profile")
     return ap.parse_args()
 
 
@@ -480,9 +489,65 @@ def run_reference(args, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def run_profile(args):
+    """A fixed number of calls of one row on cuda:0 and nothing else, for ncu captures."""
+    import torch
+    import epilogue_chains_gb300 as fc
+    from epilogue_chains_gb300 import workloads as wl
+    dev = torch.device("cuda:0")
+    lib = fc._load()
+    stream = torch.cuda.current_stream().cuda_stream
+    name, L = args.profile, args.launches
+    if name.startswith("chain"):
+        n = args.size or wl.CHAIN_N
+        relu, a, b = wl.chain_stages(args.K)
+        st = fc._stages([(int(r_), float(p_), float(q_)) for r_, p_, q_ in zip(relu, a, b)])
+        mode = {"chain_fused": fc.FUSE_FUSED, "chain_unfused": fc.FUSE_UNFUSED,
+                "chain_fat": fc.FUSE_FAT}[name]
+        xs = [wl.chain_input(n, device=dev, salt=r) for r in range(2)]
+        ys = [torch.empty_like(xs[0]) for _ in range(2)]
+        for i in range(L):
+            rc = lib.fuse_chain_run(st, args.K, xs[i % 2].data_ptr(), ys[i % 2].data_ptr(), n,
+                                    fc.FUSE_F32, mode, stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_chain_bytes(args.K, n, fc.FUSE_F32, mode)
+    elif name.startswith("rmsnorm"):
+        rows = args.size or wl.RMS_ROWS
+        mode = fc.FUSE_FUSED if name == "rmsnorm_fused" else fc.FUSE_UNFUSED
+        x, w = wl.rmsnorm_input(rows, wl.RMS_HIDDEN, device=dev)
+        ys = [torch.empty_like(x) for _ in range(2)]
+        ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.RMS_HIDDEN, mode)),
+                         dtype=torch.uint8, device=dev)
+        for i in range(L):
+            rc = lib.fuse_rmsnorm(x.data_ptr(), w.data_ptr(), ys[i % 2].data_ptr(), rows,
+                                  wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)
+    else:
+        bh = args.size or wl.SM_B * wl.SM_H
+        S = wl.SM_S
+        mode = fc.FUSE_FUSED if name == "softmax_fused" else fc.FUSE_UNFUSED
+        tile = args.tile if mode == fc.FUSE_FUSED else 0
+        s_ = wl.softmax_input(bh, S, device=dev)
+        ps = [torch.empty_like(s_) for _ in range(2)]
+        ws = torch.empty(max(1, fc.fuse_causal_softmax_workspace_bytes(bh, S, mode)),
+                         dtype=torch.uint8, device=dev)
+        for i in range(L):
+            rc = lib.fuse_causal_softmax(s_.data_ptr(), ps[i % 2].data_ptr(), bh, S, wl.SM_SCALE,
+                                         tile, fc.FUSE_BF16, mode, ws.data_ptr(), ws.numel(), stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_causal_softmax_bytes(bh, S, tile, fc.FUSE_BF16, mode)
+    torch.cuda.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    print(json.dumps({"profile": name, "launches": L, "algorithmic_bytes_per_call": nbytes}))
+
+
 def main():
     args = parse_args()
     rank, world, local = dist_env()
+    if args.profile:
+        run_profile(args)
+        return
     if args.impl == "reference":
         out = run_reference(args, rank, world)
     else:
