@@ -173,6 +173,35 @@ int fuse_causal_softmax(const void* s, void* p, int64_t batch_heads, int64_t S, 
                         size_t ws_bytes, fuse_stream_t stream);
 size_t fuse_causal_softmax_workspace_bytes(int64_t batch_heads, int64_t S, int mode);
 
+/* ===================================================================== GEMM epilogue chain
+ * [K4] §① chain_mlp_epilogue: the chain mm -> +bias -> GELU -> +residual in fp16, priced under the
+ * cut plans [1,1,1,1], [1,3], [2,2], [4]; §⑥ the decode shape M = 16.  [OFCG] §5.2: epilogue
+ * fusion writes the GEMM output once, already in its final form.  Computes
+ *     Y = fp16( GELU( A @ B + bias ) + R ),   GELU(v) = v/2 (1 + erf(v / sqrt 2)),
+ * with fp16 inputs, fp32 accumulation (tcgen05 tensor cores) and fp32 epilogue math.
+ *
+ *   A     device fp16 [M, Kdim] row-major;   B  device fp16 [Kdim, N] row-major (N contiguous)
+ *   bias  device fp16 [N];   R, Y  device fp16 [M, N] row-major.  Y must not overlap any input.
+ *   Rules: N % 8 == 0 and Kdim % 8 == 0 (16-byte row strides), every pointer 16-byte aligned
+ *          (FUSE_EALIGN otherwise); M, N, Kdim <= 2^31 - 1; Kdim >= 1.  Ragged tiles are handled.
+ *   M > 64:  persistent 128 x 256-tile kernel, one CTA per SM.
+ *   M <= 64: decode kernel (swap A/B, split K over an 8-CTA cluster, reduction in distributed
+ *            shared memory).
+ * fuse_gemm_epilogue() is plan [4]: one kernel, reads A, B, bias, R once, writes Y once.
+ * fuse_gemm_epilogue_plan(): cut_mask bit i (i = 0, 1, 2) places a kernel boundary after stage i
+ * (0 = mm, 1 = +bias, 2 = GELU): [1,1,1,1] = 7, [1,3] = 1, [2,2] = 2, [4] = 0; all 8 masks
+ * are accepted.  Each cut stores the intermediate (C, C', C'') as fp16 in Y and the next kernel
+ * reads it back in place, so the plan's DRAM traffic is fuse_gemm_bytes() and its numerics round
+ * to fp16 exactly at the cuts.  No workspace is needed.
+ */
+int fuse_gemm_epilogue(const void* A, const void* B, const void* bias, const void* R, void* Y,
+                       int64_t M, int64_t N, int64_t Kdim, fuse_stream_t stream);
+int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, const void* R, void* Y,
+                            int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask,
+                            fuse_stream_t stream);
+/* [K4] §① traffic of a plan, in bytes: 2 * (M*K + K*N + N + 2*M*N + 2*cuts*M*N). */
+int64_t fuse_gemm_bytes(int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask);
+
 /* ===================================================================== ledgers
  * [K4] §① traffic(): a cut plan splits the K stages into consecutive kernels (cut_mask bit i =
  * a kernel boundary after stage i).  Each kernel reads the previous kernel's output (the

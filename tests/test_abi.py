@@ -160,3 +160,27 @@ def test_causal_block_skip_reads_the_kept_fraction():
     assert f"{100 * (S + 1) / (2 * S):.1f}" == f"{g['kept_exact_pct']:.1f}"
     assert fc.fuse_causal_softmax_bytes(bh, S, 64, fc.FUSE_BF16, fc.FUSE_FUSED) == 1_627_389_952
     assert fc.fuse_causal_softmax_bytes(bh, S, 128, fc.FUSE_BF16, fc.FUSE_FUSED) == 1_644_167_168
+
+
+def test_gemm_bytes_match_printed_plan_ledger():
+    """fuse_gemm_bytes() (the kernels' DRAM traffic) equals [K4] §①'s four printed integers."""
+    for plan, mask, nbytes, launches in read_golden("k4_ledger_bytes.txt"):
+        assert fc.fuse_gemm_bytes(4096, 4096, 4096, int(mask)) == int(nbytes), plan
+    st = mlp_epilogue_stages(16, 4096, 4096)
+    for mask in range(8):
+        assert fc.fuse_gemm_bytes(16, 4096, 4096, mask) == fc.fuse_ledger(st, mask, 2)["bytes"]
+
+
+def test_gemm_host_validation():
+    lib = fc._load()
+    assert lib.fuse_gemm_epilogue_plan(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 60, 64, 0,
+                                       None) == fc.FUSE_EALIGN      # N % 8
+    assert lib.fuse_gemm_epilogue_plan(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 64, 60, 0,
+                                       None) == fc.FUSE_EALIGN      # K % 8
+    assert lib.fuse_gemm_epilogue_plan(0x1000, 0x2000, 0x3000, 0x4000, 0x5000, 64, 64, 64, 8,
+                                       None) == fc.FUSE_EINVAL      # mask beyond 3 cuts
+    assert lib.fuse_gemm_epilogue_plan(0x1000, 0x2000, 0x3000, 0x4000, 0x4000, 64, 64, 64, 0,
+                                       None) == fc.FUSE_EINVAL      # Y overlaps R
+    assert lib.fuse_gemm_epilogue_plan(0x1008, 0x2000, 0x3000, 0x4000, 0x9000, 64, 64, 64, 0,
+                                       None) == fc.FUSE_EALIGN      # A not 16-byte aligned
+    assert lib.fuse_gemm_epilogue_plan(None, None, None, None, None, 0, 64, 64, 0, None) == fc.FUSE_OK

@@ -1,0 +1,172 @@
+"""Parity of the GEMM + bias + GELU + residual chain (tcgen05 kernels) against the CPU oracle,
+through the C ABI, for every cut plan.
+
+Two bars on every output element:
+  * the stated one: |Y - ref| <= 2e-2 (|ref| + rms(ref)) and ||Y - ref||_2 <= 2e-2 ||ref||_2;
+  * a tighter one that the arithmetic supports.  Both sides round to fp16 at the same points
+    (every cut, and the output).  The GPU accumulates in fp32 (K/16 tensor-core steps of 16
+    products), the oracle in double, so the accumulators differ by at most about
+    (K/16 + 16) 2^-23 sum_k |a_mk b_kn| (cancellation can make that large next to a small
+    result; cuBLAS's fp16 GEMM shows the same effect on these inputs).  GELU's slope is at most
+    1.13.  At a cut the two pre-rounding values can also straddle an fp16 rounding boundary and
+    round one ulp apart (|intermediate| < 8 here, so at most 2^-8).  Hence per element
+        |Y - ref| <= 2 ulp16(ref) + 1.13 (K/16 + 16) 2^-23 (|A| |B|)_mn + cuts * 2^-8,
+    and elements beyond the plain 2-ulp bound must stay rare (under 1%).
+With the configured inputs (A, B ~ N(0, 1/64)) the GEMM term is small next to R ~ N(0, 1), so a
+"stress" variant (A, B ~ N(0, 1/8), R = 0, bias ~ N(0, 0.1)) makes the GEMM dominate the output.
+"""
+import numpy as np
+import pytest
+
+import epilogue_chains_gb300 as fc
+import oracle
+from epilogue_chains_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+PLANS = {"[1,1,1,1]": 7, "[1,3]": 1, "[2,2]": 2, "[4]": 0}
+
+
+def _ulp16(x):
+    a = np.abs(x.astype(np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return 2.0 ** (e - 10)
+
+
+def _cuts(mask):
+    return bin(mask & 7).count("1")
+
+
+def _check(y_bits, ref_bits, mask, A, B, rows=None):
+    y = y_bits.view(np.float16).astype(np.float64)
+    r = ref_bits.view(np.float16).astype(np.float64)
+    assert np.all(np.isfinite(y))
+    err = np.abs(y - r)
+    rms = np.sqrt(np.mean(r ** 2))
+    assert np.all(err <= 2e-2 * (np.abs(r) + rms)), float(err.max())
+    assert np.linalg.norm(err) <= 2e-2 * np.linalg.norm(r)
+    Af = np.abs(A.view(np.float16).astype(np.float64))
+    if rows is not None:
+        Af = Af[rows]
+    sab = Af @ np.abs(B.view(np.float16).astype(np.float64))
+    K = A.shape[1]
+    tight = 2 * _ulp16(r) + 2.0 ** -24
+    bound = tight + 1.13 * (np.ceil(K / 16) + 16) * 2.0 ** -23 * sab + _cuts(mask) * 2.0 ** -8
+    bad = err > bound
+    assert not bad.any(), (int(bad.sum()), float(err.max()), np.argwhere(bad)[:5].tolist())
+    flips = int(np.count_nonzero(err > tight))
+    assert flips <= 0.01 * err.size + 1, flips
+
+
+def _dev(bits, shape=None):
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.float16)
+    return t if shape is None else t.view(*shape)
+
+
+def _run(A, B, bias, R, mask):
+    import torch
+    M, K = A.shape
+    N = B.shape[1]
+    Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
+    fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y, cut_mask=mask)
+    torch.cuda.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    return Y.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _stress(M, N, K, salt=0):
+    A, B, bias, _ = wl.gemm_input(M, N, K, salt=salt, std=1.0 / 8.0)
+    R = np.zeros((M, N), np.uint16)
+    return A, B, bias, R
+
+
+@pytest.mark.parametrize("mask", [0, 1, 2, 7])
+def test_single_tile(cuda_device, mask):
+    """One 128 x 256 output tile, one 64-deep k-block."""
+    A, B, bias, R = _stress(128, 256, 64)
+    _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+@pytest.mark.parametrize("shape", [(128, 256, 256), (256, 512, 128), (384, 768, 1024)])
+def test_several_tiles_and_k_blocks(cuda_device, shape):
+    A, B, bias, R = _stress(*shape, salt=1)
+    _check(_run(A, B, bias, R, 0), oracle.gemm_epilogue(A, B, bias, R, 0), 0, A, B)
+    A, B, bias, R = wl.gemm_input(*shape, salt=2)
+    _check(_run(A, B, bias, R, 0), oracle.gemm_epilogue(A, B, bias, R, 0), 0, A, B)
+
+
+@pytest.mark.parametrize("shape", [(300, 520, 200), (129, 264, 72), (65, 8, 8), (200, 136, 4104)])
+@pytest.mark.parametrize("mask", [0, 7])
+def test_ragged_shapes(cuda_device, shape, mask):
+    """M, N, K not multiples of the tile (zero-filled loads, clipped stores)."""
+    A, B, bias, R = wl.gemm_input(*shape, salt=3, std=1.0 / 8.0)
+    _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+@pytest.mark.parametrize("mask", range(8))
+def test_every_cut_mask(cuda_device, mask):
+    A, B, bias, R = wl.gemm_input(256, 512, 512, salt=4, std=1.0 / 8.0)
+    _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+@pytest.mark.parametrize("M", [1, 5, 16, 17, 32, 33, 48, 64])
+@pytest.mark.parametrize("mask", [0, 7])
+def test_decode_shapes(cuda_device, M, mask):
+    """M <= 64: swap-AB, split-K cluster kernel (K split 8 ways, some splits empty)."""
+    for K in (4096, 520):
+        A, B, bias, R = wl.gemm_input(M, 384, K, salt=5 + M, std=1.0 / 8.0)
+        _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+@pytest.mark.parametrize("plan", list(PLANS))
+def test_decode_full_size_every_plan(cuda_device, plan):
+    """M = 16, N = K = 4096 as benchmarked: every element against the oracle."""
+    A, B, bias, R = wl.gemm_input(16)
+    _check(_run(A, B, bias, R, PLANS[plan]), oracle.gemm_epilogue(A, B, bias, R, PLANS[plan]),
+           PLANS[plan], A, B)
+
+
+@pytest.mark.parametrize("plan", list(PLANS))
+def test_full_size_sampled_rows(cuda_device, plan):
+    """M = N = K = 4096 as benchmarked: the GPU computes all of Y, 40 rows (tile edges, first,
+    last, random) are compared element by element with the oracle."""
+    A, B, bias, R = wl.gemm_input(4096)
+    Y = _run(A, B, bias, R, PLANS[plan])
+    g = np.random.default_rng(6)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 2047, 2048, 4094, 4095],
+                                     g.integers(0, 4096, 30)]))
+    _check(Y[rows], oracle.gemm_epilogue(A, B, bias, R, PLANS[plan], rows=rows), PLANS[plan], A, B,
+           rows)
+
+
+def test_stress_full_size_sampled_rows(cuda_device):
+    A, B, bias, R = _stress(4096, 4096, 4096, salt=7)
+    Y = _run(A, B, bias, R, 0)
+    rows = np.array([0, 63, 64, 127, 128, 1000, 3071, 4095])
+    _check(Y[rows], oracle.gemm_epilogue(A, B, bias, R, 0, rows=rows), 0, A, B, rows)
+
+
+def test_plans_agree_with_each_other(cuda_device):
+    """The fused plan and the unfused plans differ only by the fp16 roundings at the cuts."""
+    A, B, bias, R = wl.gemm_input(512, 1024, 1024, salt=8)
+    y4 = _run(A, B, bias, R, 0).view(np.float16).astype(np.float64)
+    for mask in (1, 2, 7):
+        y = _run(A, B, bias, R, mask).view(np.float16).astype(np.float64)
+        assert np.max(np.abs(y - y4)) <= 4 * np.max(_ulp16(y4)) + 1e-3
+
+
+def test_rejects_bad_arguments(cuda_device):
+    import torch
+    A = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    B = torch.zeros(64, 60, dtype=torch.float16, device="cuda")   # N % 8 != 0
+    b = torch.zeros(60, dtype=torch.float16, device="cuda")
+    R = torch.zeros(64, 60, dtype=torch.float16, device="cuda")
+    Y = torch.zeros(64, 60, dtype=torch.float16, device="cuda")
+    with pytest.raises(fc.FuseError):
+        fc.fuse_gemm_epilogue(A, B, b, R, Y)
+    B = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    b = torch.zeros(64, dtype=torch.float16, device="cuda")
+    R = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(fc.FuseError):
+        fc.fuse_gemm_epilogue(A, B, b, R, R)                       # Y aliases R
