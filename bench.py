@@ -52,13 +52,14 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     choices=["chain_fused", "chain_unfused", "chain_fat", "rmsnorm_fused",
-                             "rmsnorm_unfused", "softmax_fused", "softmax_unfused"],
+                             "rmsnorm_unfused", "softmax_fused", "softmax_unfused", "gemm"],
                     help="run only `--launches` calls of one row (for ncu), print a short line")
     ap.add_argument("--size", type=int, default=None,
                     help="profile size: chain elements, RMSNorm rows or softmax batch*heads")
     ap.add_argument("--launches", type=int, default=3)
     ap.add_argument("--K", type=int, default=8, help="chain stages for --profile")
     ap.add_argument("--tile", type=int, default=64, help="softmax skip tile for --profile")
+    ap.add_argument("--mask", type=int, default=0, help="GEMM cut mask for --profile gemm")
     return ap.parse_args()
 
 
@@ -141,13 +142,14 @@ def summarize_clocks(rows, t0, t1):
 
 
 # ------------------------------------------------------------------------------ traffic
-def committed_traffic(kernel_src: str):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary, if it was
-    captured from the current kernel source (sha256 recorded in the summary), else None."""
-    path = os.path.join(ROOT, "profiles", "chain_fused_f32_n16M.txt")
-    if not os.path.exists(path):
+def committed_traffic(group: str, src_name: str):
+    """DRAM bytes per launch of a kernel from its committed ncu summary (profiles/<group>.txt),
+    if that summary was captured from the current kernel source (sha256 recorded in it)."""
+    path = os.path.join(ROOT, "profiles", f"{group}.txt")
+    src = os.path.join(ROOT, "epilogue_chains_gb300", "csrc", src_name)
+    if not src_name or not os.path.exists(path) or not os.path.exists(src):
         return None
-    with open(kernel_src, "rb") as f:
+    with open(src, "rb") as f:
         sha = hashlib.sha256(f.read()).hexdigest()
     vals = {}
     with open(path) as f:
@@ -164,6 +166,18 @@ def committed_traffic(kernel_src: str):
 
 
 # ------------------------------------------------------------------------------ our arm
+class Group:
+    """One row of the hot path in a step: an untimed leading call, then timed calls.
+
+    calls: list of (tag, fn, units) -- units are the call's algorithmic bytes (bound "hbm") or
+    flops (bound "tensor").  `kernel` names the single kernel the calls launch (None if a call
+    launches several kernels); `launches` is the number of our kernels one call launches."""
+
+    def __init__(self, name, calls, pre, bound, kernel, launches):
+        self.name, self.calls, self.pre = name, calls, pre
+        self.bound, self.kernel, self.launches = bound, kernel, launches
+
+
 def run_ours(args, rank, world, local):
     import torch
     import epilogue_chains_gb300 as fc
@@ -178,10 +192,22 @@ def run_ours(args, rank, world, local):
     sh = stream.cuda_stream
     lib = fc._load()
     peaks, peak_src = load_peaks()
+    counter = {"launches": 0}
 
-    N = wl.CHAIN_N
-    KS = wl.CHAIN_KS
-    R = 4
+    def check(rc, where):
+        if rc != 0:
+            raise fc.FuseError(rc, where)
+
+    def rotating(n):
+        state = {"i": 0}
+
+        def nxt():
+            state["i"] += 1
+            return (state["i"] - 1) % n
+        return nxt
+
+    # ------------------------------------------------------------------ pointwise chain
+    N, KS, R = wl.CHAIN_N, wl.CHAIN_KS, 4
     with torch.cuda.stream(stream):
         xs = [wl.chain_input(N, device=dev, salt=r + 100 * rank) for r in range(R)]
         ys = [torch.empty_like(xs[0]) for _ in range(R)]
@@ -191,83 +217,121 @@ def run_ours(args, rank, world, local):
         stage_sets[K] = fc._stages([(fc.FUSE_OP_AFFINE_RELU if r_ else fc.FUSE_OP_AFFINE, p, q)
                                     for r_, p, q in zip(relu, a, b)])
     chain_bytes = fc.fuse_chain_bytes(1, N, fc.FUSE_F32, fc.FUSE_FUSED)  # 2 N b, any K
+    crot = rotating(R)
 
-    launches = {"n": 0}
-    rot = {"i": 0}
+    def chain(K, mode):
+        def fn():
+            i = crot()
+            check(lib.fuse_chain_run(stage_sets[K], K, xs[i].data_ptr(), ys[i].data_ptr(), N,
+                                     fc.FUSE_F32, mode, sh), "fuse_chain_run")
+            counter["launches"] += K if mode == fc.FUSE_UNFUSED else 1
+        return fn
 
-    def chain_call(K, mode):
-        i = rot["i"] % R
-        rot["i"] += 1
-        st = stage_sets[K]
-        rc = lib.fuse_chain_run(st, K, xs[i].data_ptr(), ys[i].data_ptr(), N, fc.FUSE_F32, mode, sh)
-        if rc != 0:
-            raise fc.FuseError(rc, "fuse_chain_run")
-        launches["n"] += K if mode == fc.FUSE_UNFUSED else 1
+    groups = [
+        Group("chain_fused", [(f"K{K}", chain(K, fc.FUSE_FUSED), chain_bytes) for K in KS],
+              chain(KS[0], fc.FUSE_FUSED), "hbm", "chain_fused_kernel<f32>", 1),
+        Group("chain_unfused", [(f"K{K}", chain(K, fc.FUSE_UNFUSED),
+                                 fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED)) for K in KS],
+              chain(KS[0], fc.FUSE_UNFUSED), "hbm", None, None),
+        # the fat probe is a fixed-point probe at K = 4 ([C05] §5: not part of the sweep)
+        Group("chain_fat", [("K4", chain(4, fc.FUSE_FAT), chain_bytes)], chain(4, fc.FUSE_FAT),
+              "hbm", "chain_fat_kernel<f32>", 1),
+    ]
 
-    rows_all = args.rows == "all"
-    if rows_all:
+    if args.rows == "all":
+        # -------------------------------------------------------------- RMSNorm
         with torch.cuda.stream(stream):
             rx, rw = wl.rmsnorm_input(device=dev, salt=rank)
-            rys = [torch.empty_like(rx) for _ in range(2)]
             rxs = [rx, rx.clone()]
-            rws = torch.empty(fc.fuse_rmsnorm_workspace_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN,
-                                                              fc.FUSE_UNFUSED),
+            rys = [torch.empty_like(rx) for _ in range(2)]
+            rws = torch.empty(fc.fuse_rmsnorm_workspace_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_UNFUSED),
                               dtype=torch.uint8, device=dev)
-            bh, S = wl.SM_B * wl.SM_H, wl.SM_S
-            ss = wl.softmax_input(bh, S, device=dev, salt=rank)
-            sps = [torch.empty_like(ss) for _ in range(2)]
+        rrot = rotating(2)
+
+        def rms(mode):
+            def fn():
+                i = rrot()
+                check(lib.fuse_rmsnorm(rxs[i].data_ptr(), rw.data_ptr(), rys[i].data_ptr(), wl.RMS_ROWS,
+                                       wl.RMS_HIDDEN, wl.RMS_EPS, mode, rws.data_ptr(), rws.numel(), sh),
+                      "fuse_rmsnorm")
+                counter["launches"] += 1 if mode == fc.FUSE_FUSED else 4
+            return fn
+        rb = {m: fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
+        groups += [
+            Group("rmsnorm_fused", [("r", rms(fc.FUSE_FUSED), rb[fc.FUSE_FUSED])] * 2, rms(fc.FUSE_FUSED),
+                  "hbm", "rmsnorm_fused_kernel", 1),
+            Group("rmsnorm_unfused", [("r", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED])] * 2,
+                  rms(fc.FUSE_UNFUSED), "hbm", None, None),
+        ]
+        # -------------------------------------------------------------- causal softmax
+        bh, S = wl.SM_B * wl.SM_H, wl.SM_S
+        with torch.cuda.stream(stream):
+            ss = [wl.softmax_input(bh, S, device=dev, salt=rank), None]
+            ss[1] = ss[0].clone()
+            sps = [torch.empty_like(ss[0]) for _ in range(2)]
             sws = torch.empty(fc.fuse_causal_softmax_workspace_bytes(bh, S, fc.FUSE_UNFUSED),
                               dtype=torch.uint8, device=dev)
-    rrot = {"i": 0}
+        srot = rotating(2)
 
-    def rms_call(mode):
-        i = rrot["i"] % 2
-        rrot["i"] += 1
-        rc = lib.fuse_rmsnorm(rxs[i].data_ptr(), rw.data_ptr(), rys[i].data_ptr(), wl.RMS_ROWS,
-                              wl.RMS_HIDDEN, wl.RMS_EPS, mode, rws.data_ptr(), rws.numel(), sh)
-        if rc != 0:
-            raise fc.FuseError(rc, "fuse_rmsnorm")
-        launches["n"] += 1 if mode == fc.FUSE_FUSED else 4
-
-    srot = {"i": 0}
-
-    def sm_call(tile, mode):
-        i = srot["i"] % 2
-        srot["i"] += 1
-        rc = lib.fuse_causal_softmax(ss.data_ptr(), sps[i].data_ptr(), bh, S, wl.SM_SCALE, tile,
-                                     fc.FUSE_BF16, mode, sws.data_ptr(), sws.numel(), sh)
-        if rc != 0:
-            raise fc.FuseError(rc, "fuse_causal_softmax")
-        launches["n"] += 1 if mode == fc.FUSE_FUSED else 5
-
-    # one step = the groups below; every timed call gets its own event pair
-    groups = [("chain_fused", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_FUSED)) for K in KS],
-               lambda: chain_call(KS[0], fc.FUSE_FUSED)),
-              ("chain_unfused", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_UNFUSED)) for K in KS],
-               lambda: chain_call(KS[0], fc.FUSE_UNFUSED)),
-              ("chain_fat", [(f"K{K}", lambda K=K: chain_call(K, fc.FUSE_FAT)) for K in KS],
-               lambda: chain_call(KS[0], fc.FUSE_FAT))]
-    if rows_all:
+        def sm(tile, mode):
+            def fn():
+                i = srot()
+                check(lib.fuse_causal_softmax(ss[i].data_ptr(), sps[i].data_ptr(), bh, S, wl.SM_SCALE,
+                                              tile, fc.FUSE_BF16, mode, sws.data_ptr(), sws.numel(), sh),
+                      "fuse_causal_softmax")
+                counter["launches"] += 1 if mode == fc.FUSE_FUSED else 5
+            return fn
         groups += [
-            ("rmsnorm_fused", [("r", lambda: rms_call(fc.FUSE_FUSED))] * 2, lambda: rms_call(fc.FUSE_FUSED)),
-            ("rmsnorm_unfused", [("r", lambda: rms_call(fc.FUSE_UNFUSED))] * 2,
-             lambda: rms_call(fc.FUSE_UNFUSED)),
-            ("softmax_fused", [(f"T{t}", lambda t=t: sm_call(t, fc.FUSE_FUSED)) for t in (0, 64, 128)],
-             lambda: sm_call(0, fc.FUSE_FUSED)),
-            ("softmax_unfused", [("T0", lambda: sm_call(0, fc.FUSE_UNFUSED))],
-             lambda: sm_call(0, fc.FUSE_UNFUSED)),
+            Group("softmax_fused", [(f"T{t}", sm(t, fc.FUSE_FUSED),
+                                     fc.fuse_causal_softmax_bytes(bh, S, t, fc.FUSE_BF16, fc.FUSE_FUSED))
+                                    for t in (0, 64, 128)], sm(0, fc.FUSE_FUSED), "hbm",
+                  "softmax_fused_kernel<bf16>", 1),
+            Group("softmax_unfused", [("T0", sm(0, fc.FUSE_UNFUSED),
+                                       fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED))],
+                  sm(0, fc.FUSE_UNFUSED), "hbm", None, None),
+        ]
+        # -------------------------------------------------------------- GEMM epilogue chain
+        plans = {"[4]": 0, "[1,3]": 1, "[2,2]": 2, "[1,1,1,1]": 7}
+        gN, gK = wl.GEMM_N, wl.GEMM_K
+        gemm_bufs = {}
+        with torch.cuda.stream(stream):
+            for M in wl.GEMM_MS:
+                A, B, bias, Rr = wl.gemm_input(M, device=dev, salt=rank)
+                nb = 4 if M < 128 else 1   # decode: rotate 4 weight copies (128 MiB > L2 share)
+                Bs = [B] + [B.clone() for _ in range(nb - 1)]
+                Ys = [torch.empty(M, gN, dtype=torch.float16, device=dev) for _ in range(2)]
+                gemm_bufs[M] = (A, Bs, bias, Rr, Ys, rotating(nb), rotating(2))
+
+        def gemm(M, mask):
+            A, Bs, bias, Rr, Ys, brot, yrot = gemm_bufs[M]
+
+            def fn():
+                b, y = Bs[brot()], Ys[yrot()]
+                check(lib.fuse_gemm_epilogue_plan(A.data_ptr(), b.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
+                                                  y.data_ptr(), M, gN, gK, mask, sh), "fuse_gemm_epilogue_plan")
+                counter["launches"] += 1 + bin(mask).count("1")
+            return fn
+        flops = {M: 2 * M * gN * gK for M in wl.GEMM_MS}
+        groups += [
+            Group("gemm_M4096_fused", [("[4]", gemm(4096, 0), flops[4096])], gemm(4096, 0), "tensor",
+                  "gemm_tc_kernel", 1),
+            Group("gemm_M4096_unfused", [(p_, gemm(4096, m_), flops[4096]) for p_, m_ in plans.items() if m_],
+                  gemm(4096, 7), "tensor", None, None),
+            Group("gemm_M16_fused", [("[4]", gemm(16, 0), fc.fuse_gemm_bytes(16, gN, gK, 0))], gemm(16, 0),
+                  "hbm", "gemm_decode_kernel<16>", 1),
+            Group("gemm_M16_unfused", [(p_, gemm(16, m_), fc.fuse_gemm_bytes(16, gN, gK, m_))
+                                       for p_, m_ in plans.items() if m_], gemm(16, 7), "hbm", None, None),
         ]
 
     def make_events():
-        return {g: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                    for _ in calls] for g, calls, _ in groups}
+        return {g.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                         for _ in g.calls] for g in groups}
 
     def step(evs):
-        # each group: its untimed leading call, then the timed calls back to back
         with torch.cuda.stream(stream):
-            for g, calls, pre in groups:
-                pre()
-                for (tag, fn), (e0, e1) in zip(calls, evs[g]):
+            for g in groups:
+                g.pre()
+                for (tag, fn, units), (e0, e1) in zip(g.calls, evs[g.name]):
                     e0.record(stream)
                     fn()
                     e1.record(stream)
@@ -282,80 +346,106 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    launches["n"] = 0
+    counter["launches"] = 0
     t0 = time.time()
-    for s in range(args.steps):
-        step(all_evs[s])
+    for s_ in range(args.steps):
+        step(all_evs[s_])
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     t1 = time.time()
     clocks = summarize_clocks(sampler.stop(), t0, t1)
-    timed_launches = launches["n"]   # every kernel of ours launched inside the timed region
+    timed_launches = counter["launches"]   # every kernel of ours launched inside the timed region
 
-    # collect
-    times = {g: [[e0.elapsed_time(e1) for e0, e1 in evs[g]] for evs in all_evs]
-             for g, _, _ in groups}   # ms, [step][call]
-    def mean_ms(g, idx):
-        return float(np.mean([st[idx] for st in times[g]]))
+    # ms per call: times[group][step][call]
+    times = {g.name: [[e0.elapsed_time(e1) for e0, e1 in evs[g.name]] for evs in all_evs] for g in groups}
+    gmap = {g.name: g for g in groups}
+
+    def mean_ms(name, idx):
+        return float(np.mean([st[idx] for st in times[name]]))
+
+    def group_total_ms(name):
+        return float(np.mean([sum(st) for st in times[name]]))
 
     fused_ms_total = sum(sum(st) for st in times["chain_fused"])
     n_fused = args.steps * len(KS)
-    my_bytes = n_fused * chain_bytes
     elapsed_s = fused_ms_total / 1e3
-    step_ms = float(np.mean([sum(sum(times[g][s]) for g in times) for s in range(args.steps)]))
+    step_ms = float(np.mean([sum(sum(times[g][s_]) for g in times) for s_ in range(args.steps)]))
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([elapsed_s, step_ms], dtype=torch.float64, device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         elapsed_s, step_ms = float(t[0]), float(t[1])
-    value = my_bytes * world / elapsed_s / 1e9
+    value = n_fused * chain_bytes * world / elapsed_s / 1e9
 
+    def roofline_of(name):
+        g = gmap[name]
+        tot_units = sum(u for _, _, u in g.calls)
+        tot_ms = group_total_ms(name)
+        if g.bound == "hbm":
+            achieved, peak, unit = tot_units / tot_ms / 1e6, peaks["hbm_gbs"], "GB/s"
+        else:
+            achieved, peak, unit = tot_units / tot_ms / 1e9, peaks["bf16_tflops"], "TFLOP/s"
+        out = {"bound": g.bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+               "frac": round(achieved / peak, 4), "kernel": g.kernel,
+               "units_per_launch": int(tot_units / len(g.calls)),
+               "avg_launch_us": round(tot_ms / len(g.calls) * 1e3, 2),
+               "step_share": round(tot_ms / step_ms, 4)}
+        if g.bound == "tensor":
+            out["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+        return out
+
+    # dominant kernel: the single-kernel group with the largest share of the step
+    single = [g.name for g in groups if g.kernel is not None]
+    dominant = max(single, key=group_total_ms)
+    roofline = roofline_of(dominant)
+    roofline["peak_source"] = peak_src
+    kernel_src = {"softmax_fused": "softmax.cu", "chain_fused": "chain.cu", "gemm_M4096_fused": "gemm.cu",
+                  "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm.cu"}
+    roofline["traffic"] = committed_traffic(dominant, kernel_src.get(dominant, ""))
+
+    rows = {"step_share": {g.name: round(group_total_ms(g.name) / step_ms, 4) for g in groups}}
     per_k = {}
     for j, K in enumerate(KS):
         f = mean_ms("chain_fused", j)
         u = mean_ms("chain_unfused", j)
-        fat = mean_ms("chain_fat", j)
-        per_k[str(K)] = {
-            "fused_us": round(f * 1e3, 2), "unfused_us": round(u * 1e3, 2),
-            "fat_us": round(fat * 1e3, 2), "speedup_fused_vs_unfused": round(u / f, 3),
-            "fat_over_fused": round(fat / f, 3),
-            "fused_GBs": round(chain_bytes / (f / 1e3) / 1e9, 1),
-            "unfused_GBs": round(fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED) / (u / 1e3) / 1e9, 1),
-        }
-    fused_avg_ms = fused_ms_total / n_fused
-    achieved = chain_bytes / (fused_avg_ms / 1e3) / 1e9
-    kernel_src = os.path.join(ROOT, "epilogue_chains_gb300", "csrc", "chain.cu")
-    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
-                "traffic": committed_traffic(kernel_src), "peak_source": peak_src,
-                "kernel": "chain_fused_kernel<f32>", "algorithmic_bytes_per_launch": chain_bytes,
-                "frac_of_nominal_7900": round(achieved / NOMINAL_HBM_GBS, 4)}
-
-    rows = {"chain": per_k}
-    if rows_all:
-        hbm = peaks["hbm_gbs"]
-        rb_f = fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_FUSED)
-        rb_u = fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_UNFUSED)
-        rf = float(np.mean([np.mean(st) for st in times["rmsnorm_fused"]]))
-        ru = float(np.mean([np.mean(st) for st in times["rmsnorm_unfused"]]))
+        per_k[str(K)] = {"fused_us": round(f * 1e3, 2), "unfused_us": round(u * 1e3, 2),
+                         "speedup_fused_vs_unfused": round(u / f, 3),
+                         "fused_GBs": round(chain_bytes / (f / 1e3) / 1e9, 1),
+                         "unfused_ledger_GBs": round(fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED)
+                                                     / (u / 1e3) / 1e9, 1)}
+    fat = mean_ms("chain_fat", 0)
+    rows["chain"] = {"per_K": per_k, "roofline_fused": roofline_of("chain_fused"),
+                     "fat_K4": {"us": round(fat * 1e3, 2), "fat_over_fused": round(fat / mean_ms("chain_fused", KS.index(4)), 3)}}
+    if args.rows == "all":
+        rf, ru = group_total_ms("rmsnorm_fused") / 2, group_total_ms("rmsnorm_unfused") / 2
         rows["rmsnorm"] = {"fused_us": round(rf * 1e3, 2), "unfused_us": round(ru * 1e3, 2),
-                           "fused_GBs": round(rb_f / rf / 1e6, 1),
-                           "fused_frac_hbm": round(rb_f / rf / 1e6 / hbm, 4),
-                           "unfused_GBs": round(rb_u / ru / 1e6, 1),
-                           "speedup": round(ru / rf, 3)}
-        sm = {}
+                           "speedup": round(ru / rf, 3), "roofline_fused": roofline_of("rmsnorm_fused")}
+        smr = {}
         for j, t in enumerate((0, 64, 128)):
             ms_ = mean_ms("softmax_fused", j)
-            b_ = fc.fuse_causal_softmax_bytes(bh, S, t, fc.FUSE_BF16, fc.FUSE_FUSED)
-            sm[f"fused_T{t}"] = {"us": round(ms_ * 1e3, 1), "bytes": b_,
-                                 "GBs": round(b_ / ms_ / 1e6, 1),
-                                 "frac_hbm": round(b_ / ms_ / 1e6 / hbm, 4)}
+            b_ = gmap["softmax_fused"].calls[j][2]
+            smr[f"fused_T{t}"] = {"us": round(ms_ * 1e3, 1), "bytes": b_, "GBs": round(b_ / ms_ / 1e6, 1),
+                                  "frac_hbm": round(b_ / ms_ / 1e6 / peaks["hbm_gbs"], 4)}
         mu = mean_ms("softmax_unfused", 0)
-        bu = fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED)
-        sm["unfused"] = {"us": round(mu * 1e3, 1), "bytes": bu, "GBs": round(bu / mu / 1e6, 1)}
-        sm["speedup_fused_T0"] = round(mu / mean_ms("softmax_fused", 0), 3)
-        rows["causal_softmax"] = sm
+        bu = gmap["softmax_unfused"].calls[0][2]
+        smr["unfused"] = {"us": round(mu * 1e3, 1), "bytes": bu, "GBs": round(bu / mu / 1e6, 1)}
+        smr["speedup_fused_T0"] = round(mu / mean_ms("softmax_fused", 0), 3)
+        smr["speedup_fused_T64"] = round(mu / mean_ms("softmax_fused", 1), 3)
+        rows["causal_softmax"] = smr
+        gm = {}
+        for M in wl.GEMM_MS:
+            fus = mean_ms(f"gemm_M{M}_fused", 0)
+            ent = {"[4]_us": round(fus * 1e3, 2), "[4]_TFLOPs": round(flops[M] / fus / 1e9, 1),
+                   "[4]_ledger_GBs": round(fc.fuse_gemm_bytes(M, gN, gK, 0) / fus / 1e6, 1)}
+            for j, (p_, _, _) in enumerate(gmap[f"gemm_M{M}_unfused"].calls):
+                u = mean_ms(f"gemm_M{M}_unfused", j)
+                ent[f"{p_}_us"] = round(u * 1e3, 2)
+                ent[f"speedup_[4]_vs_{p_}"] = round(u / fus, 3)
+            gm[f"M{M}"] = ent
+        gm["M4096"]["roofline"] = roofline_of("gemm_M4096_fused")
+        gm["M16"]["roofline"] = roofline_of("gemm_M16_fused")
+        rows["gemm_epilogue"] = gm
 
     # ---------------------------------------------------------------- e2e through host buffers
     e2e = run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world)
@@ -378,9 +468,11 @@ def run_ours(args, rank, world, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "pointwise chain fp32 N=16,777,216, K in {2,3,4,6,8}, "
                                    "a_s~U[0.9,1.1], b_s~U[-0.1,0.1], ReLU on even s",
-                       "N": N, "K": list(KS), "step": "all rows" if rows_all else "chain sweep",
-                       "l2": "4 rotating x/y pairs (512 MiB) > L2; each group led by an untimed "
-                             "same-kind launch", "parallelism": f"replicas x{world}"},
+                       "N": N, "K": list(KS),
+                       "step": "all rows" if args.rows == "all" else "chain rows",
+                       "l2": "inputs larger than L2 or rotated (chain: 4 x/y pairs = 512 MiB; decode "
+                             "GEMM: 4 weight copies); each row group led by an untimed same-kind call",
+                       "parallelism": f"replicas x{world}"},
             "frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
             "roofline": roofline,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
@@ -523,6 +615,15 @@ def run_profile(args):
                                   wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)
+    elif name == "gemm":
+        M = args.size or 4096
+        A, B, bias, Rr = wl.gemm_input(M, device=dev)
+        Ys = [torch.empty(M, wl.GEMM_N, dtype=torch.float16, device=dev) for _ in range(2)]
+        for i in range(L):
+            rc = lib.fuse_gemm_epilogue_plan(A.data_ptr(), B.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
+                                             Ys[i % 2].data_ptr(), M, wl.GEMM_N, wl.GEMM_K, args.mask, stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_gemm_bytes(M, wl.GEMM_N, wl.GEMM_K, args.mask)
     else:
         bh = args.size or wl.SM_B * wl.SM_H
         S = wl.SM_S

@@ -11,9 +11,9 @@
 //  * M > 64: one persistent CTA per SM, warp-specialised.  Warp 0 drives TMA (128B-swizzled
 //    tiles, a 4-stage mbarrier ring); warp 1 owns TMEM and issues tcgen05.mma (M=128, N=256,
 //    K=16, fp16 in, fp32 accumulate), committing each stage back to the producer and each
-//    finished tile to the epilogue; warps 2-5 drain the accumulator with tcgen05.ld, 64 columns
-//    at a time, add bias, apply GELU(erf), add the residual (brought in by TMA while the MMAs
-//    run) and TMA-store fp16 Y.  The accumulator is double-buffered in TMEM (2 x 256 columns), so
+//    finished tile to the epilogue; warps 2-9 drain the accumulator with tcgen05.ld, 32 columns
+//    at a time, add bias, apply GELU(erf), add the residual (prefetched into registers one chunk
+//    ahead) and store fp16 Y straight from registers.  The accumulator is double-buffered in TMEM (2 x 256 columns), so
 //    the epilogue of tile i overlaps the main loop of tile i+1.  A is consumed K-major, B
 //    ([K,N], N contiguous) MN-major, both straight from their row-major layouts.
 //  * M <= 64 (decode): swap A and B so N fills the 128-row MMA dimension and M becomes the MMA's
@@ -127,8 +127,35 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
 
 // ------------------------------------------------------------------------------ epilogue math
 // Stages of the chain after the GEMM: 1 = +bias, 2 = GELU(erf), 3 = +residual.
+//
+// GELU(v) = v/2 (1 + erf(v/sqrt2)).  1 + erf(x) is evaluated as erfc(-x) for x < 0 and as
+// 2 - erfc(x) for x >= 0, so there is no cancellation for strongly negative v (where 1 + erf(x)
+// is tiny).  erfc(z), z >= 0, is the Chebyshev-fitted approximation "erfcc" of Press, Teukolsky,
+// Vetterling & Flannery, Numerical Recipes (2nd ed., §6.2): erfc(z) = t exp(-z^2 + P(t)),
+// t = 1/(1 + z/2), fractional error below 1.2e-7 for every z >= 0 -- far below the fp16 output
+// resolution.  Cost: one reciprocal, one ex2 and nine FMAs.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float erfc_nonneg(float z) {
+    const float t = __frcp_rn(fmaf(0.5f, z, 1.0f));
+    float p = 0.17087277f;
+    p = fmaf(p, t, -0.82215223f);
+    p = fmaf(p, t, 1.48851587f);
+    p = fmaf(p, t, -1.13520398f);
+    p = fmaf(p, t, 0.27886807f);
+    p = fmaf(p, t, -0.18628806f);
+    p = fmaf(p, t, 0.09678418f);
+    p = fmaf(p, t, 0.37409196f);
+    p = fmaf(p, t, 1.00002368f);
+    p = fmaf(p, t, -1.26551223f);
+    return t * ex2_approx((p - z * z) * 1.44269504088896341f);
+}
 __device__ __forceinline__ float gelu_erf(float v) {
-    return 0.5f * v * (1.0f + erff(v * 0.70710678118654752f));
+    const float e = erfc_nonneg(fabsf(v) * 0.70710678118654752f);
+    return 0.5f * v * (v >= 0.0f ? 2.0f - e : e);
 }
 // apply stages first..last (inclusive, 1..3) to v
 __device__ __forceinline__ float apply_stages(float v, int first, int last, float b, float r) {
@@ -159,17 +186,16 @@ __device__ __forceinline__ uint4 pack_h8(const float* f) {
 
 // =============================================================================== main kernel
 constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
-constexpr int kMainThreads = 192;              // 6 warps
+constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
+constexpr int kMainThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t A_STAGE = BM * BK * 2;      // 16 KB
 constexpr uint32_t B_BOX = 64 * BK * 2;        // 8 KB: 64 N x 64 K
 constexpr uint32_t B_STAGE = BN * BK * 2;      // 32 KB
-constexpr uint32_t E_BUF = 32 * 64 * 2;        // 4 KB: 32 rows x 64 cols
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
-constexpr uint32_t OFF_E = OFF_B + STAGES * B_STAGE;
-constexpr uint32_t OFF_BAR = OFF_E + 4 * 2 * E_BUF;
-// barriers: full[4], empty[4], acc_full[2], acc_empty[2], rbar[4][2], drain[1]
-constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 8 + 1;
+constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_STAGE;
+// barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain[1]
+constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 1;
 constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
 constexpr uint32_t MAIN_SMEM = OFF_HOLD + 16 + 1024;  // + alignment slack
 constexpr uint32_t TMEM_COLS = 2 * BN;
@@ -177,19 +203,38 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 struct MainArgs {
     int M, N, K;
     int tiles_m, tiles_n;
+    int full_units;      // tiles processed whole; each later tile is split into two 128-wide halves
+    int units;           // full_units + 2 * (tiles - full_units)
     int epi;             // last stage applied in this kernel: 0 (C), 1 (C'), 2 (C''), 3 (Y)
     const __half* bias;
+    const __half* R;
+    __half* Y;
     int* flag;
 };
 
-__device__ __forceinline__ void tile_coords(int t, int tiles_m, int& m0, int& n0) {
-    m0 = (t % tiles_m) * BM;
-    n0 = (t / tiles_m) * BN;
+// Work unit u -> output rows [m0, m0+128), columns [n0, n0+bn).  The first full_units units are
+// whole 128 x 256 tiles; the tiles of the last, partial wave are split into 128 x 128 halves so
+// that the wave is spread over more SMs (wave quantisation: 512 tiles on 152 SMs would otherwise
+// leave a third of the SMs idle for the last tile time).
+struct Unit {
+    int m0, n0, bn;
+};
+__device__ __forceinline__ Unit unit_of(int u, const MainArgs& a) {
+    Unit r;
+    int t = u;
+    int half = -1;
+    if (u >= a.full_units) {
+        t = a.full_units + (u - a.full_units) / 2;
+        half = (u - a.full_units) % 2;
+    }
+    r.m0 = (t % a.tiles_m) * BM;
+    r.n0 = (t / a.tiles_m) * BN + (half > 0 ? BN / 2 : 0);
+    r.bn = half < 0 ? BN : BN / 2;
+    return r;
 }
 
 __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-    const __grid_constant__ CUtensorMap mapR, const __grid_constant__ CUtensorMap mapY,
     const __grid_constant__ MainArgs args) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -200,10 +245,9 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    auto r_bar = [&](int ew, int j) { return bar0 + 8u * (2 * STAGES + 4 + 2 * ew + j); };
     const uint32_t drain_bar = bar0 + 8u * (N_BARS - 1);
     const uint32_t holder = base + OFF_HOLD;
-    const int total_tiles = args.tiles_m * args.tiles_n;
+    const int total_units = args.units;
     const int nk = (args.K + BK - 1) / BK;
     int* flag = args.flag;
 
@@ -214,16 +258,12 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);
+            mbar_init(acce_bar(b), kEpiWarps);
         }
-        for (int ew = 0; ew < 4; ++ew)
-            for (int j = 0; j < 2; ++j) mbar_init(r_bar(ew, j), 1);
         mbar_init(drain_bar, 1);
         fence_mbar_init();
         prefetch_map(&mapA);
         prefetch_map(&mapB);
-        prefetch_map(&mapR);
-        prefetch_map(&mapY);
     }
     if (warp == 1) tmem_alloc(holder, TMEM_COLS);
     tc_fence_before();
@@ -236,18 +276,16 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         int stage = 0;
         uint32_t phase = 0, inflight = 0, issue_par = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            int m0, n0;
-            tile_coords(t, args.tiles_m, m0, n0);
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const Unit w = unit_of(u, args);
             for (int kb = 0; kb < nk; ++kb) {
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
                 inflight &= ~(1u << stage);  // its previous load was consumed
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(full_bar(stage), A_STAGE + B_STAGE);
-                    tma_load_2d(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, m0, full_bar(stage));
-#pragma unroll
-                    for (int j = 0; j < BN / 64; ++j)
-                        tma_load_2d(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB, n0 + 64 * j,
+                    mbar_arrive_expect_tx(full_bar(stage), A_STAGE + (w.bn / 64) * B_BOX);
+                    tma_load_2d(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, w.m0, full_bar(stage));
+                    for (int j = 0; j < w.bn / 64; ++j)
+                        tma_load_2d(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB, w.n0 + 64 * j,
                                     kb * BK, full_bar(stage));
                 }
                 inflight |= 1u << stage;
@@ -261,11 +299,13 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc = idesc_f16(BM, BN, false, true);
+        constexpr uint32_t idesc_full = idesc_f16(BM, BN, false, true);
+        constexpr uint32_t idesc_half = idesc_f16(BM, BN / 2, false, true);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true, issued = false;
-        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const uint32_t idesc = unit_of(u, args).bn == BN ? idesc_full : idesc_half;
             if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
@@ -301,93 +341,73 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
             (void)mbar_wait_bounded(drain_bar, 0, flag, kWaitBudget / 8);
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2-5)
-        const int q = warp % 4;            // TMEM lane quadrant: rows 32q..32q+31 of the tile
-        const int ew = warp - 2;           // index of this warp's buffers
-        const uint32_t ebuf0 = base + OFF_E + ew * 2 * E_BUF;
-        uint8_t* gebuf0 = gbase + OFF_E + ew * 2 * E_BUF;
+        // ------------------------------------------------------------ epilogue (warps 2-9)
+        // Warp w drains TMEM lane quadrant q = w % 4 (rows 32q..32q+31 of the unit) and one half
+        // of the unit's 32-column chunks.  Each thread owns one row: it prefetches its residual
+        // row segment for the next chunk into registers while it computes the current one, and
+        // writes its 32 fp16 results with 16-byte stores straight from registers (no shared
+        // memory staging, so no store read-back or load round trip sits between chunks).
+        constexpr int CH = 32;
+        const int q = warp % 4;
+        const int h = (warp - 2) / 4;
         const bool need_r = args.epi >= 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        int g = 0;  // chunk counter of this warp (4 per tile)
         bool ok = true;
-        auto issue_r = [&](int gi, int t) {  // residual chunk gi (of tile t) -> buffer gi % 2
-            int m0, n0;
-            tile_coords(t, args.tiles_m, m0, n0);
-            const int c = gi % 4;
-            mbar_arrive_expect_tx(r_bar(ew, gi % 2), E_BUF);
-            tma_load_2d(ebuf0 + (gi % 2) * E_BUF, &mapR, n0 + 64 * c, m0 + 32 * q, r_bar(ew, gi % 2));
+        uint4 rnext[CH / 8];
+        auto load_r = [&](int u, int cc) {  // this thread's residual segment of chunk cc of unit u
+            const Unit w = unit_of(u, args);
+            const int per = (w.bn / CH) / 2;
+            const int row = w.m0 + 32 * q + lane;
+            const int col = w.n0 + CH * (h * per + cc);
+#pragma unroll
+            for (int j = 0; j < CH / 8; ++j) {
+                rnext[j] = make_uint4(0, 0, 0, 0);
+                if (row < args.M && col + 8 * j < args.N)
+                    rnext[j] = __ldcs(reinterpret_cast<const uint4*>(args.R + static_cast<int64_t>(row) * args.N + col + 8 * j));
+            }
         };
-        uint32_t r_inflight = 0, r_par = 0;  // per buffer: a residual load in flight / its parity
-        auto note_r = [&](int gi) {
-            r_inflight |= 1u << (gi % 2);
-            r_par = (r_par & ~(1u << (gi % 2))) | (static_cast<uint32_t>((gi / 2) & 1) << (gi % 2));
-        };
-        if (need_r && static_cast<int>(blockIdx.x) < total_tiles) {
-            if (lane == 0) issue_r(0, blockIdx.x);
-            note_r(0);
-        }
-        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
-            int m0, n0;
-            tile_coords(t, args.tiles_m, m0, n0);
+        if (need_r && static_cast<int>(blockIdx.x) < total_units) load_r(blockIdx.x, 0);
+        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
+            const Unit w = unit_of(u, args);
+            const int per = (w.bn / CH) / 2;   // chunks of this warp: 4 (full unit) or 2 (half)
             if (!mbar_wait_bounded(accf_bar(acc), acc_phase, flag)) { ok = false; break; }
             tc_fence_after();
-            for (int c = 0; c < BN / 64; ++c, ++g) {
-                const int buf = g % 2;
-                // next chunk's residual into the other buffer, once the store that last used it
-                // has finished reading it
-                const bool has_next = (c + 1 < BN / 64) || (t + static_cast<int>(gridDim.x) < total_tiles);
-                if (lane == 0) bulk_wait_read0();
-                __syncwarp();
-                if (need_r && has_next) {
-                    if (lane == 0) issue_r(g + 1, c + 1 < BN / 64 ? t : t + static_cast<int>(gridDim.x));
-                    note_r(g + 1);
+            const int row = w.m0 + 32 * q + lane;
+            for (int cc = 0; cc < per; ++cc) {
+                const int c = h * per + cc;
+                uint4 rcur[CH / 8];
+#pragma unroll
+                for (int j = 0; j < CH / 8; ++j) rcur[j] = rnext[j];
+                if (need_r) {  // next chunk of this warp: same unit, or the first of the next unit
+                    if (cc + 1 < per) load_r(u, cc + 1);
+                    else if (u + static_cast<int>(gridDim.x) < total_units) load_r(u + gridDim.x, 0);
                 }
-                float v[64];
-                const uint32_t tcol = tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + 64 * c;
-                tmem_ld32(tcol, v);
-                tmem_ld32(tcol + 32, v + 32);
+                float v[CH];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c, v);
                 tmem_ld_wait();
-                if (c == BN / 64 - 1) {  // the accumulator buffer is drained: hand it back
+                if (cc == per - 1) {  // this warp is done with the accumulator buffer
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(acce_bar(acc));
                 }
-                if (need_r) {
-                    if (!mbar_wait_bounded(r_bar(ew, buf), (g / 2) & 1, flag)) { ok = false; break; }
-                    r_inflight &= ~(1u << buf);
-                }
-                // row `lane` of this warp's 32 rows; its 64 columns are 8 swizzled 16 B chunks
-                uint8_t* rowp = gebuf0 + buf * E_BUF + lane * 128;
-                const int ncol0 = n0 + 64 * c;
+                const int ncol0 = w.n0 + CH * c;
+                __half* yrow = args.Y + static_cast<int64_t>(row) * args.N + ncol0;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
+                for (int j = 0; j < CH / 8; ++j) {
                     float bv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    if (args.epi >= 1 && ncol0 + 8 * j < args.N)
+                    const bool in_n = ncol0 + 8 * j < args.N;
+                    if (args.epi >= 1 && in_n)
                         unpack_h8(__ldg(reinterpret_cast<const uint4*>(args.bias + ncol0 + 8 * j)), bv);
-                    uint4* chunk = reinterpret_cast<uint4*>(rowp + 16 * (j ^ (lane & 7)));
                     float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    if (need_r) unpack_h8(*chunk, rv);
+                    if (need_r) unpack_h8(rcur[j], rv);
                     float o[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) o[e] = apply_stages(v[8 * j + e], 1, args.epi, bv[e], rv[e]);
-                    *chunk = pack_h8(o);
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&mapY, ncol0, m0 + 32 * q, ebuf0 + buf * E_BUF);
-                    bulk_commit();
+                    if (row < args.M && in_n) __stcs(reinterpret_cast<uint4*>(yrow + 8 * j), pack_h8(o));
                 }
             }
-            if (!ok) break;
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-        }
-        if (lane == 0) bulk_wait0();
-        if (!ok) {
-            for (int j = 0; j < 2; ++j)
-                if ((r_inflight >> j) & 1u)
-                    (void)mbar_wait_bounded(r_bar(ew, j), (r_par >> j) & 1u, flag, kWaitBudget / 8);
         }
         __syncwarp();
     }
@@ -686,10 +706,7 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
         if (NM == 32) return launch_decode<32>(mA, mB, a, st);
         return launch_decode<64>(mA, mB, a, st);
     }
-    CUtensorMap mR, mY;
-    if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64) ||
-        !make_map(&mR, epi >= 3 ? R : Y, M, N, 64, 32) || !make_map(&mY, Y, M, N, 64, 32))
-        return FUSE_ECUDA;
+    if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
     static const bool attr = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                   static_cast<int>(MAIN_SMEM)) == cudaSuccess;
     if (!attr) return check_launch();
@@ -701,10 +718,16 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     a.tiles_n = static_cast<int>(ceil_div(N, BN));
     a.epi = epi;
     a.bias = static_cast<const __half*>(bias);
+    a.R = static_cast<const __half*>(R);
+    a.Y = static_cast<__half*>(Y);
     a.flag = flag;
     const int tiles = a.tiles_m * a.tiles_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
-    gemm_tc_kernel<<<grid, kMainThreads, MAIN_SMEM, st>>>(mA, mB, mR, mY, a);
+    // split the last, partial wave into half tiles when the halves still fit in one wave
+    const int tail = tiles % grid;
+    a.full_units = (tail != 0 && 2 * tail <= grid) ? tiles - tail : tiles;
+    a.units = a.full_units + 2 * (tiles - a.full_units);
+    gemm_tc_kernel<<<grid, kMainThreads, MAIN_SMEM, st>>>(mA, mB, a);
     return check_launch();
 }
 

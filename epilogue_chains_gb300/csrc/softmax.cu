@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kSmBlock) softmax_fused_generic_kernel(
 
 // ------------------------------------------------------------------------- unfused kernels
 // (1) m = rowmax(scale*s)  (2) d = bf16(scale*s - m), -inf where j > i  (3) e = bf16(exp d)
-// (4) l = rowsum(e)        (5) p = bf16(e / l)
+// (4) l = rowsum(e)        (5) p = bf16(e * (1/l))
 // Step 2 folds scale and mask into the subtraction, so no mask tensor exists ([OFCG] [A3] notes
 // that a materialised mask would add another full copy of the score tensor).  Every step streams
 // whole rows with 32-byte vectors when S % 16 == 0 and the tensors are 32-byte aligned.
@@ -398,20 +398,20 @@ __global__ void __launch_bounds__(kEwBlock) sm_div_kernel(__nv_bfloat16* __restr
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (VEC) {
         if (g >= n / 16) return;
-        const float lr = __ldg(l + g / (S / 16));
+        const float inv = __frcp_rn(__ldg(l + g / (S / 16)));  // one reciprocal per vector
         uint32_t w[8];
         ld32(e + 16 * g, w);
         float f[16];
         unpack16(w, f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(__fdiv_rn(f[2 * k], lr), __fdiv_rn(f[2 * k + 1], lr));
+            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(f[2 * k], inv), __fmul_rn(f[2 * k + 1], inv));
             w[k] = *reinterpret_cast<uint32_t*>(&h);
         }
         st32(e + 16 * g, w);
         return;
     }
-    if (g < n) e[g] = __float2bfloat16_rn(__fdiv_rn(__bfloat162float(e[g]), __ldg(l + g / S)));
+    if (g < n) e[g] = __float2bfloat16_rn(__fmul_rn(__bfloat162float(e[g]), __frcp_rn(__ldg(l + g / S))));
 }
 
 unsigned grid_for(int64_t units, int block) {

@@ -104,6 +104,31 @@ def test_ragged_shapes(cuda_device, shape, mask):
     _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
 
 
+@pytest.mark.parametrize("shape", [(2560, 2048, 128), (2500, 2040, 200)])
+@pytest.mark.parametrize("mask", [0, 7])
+def test_last_wave_split_into_half_tiles(cuda_device, shape, mask):
+    """160 tiles on 152 SMs: the last 8 tiles run as 16 half tiles (128 x 128 units)."""
+    A, B, bias, R = wl.gemm_input(*shape, salt=9, std=1.0 / 8.0)
+    _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+@pytest.mark.parametrize("M", [16, 256])
+def test_gelu_over_a_wide_range(cuda_device, M):
+    """B = I (K = N) makes acc = A exactly; A spans [-10, 10] (exact fp16 values), bias = R = 0,
+    so Y = fp16(GELU(A)) tests the epilogue's GELU itself, including the far negative tail where
+    1 + erf(v/sqrt2) is tiny, against the oracle at 2 ulps."""
+    N = 256
+    g = np.random.default_rng(10)
+    vals = np.concatenate([np.linspace(-10, 10, M * N // 2), g.uniform(-6, 3, M * N - M * N // 2)])
+    A = vals.reshape(M, N).astype(np.float16).view(np.uint16)
+    B = np.eye(N).astype(np.float16).view(np.uint16)
+    z = np.zeros(N, np.uint16)
+    R = np.zeros((M, N), np.uint16)
+    y = _run(A, B, z, R, 0).view(np.float16).astype(np.float64)
+    ref = oracle.gemm_epilogue(A, B, z, R, 0).view(np.float16).astype(np.float64)
+    assert np.all(np.abs(y - ref) <= 2 * _ulp16(ref) + 2.0 ** -24), float(np.abs(y - ref).max())
+
+
 @pytest.mark.parametrize("mask", range(8))
 def test_every_cut_mask(cuda_device, mask):
     A, B, bias, R = wl.gemm_input(256, 512, 512, salt=4, std=1.0 / 8.0)
