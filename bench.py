@@ -447,6 +447,31 @@ def run_ours(args, rank, world, local):
         gm["M16"]["roofline"] = roofline_of("gemm_M16_fused")
         rows["gemm_epilogue"] = gm
 
+    # same-size copy reference: cudaMemcpy D2D of one chain operand (64 MiB) -- the practical roof
+    # for a 2 x 64 MiB streaming kernel at this size (the measured peak is a 2 GiB copy)
+    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    with torch.cuda.stream(stream):
+        for i in range(5):
+            ys[i % R].copy_(xs[(i + 1) % R])
+        for i, (e0, e1) in enumerate(cev):
+            e0.record(stream)
+            ys[i % R].copy_(xs[(i + 1) % R])
+            e1.record(stream)
+    torch.cuda.synchronize()
+    copy_us = float(np.median([e0.elapsed_time(e1) for e0, e1 in cev])) * 1e3
+    rows["chain"]["copy_reference"] = {"us": round(copy_us, 2),
+                                       "GBs": round(chain_bytes / copy_us / 1e3, 1),
+                                       "what": "cudaMemcpy D2D of 64 MiB, same rotation"}
+
+    # register / occupancy report of every kernel variant ([K4] §③, [C05] §6.2)
+    report_rows = []
+    for i in range(fc.fuse_kernel_count()):
+        r_ = fc.fuse_kernel_report(i)
+        report_rows.append({k: r_[k] for k in ("name", "regs_per_thread", "local_bytes_per_thread",
+                                               "dynamic_smem_bytes", "block_threads", "blocks_per_sm",
+                                               "cluster_size", "max_active_clusters")})
+    rows["kernel_report"] = report_rows
+
     # ---------------------------------------------------------------- e2e through host buffers
     e2e = run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world)
     if world > 1:

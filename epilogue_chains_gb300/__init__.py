@@ -46,7 +46,8 @@ class fuse_kernel_record(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 64), ("regs_per_thread", ctypes.c_int32),
                 ("local_bytes_per_thread", ctypes.c_int32), ("static_smem_bytes", ctypes.c_int32),
                 ("dynamic_smem_bytes", ctypes.c_int32), ("block_threads", ctypes.c_int32),
-                ("blocks_per_sm", ctypes.c_int32), ("max_threads_per_block", ctypes.c_int32)]
+                ("blocks_per_sm", ctypes.c_int32), ("max_threads_per_block", ctypes.c_int32),
+                ("cluster_size", ctypes.c_int32), ("max_active_clusters", ctypes.c_int32)]
 
 
 _P, _I32, _I64, _U32, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,

@@ -68,6 +68,8 @@ int describe_kernel(const void* kernel, const char* name, int block, int dyn_sme
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, dyn_smem);
     if (e != cudaSuccess) return record_cuda_error(e);
     out->blocks_per_sm = b;
+    out->cluster_size = 1;
+    out->max_active_clusters = 0;
     return FUSE_OK;
 }
 

@@ -43,6 +43,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
         : "memory");
 }
+// Multicast: the box lands at the same shared-memory offset in every CTA of `mask` and completes
+// bytes on the mbarrier at the same offset in each of them.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                               uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "h"(mask)
+        : "memory");
+}
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int y, uint32_t src) {
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];"
                  ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(src)
@@ -80,6 +90,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
 }
+// as tc_commit, arriving on the mbarrier at the same offset in every CTA of `mask`
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(bar), "h"(mask)
+        : "memory");
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(
@@ -108,6 +125,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05): 128B swizzle, start/leading/stride in 16 B units.
 __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -133,35 +159,54 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn_major, 
 // is tiny).  erfc(z), z >= 0, is the Chebyshev-fitted approximation "erfcc" of Press, Teukolsky,
 // Vetterling & Flannery, Numerical Recipes (2nd ed., §6.2): erfc(z) = t exp(-z^2 + P(t)),
 // t = 1/(1 + z/2), fractional error below 1.2e-7 for every z >= 0 -- far below the fp16 output
-// resolution.  Cost: one reciprocal, one ex2 and nine FMAs.
+// resolution.  Cost per element: one reciprocal and one ex2 (MUFU), the rest in packed fp32x2
+// instructions (sm_100+), which evaluate two elements per instruction.
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ float erfc_nonneg(float z) {
-    const float t = __frcp_rn(fmaf(0.5f, z, 1.0f));
-    float p = 0.17087277f;
-    p = fmaf(p, t, -0.82215223f);
-    p = fmaf(p, t, 1.48851587f);
-    p = fmaf(p, t, -1.13520398f);
-    p = fmaf(p, t, 0.27886807f);
-    p = fmaf(p, t, -0.18628806f);
-    p = fmaf(p, t, 0.09678418f);
-    p = fmaf(p, t, 0.37409196f);
-    p = fmaf(p, t, 1.00002368f);
-    p = fmaf(p, t, -1.26551223f);
-    return t * ex2_approx((p - z * z) * 1.44269504088896341f);
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
-__device__ __forceinline__ float gelu_erf(float v) {
-    const float e = erfc_nonneg(fabsf(v) * 0.70710678118654752f);
-    return 0.5f * v * (v >= 0.0f ? 2.0f - e : e);
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+
+// GELU of two values at once
+__device__ __forceinline__ float2 gelu_erf2(float2 v) {
+    const float2 z = __fmul2_rn(make_float2(fabsf(v.x), fabsf(v.y)), f2(0.70710678118654752f));
+    const float2 d = __ffma2_rn(f2(0.5f), z, f2(1.0f));
+    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    float2 p = f2(0.17087277f);
+    p = __ffma2_rn(p, t, f2(-0.82215223f));
+    p = __ffma2_rn(p, t, f2(1.48851587f));
+    p = __ffma2_rn(p, t, f2(-1.13520398f));
+    p = __ffma2_rn(p, t, f2(0.27886807f));
+    p = __ffma2_rn(p, t, f2(-0.18628806f));
+    p = __ffma2_rn(p, t, f2(0.09678418f));
+    p = __ffma2_rn(p, t, f2(0.37409196f));
+    p = __ffma2_rn(p, t, f2(1.00002368f));
+    p = __ffma2_rn(p, t, f2(-1.26551223f));
+    const float2 a = __fmul2_rn(__ffma2_rn(make_float2(-z.x, -z.y), z, p), f2(1.44269504088896341f));
+    const float2 e = __fmul2_rn(t, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
+    const float2 s = make_float2(v.x >= 0.0f ? 2.0f - e.x : e.x, v.y >= 0.0f ? 2.0f - e.y : e.y);
+    return __fmul2_rn(__fmul2_rn(f2(0.5f), v), s);
 }
+__device__ __forceinline__ float gelu_erf(float v) { return gelu_erf2(make_float2(v, v)).x; }
+
 // apply stages first..last (inclusive, 1..3) to v
 __device__ __forceinline__ float apply_stages(float v, int first, int last, float b, float r) {
     if (first <= 1 && last >= 1) v += b;
     if (first <= 2 && last >= 2) v = gelu_erf(v);
     if (first <= 3 && last >= 3) v += r;
+    return v;
+}
+// the same on two values
+__device__ __forceinline__ float2 apply_stages2(float2 v, int first, int last, float2 b, float2 r) {
+    if (first <= 1 && last >= 1) v = __fadd2_rn(v, b);
+    if (first <= 2 && last >= 2) v = gelu_erf2(v);
+    if (first <= 3 && last >= 3) v = __fadd2_rn(v, r);
     return v;
 }
 
@@ -202,9 +247,10 @@ constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct MainArgs {
     int M, N, K;
-    int tiles_m, tiles_n;
-    int full_units;      // tiles processed whole; each later tile is split into two 128-wide halves
-    int units;           // full_units + 2 * (tiles - full_units)
+    int pair_rows;       // ceil(tiles_m / 2): a CTA pair covers two adjacent 128-row tiles
+    int tiles_n;
+    int full_units;      // pair tiles processed whole; each later one is split into 128-wide halves
+    int units;           // full_units + 2 * (pair tiles - full_units)
     int epi;             // last stage applied in this kernel: 0 (C), 1 (C'), 2 (C''), 3 (Y)
     const __half* bias;
     const __half* R;
@@ -212,14 +258,15 @@ struct MainArgs {
     int* flag;
 };
 
-// Work unit u -> output rows [m0, m0+128), columns [n0, n0+bn).  The first full_units units are
-// whole 128 x 256 tiles; the tiles of the last, partial wave are split into 128 x 128 halves so
-// that the wave is spread over more SMs (wave quantisation: 512 tiles on 152 SMs would otherwise
-// leave a third of the SMs idle for the last tile time).
+// Work unit u of a CTA pair -> output rows [m0, m0+128) of this CTA (rank r of the pair takes the
+// r-th of two adjacent 128-row tiles), columns [n0, n0+bn) shared by the pair.  The first
+// full_units units are whole 256-wide pair tiles; the pair tiles of the last, partial wave are
+// split into 128-wide halves so that the wave spreads over more SMs (wave quantisation: 256 pair
+// tiles on 76 pairs would otherwise leave a third of the SMs idle for the last tile time).
 struct Unit {
     int m0, n0, bn;
 };
-__device__ __forceinline__ Unit unit_of(int u, const MainArgs& a) {
+__device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank) {
     Unit r;
     int t = u;
     int half = -1;
@@ -227,8 +274,8 @@ __device__ __forceinline__ Unit unit_of(int u, const MainArgs& a) {
         t = a.full_units + (u - a.full_units) / 2;
         half = (u - a.full_units) % 2;
     }
-    r.m0 = (t % a.tiles_m) * BM;
-    r.n0 = (t / a.tiles_m) * BN + (half > 0 ? BN / 2 : 0);
+    r.m0 = (2 * (t % a.pair_rows) + static_cast<int>(rank)) * BM;
+    r.n0 = (t / a.pair_rows) * BN + (half > 0 ? BN / 2 : 0);
     r.bn = half < 0 ? BN : BN / 2;
     return r;
 }
@@ -250,11 +297,17 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const int total_units = args.units;
     const int nk = (args.K + BK - 1) / BK;
     int* flag = args.flag;
+    const uint32_t rank = cluster_rank();
+    const int cid = blockIdx.x / 2;            // CTA pair (cluster) index
+    const int nclusters = gridDim.x / 2;
+    // k-blocks this pair runs in all (both CTAs run the same sequence)
+    const int my_units = cid < total_units ? (total_units - cid + nclusters - 1) / nclusters : 0;
+    const int total_kb = my_units * nk;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), 2);  // freed by the MMAs of both CTAs of the pair
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
@@ -267,7 +320,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     }
     if (warp == 1) tmem_alloc(holder, TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before either multicasts into the other
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_HOLD);
 
@@ -276,17 +329,20 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         int stage = 0;
         uint32_t phase = 0, inflight = 0, issue_par = 0;
         bool ok = true;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const Unit w = unit_of(u, args);
+        for (int u = cid; u < total_units && ok; u += nclusters) {
+            const Unit w = unit_of(u, args, rank);
             for (int kb = 0; kb < nk; ++kb) {
+                // the stage is free in both CTAs (each MMA commit arrives on both empty barriers)
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
                 inflight &= ~(1u << stage);  // its previous load was consumed
                 if (lane == 0) {
+                    // this CTA's A rows; the pair's B tile is fetched once from L2: each CTA
+                    // multicasts every other 64-column box into both CTAs' shared memory
                     mbar_arrive_expect_tx(full_bar(stage), A_STAGE + (w.bn / 64) * B_BOX);
                     tma_load_2d(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, w.m0, full_bar(stage));
-                    for (int j = 0; j < w.bn / 64; ++j)
-                        tma_load_2d(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB, w.n0 + 64 * j,
-                                    kb * BK, full_bar(stage));
+                    for (int j = static_cast<int>(rank); j < w.bn / 64; j += 2)
+                        tma_load_2d_mc(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB, w.n0 + 64 * j,
+                                       kb * BK, full_bar(stage), 0x3);
                 }
                 inflight |= 1u << stage;
                 issue_par = (issue_par & ~(1u << stage)) | (phase << stage);
@@ -304,8 +360,9 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true, issued = false;
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const uint32_t idesc = unit_of(u, args).bn == BN ? idesc_full : idesc_half;
+        int kg = 0;  // k-blocks issued so far by this CTA (the same sequence in both CTAs)
+        for (int u = cid; u < total_units && ok; u += nclusters) {
+            const uint32_t idesc = unit_of(u, args, rank).bn == BN ? idesc_full : idesc_half;
             if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
@@ -324,8 +381,11 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                         const uint64_t bd = smem_desc_sw128(b0 + 2048u * k, B_BOX, 1024u);
                         tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
-                    tc_commit(empty_bar(stage));  // frees the stage once these MMAs are done
+                    // frees the stage in both CTAs once these MMAs are done -- unless no later load
+                    // uses it (then nothing may arrive after the peer could have left)
+                    if (kg + STAGES < total_kb) tc_commit_mc(empty_bar(stage), 0x3);
                 }
+                ++kg;
                 issued = true;
                 __syncwarp();
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -356,7 +416,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         bool ok = true;
         uint4 rnext[CH / 8];
         auto load_r = [&](int u, int cc) {  // this thread's residual segment of chunk cc of unit u
-            const Unit w = unit_of(u, args);
+            const Unit w = unit_of(u, args, rank);
             const int per = (w.bn / CH) / 2;
             const int row = w.m0 + 32 * q + lane;
             const int col = w.n0 + CH * (h * per + cc);
@@ -367,9 +427,9 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                     rnext[j] = __ldcs(reinterpret_cast<const uint4*>(args.R + static_cast<int64_t>(row) * args.N + col + 8 * j));
             }
         };
-        if (need_r && static_cast<int>(blockIdx.x) < total_units) load_r(blockIdx.x, 0);
-        for (int u = blockIdx.x; u < total_units && ok; u += gridDim.x) {
-            const Unit w = unit_of(u, args);
+        if (need_r && cid < total_units) load_r(cid, 0);
+        for (int u = cid; u < total_units && ok; u += nclusters) {
+            const Unit w = unit_of(u, args, rank);
             const int per = (w.bn / CH) / 2;   // chunks of this warp: 4 (full unit) or 2 (half)
             if (!mbar_wait_bounded(accf_bar(acc), acc_phase, flag)) { ok = false; break; }
             tc_fence_after();
@@ -381,7 +441,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                 for (int j = 0; j < CH / 8; ++j) rcur[j] = rnext[j];
                 if (need_r) {  // next chunk of this warp: same unit, or the first of the next unit
                     if (cc + 1 < per) load_r(u, cc + 1);
-                    else if (u + static_cast<int>(gridDim.x) < total_units) load_r(u + gridDim.x, 0);
+                    else if (u + nclusters < total_units) load_r(u + nclusters, 0);
                 }
                 float v[CH];
                 tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c, v);
@@ -403,7 +463,12 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                     if (need_r) unpack_h8(rcur[j], rv);
                     float o[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) o[e] = apply_stages(v[8 * j + e], 1, args.epi, bv[e], rv[e]);
+                    for (int e = 0; e < 8; e += 2) {
+                        const float2 r2 = apply_stages2(make_float2(v[8 * j + e], v[8 * j + e + 1]), 1, args.epi,
+                                                        make_float2(bv[e], bv[e + 1]), make_float2(rv[e], rv[e + 1]));
+                        o[e] = r2.x;
+                        o[e + 1] = r2.y;
+                    }
                     if (row < args.M && in_n) __stcs(reinterpret_cast<uint4*>(yrow + 8 * j), pack_h8(o));
                 }
             }
@@ -412,7 +477,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         __syncwarp();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();  // neither CTA leaves while its peer may still write into its shared memory
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
 }
@@ -447,14 +512,6 @@ struct DecodeLayout {
     static constexpr uint32_t TCOLS = NM <= 32 ? 32 : 64;
 };
 
-__device__ __forceinline__ uint32_t cluster_rank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
 __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
     uint32_t remote;
     float v;
@@ -682,6 +739,45 @@ int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs
     return check_launch();
 }
 
+bool main_attr_ok() {
+    static const bool ok = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                static_cast<int>(MAIN_SMEM)) == cudaSuccess;
+    return ok;
+}
+
+// 2-CTA clusters that can be resident at once (a cluster needs both its CTAs in one GPC, so an
+// odd SM count in a GPC leaves an SM out); persistent launches use exactly this many.
+int max_active_pairs() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        (void)cudaGetLastError();
+        return sm_count() / 2;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0 && main_attr_ok()) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
+        cfg.blockDim = dim3(kMainThreads);
+        cfg.dynamicSmemBytes = MAIN_SMEM;
+        cudaLaunchAttribute attrs[1];
+        attrs[0].id = cudaLaunchAttributeClusterDimension;
+        attrs[0].val.clusterDim.x = 2;
+        attrs[0].val.clusterDim.y = 1;
+        attrs[0].val.clusterDim.z = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = sm_count() / 2;
+        }
+        cached[dev] = n;
+    }
+    return cached[dev] > 0 ? cached[dev] : sm_count() / 2;
+}
+
 // GEMM + the stages 1..epi, fp16 result into Y
 int launch_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
                 int64_t N, int64_t K, int epi, cudaStream_t st) {
@@ -707,27 +803,39 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
         return launch_decode<64>(mA, mB, a, st);
     }
     if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
-    static const bool attr = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(MAIN_SMEM)) == cudaSuccess;
-    if (!attr) return check_launch();
+    if (!main_attr_ok()) return check_launch();
     MainArgs a;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
     a.K = static_cast<int>(K);
-    a.tiles_m = static_cast<int>(ceil_div(M, BM));
+    a.pair_rows = static_cast<int>(ceil_div(ceil_div(M, BM), 2));
     a.tiles_n = static_cast<int>(ceil_div(N, BN));
     a.epi = epi;
     a.bias = static_cast<const __half*>(bias);
     a.R = static_cast<const __half*>(R);
     a.Y = static_cast<__half*>(Y);
     a.flag = flag;
-    const int tiles = a.tiles_m * a.tiles_n;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
+    const int tiles = a.pair_rows * a.tiles_n;             // pair tiles (256 rows x 256 cols)
+    const int pairs = max_active_pairs();
+    const int clusters = tiles < pairs ? tiles : pairs;
     // split the last, partial wave into half tiles when the halves still fit in one wave
-    const int tail = tiles % grid;
-    a.full_units = (tail != 0 && 2 * tail <= grid) ? tiles - tail : tiles;
+    const int tail = tiles % clusters;
+    a.full_units = (tail != 0 && 2 * tail <= clusters) ? tiles - tail : tiles;
     a.units = a.full_units + 2 * (tiles - a.full_units);
-    gemm_tc_kernel<<<grid, kMainThreads, MAIN_SMEM, st>>>(mA, mB, a);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(kMainThreads);
+    cfg.dynamicSmemBytes = MAIN_SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = 2;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mA, mB, a);
+    if (e != cudaSuccess) return record_cuda_error(e);
     return check_launch();
 }
 
@@ -745,11 +853,24 @@ int launch_tail(void* Y, const void* bias, const void* R, int64_t M, int64_t N, 
 int gemm_report_count() { return 3; }
 int gemm_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)gemm_tc_kernel, "gemm_tc_kernel (128x256 tcgen05)",
-                                       kMainThreads, static_cast<int>(MAIN_SMEM), out);
-        case 1: return describe_kernel((const void*)gemm_decode_kernel<16>,
-                                       "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
-                                       static_cast<int>(DecodeLayout<16>::SMEM), out);
+        case 0: {
+            if (!main_attr_ok()) return check_launch();
+            const int rc = describe_kernel((const void*)gemm_tc_kernel,
+                                           "gemm_tc_kernel (2-CTA cluster, 128x256 tcgen05)",
+                                           kMainThreads, static_cast<int>(MAIN_SMEM), out);
+            if (rc == FUSE_OK) {
+                out->cluster_size = 2;
+                out->max_active_clusters = max_active_pairs();
+            }
+            return rc;
+        }
+        case 1: {
+            const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
+                                           "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
+                                           static_cast<int>(DecodeLayout<16>::SMEM), out);
+            if (rc == FUSE_OK) out->cluster_size = DEC_SPLIT;
+            return rc;
+        }
         case 2: return describe_kernel((const void*)epi_tail_kernel, "epi_tail_kernel (unfused plans)", 256, 0, out);
         default: return FUSE_EINVAL;
     }

@@ -239,6 +239,8 @@ typedef struct {
     int32_t block_threads;            /* as launched                                            */
     int32_t blocks_per_sm;            /* occupancy API at that block size and smem              */
     int32_t max_threads_per_block;
+    int32_t cluster_size;             /* CTAs per thread-block cluster as launched (1 = none)    */
+    int32_t max_active_clusters;      /* clusters resident at once on the GPU (0 if no cluster)  */
 } fuse_kernel_record;
 
 /* Number of kernel variants fuse_kernel_report() knows (index 0 .. count-1). */
