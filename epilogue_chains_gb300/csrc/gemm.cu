@@ -485,7 +485,6 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
 // =============================================================================== decode kernel
 // Y^T[N, M] = B^T[N, K] A^T[K, M] for M <= 64: MMA M = 128 rows of N, MMA N = NM >= M.
 constexpr int DEC_SPLIT = 8;    // K split = cluster size
-constexpr int DEC_STAGES = 4;
 constexpr int kDecThreads = 128;
 constexpr uint32_t DEC_BT_STAGE = 128 * BK * 2;  // 16 KB: two 64-wide N boxes
 
@@ -501,12 +500,13 @@ struct DecodeArgs {
 
 template <int NM>
 struct DecodeLayout {
+    static constexpr int STAGES = NM <= 32 ? 4 : 3;
     static constexpr uint32_t A_ST = NM * BK * 2;
     static constexpr uint32_t OFF_BT = 0;
-    static constexpr uint32_t OFF_AS = OFF_BT + DEC_STAGES * DEC_BT_STAGE;
-    static constexpr uint32_t OFF_P = OFF_AS + DEC_STAGES * A_ST;       // fp32 partial [NM][128]
+    static constexpr uint32_t OFF_AS = OFF_BT + STAGES * DEC_BT_STAGE;
+    static constexpr uint32_t OFF_P = OFF_AS + STAGES * A_ST;           // fp32 partial [NM][128]
     static constexpr uint32_t OFF_BAR = OFF_P + NM * 128 * 4;
-    static constexpr uint32_t N_BARS = 2 * DEC_STAGES + 2;           // full, empty, acc, drain
+    static constexpr uint32_t N_BARS = 2 * STAGES + 2;               // full, empty, acc, drain
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
     static constexpr uint32_t TCOLS = NM <= 32 ? 32 : 64;
@@ -536,15 +536,15 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     const int nk = max(0, min(args.kb_per_split, nk_all - kb0));
     const uint32_t bar0 = base + L::OFF_BAR;
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (DEC_STAGES + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * DEC_STAGES);
+    auto empty_bar = [&](int s) { return bar0 + 8u * (L::STAGES + s); };
+    const uint32_t acc_bar = bar0 + 8u * (2 * L::STAGES);
     const uint32_t drain_bar = acc_bar + 8u;
     const uint32_t holder = base + L::OFF_HOLD;
     float* part = reinterpret_cast<float*>(gbase + L::OFF_P);  // [NM][128]
     int* flag = args.flag;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < DEC_STAGES; ++s) {
+        for (int s = 0; s < L::STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
@@ -576,10 +576,10 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
             }
             inflight |= 1u << stage;
             issue_par = (issue_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == DEC_STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok)
-            for (int s = 0; s < DEC_STAGES; ++s)
+            for (int s = 0; s < L::STAGES; ++s)
                 if ((inflight >> s) & 1u) (void)mbar_wait_bounded(full_bar(s), (issue_par >> s) & 1u, flag, kWaitBudget / 8);
     } else if (warp == 1) {
         constexpr uint32_t idesc = idesc_f16(128, NM, true, false);
@@ -604,7 +604,7 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
             }
             issued = true;
             __syncwarp();
-            if (++stage == DEC_STAGES) { stage = 0; phase ^= 1u; }
+            if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (ok) {
             if (lane == 0) tc_commit(acc_bar);
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     tc_fence_before();
     cluster_sync();  // every CTA of the cluster has its partial in shared memory
 
-    // CTA `rank` reduces output columns [n0 + 16*rank, n0 + 16*rank + 16) for all NM rows
+    // CTA `rank` reduces output columns [n0 + COLS*rank, n0 + COLS*rank + COLS) for all NM rows
     {
         constexpr int COLS = 128 / DEC_SPLIT;  // 16
         const uint32_t part_addr = smem_addr(part);
@@ -719,8 +719,13 @@ bool overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
 template <int NM>
 int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs& a, cudaStream_t st) {
     using L = DecodeLayout<NM>;
-    static const bool attr = cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                  static_cast<int>(L::SMEM)) == cudaSuccess;
+    // all of an SM's shared memory as shared (not L1) lets two decode CTAs share an SM, so the
+    // whole grid (ceil(N/128) x 8 CTAs) is resident in one wave
+    static const bool attr =
+        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(L::SMEM)) == cudaSuccess &&
+        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
     if (!attr) return check_launch();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.N, 128) * DEC_SPLIT));
@@ -865,6 +870,10 @@ int gemm_report(int i, fuse_kernel_record* out) {
             return rc;
         }
         case 1: {
+            (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(DecodeLayout<16>::SMEM));
+            (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
             const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
                                            "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
                                            static_cast<int>(DecodeLayout<16>::SMEM), out);
