@@ -42,6 +42,12 @@ class fuse_ledger_t(ctypes.Structure):
                 ("reg_peak", ctypes.c_int64), ("flops", ctypes.c_int64)]
 
 
+class fuse_cost_model(ctypes.Structure):
+    _fields_ = [("hbm_bytes_per_s", ctypes.c_double), ("flops_per_s", ctypes.c_double),
+                ("launch_s", ctypes.c_double), ("spill_penalty", ctypes.c_double),
+                ("reg_limit", ctypes.c_int32)]
+
+
 class fuse_kernel_record(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 64), ("regs_per_thread", ctypes.c_int32),
                 ("local_bytes_per_thread", ctypes.c_int32), ("static_smem_bytes", ctypes.c_int32),
@@ -64,6 +70,10 @@ SIGNATURES = {
     "fuse_gemm_epilogue_plan": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P], _I32),
     "fuse_gemm_bytes": ([_I64, _I64, _I64, _U32], _I64),
     "fuse_ledger": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_ledger_t)], _I32),
+    "fuse_plan_time": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_cost_model),
+                        ctypes.POINTER(ctypes.c_double)], _I32),
+    "fuse_best_plan": ([ctypes.POINTER(fuse_stage), _I32, _I32, ctypes.POINTER(fuse_cost_model),
+                        ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_double)], _I32),
     "fuse_chain_bytes": ([_I32, _I64, _I32, _I32], _I64),
     "fuse_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
     "fuse_causal_softmax_bytes": ([_I64, _I64, _I32, _I32, _I32], _I64),
@@ -228,6 +238,30 @@ def fuse_ledger(stages, cut_mask: int, elem_bytes: int) -> dict:
     _check(_load().fuse_ledger(st, len(st), cut_mask, elem_bytes, ctypes.byref(out)), "fuse_ledger")
     return {"bytes": out.bytes, "launches": out.launches, "reg_peak": out.reg_peak,
             "flops": out.flops}
+
+
+def _model(model) -> fuse_cost_model:
+    if isinstance(model, fuse_cost_model):
+        return model
+    return fuse_cost_model(**model)
+
+
+def fuse_plan_time(stages, cut_mask: int, elem_bytes: int, model) -> float:
+    """[K4] time_estimate of one cut plan, seconds."""
+    st = _stages(stages)
+    out = ctypes.c_double()
+    _check(_load().fuse_plan_time(st, len(st), cut_mask, elem_bytes, ctypes.byref(_model(model)),
+                                  ctypes.byref(out)), "fuse_plan_time")
+    return out.value
+
+
+def fuse_best_plan(stages, elem_bytes: int, model) -> tuple:
+    """[K4] best_plan: (cut_mask, seconds) of the cheapest of the 2^(K-1) plans."""
+    st = _stages(stages)
+    mask, sec = ctypes.c_uint32(), ctypes.c_double()
+    _check(_load().fuse_best_plan(st, len(st), elem_bytes, ctypes.byref(_model(model)),
+                                  ctypes.byref(mask), ctypes.byref(sec)), "fuse_best_plan")
+    return mask.value, sec.value
 
 
 def fuse_chain_bytes(K: int, n: int, dtype: int, mode: int) -> int:

@@ -219,6 +219,25 @@ typedef struct {
 int fuse_ledger(const fuse_stage* stages, int K, uint32_t cut_mask, int elem_bytes,
                 fuse_ledger_t* out);
 
+/* [K4] §② time_estimate / best_plan: a roofline + launch cost model over cut plans.  For every
+ * kernel of a plan:  t = max(mem, compute) + launch,  mem = bytes / hbm_bytes_per_s (the ledger
+ * bytes above), compute = flops / flops_per_s; when the kernel's live_regs sum exceeds reg_limit
+ * the memory time is multiplied by spill_penalty ([K4] §③).  fuse_plan_time() returns a plan's
+ * total in *seconds; fuse_best_plan() enumerates all 2^(K-1) cut masks and returns the cheapest
+ * (ties go to the lower mask).  Host only, no CUDA call. */
+typedef struct {
+    double hbm_bytes_per_s;
+    double flops_per_s;
+    double launch_s;
+    double spill_penalty;
+    int32_t reg_limit;
+} fuse_cost_model;
+
+int fuse_plan_time(const fuse_stage* stages, int K, uint32_t cut_mask, int elem_bytes,
+                   const fuse_cost_model* model, double* seconds);
+int fuse_best_plan(const fuse_stage* stages, int K, int elem_bytes, const fuse_cost_model* model,
+                   uint32_t* best_mask, double* best_seconds);
+
 /* Algorithmic DRAM bytes of one call of the entry points above (what the kernel must move at
  * minimum; the unfused forms count every intermediate round trip).  Negative = fuse_status. */
 int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode);
