@@ -74,6 +74,9 @@ SIGNATURES = {
                         ctypes.POINTER(ctypes.c_double)], _I32),
     "fuse_best_plan": ([ctypes.POINTER(fuse_stage), _I32, _I32, ctypes.POINTER(fuse_cost_model),
                         ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_double)], _I32),
+    "fuse_launch_model": ([_I64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
+                           ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
+                           ctypes.POINTER(ctypes.c_double)], _I32),
     "fuse_chain_bytes": ([_I32, _I64, _I32, _I32], _I64),
     "fuse_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
     "fuse_causal_softmax_bytes": ([_I64, _I64, _I32, _I32, _I32], _I64),
@@ -83,6 +86,11 @@ SIGNATURES = {
     "fuse_last_cuda_error": ([], ctypes.c_char_p),
     "fuse_check": ([_P], _I32),
     "fuse_debug_expire_wait": ([_I64, _P], _I32),
+    "fuse_graph_begin": ([_P], _I32),
+    "fuse_graph_end": ([_P, ctypes.POINTER(ctypes.c_void_p)], _I32),
+    "fuse_graph_launch": ([_P, _P], _I32),
+    "fuse_graph_kernel_count": ([_P], _I32),
+    "fuse_graph_destroy": ([_P], None),
     "fuse_version": ([], _I32),
 }
 
@@ -264,6 +272,14 @@ def fuse_best_plan(stages, elem_bytes: int, model) -> tuple:
     return mask.value, sec.value
 
 
+def fuse_launch_model(n_kernels: int, t_launch: float, t_exec: float, t_dispatch: float) -> dict:
+    """Eager vs CUDA-graph timeline of n_kernels kernels; see fusechain.h."""
+    e, i, g = ctypes.c_double(), ctypes.c_double(), ctypes.c_double()
+    _check(_load().fuse_launch_model(n_kernels, t_launch, t_exec, t_dispatch, ctypes.byref(e),
+                                     ctypes.byref(i), ctypes.byref(g)), "fuse_launch_model")
+    return {"eager": e.value, "eager_idle": i.value, "graph": g.value}
+
+
 def fuse_chain_bytes(K: int, n: int, dtype: int, mode: int) -> int:
     return _load().fuse_chain_bytes(K, n, dtype, mode)
 
@@ -303,6 +319,33 @@ def fuse_check(stream=None) -> int:
 def fuse_debug_expire_wait(budget_cycles: int, stream=None) -> None:
     _check(_load().fuse_debug_expire_wait(int(budget_cycles), _stream(stream)),
            "fuse_debug_expire_wait")
+
+
+# ------------------------------------------------------------------------------- graphs
+def fuse_graph_begin(stream=None) -> None:
+    """Start capturing this library's calls on `stream` (a non-default stream)."""
+    _check(_load().fuse_graph_begin(_stream(stream)), "fuse_graph_begin")
+
+
+def fuse_graph_end(stream=None) -> int:
+    """End the capture; returns the executable graph's handle (free with fuse_graph_destroy)."""
+    g = ctypes.c_void_p()
+    _check(_load().fuse_graph_end(_stream(stream), ctypes.byref(g)), "fuse_graph_end")
+    return g.value
+
+
+def fuse_graph_launch(graph: int, stream=None) -> None:
+    _check(_load().fuse_graph_launch(graph, _stream(stream)), "fuse_graph_launch")
+
+
+def fuse_graph_kernel_count(graph: int) -> int:
+    n = _load().fuse_graph_kernel_count(graph)
+    _check(min(n, 0), "fuse_graph_kernel_count")
+    return n
+
+
+def fuse_graph_destroy(graph: int) -> None:
+    _load().fuse_graph_destroy(graph)
 
 
 def fuse_strerror(status: int) -> str:

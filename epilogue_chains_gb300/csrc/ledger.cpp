@@ -92,3 +92,22 @@ extern "C" int fuse_best_plan(const fuse_stage* st, int K, int elem_bytes, const
     *best_seconds = best;
     return FUSE_OK;
 }
+
+// "AIGC fundamentals | operator fusion and CUDA Graph" §3.4: single-stream timeline of N kernels.
+// Eager: kernel i starts at max(end of kernel i-1, (i+1) t_launch), which solves to
+// t_launch + N t_exec when the host keeps ahead (t_launch <= t_exec) and N t_launch + t_exec when
+// it does not.  Graph: one submission, then t_exec + t_dispatch per node.
+extern "C" int fuse_launch_model(int64_t n_kernels, double t_launch, double t_exec,
+                                 double t_dispatch, double* eager, double* eager_idle,
+                                 double* graph) {
+    if (n_kernels < 0 || !(t_launch >= 0) || !(t_exec >= 0) || !(t_dispatch >= 0) || !eager ||
+        !eager_idle || !graph)
+        return FUSE_EINVAL;
+    const double n = static_cast<double>(n_kernels);
+    double total = 0.0;
+    if (n_kernels > 0) total = t_launch <= t_exec ? t_launch + n * t_exec : n * t_launch + t_exec;
+    *eager = total;
+    *eager_idle = total - n * t_exec;
+    *graph = t_launch + n * (t_exec + t_dispatch);
+    return FUSE_OK;
+}

@@ -238,6 +238,14 @@ int fuse_plan_time(const fuse_stage* stages, int K, uint32_t cut_mask, int elem_
 int fuse_best_plan(const fuse_stage* stages, int K, int elem_bytes, const fuse_cost_model* model,
                    uint32_t* best_mask, double* best_seconds);
 
+/* "AIGC fundamentals | operator fusion and CUDA Graph" §3.4: timeline of n_kernels kernels on one
+ * stream.  Eager: the host spends t_launch per submission and does not wait; kernel i starts at
+ * max(end of kernel i-1, (i+1) t_launch) and runs t_exec.  Graph: one submission, then the GPU
+ * front end spends t_dispatch per node.  Outputs (any time unit, the inputs' own): *eager = total
+ * eager time, *eager_idle = the GPU's idle part of it, *graph = total graph time.  Host only. */
+int fuse_launch_model(int64_t n_kernels, double t_launch, double t_exec, double t_dispatch,
+                      double* eager, double* eager_idle, double* graph);
+
 /* Algorithmic DRAM bytes of one call of the entry points above (what the kernel must move at
  * minimum; the unfused forms count every intermediate round trip).  Negative = fuse_status. */
 int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode);
@@ -266,6 +274,29 @@ typedef struct {
 int fuse_kernel_count(void);
 /* Fill *out for variant `index` (needs a CUDA device; the current device is used). */
 int fuse_kernel_report(int index, fuse_kernel_record* out);
+
+/* CUDA-graph capture of this library's calls ("AIGC fundamentals | operator fusion and CUDA
+ * Graph" §3.4: one submission for N kernels; §6.4: shapes and addresses are frozen, no host
+ * synchronisation inside).  Typical use, e.g. an unfused plan whose kernels are launch-bound:
+ *     fuse_graph_begin(s); fuse_chain_run(..., FUSE_UNFUSED, s); fuse_graph_end(s, &g);
+ *     fuse_graph_launch(g, s);  ...  fuse_graph_destroy(g);
+ *   fuse_graph_begin(stream)   stream must not be NULL (the legacy stream cannot be captured).
+ *       Makes every kernel of the library resident on the current device first (once per
+ *       device), then starts a thread-local capture.  Calls of this library issued on `stream`
+ *       until fuse_graph_end() are recorded, not run.  Do not call fuse_check() or anything that
+ *       synchronizes while capturing (the capture fails; fuse_graph_end() then reports it).
+ *   fuse_graph_end(stream, &g) ends the capture and instantiates it; *g is NULL on error.  If a
+ *       call inside the capture returned an error, end the capture anyway and drop the result.
+ *   fuse_graph_launch(g, stream) replays the recorded kernels in order on any stream, with the
+ *       same pointers, sizes and parameters; update inputs in place between replays.
+ *   fuse_graph_kernel_count(g) = the number of kernel nodes (launches per replay).
+ *   fuse_graph_destroy(g) frees the executable graph (NULL is ignored); the caller owns g. */
+typedef struct fuse_graph_s* fuse_graph_t;
+int fuse_graph_begin(fuse_stream_t stream);
+int fuse_graph_end(fuse_stream_t stream, fuse_graph_t* out);
+int fuse_graph_launch(fuse_graph_t graph, fuse_stream_t stream);
+int fuse_graph_kernel_count(fuse_graph_t graph);
+void fuse_graph_destroy(fuse_graph_t graph);
 
 const char* fuse_strerror(int status);
 /* Message of the last CUDA error seen by this library on this thread ("" if none). */
