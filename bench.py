@@ -324,14 +324,15 @@ def run_ours(args, rank, world, local):
         ]
 
     def make_events():
+        # per group: the untimed leading call's events first, then one pair per timed call
         return {g.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                         for _ in g.calls] for g in groups}
+                         for _ in range(len(g.calls) + 1)] for g in groups}
 
     def step(evs):
         with torch.cuda.stream(stream):
             for g in groups:
-                g.pre()
-                for (tag, fn, units), (e0, e1) in zip(g.calls, evs[g.name]):
+                fns = [g.pre] + [fn for _, fn, _ in g.calls]
+                for fn, (e0, e1) in zip(fns, evs[g.name]):
                     e0.record(stream)
                     fn()
                     e1.record(stream)
@@ -357,8 +358,9 @@ def run_ours(args, rank, world, local):
     clocks = summarize_clocks(sampler.stop(), t0, t1)
     timed_launches = counter["launches"]   # every kernel of ours launched inside the timed region
 
-    # ms per call: times[group][step][call]
-    times = {g.name: [[e0.elapsed_time(e1) for e0, e1 in evs[g.name]] for evs in all_evs] for g in groups}
+    # ms per call: times[group][step][call] (timed calls); lead[group][step] (the untimed lead call)
+    times = {g.name: [[e0.elapsed_time(e1) for e0, e1 in evs[g.name][1:]] for evs in all_evs] for g in groups}
+    lead = {g.name: [evs[g.name][0][0].elapsed_time(evs[g.name][0][1]) for evs in all_evs] for g in groups}
     gmap = {g.name: g for g in groups}
 
     def mean_ms(name, idx):
@@ -405,6 +407,10 @@ def run_ours(args, rank, world, local):
     roofline["traffic"] = committed_traffic(dominant, kernel_src.get(dominant, ""))
 
     rows = {"step_share": {g.name: round(group_total_ms(g.name) / step_ms, 4) for g in groups}}
+    # the same shares over every launch of the step, the untimed lead calls included: the figure an
+    # ncu launch list of this command (all launches, serialised) can be compared with
+    all_ms = {g.name: group_total_ms(g.name) + float(np.mean(lead[g.name])) for g in groups}
+    rows["step_share_all_launches"] = {k: round(v / sum(all_ms.values()), 4) for k, v in all_ms.items()}
     per_k = {}
     for j, K in enumerate(KS):
         f = mean_ms("chain_fused", j)
@@ -447,7 +453,7 @@ def run_ours(args, rank, world, local):
         gm["M16"]["roofline"] = roofline_of("gemm_M16_fused")
         rows["gemm_epilogue"] = gm
         rows["launch_graph"] = launch_graph_rows(fc, lib, wl, torch, dev, gemm_bufs[16], check)
-        rows["planner"] = planner_rows(fc, wl, peaks, rows["launch_graph"]["t_exec_us"],
+        rows["planner"] = planner_rows(fc, wl, peaks, rows["launch_graph"]["t_exec_queued_us"],
                                        {M: {p_: (mean_ms(f"gemm_M{M}_fused", 0) if m_ == 0 else
                                                  mean_ms(f"gemm_M{M}_unfused",
                                                          [c[0] for c in gmap[f"gemm_M{M}_unfused"].calls].index(p_)))
@@ -583,18 +589,28 @@ def launch_graph_rows(fc, lib, wl, torch, dev, gemm16, check):
                 ent[f"{pname}_kernels"] = lib.fuse_graph_kernel_count(g)
                 ent[f"{pname}_graph_speedup"] = round(ent[f"{pname}_eager_us"] / ent[f"{pname}_graph_us"], 3)
             out[cname] = ent
-        # the model's inputs, measured: host cost of one submission through the C ABI (ctypes
-        # call included), the kernel's duration when queued behind other work, and the per-node
-        # graph cost; then the model's prediction for the unfused chain next to the measurement
+        # the model's inputs, measured: the host cost of one submission through the C ABI (ctypes
+        # call included) for a kernel and for a graph, and the GPU's cost per kernel when kernels
+        # are queued behind other work, eager and as graph nodes
         small = chain(fc.FUSE_FUSED)
-        s.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(2000):
-            small()
-        t_launch = (time.perf_counter() - t0) / 2000 * 1e6
-        s.synchronize()
-        big = torch.empty(1 << 26, dtype=torch.float32, device=dev)
         nq = 64
+        g64 = capture(lambda: [small() for _ in range(nq)])
+        graphs.append(g64)
+        g1 = capture(small)
+        graphs.append(g1)
+
+        def host_us(fn, reps=2000):
+            s.synchronize()
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                fn()
+            t = (time.perf_counter() - t0) / reps * 1e6
+            s.synchronize()
+            return t
+
+        t_launch = host_us(small)
+        t_launch_graph = host_us(lambda: check(lib.fuse_graph_launch(g1, sh), "fuse_graph_launch"))
+        big = torch.empty(1 << 26, dtype=torch.float32, device=dev)
 
         def queued_us(fn_many):
             ts = []
@@ -602,7 +618,7 @@ def launch_graph_rows(fc, lib, wl, torch, dev, gemm16, check):
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 with torch.cuda.stream(s):
                     for _ in range(6):
-                        big.mul_(1.0)      # ~0.25 ms of HBM work so the queue fills ahead of it
+                        big.mul_(1.0)      # ~0.5 ms of HBM work, so the submissions get ahead
                 e0.record(s)
                 fn_many()
                 e1.record(s)
@@ -611,15 +627,14 @@ def launch_graph_rows(fc, lib, wl, torch, dev, gemm16, check):
             return float(np.median(ts)) * 1e3
 
         t_exec = queued_us(lambda: [small() for _ in range(nq)]) / nq
-        g64 = capture(lambda: [small() for _ in range(nq)])
-        graphs.append(g64)
         t_node = queued_us(lambda: check(lib.fuse_graph_launch(g64, sh), "fuse_graph_launch")) / nq
-        t_disp = max(t_node - t_exec, 0.0)
-        pred = fc.fuse_launch_model(K, t_launch, t_exec, t_disp)
         ach = out["affine_K8_N4096"]
-        out.update({"t_launch_us": round(t_launch, 3), "t_exec_us": round(t_exec, 3),
-                    "t_dispatch_us": round(t_disp, 3),
-                    "model_unfused_K8": {"eager_us": round(pred["eager"], 2), "graph_us": round(pred["graph"], 2),
+        eager = fc.fuse_launch_model(K, t_launch, t_exec, 0.0)["eager"]
+        graph = fc.fuse_launch_model(K, t_launch_graph, t_node, 0.0)["graph"]
+        out.update({"t_launch_us": round(t_launch, 3), "t_launch_graph_us": round(t_launch_graph, 3),
+                    "t_exec_queued_us": round(t_exec, 3), "t_node_queued_us": round(t_node, 3),
+                    "t_dispatch_us": round(t_node - t_exec, 3),
+                    "model_unfused_K8": {"eager_us": round(eager, 2), "graph_us": round(graph, 2),
                                          "measured_eager_us": ach["unfused_eager_us"],
                                          "measured_graph_us": ach["unfused_graph_us"]}})
         del big

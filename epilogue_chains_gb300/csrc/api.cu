@@ -26,6 +26,9 @@ thread_local char t_last_error[256] = "";
 int record_cuda_error(cudaError_t e) {
     snprintf(t_last_error, sizeof(t_last_error), "%s: %s", cudaGetErrorName(e),
              cudaGetErrorString(e));
+    // A failed runtime call also leaves its error as the thread's "last error"; clear it (where it
+    // is not sticky) so that it is not reported again by the next call's launch check.
+    (void)cudaGetLastError();
     return FUSE_ECUDA;
 }
 
