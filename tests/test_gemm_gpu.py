@@ -195,3 +195,27 @@ def test_rejects_bad_arguments(cuda_device):
     R = torch.zeros(64, 64, dtype=torch.float16, device="cuda")
     with pytest.raises(fc.FuseError):
         fc.fuse_gemm_epilogue(A, B, b, R, R)                       # Y aliases R
+
+
+def test_accumulation_term_is_needed_by_cublas_too(cuda_device):
+    """The tolerance's fp32-accumulation term is not tailored to this kernel: cuBLAS's fp16 GEMM
+    (fp32 accumulation, through torch.mm) also leaves elements beyond the plain 2-ulp bar against
+    the exact (double) sum on the stress inputs at K = 4096, stays inside the same derived bound, and
+    this kernel's error is of the same order as cuBLAS's."""
+    import torch
+    M, N, K = 256, 512, 4096
+    A, B, _, _ = wl.gemm_input(M, N, K, salt=11, std=1.0 / 8.0)
+    z, R = np.zeros(N, np.uint16), np.zeros((M, N), np.uint16)
+    Ah, Bh = _dev(A, (M, K)), _dev(B, (K, N))
+    try:
+        acc32 = torch.mm(Ah, Bh, out_dtype=torch.float32).double().cpu().numpy()
+    except TypeError:
+        pytest.skip("torch.mm has no out_dtype here")
+    ref = oracle.gemm_epilogue(A, B, z, R, 0).view(np.float16).astype(np.float64)
+    cub = np.vectorize(oracle.gelu)(acc32).astype(np.float16).astype(np.float64)
+    ours = _run(A, B, z, R, 0).view(np.float16).astype(np.float64)
+    tight = 2 * _ulp16(ref) + 2.0 ** -24
+    assert np.count_nonzero(np.abs(cub - ref) > tight) > 0
+    _check(cub.astype(np.float16).view(np.uint16), ref.astype(np.float16).view(np.uint16), 0, A, B)
+    rms = lambda d: float(np.sqrt(np.mean(d ** 2)))
+    assert rms(ours - ref) <= 3 * rms(cub - ref) + 1e-6
