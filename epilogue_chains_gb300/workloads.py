@@ -15,6 +15,11 @@ Workload recipes (the five configurations of the hot path):
   3  causal softmax s bf16 [8, 16, 2048, 2048] ~ N(0,1) rounded to bf16, scale 1/16
   4  GEMM + bias + GELU + residual, fp16: A [M,4096], B [4096,4096] ~ N(0, std 1/64),
      bias [4096] ~ N(0, 0.1), R [M,4096] ~ N(0,1); M in {4096, 16}
+  5  residual add + RMSNorm: x, r fp32 [2048, 4096] ~ N(0,1), w fp32 [4096] ~ N(1, 0.02),
+     eps 1e-6 (config 2's rows and hidden size, plus the residual input)
+  6  SiLU(gate) * up: one merged gate/up output gu bf16 [2048, 2 x 14336] ~ N(0,1) (gate the
+     first 14336 columns, up the rest); 14336 is the FFN width of the Llama-3-8B configuration
+     the pages count kernels for, 2048 rows as config 2
 """
 from __future__ import annotations
 
@@ -31,6 +36,8 @@ SM_SCALE = 1.0 / 16.0          # 1/sqrt(256)
 GEMM_N, GEMM_K = 4096, 4096
 GEMM_MS = (4096, 16)
 GEMM_STD = 1.0 / 64.0          # "N(0, 1/sqrt(4096))", second parameter read as the std
+ADDRMS_ROWS, ADDRMS_HIDDEN = 2048, 4096
+SILU_ROWS, SILU_COLS = 2048, 14336
 
 
 def rng(config: int, salt: int = 0) -> np.random.Generator:
@@ -98,6 +105,41 @@ def rmsnorm_input(rows: int = RMS_ROWS, hidden: int = RMS_HIDDEN, config: int = 
     x = torch.randn(rows, hidden, generator=g, device=device, dtype=torch.float32)
     w = 1.0 + 0.02 * torch.randn(hidden, generator=g, device=device, dtype=torch.float32)
     return x, w
+
+
+def add_rmsnorm_input(rows: int = ADDRMS_ROWS, hidden: int = ADDRMS_HIDDEN, config: int = 5,
+                      salt: int = 0, device=None):
+    """x, r ~ N(0,1) fp32 [rows, hidden], w ~ N(1, 0.02) fp32 [hidden]."""
+    if device is None:
+        g = rng(config, salt)
+        x = g.standard_normal((rows, hidden)).astype(np.float32)
+        r = g.standard_normal((rows, hidden)).astype(np.float32)
+        w = (1.0 + 0.02 * g.standard_normal(hidden)).astype(np.float32)
+        return x, r, w
+    import torch
+    g = _torch_gen(config, salt, device)
+    x = torch.randn(rows, hidden, generator=g, device=device, dtype=torch.float32)
+    r = torch.randn(rows, hidden, generator=g, device=device, dtype=torch.float32)
+    w = 1.0 + 0.02 * torch.randn(hidden, generator=g, device=device, dtype=torch.float32)
+    return x, r, w
+
+
+# ----------------------------------------------------------------------------- SiLU * up
+def silu_input(rows: int = SILU_ROWS, cols: int = SILU_COLS, dtype: str = "bf16", config: int = 6,
+               salt: int = 0, scale: float = 1.0, device=None):
+    """Merged gate/up tensor [rows, 2 cols] ~ N(0, scale^2): float32 for "f32", else uint16 bit
+    patterns of fp16/bf16 on the host; a torch tensor of that dtype on ``device``."""
+    if device is None:
+        x = scale * rng(config, salt).standard_normal((rows, 2 * cols))
+        if dtype == "f32":
+            return x.astype(np.float32)
+        if dtype == "f16":
+            return f16_bits_from_f64(x)
+        return bf16_bits_from_f32(x.astype(np.float32))
+    import torch
+    tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+    g = _torch_gen(config, salt, device)
+    return (scale * torch.randn(rows, 2 * cols, generator=g, device=device)).to(tdt)
 
 
 # ----------------------------------------------------------------------------- softmax

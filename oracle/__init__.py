@@ -12,7 +12,7 @@ invariants and brute force on tiny inputs.
 
 Parity status of each function:
   chain, affine_closed_form, rmsnorm, causal_softmax, causal_softmax_unfused, gemm_epilogue,
-  gelu: pinned (tests/test_oracle_pins.py).
+  gelu, add_rmsnorm, silu, silu_mul: pinned (tests/test_oracle_pins.py).
 """
 from __future__ import annotations
 
@@ -68,6 +68,9 @@ def _load():
             "orc_causal_softmax_unfused": ([P, P, I64, I64, F64, I32], None),
             "orc_gemm_epilogue": ([P, P, P, P, P, I64, I64, I64, U32, P, I64], None),
             "orc_gelu": ([F64], F64),
+            "orc_add_rmsnorm": ([P, P, P, P, P, I64, I64, F64], None),
+            "orc_silu": ([F64], F64),
+            "orc_silu_mul": ([P, P, I64, P, I64, I64, I32, I32], None),
             "orc_version": ([], I32),
         }
         for name, (args, res) in sig.items():
@@ -187,3 +190,49 @@ def gemm_epilogue(A: np.ndarray, B: np.ndarray, bias: np.ndarray, R: np.ndarray,
         _load().orc_gemm_epilogue(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(Y), M, N, K,
                                   int(cut_mask), _ptr(rows), rows.size)
     return Y
+
+
+def add_rmsnorm(x: np.ndarray, r: np.ndarray, w: np.ndarray, eps: float):
+    """Residual add + RMSNorm over rows: h = fl32(x + r); y = RMSNorm(h) * w.  Returns (h, y)."""
+    x = _c(x, np.float32)
+    r = _c(r, np.float32)
+    w = _c(w, np.float32)
+    rows, hidden = x.shape
+    assert r.shape == x.shape and w.size == hidden
+    h = np.empty_like(x)
+    y = np.empty_like(x)
+    _load().orc_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), rows, hidden, float(eps))
+    return h, y
+
+
+def silu(v: float) -> float:
+    return _load().orc_silu(float(v))
+
+
+def silu_mul(g: np.ndarray, u: np.ndarray, dtype: str = "bf16", unfused: bool = False) -> np.ndarray:
+    """y = SiLU(g) * u element-wise over two [rows, cols] arrays (float32 for "f32", else uint16
+    bit patterns of fp16/bf16).  Returns y [rows, cols] in the storage type."""
+    edt = np.float32 if dtype == "f32" else np.uint16
+    g = _c(g, edt)
+    u = _c(u, edt)
+    assert g.shape == u.shape and g.ndim == 2
+    rows, cols = g.shape
+    y = np.empty((rows, cols), dtype=edt)
+    _load().orc_silu_mul(_ptr(g), _ptr(u), cols, _ptr(y), rows, cols, DTYPE_CODES[dtype],
+                         1 if unfused else 0)
+    return y
+
+
+def silu_mul_merged(gu: np.ndarray, dtype: str = "bf16", unfused: bool = False) -> np.ndarray:
+    """The same on one merged gate/up output [rows, 2 cols]: gate = gu[:, :cols], up =
+    gu[:, cols:], both read with row stride 2 cols."""
+    edt = np.float32 if dtype == "f32" else np.uint16
+    gu = _c(gu, edt)
+    rows, ld = gu.shape
+    assert ld % 2 == 0
+    cols = ld // 2
+    flat = gu.reshape(-1)
+    y = np.empty((rows, cols), dtype=edt)
+    _load().orc_silu_mul(_ptr(flat), _ptr(flat[cols:]), ld, _ptr(y), rows, cols,
+                         DTYPE_CODES[dtype], 1 if unfused else 0)
+    return y

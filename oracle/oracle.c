@@ -291,4 +291,59 @@ void orc_gemm_epilogue(const uint16_t* A, const uint16_t* B, const uint16_t* bia
     free(bt);
 }
 
+/* ------------------------------------------------------------------------------------ */
+/* Residual add + RMSNorm.  [OFCG] appendix launch_model [F3], the per-layer list after    */
+/* fusion: "residual + RMSNorm fused" replaces the residual-add kernel and the four        */
+/* RMSNorm kernels of the unfused list ([OFCG] §2: "residual 1, post RMSNorm 4").          */
+/* Reading: the residual stream h = x + r (one fp32 rounding) is an output too, since it   */
+/* feeds the next residual add; y is RMSNorm of h with the same definition as orc_rmsnorm. */
+/* ------------------------------------------------------------------------------------ */
+void orc_add_rmsnorm(const float* x, const float* r, const float* w, float* h, float* y,
+                     int64_t rows, int64_t hidden, double eps)
+{
+    for (int64_t i = 0; i < rows * hidden; ++i) {
+        float sum = x[i] + r[i];   /* one fp32 rounding */
+        h[i] = sum;
+    }
+    orc_rmsnorm(h, w, y, rows, hidden, eps);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* SiLU(gate) * up.  [OFCG] appendix launch_model [F3]: the gate/up projection is one GEMM  */
+/* and "SiLU + mul fused" one kernel, where the unfused list has a SiLU kernel and an     */
+/* element-wise multiply kernel.  SiLU(v) = v * logistic(v) = v / (1 + e^-v).             */
+/* Readings: g and u are rows x cols with a common row stride ld (ld = 2 cols when both   */
+/* halves of one merged gate/up output are passed); y is rows x cols, contiguous.  The    */
+/* math is in double; the fused form rounds once to the storage type, the unfused form    */
+/* also rounds the SiLU tensor it stores between its two kernels.                          */
+/* ------------------------------------------------------------------------------------ */
+static double silu(double v) { return v / (1.0 + exp(-v)); }
+static double round_storage(double v, int dtype)
+{
+    if (dtype == 0) return (double)(float)v;
+    if (dtype == 1) return orc_round_half(v);
+    return orc_round_bf16(v);
+}
+static void store_elem_d(void* base, int dtype, int64_t i, double v)
+{
+    if (dtype == 0) ((float*)base)[i] = (float)v;
+    else if (dtype == 1) ((uint16_t*)base)[i] = orc_half_bits(v);
+    else ((uint16_t*)base)[i] = orc_bf16_bits(v);
+}
+double orc_silu(double v) { return silu(v); }
+
+void orc_silu_mul(const void* g, const void* u, int64_t ld, void* y, int64_t rows, int64_t cols,
+                  int dtype, int unfused)
+{
+    for (int64_t i = 0; i < rows; ++i) {
+        for (int64_t j = 0; j < cols; ++j) {
+            double gv = load_elem(g, dtype, i * ld + j);
+            double uv = load_elem(u, dtype, i * ld + j);
+            double s = silu(gv);
+            if (unfused) s = round_storage(s, dtype);
+            store_elem_d(y, dtype, i * cols + j, s * uv);
+        }
+    }
+}
+
 int orc_version(void) { return 1; }

@@ -474,3 +474,144 @@ def test_gemm_brute_force_tiny_fractions():
             v = acc + bv[n]
             g = 0.5 * v * (1.0 + math.erf(v / math.sqrt(2.0)))
             assert Y[m, n] == _h(g + Rv[m, n])
+
+
+# ============================================================== residual add + RMSNorm
+def test_add_rmsnorm_zero_residual_is_rmsnorm():
+    """r = 0: h = x exactly and y is the (independently pinned) RMSNorm of x."""
+    x, _, w = wl.add_rmsnorm_input(6, 256)
+    h, y = oracle.add_rmsnorm(x, np.zeros_like(x), w, 1e-6)
+    assert np.array_equal(h.view(np.uint32), x.view(np.uint32))
+    assert np.array_equal(y, oracle.rmsnorm(x, w, 1e-6))
+
+
+def test_add_rmsnorm_sum_is_one_ieee_fp32_addition():
+    """h against numpy's float32 addition (IEEE round-to-nearest-even), element by element,
+    including cancellation, ties and sums that overflow to inf."""
+    x, r, w = wl.add_rmsnorm_input(4, 512, salt=1)
+    x[0, :4] = [1.0, 3.4e38, 2.0 ** -24, -5.5]
+    r[0, :4] = [2.0 ** -24, 3.4e38, 1.0, 5.5]
+    h, _ = oracle.add_rmsnorm(x, r, w, 1e-6)
+    assert np.array_equal(h.view(np.uint32), (x + r).view(np.uint32))
+    assert h[0, 0] == np.float32(1.0) and np.isinf(h[0, 1]) and h[0, 3] == 0.0
+
+
+def test_add_rmsnorm_normalises_the_sum_not_the_inputs():
+    """A constant row split between x and r: h = c and y = c / sqrt(c^2 + eps) (w = 1)."""
+    H, eps, c = 64, 1e-6, 3.0
+    g = np.random.default_rng(15)
+    parts = g.integers(-8, 8, (2, H)).astype(np.float32)
+    x = parts
+    r = (np.float32(c) - parts).astype(np.float32)
+    h, y = oracle.add_rmsnorm(x, r, np.ones(H, np.float32), eps)
+    assert np.all(h == np.float32(c))
+    cf = c / math.sqrt(c * c + eps)
+    assert np.all(np.abs(y - np.float32(cf)) <= _ulp32(cf))
+
+
+def test_add_rmsnorm_is_symmetric_in_x_and_r():
+    x, r, w = wl.add_rmsnorm_input(3, 128, salt=2)
+    h1, y1 = oracle.add_rmsnorm(x, r, w, 1e-6)
+    h2, y2 = oracle.add_rmsnorm(r, x, w, 1e-6)
+    assert np.array_equal(h1, h2) and np.array_equal(y1, y2)
+
+
+def test_add_rmsnorm_brute_force_tiny():
+    x = np.array([[1, 2, 3, 4], [0.5, -1, 0.25, 8]], np.float32)
+    r = np.array([[0.5, -2, 1, 0], [0.5, 1, -0.25, -4]], np.float32)
+    w = np.array([1, 2, 0.5, -1], np.float32)
+    h, y = oracle.add_rmsnorm(x, r, w, 0.0)
+    for i in range(2):
+        hs = [float(a) + float(b) for a, b in zip(x[i], r[i])]   # exact in fp32 here
+        ms = math.fsum(v * v for v in hs) / 4
+        for j in range(4):
+            assert h[i, j] == np.float32(hs[j])
+            want = np.float32(hs[j] / math.sqrt(ms) * float(w[j]))
+            assert abs(y[i, j] - want) <= _ulp32(want)
+
+
+# ============================================================== SiLU(gate) * up
+def test_silu_values_against_the_logistic_function():
+    """SiLU(v) = v * logistic(v), with scipy's logistic (expit) as the independent routine."""
+    from scipy.special import expit
+    for v in [-30.0, -5.0, -1.0, -1e-3, 0.0, 1e-3, 0.5, 1.0, 2.0, 7.5, 30.0]:
+        assert oracle.silu(v) == pytest.approx(v * expit(v), rel=1e-14, abs=1e-300)
+    assert oracle.silu(1.0) == pytest.approx(math.e / (1 + math.e), rel=1e-15)
+
+
+def test_silu_odd_part_identity():
+    """SiLU(v) - SiLU(-v) = v (logistic(v) + logistic(-v) = 1)."""
+    for v in np.linspace(-12, 12, 97):
+        assert oracle.silu(v) - oracle.silu(-v) == pytest.approx(v, abs=1e-14)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_silu_mul_with_unit_up_is_rounded_silu(dtype):
+    gu = wl.silu_input(4, 64, dtype=dtype, salt=1)
+    g = gu[:, :64].copy()
+    one = {"f32": np.ones((4, 64), np.float32),
+           "f16": np.full((4, 64), 0x3C00, np.uint16),
+           "bf16": np.full((4, 64), 0x3F80, np.uint16)}[dtype]
+    y = oracle.silu_mul(g, one, dtype)
+    dec = (lambda a: a.astype(np.float64)) if dtype == "f32" else (
+        np.vectorize(oracle.half_value) if dtype == "f16" else np.vectorize(oracle.bf16_value))
+    rnd = {"f32": lambda v: float(np.float32(v)), "f16": oracle.round_half,
+           "bf16": oracle.round_bf16}[dtype]
+    want = np.vectorize(lambda v: rnd(oracle.silu(v)))(dec(g))
+    assert np.array_equal(dec(y), want)
+    # with up = 1 the unfused form rounds the same value twice: identical
+    assert np.array_equal(oracle.silu_mul(g, one, dtype, unfused=True), y)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "f16", "bf16"])
+def test_silu_mul_power_of_two_up_scales_exactly(dtype):
+    gu = wl.silu_input(3, 40, dtype=dtype, salt=2)
+    g = gu[:, :40].copy()
+    two = {"f32": np.full((3, 40), 2.0, np.float32), "f16": np.full((3, 40), 0x4000, np.uint16),
+           "bf16": np.full((3, 40), 0x4000, np.uint16)}[dtype]
+    one = {"f32": np.ones((3, 40), np.float32), "f16": np.full((3, 40), 0x3C00, np.uint16),
+           "bf16": np.full((3, 40), 0x3F80, np.uint16)}[dtype]
+    y1 = oracle.silu_mul(g, one, dtype)
+    y2 = oracle.silu_mul(g, two, dtype)
+    if dtype == "f32":
+        assert np.array_equal(y2, y1 * np.float32(2))
+    else:
+        dec = np.vectorize(oracle.half_value if dtype == "f16" else oracle.bf16_value)
+        assert np.array_equal(dec(y2), 2 * dec(y1))
+
+
+def test_silu_mul_unfused_rounds_the_intermediate():
+    """bf16: the unfused form is RNE(RNE(SiLU(g)) * u), the fused form RNE(SiLU(g) * u); the two
+    differ on some elements, and each matches its definition written with numpy/torch roundings."""
+    import torch
+    gu = wl.silu_input(8, 256, salt=3)
+    g, u = gu[:, :256].copy(), gu[:, 256:].copy()
+    yf = oracle.silu_mul(g, u, "bf16")
+    yu = oracle.silu_mul(g, u, "bf16", unfused=True)
+    gd = torch.from_numpy(g.view(np.int16)).view(torch.bfloat16).double().numpy()
+    ud = torch.from_numpy(u.view(np.int16)).view(torch.bfloat16).double().numpy()
+    s = gd / (1.0 + np.exp(-gd))
+
+    def to_bf16(v):   # double -> bf16 (RNE) through an exact fp32 stage where it is exact
+        return np.vectorize(oracle.bf16_bits)(v).astype(np.uint16)
+    assert np.array_equal(yf, to_bf16(s * ud))
+    sb = np.vectorize(oracle.bf16_value)(to_bf16(s))
+    assert np.array_equal(yu, to_bf16(sb * ud))
+    assert np.count_nonzero(yf != yu) > 0
+
+
+def test_silu_mul_merged_layout_matches_separate_arrays():
+    gu = wl.silu_input(5, 96, salt=4)
+    for unfused in (False, True):
+        assert np.array_equal(oracle.silu_mul_merged(gu, "bf16", unfused),
+                              oracle.silu_mul(gu[:, :96], gu[:, 96:], "bf16", unfused))
+
+
+def test_silu_mul_brute_force_tiny_fp32():
+    g = np.array([[-2.0, -0.5, 0.0, 0.5, 3.0]], np.float32)
+    u = np.array([[1.5, -2.0, 7.0, 0.25, -1.0]], np.float32)
+    y = oracle.silu_mul(g, u, "f32")
+    for j in range(5):
+        gv, uv = float(g[0, j]), float(u[0, j])
+        want = np.float32(gv / (1.0 + math.exp(-gv)) * uv)
+        assert y[0, j] == want
