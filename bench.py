@@ -52,7 +52,9 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", default=None,
                     choices=["chain_fused", "chain_unfused", "chain_fat", "rmsnorm_fused",
-                             "rmsnorm_unfused", "softmax_fused", "softmax_unfused", "gemm"],
+                             "rmsnorm_unfused", "softmax_fused", "softmax_unfused", "gemm",
+                             "add_rmsnorm_fused", "add_rmsnorm_unfused", "silu_mul_fused",
+                             "silu_mul_unfused"],
                     help="run only `--launches` calls of one row (for ncu), print a short line")
     ap.add_argument("--size", type=int, default=None,
                     help="profile size: chain elements, RMSNorm rows or softmax batch*heads")
@@ -263,6 +265,51 @@ def run_ours(args, rank, world, local):
             Group("rmsnorm_unfused", [("r", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED])] * 2,
                   rms(fc.FUSE_UNFUSED), "hbm", None, None),
         ]
+        # -------------------------------------------------------------- residual add + RMSNorm
+        with torch.cuda.stream(stream):
+            ax, ar, aw = wl.add_rmsnorm_input(device=dev, salt=rank)
+            axs, ars = [ax, ax.clone()], [ar, ar.clone()]
+            ahs = [torch.empty_like(ax) for _ in range(2)]
+            ays = [torch.empty_like(ax) for _ in range(2)]
+        arot = rotating(2)
+        AR, AH = wl.ADDRMS_ROWS, wl.ADDRMS_HIDDEN
+
+        def addrms(mode):
+            def fn():
+                i = arot()
+                check(lib.fuse_add_rmsnorm(axs[i].data_ptr(), ars[i].data_ptr(), aw.data_ptr(),
+                                           ahs[i].data_ptr(), ays[i].data_ptr(), AR, AH, wl.RMS_EPS, mode,
+                                           rws.data_ptr(), rws.numel(), sh), "fuse_add_rmsnorm")
+                counter["launches"] += 1 if mode == fc.FUSE_FUSED else 5
+            return fn
+        ab = {m: fc.fuse_add_rmsnorm_bytes(AR, AH, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
+        # -------------------------------------------------------------- SiLU(gate) * up
+        SR, SC = wl.SILU_ROWS, wl.SILU_COLS
+        with torch.cuda.stream(stream):
+            gu0 = wl.silu_input(device=dev, salt=rank)
+            gus = [gu0, gu0.clone()]
+            sys_ = [torch.empty(SR, SC, dtype=gu0.dtype, device=dev) for _ in range(2)]
+        grot = rotating(2)
+
+        def silu(mode):
+            def fn():
+                i = grot()
+                base = gus[i].data_ptr()
+                check(lib.fuse_silu_mul(base, base + SC * 2, 2 * SC, sys_[i].data_ptr(), SR, SC,
+                                        fc.FUSE_BF16, mode, sh), "fuse_silu_mul")
+                counter["launches"] += 1 if mode == fc.FUSE_FUSED else 2
+            return fn
+        sb = {m: fc.fuse_silu_mul_bytes(SR, SC, fc.FUSE_BF16, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
+        groups += [
+            Group("add_rmsnorm_fused", [("r", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED])] * 2,
+                  addrms(fc.FUSE_FUSED), "hbm", "rmsnorm_fused_kernel<+residual>", 1),
+            Group("add_rmsnorm_unfused", [("r", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED])] * 2,
+                  addrms(fc.FUSE_UNFUSED), "hbm", None, None),
+            Group("silu_mul_fused", [("s", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED])] * 2,
+                  silu(fc.FUSE_FUSED), "hbm", "silu_mul_vec_kernel<bf16>", 1),
+            Group("silu_mul_unfused", [("s", silu(fc.FUSE_UNFUSED), sb[fc.FUSE_UNFUSED])] * 2,
+                  silu(fc.FUSE_UNFUSED), "hbm", None, None),
+        ]
         # -------------------------------------------------------------- causal softmax
         bh, S = wl.SM_B * wl.SM_H, wl.SM_S
         with torch.cuda.stream(stream):
@@ -381,7 +428,8 @@ def run_ours(args, rank, world, local):
     value = n_fused * chain_bytes * world / elapsed_s / 1e9
 
     kernel_src = {"softmax_fused": "softmax.cu", "chain_fused": "chain.cu", "gemm_M4096_fused": "gemm.cu",
-                  "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm.cu"}
+                  "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm.cu",
+                  "add_rmsnorm_fused": "rmsnorm.cu", "silu_mul_fused": "silu_mul.cu"}
 
     def roofline_of(name):
         g = gmap[name]
@@ -429,6 +477,16 @@ def run_ours(args, rank, world, local):
         rf, ru = group_total_ms("rmsnorm_fused") / 2, group_total_ms("rmsnorm_unfused") / 2
         rows["rmsnorm"] = {"fused_us": round(rf * 1e3, 2), "unfused_us": round(ru * 1e3, 2),
                            "speedup": round(ru / rf, 3), "roofline_fused": roofline_of("rmsnorm_fused")}
+        af, au = group_total_ms("add_rmsnorm_fused") / 2, group_total_ms("add_rmsnorm_unfused") / 2
+        rows["add_rmsnorm"] = {"fused_us": round(af * 1e3, 2), "unfused_us": round(au * 1e3, 2),
+                               "speedup": round(au / af, 3),
+                               "unfused_ledger_GBs": round(ab[fc.FUSE_UNFUSED] / au / 1e6, 1),
+                               "roofline_fused": roofline_of("add_rmsnorm_fused")}
+        sf, su = group_total_ms("silu_mul_fused") / 2, group_total_ms("silu_mul_unfused") / 2
+        rows["silu_mul"] = {"fused_us": round(sf * 1e3, 2), "unfused_us": round(su * 1e3, 2),
+                            "speedup": round(su / sf, 3),
+                            "unfused_ledger_GBs": round(sb[fc.FUSE_UNFUSED] / su / 1e6, 1),
+                            "roofline_fused": roofline_of("silu_mul_fused")}
         smr = {}
         for j, t in enumerate((0, 64, 128)):
             ms_ = mean_ms("softmax_fused", j)
@@ -799,6 +857,32 @@ def run_profile(args):
                                   wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)
+    elif name.startswith("add_rmsnorm"):
+        rows = args.size or wl.ADDRMS_ROWS
+        mode = fc.FUSE_FUSED if name == "add_rmsnorm_fused" else fc.FUSE_UNFUSED
+        x, r, w = wl.add_rmsnorm_input(rows, wl.ADDRMS_HIDDEN, device=dev)
+        xs, rs = [x, x.clone()], [r, r.clone()]
+        hs, ys = [torch.empty_like(x) for _ in range(2)], [torch.empty_like(x) for _ in range(2)]
+        ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.ADDRMS_HIDDEN, mode)),
+                         dtype=torch.uint8, device=dev)
+        for i in range(L):
+            rc = lib.fuse_add_rmsnorm(xs[i % 2].data_ptr(), rs[i % 2].data_ptr(), w.data_ptr(),
+                                      hs[i % 2].data_ptr(), ys[i % 2].data_ptr(), rows, wl.ADDRMS_HIDDEN,
+                                      wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_add_rmsnorm_bytes(rows, wl.ADDRMS_HIDDEN, mode)
+    elif name.startswith("silu_mul"):
+        rows = args.size or wl.SILU_ROWS
+        mode = fc.FUSE_FUSED if name == "silu_mul_fused" else fc.FUSE_UNFUSED
+        gus = [wl.silu_input(rows, wl.SILU_COLS, device=dev, salt=r_) for r_ in range(2)]
+        ys = [torch.empty(rows, wl.SILU_COLS, dtype=gus[0].dtype, device=dev) for _ in range(2)]
+        C = wl.SILU_COLS
+        for i in range(L):
+            base = gus[i % 2].data_ptr()
+            rc = lib.fuse_silu_mul(base, base + 2 * C, 2 * C, ys[i % 2].data_ptr(), rows, C,
+                                   fc.FUSE_BF16, mode, stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_silu_mul_bytes(rows, C, fc.FUSE_BF16, mode)
     elif name == "gemm":
         M = args.size or 4096
         A, B, bias, Rr = wl.gemm_input(M, device=dev)

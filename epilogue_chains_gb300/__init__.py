@@ -77,6 +77,10 @@ SIGNATURES = {
     "fuse_launch_model": ([_I64, ctypes.c_double, ctypes.c_double, ctypes.c_double,
                            ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_double),
                            ctypes.POINTER(ctypes.c_double)], _I32),
+    "fuse_add_rmsnorm": ([_P, _P, _P, _P, _P, _I64, _I64, _F32, _I32, _P, _SZ, _P], _I32),
+    "fuse_silu_mul": ([_P, _P, _I64, _P, _I64, _I64, _I32, _I32, _P], _I32),
+    "fuse_add_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
+    "fuse_silu_mul_bytes": ([_I64, _I64, _I32, _I32], _I64),
     "fuse_chain_bytes": ([_I32, _I64, _I32, _I32], _I64),
     "fuse_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
     "fuse_causal_softmax_bytes": ([_I64, _I64, _I32, _I32, _I32], _I64),
@@ -194,6 +198,37 @@ def fuse_rmsnorm(x, w, y, eps: float, mode: int = FUSE_FUSED, workspace=None, st
                             _ptr(workspace), ws_size, _stream(stream)), "fuse_rmsnorm")
 
 
+def fuse_add_rmsnorm(x, r, w, h, y, eps: float, mode: int = FUSE_FUSED, workspace=None,
+                     stream=None) -> None:
+    """h = x + r; y = h * rsqrt(mean(h^2, -1) + eps) * w over rows of [rows, hidden] fp32."""
+    import torch
+    _need_device(x, r, w, h, y)
+    rows, hidden = x.shape
+    lib = _load()
+    ws_bytes = lib.fuse_rmsnorm_workspace_bytes(rows, hidden, mode)
+    if ws_bytes and workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=x.device)
+    ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib.fuse_add_rmsnorm(_ptr(x), _ptr(r), _ptr(w), _ptr(h), _ptr(y), rows, hidden,
+                                float(eps), mode, _ptr(workspace), ws_size, _stream(stream)),
+           "fuse_add_rmsnorm")
+
+
+def fuse_silu_mul(g, u, y, mode: int = FUSE_FUSED, stream=None) -> None:
+    """y = SiLU(g) * u.  g and u: [rows, cols] tensors (possibly the two column halves of one
+    merged [rows, 2 cols] tensor: same row stride); y: contiguous [rows, cols]."""
+    for t in (g, u, y):
+        if not t.is_cuda or t.dim() != 2 or t.stride(1) != 1:
+            raise ValueError("g, u, y must be 2-D CUDA tensors with unit column stride")
+    if g.shape != u.shape or g.shape != y.shape or g.stride(0) != u.stride(0):
+        raise ValueError("g, u, y must have one shape and g, u one row stride")
+    if not y.is_contiguous() or g.dtype != u.dtype or g.dtype != y.dtype:
+        raise ValueError("y must be contiguous and all three of one dtype")
+    rows, cols = g.shape
+    _check(_load().fuse_silu_mul(_ptr(g), _ptr(u), g.stride(0), _ptr(y), rows, cols,
+                                 _dtype_code(g), mode, _stream(stream)), "fuse_silu_mul")
+
+
 def fuse_rmsnorm_unfused_static(x, w, y, eps: float, stream=None) -> None:
     """Unfused RMSNorm with its row statistics in the library's own fixed device array (no
     workspace, no allocation; rows <= FUSE_RMSNORM_STATIC_MAX_ROWS)."""
@@ -270,6 +305,14 @@ def fuse_best_plan(stages, elem_bytes: int, model) -> tuple:
     _check(_load().fuse_best_plan(st, len(st), elem_bytes, ctypes.byref(_model(model)),
                                   ctypes.byref(mask), ctypes.byref(sec)), "fuse_best_plan")
     return mask.value, sec.value
+
+
+def fuse_add_rmsnorm_bytes(rows: int, hidden: int, mode: int) -> int:
+    return _load().fuse_add_rmsnorm_bytes(rows, hidden, mode)
+
+
+def fuse_silu_mul_bytes(rows: int, cols: int, dtype: int, mode: int) -> int:
+    return _load().fuse_silu_mul_bytes(rows, cols, dtype, mode)
 
 
 def fuse_launch_model(n_kernels: int, t_launch: float, t_exec: float, t_dispatch: float) -> dict:

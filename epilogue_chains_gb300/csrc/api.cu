@@ -17,6 +17,8 @@ int softmax_report_count();
 int softmax_report(int i, fuse_kernel_record* out);
 int gemm_report_count();
 int gemm_report(int i, fuse_kernel_record* out);
+int silu_report_count();
+int silu_report(int i, fuse_kernel_record* out);
 int watchdog_take();  // 1 if a bounded device wait expired since the last call (and clears it)
 
 namespace {
@@ -88,6 +90,7 @@ const ReportTable kTables[] = {
     {fc::rmsnorm_report_count, fc::rmsnorm_report},
     {fc::softmax_report_count, fc::softmax_report},
     {fc::gemm_report_count, fc::gemm_report},
+    {fc::silu_report_count, fc::silu_report},
 };
 }  // namespace
 

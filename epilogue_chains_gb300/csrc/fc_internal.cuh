@@ -123,4 +123,24 @@ template <> struct Vec16<__nv_bfloat16> {
 __device__ __forceinline__ uint4 ld_stream(const uint4* p) { return __ldcs(p); }
 __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) { __stcs(p, v); }
 
+// 32-byte vectors (8 fp32 or 16 fp16/bf16 values) with streaming 256-bit ld/st.global.cs (sm_100+)
+template <typename T> struct Vec32 {
+    static constexpr int N = 32 / sizeof(T);
+    __device__ __forceinline__ static void load(const T* p, float* f) {
+        uint32_t w[8];
+        asm volatile("ld.global.cs.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                     : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]),
+                       "=r"(w[6]), "=r"(w[7])
+                     : "l"(p));
+        Vec16<T>::unpack(make_uint4(w[0], w[1], w[2], w[3]), f);
+        Vec16<T>::unpack(make_uint4(w[4], w[5], w[6], w[7]), f + N / 2);
+    }
+    __device__ __forceinline__ static void store(T* p, const float* f) {
+        const uint4 lo = Vec16<T>::pack(f), hi = Vec16<T>::pack(f + N / 2);
+        asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(lo.x),
+                     "r"(lo.y), "r"(lo.z), "r"(lo.w), "r"(hi.x), "r"(hi.y), "r"(hi.z), "r"(hi.w)
+                     : "memory");
+    }
+};
+
 }  // namespace fc

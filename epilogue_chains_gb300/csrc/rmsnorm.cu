@@ -1,8 +1,11 @@
-// rmsnorm.cu -- RMSNorm, fused (one pass) and unfused (four kernels).
+// rmsnorm.cu -- RMSNorm, fused (one pass) and unfused (four kernels); and residual add + RMSNorm.
 //
 // [OFCG] §3.2 and fusion_lab [A2]: unfused RMSNorm is x*x -> reduce-mean -> x*r -> *g, each step
 // a kernel that reads and writes HBM; fused it is one pass.  Per row i:
 //     r_i = 1/sqrt(mean_j x_ij^2 + eps),   y_ij = (x_ij * r_i) * w_j.
+// [OFCG] appendix launch_model [F3] also fuses the residual add into the RMSNorm that follows
+// it: h = x + r (the new residual stream, written out), y = RMSNorm(h) * w, one pass, against a
+// residual-add kernel followed by the four RMSNorm kernels unfused.
 //
 // GB300 design (fused): persistent CTAs (one wave: SM count x occupancy), each holding a whole row
 // in registers (16 B vector loads, VPT vectors per thread) while the next row's loads are already
@@ -40,10 +43,12 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // Persistent: CTA b handles rows b, b + gridDim.x, ...; while it reduces and writes one row, the
 // next row's loads are already in flight (PREFETCH).  The per-warp partial sums are double
 // buffered, so one barrier per row suffices: a warp that runs ahead writes the other buffer.
-template <int VPT, bool PREFETCH>
+// ADD: the row is h = x + res (one fp32 rounding per element), stored to h before it is
+// normalised; h may be x or res itself (each element is read before the same thread writes it).
+template <int VPT, bool PREFETCH, bool ADD>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
-    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int64_t rows,
-    int hidden, float eps) {
+    const float* x, const float* res, const float* __restrict__ w, float* h,
+    float* __restrict__ y, int64_t rows, int hidden, float eps) {
     __shared__ float red[2][kRowThreads / 32];
     const int nv = hidden / 4;
     const float4* wv = reinterpret_cast<const float4*>(w);
@@ -51,10 +56,16 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
     float4 nxt[VPT];
     auto load_row = [&](int64_t r) {
         const float4* xr = reinterpret_cast<const float4*>(x + r * hidden);
+        const float4* rr = reinterpret_cast<const float4*>(res + r * hidden);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
             const int idx = threadIdx.x + k * kRowThreads;
             nxt[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (ADD && idx < nv) {
+                const float4 b = __ldcs(rr + idx);
+                nxt[k].x = __fadd_rn(nxt[k].x, b.x); nxt[k].y = __fadd_rn(nxt[k].y, b.y);
+                nxt[k].z = __fadd_rn(nxt[k].z, b.z); nxt[k].w = __fadd_rn(nxt[k].w, b.w);
+            }
         }
     };
     int64_t row = blockIdx.x;
@@ -64,6 +75,14 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
         float4 v[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) v[k] = nxt[k];
+        if (ADD) {
+            float4* hr = reinterpret_cast<float4*>(h + row * hidden);
+#pragma unroll
+            for (int k = 0; k < VPT; ++k) {
+                const int idx = threadIdx.x + k * kRowThreads;
+                if (idx < nv) __stcs(hr + idx, v[k]);
+            }
+        }
         if (PREFETCH && row + gridDim.x < rows) load_row(row + gridDim.x);
         float ss = 0.0f;
 #pragma unroll
@@ -97,10 +116,10 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
 }
 
 // Element-wise variant for rows that are not whole 16-byte vectors (odd hidden or offsets).
-template <int EPT>
+template <int EPT, bool ADD>
 __global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel(
-    const float* __restrict__ x, const float* __restrict__ w, float* __restrict__ y, int hidden,
-    float eps) {
+    const float* x, const float* res, const float* __restrict__ w, float* h, float* __restrict__ y,
+    int hidden, float eps) {
     __shared__ float red[kRowThreadsScalar / 32];
     const int64_t row = blockIdx.x;
     const float* xr = x + row * hidden;
@@ -111,6 +130,10 @@ __global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel
     for (int k = 0; k < EPT; ++k) {
         const int j = threadIdx.x + k * kRowThreadsScalar;
         v[k] = j < hidden ? xr[j] : 0.0f;
+        if (ADD && j < hidden) {
+            v[k] = __fadd_rn(v[k], res[row * hidden + j]);
+            h[row * hidden + j] = v[k];
+        }
         ss += v[k] * v[k];
     }
     const float total = block_sum<kRowThreadsScalar>(ss, red);
@@ -123,6 +146,26 @@ __global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel
 }
 
 // ------------------------------------------------------------------------- unfused kernels
+// (0, residual form only) h = x + res
+__global__ void __launch_bounds__(kEwBlock) residual_add_kernel(const float* x, const float* res,
+                                                                float* h, int64_t n, bool vec) {
+    const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t done = 0;
+    if (vec) {
+        const int64_t nv = n / 4;
+        for (int64_t i = tid; i < nv; i += nthr) {
+            float4 a = __ldcs(reinterpret_cast<const float4*>(x) + i);
+            const float4 b = __ldcs(reinterpret_cast<const float4*>(res) + i);
+            a.x = __fadd_rn(a.x, b.x); a.y = __fadd_rn(a.y, b.y);
+            a.z = __fadd_rn(a.z, b.z); a.w = __fadd_rn(a.w, b.w);
+            __stcs(reinterpret_cast<float4*>(h) + i, a);
+        }
+        done = nv * 4;
+    }
+    for (int64_t i = done + tid; i < n; i += nthr) h[i] = __fadd_rn(x[i], res[i]);
+}
+
 // (1) sq = x*x   (2) ms = rowmean(sq)   (3) t = x * rsqrt(ms + eps)   (4) y = t * w
 __global__ void __launch_bounds__(kEwBlock) rms_square_kernel(const float* __restrict__ x,
                                                               float* __restrict__ y, int64_t n,
@@ -195,24 +238,47 @@ __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict_
     for (int64_t i = tid; i < n; i += nthr) y[i] = __fmul_rn(y[i], w[i % hidden]);
 }
 
-template <int VPT>
-int launch_fused_vec(const float* x, const float* w, float* y, int64_t rows, int hidden, float eps,
-                     cudaStream_t st) {
-    constexpr bool kPrefetch = VPT <= 8;  // two rows in registers up to hidden 8192
-    static const int occ = blocks_per_sm(rmsnorm_fused_kernel<VPT, kPrefetch>, kRowThreads);
+template <int VPT, bool ADD>
+int launch_fused_vec(const float* x, const float* res, const float* w, float* h, float* y,
+                     int64_t rows, int hidden, float eps, cudaStream_t st) {
+    // two rows in registers (the prefetch) up to hidden 8192, 4096 when the residual is added
+    constexpr bool kPrefetch = ADD ? VPT <= 4 : VPT <= 8;
+    static const int occ = blocks_per_sm(rmsnorm_fused_kernel<VPT, kPrefetch, ADD>, kRowThreads);
     int64_t grid = static_cast<int64_t>(sm_count()) * occ;
     if (grid > rows) grid = rows;
-    rmsnorm_fused_kernel<VPT, kPrefetch><<<static_cast<unsigned>(grid), kRowThreads, 0, st>>>(
-        x, w, y, rows, hidden, eps);
+    rmsnorm_fused_kernel<VPT, kPrefetch, ADD><<<static_cast<unsigned>(grid), kRowThreads, 0, st>>>(
+        x, res, w, h, y, rows, hidden, eps);
     return check_launch();
 }
 
-template <int EPT>
-int launch_fused_scalar(const float* x, const float* w, float* y, int64_t rows, int hidden,
-                        float eps, cudaStream_t st) {
-    rmsnorm_fused_scalar_kernel<EPT><<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(
-        x, w, y, hidden, eps);
+template <int EPT, bool ADD>
+int launch_fused_scalar(const float* x, const float* res, const float* w, float* h, float* y,
+                        int64_t rows, int hidden, float eps, cudaStream_t st) {
+    rmsnorm_fused_scalar_kernel<EPT, ADD><<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(
+        x, res, w, h, y, hidden, eps);
     return check_launch();
+}
+
+// The fused form for hidden <= 16384: the row lives in registers (VPT float4 or EPT floats per
+// thread).  With ADD the row is x + res and is also stored to h.
+template <bool ADD>
+int fused_dispatch(const float* x, const float* res, const float* w, float* h, float* y,
+                   int64_t rows, int H, float eps, bool vec, cudaStream_t st) {
+    if (H > 16384) return FUSE_EUNSUPPORTED;
+    if (vec) {
+        const int nv = H / 4;
+        if (nv <= 1 * kRowThreads) return launch_fused_vec<1, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 2 * kRowThreads) return launch_fused_vec<2, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 4 * kRowThreads) return launch_fused_vec<4, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 8 * kRowThreads) return launch_fused_vec<8, ADD>(x, res, w, h, y, rows, H, eps, st);
+        return launch_fused_vec<16, ADD>(x, res, w, h, y, rows, H, eps, st);
+    }
+    if (H <= 1 * kRowThreadsScalar) return launch_fused_scalar<1, ADD>(x, res, w, h, y, rows, H, eps, st);
+    if (H <= 2 * kRowThreadsScalar) return launch_fused_scalar<2, ADD>(x, res, w, h, y, rows, H, eps, st);
+    if (H <= 4 * kRowThreadsScalar) return launch_fused_scalar<4, ADD>(x, res, w, h, y, rows, H, eps, st);
+    if (H <= 8 * kRowThreadsScalar) return launch_fused_scalar<8, ADD>(x, res, w, h, y, rows, H, eps, st);
+    if (H <= 16 * kRowThreadsScalar) return launch_fused_scalar<16, ADD>(x, res, w, h, y, rows, H, eps, st);
+    return launch_fused_scalar<32, ADD>(x, res, w, h, y, rows, H, eps, st);
 }
 
 unsigned ew_grid(int64_t units) {
@@ -224,11 +290,30 @@ unsigned ew_grid(int64_t units) {
 
 }  // namespace
 
-int rmsnorm_report_count() { return 3; }
+// The four unfused RMSNorm kernels on x (the residual form passes h as x); y != x.
+int unfused_steps(const float* x, const float* w, float* y, float* ms, int64_t rows, int H,
+                  float eps, bool vec, cudaStream_t st) {
+    const int64_t n = rows * H;
+    const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
+    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
+    int rc = check_launch();
+    if (rc) return rc;
+    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
+    if ((rc = check_launch())) return rc;
+    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
+    if ((rc = check_launch())) return rc;
+    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
+    return check_launch();
+}
+
+int rmsnorm_report_count() { return 4; }
 int rmsnorm_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true>,
+        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true, false>,
                                        "rmsnorm_fused_kernel<VPT=4> (hidden 4096)", kRowThreads, 0, out);
+        case 3: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true, true>,
+                                       "rmsnorm_fused_kernel<VPT=4, +residual> (hidden 4096)",
+                                       kRowThreads, 0, out);
         case 1: return describe_kernel((const void*)rms_rowmean_kernel,
                                        "rms_rowmean_kernel (unfused step 2)", kRowThreadsScalar, 0, out);
         case 2: return describe_kernel((const void*)rms_scale_kernel,
@@ -259,40 +344,53 @@ extern "C" int fuse_rmsnorm(const float* x, const float* w, float* y, int64_t ro
     const int H = static_cast<int>(hidden);
     const bool vec = (H % 4 == 0) && is_aligned(x, 16) && is_aligned(y, 16) && is_aligned(w, 16);
 
-    if (mode == FUSE_FUSED) {
-        if (H > 16384) return FUSE_EUNSUPPORTED;
-        if (vec) {
-            const int nv = H / 4;
-            if (nv <= 1 * kRowThreads) return launch_fused_vec<1>(x, w, y, rows, H, eps, st);
-            if (nv <= 2 * kRowThreads) return launch_fused_vec<2>(x, w, y, rows, H, eps, st);
-            if (nv <= 4 * kRowThreads) return launch_fused_vec<4>(x, w, y, rows, H, eps, st);
-            if (nv <= 8 * kRowThreads) return launch_fused_vec<8>(x, w, y, rows, H, eps, st);
-            return launch_fused_vec<16>(x, w, y, rows, H, eps, st);
-        }
-        if (H <= 1 * kRowThreadsScalar) return launch_fused_scalar<1>(x, w, y, rows, H, eps, st);
-        if (H <= 2 * kRowThreadsScalar) return launch_fused_scalar<2>(x, w, y, rows, H, eps, st);
-        if (H <= 4 * kRowThreadsScalar) return launch_fused_scalar<4>(x, w, y, rows, H, eps, st);
-        if (H <= 8 * kRowThreadsScalar) return launch_fused_scalar<8>(x, w, y, rows, H, eps, st);
-        if (H <= 16 * kRowThreadsScalar) return launch_fused_scalar<16>(x, w, y, rows, H, eps, st);
-        return launch_fused_scalar<32>(x, w, y, rows, H, eps, st);
-    }
+    if (mode == FUSE_FUSED) return fused_dispatch<false>(x, nullptr, w, nullptr, y, rows, H, eps, vec, st);
 
     // FUSE_UNFUSED: four kernels; the N-sized intermediates live in y, the row means in workspace.
     if (!workspace || ws_bytes < fuse_rmsnorm_workspace_bytes(rows, hidden, mode)) return FUSE_EWORKSPACE;
     if (!is_aligned(workspace, 4)) return FUSE_EALIGN;
     if (x == y) return FUSE_EINVAL;  // step 3 re-reads x after step 1 overwrote y
-    float* ms = static_cast<float*>(workspace);
+    return unfused_steps(x, w, y, static_cast<float*>(workspace), rows, H, eps, vec, st);
+}
+
+extern "C" int fuse_add_rmsnorm(const float* x, const float* r, const float* w, float* h, float* y,
+                                int64_t rows, int64_t hidden, float eps, int mode, void* workspace,
+                                size_t ws_bytes, fuse_stream_t stream) {
+    using namespace fc;
+    if (rows < 0 || hidden < 1 || hidden > 65536 || !(eps >= 0.0f)) return FUSE_EINVAL;
+    if (mode != FUSE_FUSED && mode != FUSE_UNFUSED) return FUSE_EINVAL;
+    if (rows > 2147483647LL) return FUSE_EUNSUPPORTED;
+    if (rows == 0) return FUSE_OK;
+    if (!x || !r || !w || !h || !y) return FUSE_EINVAL;
+    if (y == x || y == r || y == h) return FUSE_EINVAL;  // h may be x or r (in place), y may not
+    if (!is_aligned(x, 4) || !is_aligned(r, 4) || !is_aligned(w, 4) || !is_aligned(h, 4) ||
+        !is_aligned(y, 4))
+        return FUSE_EALIGN;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int H = static_cast<int>(hidden);
+    const bool vec = (H % 4 == 0) && is_aligned(x, 16) && is_aligned(r, 16) && is_aligned(h, 16) &&
+                     is_aligned(y, 16) && is_aligned(w, 16);
+    if (mode == FUSE_FUSED) return fused_dispatch<true>(x, r, w, h, y, rows, H, eps, vec, st);
+
+    // FUSE_UNFUSED: the residual-add kernel, then the four RMSNorm kernels on h.
+    if (!workspace || ws_bytes < fuse_rmsnorm_workspace_bytes(rows, hidden, mode)) return FUSE_EWORKSPACE;
+    if (!is_aligned(workspace, 4)) return FUSE_EALIGN;
     const int64_t n = rows * hidden;
-    const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
-    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
-    int rc = check_launch();
+    const bool avec = is_aligned(x, 16) && is_aligned(r, 16) && is_aligned(h, 16);
+    residual_add_kernel<<<ew_grid(avec ? n / 4 : n), kEwBlock, 0, st>>>(x, r, h, n, avec);
+    const int rc = check_launch();
     if (rc) return rc;
-    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
-    if ((rc = check_launch())) return rc;
-    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
-    if ((rc = check_launch())) return rc;
-    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
-    return check_launch();
+    return unfused_steps(h, w, y, static_cast<float*>(workspace), rows, H, eps, vec, st);
+}
+
+extern "C" int64_t fuse_add_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode) {
+    if (rows < 0 || hidden < 1) return FUSE_EINVAL;
+    const int64_t n = rows * hidden, b = 4;
+    // fused: read x and r, write h and y, read w once
+    if (mode == FUSE_FUSED) return 4 * n * b + hidden * b;
+    // unfused: add (r x, r r, w h) + the four RMSNorm kernels on h (7 N b + row means + w)
+    if (mode == FUSE_UNFUSED) return 10 * n * b + 2 * rows * b + hidden * b;
+    return FUSE_EINVAL;
 }
 
 extern "C" int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode) {
@@ -345,18 +443,7 @@ extern "C" int fuse_rmsnorm_unfused_static(const float* x, const float* w, float
 
     // Same four kernels as the unfused mode of fuse_rmsnorm().  Every row statistic the later
     // kernels read is written by the row-mean kernel of the same call, so nothing is cleared.
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int H = static_cast<int>(hidden);
-    const int64_t n = rows * hidden;
-    const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
-    const bool vec = (H % 4 == 0) && fvec && is_aligned(w, 16);
-    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
-    int rc = check_launch();
-    if (rc) return rc;
-    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
-    if ((rc = check_launch())) return rc;
-    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
-    if ((rc = check_launch())) return rc;
-    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
-    return check_launch();
+    const bool vec = (H % 4 == 0) && is_aligned(x, 16) && is_aligned(y, 16) && is_aligned(w, 16);
+    return unfused_steps(x, w, y, ms, rows, H, eps, vec, reinterpret_cast<cudaStream_t>(stream));
 }

@@ -146,6 +146,43 @@ size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode);
 int fuse_rmsnorm_unfused_static(const float* x, const float* w, float* y, int64_t rows,
                                 int64_t hidden, float eps, fuse_stream_t stream);
 
+/* ===================================================================== residual add + RMSNorm
+ * [OFCG] appendix launch_model [F3]: after fusion a decoder layer runs "residual + RMSNorm" as one
+ * kernel where the unfused layer runs a residual-add kernel and four RMSNorm kernels.  Per row i:
+ *     h_ij = x_ij + r_ij  (one fp32 rounding; the new residual stream, written out),
+ *     y_ij = (h_ij * rsqrt(mean_j h_ij^2 + eps)) * w_j   (RMSNorm of h as fuse_rmsnorm()).
+ *   x, r, h, y  device fp32 [rows, hidden]; w device fp32 [hidden].  h may be x or r itself (in
+ *           place); y must differ from x, r and h.  Otherwise no two of them may overlap.
+ *   mode    FUSE_FUSED: one kernel, reads x and r once, writes h and y once (4 N b + 4 hidden);
+ *             hidden <= 16384 (larger -> FUSE_EUNSUPPORTED).
+ *           FUSE_UNFUSED: five kernels, h = x + r, then the four RMSNorm kernels of fuse_rmsnorm()
+ *             on h (10 N b + row means + w).  Needs workspace of
+ *             fuse_rmsnorm_workspace_bytes(rows, hidden, FUSE_UNFUSED) bytes.
+ * Numerics: h is bit-identical in both modes; y as fuse_rmsnorm() (fp32 accumulation).
+ */
+int fuse_add_rmsnorm(const float* x, const float* r, const float* w, float* h, float* y,
+                     int64_t rows, int64_t hidden, float eps, int mode, void* workspace,
+                     size_t ws_bytes, fuse_stream_t stream);
+
+/* ===================================================================== SiLU(gate) * up
+ * [OFCG] appendix launch_model [F3]: "SiLU + multiply" fused into one kernel after the gate/up
+ * GEMM, where the unfused layer runs a SiLU kernel and an element-wise multiply kernel.
+ *     y_ij = SiLU(g_ij) * u_ij,   SiLU(v) = v / (1 + e^-v).
+ *   g, u    device [rows, cols] of `dtype` with a common row stride ld >= cols elements (the two
+ *           halves of one merged [rows, 2 cols] gate/up output: g = base, u = base + cols,
+ *           ld = 2 cols; separate dense tensors: ld = cols).  This is the one strided operand
+ *           layout of the library.
+ *   y       device [rows, cols], dense.  y must not overlap u; it may be g itself when ld == cols.
+ *   dtype   FUSE_F32 / FUSE_F16 / FUSE_BF16 storage, fp32 math (SiLU via exp2 and reciprocal on
+ *           the special-function unit: about 2^-21 relative error before the final rounding).
+ *   mode    FUSE_FUSED: one kernel (3 N b).  FUSE_UNFUSED: two kernels, s = SiLU(g) stored in y
+ *           (rounded to dtype), then y = s * u (5 N b).
+ * The 32-byte vector path needs cols and ld multiples of 32 bytes and 32-byte aligned pointers;
+ * other shapes use an element-wise kernel.
+ */
+int fuse_silu_mul(const void* g, const void* u, int64_t ld, void* y, int64_t rows, int64_t cols,
+                  int dtype, int mode, fuse_stream_t stream);
+
 /* ===================================================================== causal softmax
  * [OFCG] fusion_lab [E] (max -> subtract -> exp -> sum -> divide over the last axis), §3.5
  * (causal mask: query i sees keys j <= i; block-granular skipping) and [A3] (8 copies of the
@@ -252,6 +289,8 @@ int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode);
 int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode);
 int64_t fuse_causal_softmax_bytes(int64_t batch_heads, int64_t S, int skip_tile, int out_dtype,
                                   int mode);
+int64_t fuse_add_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode);
+int64_t fuse_silu_mul_bytes(int64_t rows, int64_t cols, int dtype, int mode);
 
 /* ===================================================================== reports and status
  * [K4] §③ and [C05] §6.2: registers per thread, spills and blocks per SM decide when fusion
