@@ -244,11 +244,11 @@ def run_ours(args, rank, world, local):
         # -------------------------------------------------------------- RMSNorm
         with torch.cuda.stream(stream):
             rx, rw = wl.rmsnorm_input(device=dev, salt=rank)
-            rxs = [rx, rx.clone()]
-            rys = [torch.empty_like(rx) for _ in range(2)]
+            rxs = [rx] + [rx.clone() for _ in range(3)]   # 4 x/y pairs: 256 MiB, twice the L2
+            rys = [torch.empty_like(rx) for _ in range(4)]
             rws = torch.empty(fc.fuse_rmsnorm_workspace_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_UNFUSED),
                               dtype=torch.uint8, device=dev)
-        rrot = rotating(2)
+        rrot = rotating(4)
 
         def rms(mode):
             def fn():
@@ -261,7 +261,7 @@ def run_ours(args, rank, world, local):
         rb = {m: fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
         groups += [
             Group("rmsnorm_fused", [("r", rms(fc.FUSE_FUSED), rb[fc.FUSE_FUSED])] * 2, rms(fc.FUSE_FUSED),
-                  "hbm", "rmsnorm_fused_kernel", 1),
+                  "hbm", "rmsnorm_row_kernel", 1),
             Group("rmsnorm_unfused", [("r", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED])] * 2,
                   rms(fc.FUSE_UNFUSED), "hbm", None, None),
         ]
@@ -302,7 +302,7 @@ def run_ours(args, rank, world, local):
         sb = {m: fc.fuse_silu_mul_bytes(SR, SC, fc.FUSE_BF16, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
         groups += [
             Group("add_rmsnorm_fused", [("r", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED])] * 2,
-                  addrms(fc.FUSE_FUSED), "hbm", "rmsnorm_fused_kernel<+residual>", 1),
+                  addrms(fc.FUSE_FUSED), "hbm", "rmsnorm_row_kernel<+residual>", 1),
             Group("add_rmsnorm_unfused", [("r", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED])] * 2,
                   addrms(fc.FUSE_UNFUSED), "hbm", None, None),
             Group("silu_mul_fused", [("s", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED])] * 2,
@@ -567,8 +567,9 @@ def run_ours(args, rank, world, local):
                                    "a_s~U[0.9,1.1], b_s~U[-0.1,0.1], ReLU on even s",
                        "N": N, "K": list(KS),
                        "step": "all rows" if args.rows == "all" else "chain rows",
-                       "l2": "inputs larger than L2 or rotated (chain: 4 x/y pairs = 512 MiB; decode "
-                             "GEMM: 4 weight copies); each row group led by an untimed same-kind call",
+                       "l2": "inputs larger than L2 or rotated (chain: 4 x/y pairs = 512 MiB; RMSNorm: "
+                             "4 pairs = 256 MiB; decode GEMM: 4 weight copies); each row group led by "
+                             "an untimed same-kind call",
                        "parallelism": f"replicas x{world}"},
             "frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
             "roofline": roofline,
@@ -848,12 +849,13 @@ def run_profile(args):
     elif name.startswith("rmsnorm"):
         rows = args.size or wl.RMS_ROWS
         mode = fc.FUSE_FUSED if name == "rmsnorm_fused" else fc.FUSE_UNFUSED
-        x, w = wl.rmsnorm_input(rows, wl.RMS_HIDDEN, device=dev)
-        ys = [torch.empty_like(x) for _ in range(2)]
+        x0, w = wl.rmsnorm_input(rows, wl.RMS_HIDDEN, device=dev)
+        xs = [x0] + [x0.clone() for _ in range(3)]
+        ys = [torch.empty_like(x0) for _ in range(4)]
         ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.RMS_HIDDEN, mode)),
                          dtype=torch.uint8, device=dev)
         for i in range(L):
-            rc = lib.fuse_rmsnorm(x.data_ptr(), w.data_ptr(), ys[i % 2].data_ptr(), rows,
+            rc = lib.fuse_rmsnorm(xs[i % 4].data_ptr(), w.data_ptr(), ys[i % 4].data_ptr(), rows,
                                   wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)

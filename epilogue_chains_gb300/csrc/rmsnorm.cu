@@ -7,14 +7,16 @@
 // it: h = x + r (the new residual stream, written out), y = RMSNorm(h) * w, one pass, against a
 // residual-add kernel followed by the four RMSNorm kernels unfused.
 //
-// GB300 design (fused): persistent CTAs (one wave: SM count x occupancy), each holding a whole row
-// in registers (16 B vector loads, VPT vectors per thread) while the next row's loads are already
-// in flight; a warp-shuffle reduction followed by a shared-memory reduction across the CTA's
-// warps, then the scaled row is written with 16 B streaming stores.  x is read from HBM exactly
-// once; w (16 KB at hidden 4096) stays in L1/L2.  At [2048, 4096] fp32 (32 MiB each way) this
-// runs at the speed of a cudaMemcpy of the same 32 MiB on GB300 (about 16 us): at this size the
-// fixed cost of filling and draining the memory pipeline dominates, for copies and for this
-// kernel alike (warp-per-row and TMA-fed variants measured no faster).
+// GB300 design (fused): one CTA per row, the whole row in registers (16-byte vector loads, VPT
+// vectors per thread, 512 threads for rows of 4096), a warp-shuffle reduction followed by a
+// shared-memory reduction across the CTA's warps, then the scaled row written with 16-byte
+// streaming stores.  x (and the residual) are read from HBM exactly once; w (16 KB at hidden 4096)
+// stays in L1/L2.  An exact grid of short CTAs lets the hardware scheduler balance rows over the
+// SMs: on GB300 this matches a plain 2-in/2-out streaming copy of the same bytes for the residual
+// form (24.4 us at [2048, 4096]), where a persistent grid that prefetched the next row lost ~8 %
+// to its last, partial round of rows; for RMSNorm alone (32 MiB each way) both run at the speed of
+// a cudaMemcpy of the same 32 MiB (about 16 us), the fixed cost of filling and draining the memory
+// pipeline dominating at that size.
 #include <mutex>
 
 #include "fc_internal.cuh"
@@ -22,7 +24,6 @@
 namespace fc {
 namespace {
 
-constexpr int kRowThreads = 256;     // vector path: 256 threads x VPT float4 per row
 constexpr int kRowThreadsScalar = 512;
 constexpr int kEwBlock = 256;
 
@@ -40,78 +41,57 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
     return t;
 }
 
-// Persistent: CTA b handles rows b, b + gridDim.x, ...; while it reduces and writes one row, the
-// next row's loads are already in flight (PREFETCH).  The per-warp partial sums are double
-// buffered, so one barrier per row suffices: a warp that runs ahead writes the other buffer.
-// ADD: the row is h = x + res (one fp32 rounding per element), stored to h before it is
-// normalised; h may be x or res itself (each element is read before the same thread writes it).
-template <int VPT, bool PREFETCH, bool ADD>
-__global__ void __launch_bounds__(kRowThreads) rmsnorm_fused_kernel(
-    const float* x, const float* res, const float* __restrict__ w, float* h,
-    float* __restrict__ y, int64_t rows, int hidden, float eps) {
-    __shared__ float red[2][kRowThreads / 32];
+// One CTA per row.  ADD: the row is h = x + res (one fp32 rounding per element), stored to h
+// before it is normalised; h may be x or res itself (each element is read before the same thread
+// writes it).
+template <int THR, int VPT, bool ADD>
+__global__ void __launch_bounds__(THR) rmsnorm_row_kernel(const float* x, const float* res,
+                                                          const float* __restrict__ w, float* h,
+                                                          float* __restrict__ y, int hidden, float eps) {
+    __shared__ float red[THR / 32];
+    const int64_t row = blockIdx.x;
     const int nv = hidden / 4;
-    const float4* wv = reinterpret_cast<const float4*>(w);
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    float4 nxt[VPT];
-    auto load_row = [&](int64_t r) {
-        const float4* xr = reinterpret_cast<const float4*>(x + r * hidden);
-        const float4* rr = reinterpret_cast<const float4*>(res + r * hidden);
+    const float4* xr = reinterpret_cast<const float4*>(x + row * hidden);
+    float4 v[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int idx = threadIdx.x + k * THR;
+        v[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (ADD) {
+        const float4* rr = reinterpret_cast<const float4*>(res + row * hidden);
+        float4* hr = reinterpret_cast<float4*>(h + row * hidden);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-            const int idx = threadIdx.x + k * kRowThreads;
-            nxt[k] = idx < nv ? __ldcs(xr + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (ADD && idx < nv) {
-                const float4 b = __ldcs(rr + idx);
-                nxt[k].x = __fadd_rn(nxt[k].x, b.x); nxt[k].y = __fadd_rn(nxt[k].y, b.y);
-                nxt[k].z = __fadd_rn(nxt[k].z, b.z); nxt[k].w = __fadd_rn(nxt[k].w, b.w);
-            }
-        }
-    };
-    int64_t row = blockIdx.x;
-    if (row < rows) load_row(row);
-    int buf = 0;
-    for (; row < rows; row += gridDim.x) {
-        float4 v[VPT];
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) v[k] = nxt[k];
-        if (ADD) {
-            float4* hr = reinterpret_cast<float4*>(h + row * hidden);
-#pragma unroll
-            for (int k = 0; k < VPT; ++k) {
-                const int idx = threadIdx.x + k * kRowThreads;
-                if (idx < nv) __stcs(hr + idx, v[k]);
-            }
-        }
-        if (PREFETCH && row + gridDim.x < rows) load_row(row + gridDim.x);
-        float ss = 0.0f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k)
-            ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-        if (lane == 0) red[buf][warp] = ss;
-        __syncthreads();
-        float total = 0.0f;
-#pragma unroll
-        for (int k = 0; k < kRowThreads / 32; ++k) total += red[buf][k];
-        buf ^= 1;
-        const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
-        float4* yr = reinterpret_cast<float4*>(y + row * hidden);
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-            const int idx = threadIdx.x + k * kRowThreads;
+            const int idx = threadIdx.x + k * THR;
             if (idx < nv) {
-                const float4 g = __ldg(wv + idx);
-                float4 o;
-                o.x = __fmul_rn(__fmul_rn(v[k].x, r), g.x);
-                o.y = __fmul_rn(__fmul_rn(v[k].y, r), g.y);
-                o.z = __fmul_rn(__fmul_rn(v[k].z, r), g.z);
-                o.w = __fmul_rn(__fmul_rn(v[k].w, r), g.w);
-                __stcs(yr + idx, o);
+                const float4 b = __ldcs(rr + idx);
+                v[k].x = __fadd_rn(v[k].x, b.x); v[k].y = __fadd_rn(v[k].y, b.y);
+                v[k].z = __fadd_rn(v[k].z, b.z); v[k].w = __fadd_rn(v[k].w, b.w);
+                __stcs(hr + idx, v[k]);
             }
         }
-        if (!PREFETCH && row + gridDim.x < rows) load_row(row + gridDim.x);
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+        ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+    const float total = block_sum<THR>(ss, red);
+    const float r = rsqrtf(__fdiv_rn(total, static_cast<float>(hidden)) + eps);
+    const float4* wv = reinterpret_cast<const float4*>(w);
+    float4* yr = reinterpret_cast<float4*>(y + row * hidden);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int idx = threadIdx.x + k * THR;
+        if (idx < nv) {
+            const float4 g = __ldg(wv + idx);
+            float4 o;
+            o.x = __fmul_rn(__fmul_rn(v[k].x, r), g.x);
+            o.y = __fmul_rn(__fmul_rn(v[k].y, r), g.y);
+            o.z = __fmul_rn(__fmul_rn(v[k].z, r), g.z);
+            o.w = __fmul_rn(__fmul_rn(v[k].w, r), g.w);
+            __stcs(yr + idx, o);
+        }
     }
 }
 
@@ -238,16 +218,11 @@ __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict_
     for (int64_t i = tid; i < n; i += nthr) y[i] = __fmul_rn(y[i], w[i % hidden]);
 }
 
-template <int VPT, bool ADD>
+template <int THR, int VPT, bool ADD>
 int launch_fused_vec(const float* x, const float* res, const float* w, float* h, float* y,
                      int64_t rows, int hidden, float eps, cudaStream_t st) {
-    // two rows in registers (the prefetch) up to hidden 8192, 4096 when the residual is added
-    constexpr bool kPrefetch = ADD ? VPT <= 4 : VPT <= 8;
-    static const int occ = blocks_per_sm(rmsnorm_fused_kernel<VPT, kPrefetch, ADD>, kRowThreads);
-    int64_t grid = static_cast<int64_t>(sm_count()) * occ;
-    if (grid > rows) grid = rows;
-    rmsnorm_fused_kernel<VPT, kPrefetch, ADD><<<static_cast<unsigned>(grid), kRowThreads, 0, st>>>(
-        x, res, w, h, y, rows, hidden, eps);
+    rmsnorm_row_kernel<THR, VPT, ADD><<<static_cast<unsigned>(rows), THR, 0, st>>>(x, res, w, h, y,
+                                                                                 hidden, eps);
     return check_launch();
 }
 
@@ -267,11 +242,12 @@ int fused_dispatch(const float* x, const float* res, const float* w, float* h, f
     if (H > 16384) return FUSE_EUNSUPPORTED;
     if (vec) {
         const int nv = H / 4;
-        if (nv <= 1 * kRowThreads) return launch_fused_vec<1, ADD>(x, res, w, h, y, rows, H, eps, st);
-        if (nv <= 2 * kRowThreads) return launch_fused_vec<2, ADD>(x, res, w, h, y, rows, H, eps, st);
-        if (nv <= 4 * kRowThreads) return launch_fused_vec<4, ADD>(x, res, w, h, y, rows, H, eps, st);
-        if (nv <= 8 * kRowThreads) return launch_fused_vec<8, ADD>(x, res, w, h, y, rows, H, eps, st);
-        return launch_fused_vec<16, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 128) return launch_fused_vec<128, 1, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 256) return launch_fused_vec<256, 1, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 512) return launch_fused_vec<512, 1, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 1024) return launch_fused_vec<512, 2, ADD>(x, res, w, h, y, rows, H, eps, st);
+        if (nv <= 2048) return launch_fused_vec<512, 4, ADD>(x, res, w, h, y, rows, H, eps, st);
+        return launch_fused_vec<512, 8, ADD>(x, res, w, h, y, rows, H, eps, st);
     }
     if (H <= 1 * kRowThreadsScalar) return launch_fused_scalar<1, ADD>(x, res, w, h, y, rows, H, eps, st);
     if (H <= 2 * kRowThreadsScalar) return launch_fused_scalar<2, ADD>(x, res, w, h, y, rows, H, eps, st);
@@ -309,11 +285,11 @@ int unfused_steps(const float* x, const float* w, float* y, float* ms, int64_t r
 int rmsnorm_report_count() { return 4; }
 int rmsnorm_report(int i, fuse_kernel_record* out) {
     switch (i) {
-        case 0: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true, false>,
-                                       "rmsnorm_fused_kernel<VPT=4> (hidden 4096)", kRowThreads, 0, out);
-        case 3: return describe_kernel((const void*)rmsnorm_fused_kernel<4, true, true>,
-                                       "rmsnorm_fused_kernel<VPT=4, +residual> (hidden 4096)",
-                                       kRowThreads, 0, out);
+        case 0: return describe_kernel((const void*)rmsnorm_row_kernel<512, 2, false>,
+                                       "rmsnorm_row_kernel<512 thr, VPT=2> (hidden 4096)", 512, 0, out);
+        case 3: return describe_kernel((const void*)rmsnorm_row_kernel<512, 2, true>,
+                                       "rmsnorm_row_kernel<512 thr, VPT=2, +residual> (hidden 4096)",
+                                       512, 0, out);
         case 1: return describe_kernel((const void*)rms_rowmean_kernel,
                                        "rms_rowmean_kernel (unfused step 2)", kRowThreadsScalar, 0, out);
         case 2: return describe_kernel((const void*)rms_scale_kernel,
