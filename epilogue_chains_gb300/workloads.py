@@ -20,6 +20,9 @@ Workload recipes (the five configurations of the hot path):
   6  SiLU(gate) * up: one merged gate/up output gu bf16 [2048, 2 x 14336] ~ N(0,1) (gate the
      first 14336 columns, up the rest); 14336 is the FFN width of the Llama-3-8B configuration
      the pages count kernels for, 2048 rows as config 2
+  7  causal attention without the score matrix: q, k, v bf16 [8 x 16, 2048, 256] ~ N(0,1)
+     rounded to bf16 (B=8, H=16, S=2048, d=4096 -> head size 256: the shape whose score tensor
+     is config 3), scale 1/16 = 1/sqrt(256)
 """
 from __future__ import annotations
 
@@ -38,6 +41,8 @@ GEMM_MS = (4096, 16)
 GEMM_STD = 1.0 / 64.0          # "N(0, 1/sqrt(4096))", second parameter read as the std
 ADDRMS_ROWS, ADDRMS_HIDDEN = 2048, 4096
 SILU_ROWS, SILU_COLS = 2048, 14336
+ATT_BH, ATT_S, ATT_D = SM_B * SM_H, SM_S, 256
+ATT_SCALE = 1.0 / 16.0          # 1/sqrt(256)
 
 
 def rng(config: int, salt: int = 0) -> np.random.Generator:
@@ -140,6 +145,21 @@ def silu_input(rows: int = SILU_ROWS, cols: int = SILU_COLS, dtype: str = "bf16"
     tdt = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[dtype]
     g = _torch_gen(config, salt, device)
     return (scale * torch.randn(rows, 2 * cols, generator=g, device=device)).to(tdt)
+
+
+# ----------------------------------------------------------------------------- attention
+def attention_input(bh: int = ATT_BH, S: int = ATT_S, D: int = ATT_D, config: int = 7,
+                    salt: int = 0, device=None):
+    """q, k, v ~ N(0,1) rounded to bf16, [bh, S, D]: uint16 bit patterns on the host, torch
+    bfloat16 tensors on ``device``."""
+    if device is None:
+        g = rng(config, salt)
+        return tuple(bf16_bits_from_f32(g.standard_normal((bh, S, D)).astype(np.float32))
+                     for _ in range(3))
+    import torch
+    g = _torch_gen(config, salt, device)
+    return tuple(torch.randn(bh, S, D, generator=g, device=device, dtype=torch.float32).to(
+        torch.bfloat16) for _ in range(3))
 
 
 # ----------------------------------------------------------------------------- softmax

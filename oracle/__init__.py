@@ -12,7 +12,7 @@ invariants and brute force on tiny inputs.
 
 Parity status of each function:
   chain, affine_closed_form, rmsnorm, causal_softmax, causal_softmax_unfused, gemm_epilogue,
-  gelu, add_rmsnorm, silu, silu_mul: pinned (tests/test_oracle_pins.py).
+  gelu, add_rmsnorm, silu, silu_mul, attention: pinned (tests/test_oracle_pins.py).
 """
 from __future__ import annotations
 
@@ -71,6 +71,7 @@ def _load():
             "orc_add_rmsnorm": ([P, P, P, P, P, I64, I64, F64], None),
             "orc_silu": ([F64], F64),
             "orc_silu_mul": ([P, P, I64, P, I64, I64, I32, I32], None),
+            "orc_attention": ([P, P, P, P, I64, I64, I64, F64, P, I64], None),
             "orc_version": ([], I32),
         }
         for name, (args, res) in sig.items():
@@ -236,3 +237,27 @@ def silu_mul_merged(gu: np.ndarray, dtype: str = "bf16", unfused: bool = False) 
     _load().orc_silu_mul(_ptr(flat), _ptr(flat[cols:]), ld, _ptr(y), rows, cols,
                          DTYPE_CODES[dtype], 1 if unfused else 0)
     return y
+
+
+def attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float, rows=None) -> np.ndarray:
+    """Causal attention o = softmax(scale q k^T, j <= i) v per slice; q, k, v uint16 bf16 bit
+    patterns [BH, S, D] (or [S, D]).  rows: optional query rows of every slice.  Returns uint16
+    bf16 patterns [BH, S or len(rows), D]."""
+    q = _c(q, np.uint16)
+    k = _c(k, np.uint16)
+    v = _c(v, np.uint16)
+    squeeze = q.ndim == 2
+    if squeeze:
+        q, k, v = q[None], k[None], v[None]
+    BH, S, D = q.shape
+    assert k.shape == q.shape and v.shape == q.shape
+    if rows is None:
+        o = np.empty((BH, S, D), np.uint16)
+        _load().orc_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), BH, S, D, float(scale), None, 0)
+    else:
+        r = _c(rows, np.int64)
+        assert r.ndim == 1 and (r.size == 0 or (r.min() >= 0 and r.max() < S))
+        o = np.empty((BH, r.size, D), np.uint16)
+        _load().orc_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), BH, S, D, float(scale), _ptr(r),
+                              r.size)
+    return o[0] if squeeze else o

@@ -346,4 +346,53 @@ void orc_silu_mul(const void* g, const void* u, int64_t ld, void* y, int64_t row
     }
 }
 
+/* ------------------------------------------------------------------------------------ */
+/* Causal attention without the score matrix.  [OFCG] §6.3 and its reading list            */
+/* (FlashAttention, arXiv:2205.14135): the fused attention never materialises the S x S    */
+/* scores of the softmax row above and normalises online.  What it computes is plain       */
+/* causal scaled-dot-product attention, written out here from its definition:              */
+/*     s_ij = scale * sum_d q_id k_jd   (j <= i),   p_ij = exp(s_ij - max_j s_ij),          */
+/*     o_id = sum_j p_ij v_jd / sum_j p_ij,                                                 */
+/* per (batch, head) slice, in double from the bf16 inputs, one rounding of o to bf16.      */
+/* Reading: q, k, v, o are bf16 [BH, S, D] with D = d_model / heads (4096 / 16 = 256 for    */
+/* the pages' B=8, H=16, S=2048 shape) and scale = 1/sqrt(D); mask j > i, 0-based.          */
+/* rows (optional): only these query rows of every slice are computed (o has nrows rows    */
+/* per slice then).                                                                         */
+/* ------------------------------------------------------------------------------------ */
+void orc_attention(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o,
+                   int64_t BH, int64_t S, int64_t D, double scale, const int64_t* rows,
+                   int64_t nrows)
+{
+    double* srow = (double*)malloc(sizeof(double) * (size_t)S);
+    double* acc = (double*)malloc(sizeof(double) * (size_t)D);
+    const int64_t nr = rows ? nrows : S;
+    for (int64_t b = 0; b < BH; ++b) {
+        const uint16_t* qb = q + b * S * D;
+        const uint16_t* kb = k + b * S * D;
+        const uint16_t* vb = v + b * S * D;
+        for (int64_t t = 0; t < nr; ++t) {
+            const int64_t i = rows ? rows[t] : t;
+            double m = -INFINITY;
+            for (int64_t j = 0; j <= i; ++j) {
+                double dot = 0.0;
+                for (int64_t d = 0; d < D; ++d)
+                    dot += orc_bf16_value(qb[i * D + d]) * orc_bf16_value(kb[j * D + d]);
+                srow[j] = scale * dot;
+                if (srow[j] > m) m = srow[j];
+            }
+            double l = 0.0;
+            for (int64_t d = 0; d < D; ++d) acc[d] = 0.0;
+            for (int64_t j = 0; j <= i; ++j) {
+                const double pj = exp(srow[j] - m);
+                l += pj;
+                for (int64_t d = 0; d < D; ++d) acc[d] += pj * orc_bf16_value(vb[j * D + d]);
+            }
+            uint16_t* ob = o + (b * nr + t) * D;
+            for (int64_t d = 0; d < D; ++d) ob[d] = orc_bf16_bits(acc[d] / l);
+        }
+    }
+    free(srow);
+    free(acc);
+}
+
 int orc_version(void) { return 1; }

@@ -615,3 +615,72 @@ def test_silu_mul_brute_force_tiny_fp32():
         gv, uv = float(g[0, j]), float(u[0, j])
         want = np.float32(gv / (1.0 + math.exp(-gv)) * uv)
         assert y[0, j] == want
+
+
+# ============================================================== causal attention (no score matrix)
+def _bf16_to_f64(a):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _f64_to_bf16(a):
+    return np.vectorize(oracle.bf16_bits)(a).astype(np.uint16)
+
+
+def test_attention_first_row_is_the_first_value_row():
+    q, k, v = wl.attention_input(3, 40, 32, salt=1)
+    o = oracle.attention(q, k, v, 1 / math.sqrt(32))
+    assert np.array_equal(o[:, 0], v[:, 0])
+
+
+def test_attention_zero_queries_average_the_visible_values():
+    """q = 0: every visible key scores 0, so o_i is the mean of v_0..v_i (rounded once)."""
+    _, k, v = wl.attention_input(2, 48, 16, salt=2)
+    q = np.zeros_like(k)
+    o = oracle.attention(q, k, v, 0.25)
+    vd = _bf16_to_f64(v)
+    mean = np.cumsum(vd, axis=1) / np.arange(1, 49)[None, :, None]
+    assert np.array_equal(o, _f64_to_bf16(mean))
+
+
+def test_attention_is_causal():
+    """o_i ignores keys and values after i: changing them leaves o_0..o_i bit-identical."""
+    q, k, v = wl.attention_input(2, 64, 32, salt=3)
+    o = oracle.attention(q, k, v, 1 / math.sqrt(32))
+    k2, v2 = k.copy(), v.copy()
+    k2[:, 40:], v2[:, 40:] = v[:, 40:], k[:, 40:]
+    o2 = oracle.attention(q, k2, v2, 1 / math.sqrt(32))
+    assert np.array_equal(o[:, :40], o2[:, :40])
+    assert not np.array_equal(o[:, 40:], o2[:, 40:])
+
+
+def test_attention_sharp_query_selects_one_key():
+    """With orthogonal keys and a query aligned to key j at a large scale, o_i = v_j."""
+    S, D = 16, 16
+    k = _f64_to_bf16(np.eye(S, D))
+    v = wl.attention_input(1, S, D, salt=4)[2][0]
+    sel = np.array([0, 1, 1, 3, 2, 5, 0, 7, 8, 4, 10, 11, 12, 6, 14, 15])
+    q = _f64_to_bf16(np.eye(S, D)[sel])
+    o = oracle.attention(q, k, v, 100.0)
+    assert np.array_equal(o, v[sel])
+
+
+def test_attention_against_scipy_softmax():
+    """Tiny slices against scipy's softmax of the masked score matrix times v."""
+    from scipy.special import softmax
+    q, k, v = wl.attention_input(2, 24, 8, salt=5)
+    o = oracle.attention(q, k, v, 0.3)
+    qd, kd, vd = _bf16_to_f64(q), _bf16_to_f64(k), _bf16_to_f64(v)
+    for b in range(2):
+        s = 0.3 * qd[b] @ kd[b].T
+        s[np.triu_indices(24, 1)] = -np.inf
+        ref = softmax(s, axis=1) @ vd[b]
+        got = _bf16_to_f64(o[b])
+        assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-300)
+
+
+def test_attention_row_subset_matches_full():
+    q, k, v = wl.attention_input(2, 96, 32, salt=6)
+    o = oracle.attention(q, k, v, 1 / math.sqrt(32))
+    rows = np.array([0, 5, 63, 64, 95])
+    assert np.array_equal(oracle.attention(q, k, v, 1 / math.sqrt(32), rows=rows), o[:, rows])
