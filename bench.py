@@ -54,7 +54,7 @@ def parse_args():
                     choices=["chain_fused", "chain_unfused", "chain_fat", "rmsnorm_fused",
                              "rmsnorm_unfused", "softmax_fused", "softmax_unfused", "gemm",
                              "add_rmsnorm_fused", "add_rmsnorm_unfused", "silu_mul_fused",
-                             "silu_mul_unfused"],
+                             "silu_mul_unfused", "attention"],
                     help="run only `--launches` calls of one row (for ncu), print a short line")
     ap.add_argument("--size", type=int, default=None,
                     help="profile size: chain elements, RMSNorm rows or softmax batch*heads")
@@ -337,6 +337,22 @@ def run_ours(args, rank, world, local):
                                        fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED))],
                   sm(0, fc.FUSE_UNFUSED), "hbm", None, None),
         ]
+        # -------------------------------------------------------------- attention, no score matrix
+        with torch.cuda.stream(stream):
+            aq, ak, av = wl.attention_input(device=dev, salt=rank)
+            aos = [torch.empty_like(aq) for _ in range(2)]
+        orot = rotating(2)
+        ABH, AS, AD = wl.ATT_BH, wl.ATT_S, wl.ATT_D
+
+        def attn():
+            def fn():
+                check(lib.fuse_attention(aq.data_ptr(), ak.data_ptr(), av.data_ptr(), aos[orot()].data_ptr(),
+                                         ABH, AS, AD, wl.ATT_SCALE, sh), "fuse_attention")
+                counter["launches"] += 1
+            return fn
+        att_flops = fc.fuse_attention_flops(ABH, AS, AD)
+        groups += [Group("attention_fused", [("a", attn(), att_flops)] * 2, attn(), "tensor",
+                         "attn_fwd_kernel<D=256>", 1)]
         # -------------------------------------------------------------- GEMM epilogue chain
         plans = {"[4]": 0, "[1,3]": 1, "[2,2]": 2, "[1,1,1,1]": 7}
         gN, gK = wl.GEMM_N, wl.GEMM_K
@@ -429,7 +445,8 @@ def run_ours(args, rank, world, local):
 
     kernel_src = {"softmax_fused": "softmax.cu", "chain_fused": "chain.cu", "gemm_M4096_fused": "gemm.cu",
                   "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm.cu",
-                  "add_rmsnorm_fused": "rmsnorm.cu", "silu_mul_fused": "silu_mul.cu"}
+                  "add_rmsnorm_fused": "rmsnorm.cu", "silu_mul_fused": "silu_mul.cu",
+                  "attention_fused": "attention.cu"}
 
     def roofline_of(name):
         g = gmap[name]
@@ -487,6 +504,16 @@ def run_ours(args, rank, world, local):
                             "speedup": round(su / sf, 3),
                             "unfused_ledger_GBs": round(sb[fc.FUSE_UNFUSED] / su / 1e6, 1),
                             "roofline_fused": roofline_of("silu_mul_fused")}
+        at = group_total_ms("attention_fused") / 2
+        rows["attention"] = {"us": round(at * 1e3, 1), "flops": att_flops,
+                             "TFLOPs": round(att_flops / at / 1e9, 1),
+                             "bytes": fc.fuse_attention_bytes(ABH, AS, AD),
+                             "roofline": roofline_of("attention_fused"),
+                             "softmax_alone_T0_us": round(mean_ms("softmax_fused", 0) * 1e3, 1),
+                             "vs_softmax_alone": round(mean_ms("softmax_fused", 0) / at, 3),
+                             "note": "the materialised path needs Q K^T and P V GEMMs besides the "
+                                     "softmax over the 1 GiB score tensor; the softmax alone is its "
+                                     "lower bound"}
         smr = {}
         for j, t in enumerate((0, 64, 128)):
             ms_ = mean_ms("softmax_fused", j)
@@ -885,6 +912,15 @@ def run_profile(args):
                                    fc.FUSE_BF16, mode, stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_silu_mul_bytes(rows, C, fc.FUSE_BF16, mode)
+    elif name == "attention":
+        bh = args.size or wl.ATT_BH
+        q, k, v = wl.attention_input(bh, wl.ATT_S, wl.ATT_D, device=dev)
+        os_ = [torch.empty_like(q) for _ in range(2)]
+        for i in range(L):
+            rc = lib.fuse_attention(q.data_ptr(), k.data_ptr(), v.data_ptr(), os_[i % 2].data_ptr(), bh,
+                                    wl.ATT_S, wl.ATT_D, wl.ATT_SCALE, stream)
+            assert rc == 0, fc.fuse_strerror(rc)
+        nbytes = fc.fuse_attention_bytes(bh, wl.ATT_S, wl.ATT_D)
     elif name == "gemm":
         M = args.size or 4096
         A, B, bias, Rr = wl.gemm_input(M, device=dev)

@@ -80,6 +80,9 @@ SIGNATURES = {
     "fuse_add_rmsnorm": ([_P, _P, _P, _P, _P, _I64, _I64, _F32, _I32, _P, _SZ, _P], _I32),
     "fuse_silu_mul": ([_P, _P, _I64, _P, _I64, _I64, _I32, _I32, _P], _I32),
     "fuse_add_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
+    "fuse_attention": ([_P, _P, _P, _P, _I64, _I64, _I64, _F32, _P], _I32),
+    "fuse_attention_bytes": ([_I64, _I64, _I64], _I64),
+    "fuse_attention_flops": ([_I64, _I64, _I64], _I64),
     "fuse_silu_mul_bytes": ([_I64, _I64, _I32, _I32], _I64),
     "fuse_chain_bytes": ([_I32, _I64, _I32, _I32], _I64),
     "fuse_rmsnorm_bytes": ([_I64, _I64, _I32], _I64),
@@ -229,6 +232,16 @@ def fuse_silu_mul(g, u, y, mode: int = FUSE_FUSED, stream=None) -> None:
                                  _dtype_code(g), mode, _stream(stream)), "fuse_silu_mul")
 
 
+def fuse_attention(q, k, v, o, scale: float, stream=None) -> None:
+    """o = causal softmax(scale q k^T) v over bf16 [bh, S, D] tensors, no score matrix."""
+    _need_device(q, k, v, o)
+    if q.shape != k.shape or q.shape != v.shape or q.shape != o.shape or q.dim() != 3:
+        raise ValueError("q, k, v, o must be [bh, S, D] tensors of one shape")
+    bh, S, D = q.shape
+    _check(_load().fuse_attention(_ptr(q), _ptr(k), _ptr(v), _ptr(o), bh, S, D, float(scale),
+                                  _stream(stream)), "fuse_attention")
+
+
 def fuse_rmsnorm_unfused_static(x, w, y, eps: float, stream=None) -> None:
     """Unfused RMSNorm with its row statistics in the library's own fixed device array (no
     workspace, no allocation; rows <= FUSE_RMSNORM_STATIC_MAX_ROWS)."""
@@ -313,6 +326,14 @@ def fuse_add_rmsnorm_bytes(rows: int, hidden: int, mode: int) -> int:
 
 def fuse_silu_mul_bytes(rows: int, cols: int, dtype: int, mode: int) -> int:
     return _load().fuse_silu_mul_bytes(rows, cols, dtype, mode)
+
+
+def fuse_attention_bytes(bh: int, S: int, D: int) -> int:
+    return _load().fuse_attention_bytes(bh, S, D)
+
+
+def fuse_attention_flops(bh: int, S: int, D: int) -> int:
+    return _load().fuse_attention_flops(bh, S, D)
 
 
 def fuse_launch_model(n_kernels: int, t_launch: float, t_exec: float, t_dispatch: float) -> dict:

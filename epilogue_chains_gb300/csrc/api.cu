@@ -5,6 +5,7 @@
 #include <mutex>
 
 #include "fc_internal.cuh"
+#include "fc_tc.cuh"
 
 namespace fc {
 
@@ -19,6 +20,8 @@ int gemm_report_count();
 int gemm_report(int i, fuse_kernel_record* out);
 int silu_report_count();
 int silu_report(int i, fuse_kernel_record* out);
+int attn_report_count();
+int attn_report(int i, fuse_kernel_record* out);
 int watchdog_take();  // 1 if a bounded device wait expired since the last call (and clears it)
 
 namespace {
@@ -78,6 +81,39 @@ int describe_kernel(const void* kernel, const char* name, int block, int dyn_sme
     return FUSE_OK;
 }
 
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::mutex mu;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            (void)cudaGetLastError();
+    }
+    return fn;
+}
+}  // namespace
+
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t cols, int box_cols,
+              int box_rows, bool bf16) {
+    auto enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                     const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 }  // namespace fc
 
 namespace {
@@ -91,6 +127,7 @@ const ReportTable kTables[] = {
     {fc::softmax_report_count, fc::softmax_report},
     {fc::gemm_report_count, fc::gemm_report},
     {fc::silu_report_count, fc::silu_report},
+    {fc::attn_report_count, fc::attn_report},
 };
 }  // namespace
 

@@ -1,5 +1,5 @@
 // fc_ptx.cuh -- inline-PTX building blocks for sm_103a: mbarriers with bounded waits.
-// (TMA and tcgen05 wrappers live in gemm.cu, their only user.)
+// (TMA and tcgen05 wrappers live in fc_tc.cuh.)
 #pragma once
 
 #include <stdint.h>
@@ -59,6 +59,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                 return false;
             }
         }
+    }
+    return true;
+}
+
+// Drain wait after a failure: the copies or MMAs this CTA already issued must land before its
+// shared memory and TMEM are released, whatever other CTAs reported, so the watchdog flag is not
+// consulted; only the time budget bounds the wait.  Returns false if it ran out.
+__device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
+                                                long long budget = kWaitBudget / 8) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    uint32_t spins = 0;
+    while (!mbar_try_wait(bar, parity)) {
+        if (++spins % 64u == 0u && clock64() - t0 > budget) return false;
     }
     return true;
 }

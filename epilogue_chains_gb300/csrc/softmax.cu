@@ -164,7 +164,7 @@ __global__ void __launch_bounds__(kSmBlock, 2) softmax_fused_kernel(
         if (!mbar_wait_bounded(bars + 8 * st, (phase >> st) & 1u, flag)) {
             // give up: let the copies still in flight land (bounded) before the CTA exits
             for (int k = 0; k < kStages; ++k)
-                if ((pending >> k) & 1u) (void)mbar_wait_bounded(bars + 8 * k, (phase >> k) & 1u, flag, kWaitBudget / 8);
+                if ((pending >> k) & 1u) (void)mbar_wait_drain(bars + 8 * k, (phase >> k) & 1u);
             return;
         }
         phase ^= 1u << st;

@@ -239,6 +239,25 @@ int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, cons
 /* [K4] §① traffic of a plan, in bytes: 2 * (M*K + K*N + N + 2*M*N + 2*cuts*M*N). */
 int64_t fuse_gemm_bytes(int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask);
 
+/* ===================================================================== attention, no score matrix
+ * "AIGC fundamentals | operator fusion and CUDA Graph" §6.3 and its reading list (FlashAttention):
+ * the causal softmax's S x S score tensor is never written; the softmax is fused into the
+ * attention and normalised online.  Per slice b of batch x heads:
+ *     O_b = softmax(scale Q_b K_b^T with keys j <= query i) V_b.
+ *   q, k, v, o  device bf16 [bh, S, D] row-major, 16-byte aligned; o must not overlap q, k, v.
+ *   S       a multiple of 128 (else FUSE_EUNSUPPORTED); D in {64, 128, 256} (else
+ *           FUSE_EUNSUPPORTED); bh * S < 2^31.
+ *   scale   > 0 (1/sqrt(D) for the usual attention).
+ * One kernel (tcgen05 MMAs, scores and output accumulator in TMEM).  P is rounded to bf16 before
+ * it multiplies V and O is rounded once to bf16; scores and sums are fp32.
+ */
+int fuse_attention(const void* q, const void* k, const void* v, void* o, int64_t bh, int64_t S,
+                   int64_t D, float scale, fuse_stream_t stream);
+/* Algorithmic DRAM bytes (read Q, K, V, write O once: 8 bh S D) and useful flops (2 x 2 D per
+ * visible query-key pair: 2 D bh S (S + 1)) of one fuse_attention() call. */
+int64_t fuse_attention_bytes(int64_t bh, int64_t S, int64_t D);
+int64_t fuse_attention_flops(int64_t bh, int64_t S, int64_t D);
+
 /* ===================================================================== ledgers
  * [K4] §① traffic(): a cut plan splits the K stages into consecutive kernels (cut_mask bit i =
  * a kernel boundary after stage i).  Each kernel reads the previous kernel's output (the

@@ -1,0 +1,121 @@
+"""Parity of the causal attention kernel (tcgen05, no score matrix) against the CPU oracle
+(plain causal softmax(scale q k^T) v in double), through the C ABI.
+
+Bar per output element: P is rounded to bf16 before it multiplies V (relative 2^-9 per weight),
+the row sum uses the unrounded weights, the scores and O accumulate in fp32 and O is rounded once
+to bf16, so |O - ref| <= 2^-8 max_j<=i |v_j| + 2^-8 |ref| (per column), and the RMS error stays
+at the level of the bf16 rounding of P (2^-9 of the values' RMS).  Row 0 of every slice sees only
+key 0 and must equal v_0 bit for bit."""
+import numpy as np
+import pytest
+
+import epilogue_chains_gb300 as fc
+import oracle
+from epilogue_chains_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+def _dev(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _f(bits):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).double().numpy()
+
+
+def _run(q, k, v, scale):
+    import torch
+    o = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device="cuda")
+    fc.fuse_attention(_dev(q), _dev(k), _dev(v), o, scale)
+    torch.cuda.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    return o.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _check(o, ref, v, rows=None):
+    od, rd, vd = _f(o), _f(ref), _f(v)
+    assert np.all(np.isfinite(od))
+    S = v.shape[1]
+    rows = np.arange(S) if rows is None else np.asarray(rows)
+    vmax = np.maximum.accumulate(np.abs(vd), axis=1)[:, rows]          # max_j<=i |v_j| per column
+    err = np.abs(od - rd)
+    bound = 2.0 ** -8 * vmax + 2.0 ** -8 * np.abs(rd) + 2.0 ** -133
+    bad = err > bound
+    assert not bad.any(), (int(bad.sum()), float(err.max()), np.argwhere(bad)[:4].tolist())
+    assert np.sqrt(np.mean(err ** 2)) <= 2.0 ** -9 * np.sqrt(np.mean(vd ** 2))
+
+
+@pytest.mark.parametrize("shape", [(2, 256, 256), (1, 128, 64), (3, 384, 128), (2, 512, 256)])
+def test_small_shapes_every_row(cuda_device, shape):
+    bh, S, D = shape
+    q, k, v = wl.attention_input(bh, S, D, salt=S + D)
+    scale = 1.0 / np.sqrt(D)
+    o = _run(q, k, v, scale)
+    _check(o, oracle.attention(q, k, v, scale), v)
+    assert np.array_equal(o[:, 0], v[:, 0])
+
+
+def test_full_size_sampled_rows(cuda_device):
+    """[128, 2048, 256] as benchmarked: the GPU computes all of O; rows at tile edges, first,
+    last and random are compared in every slice."""
+    q, k, v = wl.attention_input()
+    o = _run(q, k, v, wl.ATT_SCALE)
+    g = np.random.default_rng(21)
+    rows = np.unique(np.concatenate([[0, 1, 127, 128, 129, 255, 1023, 1024, 2046, 2047],
+                                     g.integers(0, 2048, 6)]))
+    _check(o[:, rows], oracle.attention(q, k, v, wl.ATT_SCALE, rows=rows), v, rows)
+    assert np.array_equal(o[:, 0], v[:, 0])
+
+
+def test_sharp_queries_select_exactly_one_value_row(cuda_device):
+    """Keys 0..63 are the unit vectors, keys 64..127 zero; query i points at key sel(i) <= i with
+    score 32 against 0 elsewhere, so O_i = v_sel(i) bit for bit."""
+    S, D = 128, 64
+    k = np.zeros((S, D))
+    k[:64] = np.eye(64)
+    g = np.random.default_rng(22)
+    sel = np.array([g.integers(0, min(i, 63) + 1) for i in range(S)])
+    q = np.zeros((S, D))
+    q[np.arange(S), sel] = 32.0
+    qb, kb = wl.bf16_bits_from_f32(q.astype(np.float32)), wl.bf16_bits_from_f32(k.astype(np.float32))
+    v = wl.attention_input(1, S, D, salt=23)[2][0]
+    o = _run(qb[None], kb[None], v[None], 1.0)[0]
+    assert np.array_equal(o, v[sel])
+
+
+def test_growing_scores_rescale_every_block(cuda_device):
+    """Scores that rise by 64 (natural units) per 128-key block force the O rescale in every block
+    of every row; large magnitudes also exercise the far tails of exp."""
+    S, D = 512, 64
+    k = np.zeros((S, D), np.float32)
+    k[:, 0] = np.arange(S) / 2.0                      # rounded to bf16 below; both sides see it
+    g = np.random.default_rng(24)
+    q = g.standard_normal((S, D)).astype(np.float32) * 0.1
+    q[:, 0] = 1.0
+    qb, kb = wl.bf16_bits_from_f32(q), wl.bf16_bits_from_f32(k)
+    v = wl.attention_input(1, S, D, salt=25)[2]
+    o = _run(qb[None], kb[None], v, 1.0)
+    _check(o, oracle.attention(qb[None], kb[None], v, 1.0), v)
+
+
+def test_large_scale_and_wide_values(cuda_device):
+    q, k, v = wl.attention_input(2, 256, 128, salt=26)
+    o = _run(q, k, v, 0.5)              # sharper softmax than 1/sqrt(D)
+    _check(o, oracle.attention(q, k, v, 0.5), v)
+
+
+def test_rejects_unsupported_and_bad_arguments(cuda_device):
+    import torch
+    lib = fc._load()
+    t = torch.zeros(2, 256, 256, dtype=torch.bfloat16, device="cuda")
+    o = torch.zeros_like(t)
+    p = t.data_ptr()
+    assert lib.fuse_attention(p, p, p, o.data_ptr(), 2, 200, 256, 0.1, None) == fc.FUSE_EUNSUPPORTED
+    assert lib.fuse_attention(p, p, p, o.data_ptr(), 2, 128, 96, 0.1, None) == fc.FUSE_EUNSUPPORTED
+    assert lib.fuse_attention(p + 2, p, p, o.data_ptr(), 1, 128, 256, 0.1, None) == fc.FUSE_EALIGN
+    assert lib.fuse_attention(p, p, p, p, 1, 128, 256, 0.1, None) == fc.FUSE_EINVAL      # o over q
+    assert lib.fuse_attention(p, p, p, o.data_ptr(), 1, 128, 256, 0.0, None) == fc.FUSE_EINVAL
+    assert lib.fuse_attention(p, p, p, o.data_ptr(), 0, 128, 256, 0.1, None) == fc.FUSE_OK
