@@ -6,22 +6,25 @@
 // arXiv:2205.14135), which also skips the masked half of the scores.  Per (batch, head) slice:
 //     O = softmax(scale Q K^T, keys j <= query i) V,   Q, K, V, O bf16 [S, D].
 //
-// GB300 design: one CTA per 128-row query tile, heaviest (most key blocks) tiles first, 192
-// threads in three roles.
-//  * warp 0 (one lane) loads Q once and then, per 128-key block j, K_j and V_j with TMA
-//    (128-byte swizzle; single buffers: K_j+1 streams in as soon as S_j is computed, V_j+1 as
-//    soon as PV_j is);
-//  * warp 1 owns TMEM (512 columns: two 128-column score buffers and the D-column output
-//    accumulator) and issues the tcgen05 MMAs: S_j = Q K_j^T (M 128, N 128, bf16, K-major both)
-//    into score buffer j % 2, and O += P_j V_j (M 128, N D, P K-major from shared memory, V
-//    MN-major) -- S_j+1 is issued before PV_j, so the next scores are computed while the softmax
-//    warps work on the current ones;
-//  * warps 2-5 (one TMEM lane quadrant each, one query row per thread) read the scores with
-//    tcgen05.ld, mask the diagonal block, keep the running row maximum m and sum l in base-2
-//    units, write P = 2^(s c - m) as bf16 into shared memory in the MMA's swizzled layout, and
-//    rescale the O accumulator in TMEM only when the maximum has grown by more than 2^8 since it
-//    was last applied (P stays <= 256, exact in the final O / l).  After the last block they
-//    divide O by l and store it.
+// GB300 design: one CTA per 128-row query tile, heaviest (most key blocks) tiles first; two CTAs
+// with adjacent tiles of one slice form a cluster and multicast the key/value blocks they share.
+// Keys go in blocks of 128 (the MMA re-reads the whole Q tile from shared memory for every block,
+// so longer blocks cost less shared-memory bandwidth per flop), which at a head size of 256 leaves
+// room for one K, one V and one P buffer (Q 64 KB + K 64 KB + V 64 KB + P 32 KB) and two score
+// buffers in TMEM (2 x 128 score columns + 256 O columns).  320 threads in three roles:
+//  * warp 0: lane 0 loads Q once and the K blocks, lane 1 the V blocks (TMA, 128-byte swizzle),
+//    each as soon as its buffer is free (K_j+1 once S_j is computed, V_j+1 once PV_j is);
+//  * warp 1 owns TMEM and issues the tcgen05 MMAs: S_j = Q K_j^T (M 128, N 128, bf16, K-major
+//    both) into score buffer j % 2, and O += P_j V_j (M 128, N D, P K-major, V MN-major), in the
+//    order S_0, S_1, PV_0, S_2, PV_1, ... so the next scores are computed while the softmax warps
+//    work on the current ones;
+//  * warps 2-9 (two per TMEM lane quadrant, one query row per thread, each warp half of a
+//    block's keys and half of O's columns) read the scores with tcgen05.ld, mask the diagonal
+//    blocks, keep the running row maximum m and sum l in base-2 units, write P = 2^(s c - m) as
+//    bf16 into shared memory in the MMA's swizzled layout, and rescale their half of the O
+//    accumulator in TMEM only when the maximum has grown by more than 2^8 since it was last
+//    applied (P stays <= 256, exact in the final O / l).  After the last block they divide O by
+//    l and store it.
 // All waits are bounded (watchdog); a CTA whose wait runs out drains its MMAs and copies and
 // frees its TMEM before it returns.
 #include <math.h>
@@ -37,28 +40,36 @@ namespace {
 
 constexpr int kAttnQ = 128;          // query rows per CTA
 constexpr int kAttnK = 128;          // keys per block
-constexpr int kAttnThreads = 192;    // producer, MMA, 4 softmax warps
+constexpr int kKVStages = 1;         // K and V buffers (each a ring of this many blocks)
+constexpr int kPBuf = 1;             // P buffers in shared memory
+constexpr int kAttnSoftmaxWarps = 8; // two per TMEM lane quadrant, each exponentiating 32 keys
+constexpr int kAttnThreads = 32 * (2 + kAttnSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.0f; // rescale O only when the row maximum grew by more than this
+constexpr int kSBuf = 2;             // score buffers in TMEM: S_j+kSBuf-1 is computed before PV_j
 
+// Shared memory: Q (128 x D), two K and two V stages (64 keys x D each) and two P buffers
+// (128 x 64 bf16), all in 128-byte-swizzled 64-column atoms.  TMEM: two 64-column score buffers
+// and the D-column O accumulator.
 template <int D>
 struct AttnLayout {
     static constexpr int ATOMS = D / 64;                   // 128-byte swizzle atoms along D
-    static constexpr uint32_t REGION = 128 * 128;          // 128 rows x 128 B
+    static constexpr uint32_t Q_REGION = kAttnQ * 128;     // one atom of Q: 128 rows x 128 B
+    static constexpr uint32_t KV_REGION = kAttnK * 128;    // one atom of a K or V block
     static constexpr uint32_t Q_BYTES = kAttnQ * D * 2;
-    static constexpr uint32_t K_BYTES = kAttnK * D * 2;
-    static constexpr uint32_t V_BYTES = kAttnK * D * 2;
+    static constexpr uint32_t KV_BYTES = kAttnK * D * 2;
     static constexpr uint32_t P_BYTES = kAttnQ * kAttnK * 2;
     static constexpr uint32_t OFF_Q = 0;
-    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;
-    static constexpr uint32_t OFF_V = OFF_K + K_BYTES;
-    static constexpr uint32_t OFF_P = OFF_V + V_BYTES;
-    static constexpr uint32_t OFF_BAR = OFF_P + P_BYTES;
-    static constexpr int N_BARS = 12;
+    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                 // + stage * KV_BYTES
+    static constexpr uint32_t OFF_V = OFF_K + kKVStages * KV_BYTES;    // + stage * KV_BYTES
+    static constexpr uint32_t OFF_P = OFF_V + kKVStages * KV_BYTES;    // + buffer * P_BYTES
+    static constexpr uint32_t OFF_BAR = OFF_P + kPBuf * P_BYTES;
+    static constexpr int N_BARS = 3 + 4 * kKVStages + 2 * kPBuf + 2 * kSBuf;
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
-    static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;  // + alignment slack
+    static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;       // + alignment slack
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t O_COL = 2 * kAttnK;
-    static_assert(O_COL + D <= TMEM_COLS, "score buffers and O must fit in TMEM");
+    static constexpr uint32_t O_COL = 256;
+    static_assert(kSBuf * kAttnK <= O_COL && O_COL + D <= TMEM_COLS, "TMEM budget");
+    static_assert(SMEM <= 232448, "shared-memory budget");
 };
 
 struct AttnArgs {
@@ -79,7 +90,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int D>
+template <int D, int CL>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
@@ -88,114 +99,153 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // barriers: q_full, drain, l_ready, then per K/V stage k_full, k_empty, v_full, v_empty, per
+    // P buffer p_full, o_done, per score buffer s_full, s_free.  A ring of n buffers used by
+    // blocks j = 0, 1, ...: buffer j % n, completion number j / n, parity (j / n) & 1.
     const uint32_t bar0 = base + L::OFF_BAR;
-    const uint32_t q_full = bar0, k_full = bar0 + 8, k_empty = bar0 + 16, v_full = bar0 + 24,
-                   v_empty = bar0 + 32, p_full = bar0 + 72, o_done = bar0 + 80, drain = bar0 + 88;
-    auto s_full = [&](int b) { return bar0 + 40u + 8u * b; };
-    auto s_free = [&](int b) { return bar0 + 56u + 8u * b; };
+    const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16;
+    constexpr int KV = kKVStages, PB = kPBuf, SB = kSBuf;
+    auto k_full = [&](int i) { return bar0 + 8u * (3 + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (3 + KV + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (3 + 2 * KV + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (3 + 3 * KV + i); };
+    auto p_full = [&](int i) { return bar0 + 8u * (3 + 4 * KV + i); };
+    auto o_done = [&](int i) { return bar0 + 8u * (3 + 4 * KV + PB + i); };
+    auto s_full = [&](int i) { return bar0 + 8u * (3 + 4 * KV + 2 * PB + i); };
+    auto s_free = [&](int i) { return bar0 + 8u * (3 + 4 * KV + 2 * PB + SB + i); };
     int* flag = a.flag;
 
+    // CL = 2: the two CTAs of a cluster take adjacent query tiles 2u, 2u + 1 of one slice and
+    // share the key blocks both need: each loads half of every shared K and V block and
+    // multicasts it to both, halving the L2 traffic of the key/value stream.  Heaviest tiles first.
     const int ntile = a.S / kAttnQ;
-    const int t = blockIdx.x;
-    const int qt = ntile - 1 - t / a.BH;   // heaviest query tiles first
-    const int bh = t % a.BH;
-    const int nb = qt + 1;                 // key blocks 0..qt (causal)
+    const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
+    const int group = blockIdx.x / CL;
+    const int u = ntile / CL - 1 - group / a.BH;
+    const int bh = group % a.BH;
+    const int qt = CL * u + static_cast<int>(rank);
+    constexpr int kBlocksPerTile = kAttnQ / kAttnK;
+    const int nb = (qt + 1) * kBlocksPerTile;             // key blocks up to the diagonal
+    const int nshared = (CL * u + 1) * kBlocksPerTile;    // needed by every CTA of the cluster
     const int row0 = bh * a.S + qt * kAttnQ;
     const int krow0 = bh * a.S;
+    constexpr uint16_t kAll = static_cast<uint16_t>((1u << CL) - 1u);
+    constexpr int kAtomsPerCta = L::ATOMS / CL;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        mbar_init(k_full, 1);
-        mbar_init(k_empty, 1);
-        mbar_init(v_full, 1);
-        mbar_init(v_empty, 1);
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(s_full(b), 1);
-            mbar_init(s_free(b), 4);
+        for (int i = 0; i < KV; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), CL);   // a shared block is free once every CTA is done with it
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), CL);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
+        for (int i = 0; i < PB; ++i) {
+            mbar_init(p_full(i), kAttnSoftmaxWarps);
+            mbar_init(o_done(i), 1);
+        }
+        for (int i = 0; i < SB; ++i) {
+            mbar_init(s_full(i), 1);
+            mbar_init(s_free(i), kAttnSoftmaxWarps);
+        }
         mbar_init(drain, 1);
+        mbar_init(l_ready, kAttnSoftmaxWarps);
         fence_mbar_init();
     }
     if (warp == 1) tmem_alloc(base + L::OFF_HOLD, L::TMEM_COLS);
     tc_fence_before();
-    __syncthreads();
+    if (CL > 1) cluster_sync();   // the peer's multicast copies and commits find initialised barriers
+    else __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
 
     if (warp == 0) {
-        // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            prefetch_map(&mQ);
-            prefetch_map(&mK);
-            prefetch_map(&mV);
-            mbar_arrive_expect_tx(q_full, L::Q_BYTES);
-            for (int c = 0; c < L::ATOMS; ++c)
-                tma_load_2d(base + L::OFF_Q + c * L::REGION, &mQ, 64 * c, row0, q_full);
-            int k_loads = 0, v_loads = 0;
-            bool ok = true;
-            for (int j = 0; j < nb && ok; ++j) {
-                if (j > 0 && !mbar_wait_bounded(k_empty, (j - 1) & 1, flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(k_full, L::K_BYTES);
+        // ---------------------------------------------------------------- TMA producers
+        // lane 0 loads Q and the K blocks, lane 1 the V blocks, each into a two-stage ring: block
+        // j + 2 streams in while blocks j and j + 1 are being used
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            const CUtensorMap* map = is_k ? &mK : &mV;
+            const uint32_t off = is_k ? L::OFF_K : L::OFF_V;
+            prefetch_map(map);
+            if (is_k) {
+                prefetch_map(&mQ);
+                mbar_arrive_expect_tx(q_full, L::Q_BYTES);
                 for (int c = 0; c < L::ATOMS; ++c)
-                    tma_load_2d(base + L::OFF_K + c * L::REGION, &mK, 64 * c, krow0 + j * kAttnK, k_full);
-                ++k_loads;
-                if (j > 0 && !mbar_wait_bounded(v_empty, (j - 1) & 1, flag)) { ok = false; break; }
-                mbar_arrive_expect_tx(v_full, L::V_BYTES);
-                for (int c = 0; c < L::ATOMS; ++c)
-                    tma_load_2d(base + L::OFF_V + c * L::REGION, &mV, 64 * c, krow0 + j * kAttnK, v_full);
-                ++v_loads;
+                    tma_load_2d(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, q_full);
             }
-            if (!ok) {  // let the copies in flight land before the CTA's shared memory goes away
-                (void)mbar_wait_drain(q_full, 0);
-                if (k_loads) (void)mbar_wait_drain(k_full, (k_loads - 1) & 1);
-                if (v_loads) (void)mbar_wait_drain(v_full, (v_loads - 1) & 1);
+            int loads = 0;
+            for (int j = 0; j < nb; ++j) {
+                const int st = j % KV;
+                const uint32_t full = is_k ? k_full(st) : v_full(st);
+                const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+                if (j >= KV && !mbar_wait_bounded(empty, ((j - KV) / KV) & 1, flag)) break;
+                mbar_arrive_expect_tx(full, L::KV_BYTES);
+                const int y = krow0 + j * kAttnK;
+                const uint32_t dst = base + off + st * L::KV_BYTES;
+                if (CL > 1 && j < nshared) {
+                    for (int c = kAtomsPerCta * rank; c < kAtomsPerCta * (rank + 1); ++c)
+                        tma_load_2d_mc(dst + c * L::KV_REGION, map, 64 * c, y, full, kAll);
+                } else {
+                    for (int c = 0; c < L::ATOMS; ++c) tma_load_2d(dst + c * L::KV_REGION, map, 64 * c, y, full);
+                }
+                ++loads;
+            }
+            if (loads < nb) {  // let the copies in flight land before the shared memory goes away
+                if (is_k) (void)mbar_wait_drain(q_full, 0);
+                for (int j = loads - KV < 0 ? 0 : loads - KV; j < loads; ++j)
+                    (void)mbar_wait_drain(is_k ? k_full(j % KV) : v_full(j % KV), (j / KV) & 1);
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
+        // order: S_0, S_1, S_2, PV_0, S_3, PV_1, ...: the scores of the next two blocks are
+        // computed while the softmax warps work on the current ones
         if (lane == 0) {
             constexpr uint32_t idS = idesc_f16(kAttnQ, kAttnK, false, false, true);
             constexpr uint32_t idO = idesc_f16(kAttnQ, D, false, true, true);
             bool issued = false;
             auto issue_s = [&](int j) -> bool {
-                const int b = j & 1;
-                if (!mbar_wait_bounded(k_full, j & 1, flag)) return false;
-                if (j >= 2 && !mbar_wait_bounded(s_free(b), ((j - 2) >> 1) & 1, flag)) return false;
+                const int st = j % KV, sb = j % SB;
+                if (!mbar_wait_bounded(k_full(st), (j / KV) & 1, flag)) return false;
+                if (j >= SB && !mbar_wait_bounded(s_free(sb), ((j - SB) / SB) & 1, flag)) return false;
                 tc_fence_after();
+                const uint32_t kb = base + L::OFF_K + st * L::KV_BYTES;
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s) {
-                    const uint32_t off = (s / 4) * L::REGION + (s % 4) * 32;
-                    tc_mma(tmem + b * kAttnK, smem_desc_sw128(base + L::OFF_Q + off, 16, 1024),
-                           smem_desc_sw128(base + L::OFF_K + off, 16, 1024), idS, s > 0 ? 1u : 0u);
-                }
-                tc_commit(s_full(b));
-                tc_commit(k_empty);
+                for (int s = 0; s < D / 16; ++s)   // K = 16 steps: atom s / 4, 32 B apart within it
+                    tc_mma(tmem + sb * kAttnK,
+                           smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
+                           smem_desc_sw128(kb + (s / 4) * L::KV_REGION + (s % 4) * 32, 16, 1024), idS,
+                           s > 0 ? 1u : 0u);
+                tc_commit(s_full(sb));
+                if (CL > 1 && j < nshared) tc_commit_mc(k_empty(st), kAll);   // free in every CTA
+                else tc_commit(k_empty(st));
                 issued = true;
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait_bounded(p_full, j & 1, flag)) return false;
-                if (!mbar_wait_bounded(v_full, j & 1, flag)) return false;
+                const int st = j % KV, pi = j % PB;
+                if (!mbar_wait_bounded(p_full(pi), (j / PB) & 1, flag)) return false;
+                if (!mbar_wait_bounded(v_full(st), (j / KV) & 1, flag)) return false;
                 tc_fence_after();
+                const uint32_t pb = base + L::OFF_P + pi * L::P_BYTES;
+                const uint32_t vb = base + L::OFF_V + st * L::KV_BYTES;
 #pragma unroll
-                for (int s = 0; s < kAttnK / 16; ++s) {
-                    const uint32_t poff = (s / 4) * L::REGION + (s % 4) * 32;
-                    tc_mma(tmem + L::O_COL, smem_desc_sw128(base + L::OFF_P + poff, 16, 1024),
-                           smem_desc_sw128(base + L::OFF_V + s * 2048, L::REGION, 1024), idO,
+                for (int s = 0; s < kAttnK / 16; ++s)   // K = 16 keys: P atom s / 4; V rows 16 s..
+                    tc_mma(tmem + L::O_COL, smem_desc_sw128(pb + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
+                           smem_desc_sw128(vb + s * 2048, L::KV_REGION, 1024), idO,
                            (j > 0 || s > 0) ? 1u : 0u);
-                }
-                tc_commit(o_done);
-                tc_commit(v_empty);
+                tc_commit(o_done(pi));
+                if (CL > 1 && j < nshared) tc_commit_mc(v_empty(st), kAll);
+                else tc_commit(v_empty(st));
                 issued = true;
                 return true;
             };
             bool ok = mbar_wait_bounded(q_full, 0, flag);
-            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < SB - 1 && j < nb; ++j) ok = issue_s(j);
             for (int j = 0; ok && j < nb; ++j) {
-                if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
+                if (j + SB - 1 < nb && !issue_s(j + SB - 1)) { ok = false; break; }
                 ok = issue_pv(j);
             }
             if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
@@ -206,35 +256,52 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
         __syncwarp();
     } else {
         // ---------------------------------------------------------------- softmax warps
+        // Warp w serves TMEM lane quadrant w % 4 (query rows 32 (w % 4) + lane) and half hh of each
+        // block's keys and of O's columns.  Both warps of a quadrant read the whole score row, so
+        // they reach the same row maximum without exchanging it; each exponentiates and writes its
+        // 32 keys of P and keeps the partial row sum of its own keys.
         const int qd = warp % 4;
-        const int r = 32 * qd + lane;                       // query row within the tile
+        const int hh = (warp - 2) / 4;
+        const int r = 32 * qd + lane;                        // query row within the tile
+        const int qrow = qt * kAttnQ + r;                    // query index within the slice
         const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
-        float m_used = -INFINITY, l = 0.0f;
+        const float c = a.c;
+        float m_used = -INFINITY, l = 0.0f;                  // m_used in base-2 units
         bool ok = true;
         // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform before them
         for (int j = 0; j < nb; ++j) {
-            const int b = j & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full(b), (j >> 1) & 1, flag))) {
+            const int pi = j % PB, sb = j % SB;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full(sb), (j / SB) & 1, flag))) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float s[kAttnK];
+            // own keys HK hh .. HK hh + HK - 1, then the other half (for the row maximum only)
+            constexpr int HK = kAttnK / 2;
+            float s[HK], so[HK];
+            const uint32_t sbase = tmem + lanes + sb * kAttnK;
 #pragma unroll
-            for (int k = 0; k < kAttnK / 32; ++k) tmem_ld32(tmem + lanes + b * kAttnK + 32 * k, s + 32 * k);
+            for (int k = 0; k < HK / 32; ++k) {
+                tmem_ld32(sbase + HK * hh + 32 * k, s + 32 * k);
+                tmem_ld32(sbase + HK * (1 - hh) + 32 * k, so + 32 * k);
+            }
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(b));   // the score buffer may be overwritten now
+            if (lane == 0) mbar_arrive(s_free(sb));   // the score buffer may be overwritten now
 
-            const bool diag = (j == nb - 1);
-            float mx = -INFINITY;
+            // keys with index > query index are masked (only in the blocks at the diagonal)
+            const int lim = qrow - j * kAttnK;           // last visible key of this block
+            const bool masked = lim < kAttnK - 1;
+            const int k0 = HK * hh, ko = HK * (1 - hh);
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int k = 0; k < kAttnK; ++k) {
-                const float x = (diag && k > r) ? -INFINITY : s[k] * a.c;
-                s[k] = x;
-                mx = fmaxf(mx, x);
+            for (int k = 0; k < HK; ++k) {
+                const float x = (masked && k0 + k > lim) ? -INFINITY : s[k];
+                const float y = (masked && ko + k > lim) ? -INFINITY : so[k];
+                mx4[k & 3] = fmaxf(mx4[k & 3], fmaxf(x, y));
             }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
             float alpha = 1.0f;
             bool rescale = false;
             if (mx > m_used + kRescaleLog2) {   // always true for the first block (m_used = -inf)
@@ -244,70 +311,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
                 }
                 m_used = mx;
             }
-            float sum = 0.0f;
-            uint32_t pk[kAttnK / 2];
+            // p = 2^(s c - m) for this warp's HK keys, two at a time
+            const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_used, -m_used);
+            float2 sum2 = make_float2(0.0f, 0.0f);
+            uint32_t pk[HK / 2];
 #pragma unroll
-            for (int k = 0; k < kAttnK; k += 2) {
-                const float p0 = ex2f(s[k] - m_used), p1 = ex2f(s[k + 1] - m_used);
-                sum += p0 + p1;
-                pk[k / 2] = pack_bf16x2(p0, p1);
+            for (int k = 0; k < HK; k += 2) {
+                const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+                float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+                if (masked) {
+                    if (k0 + k > lim) p.x = 0.0f;
+                    if (k0 + k + 1 > lim) p.y = 0.0f;
+                }
+                sum2 = __fadd2_rn(sum2, p);
+                pk[k / 2] = pack_bf16x2(p.x, p.y);
             }
-            l = l * alpha + sum;
+            l = l * alpha + (sum2.x + sum2.y);
 
-            // PV_{j-1} must be complete: the P buffer is free and O holds blocks 0..j-1
-            if (j > 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done, (j - 1) & 1, flag))) {
+            // P buffer pi was last read by PV_{j-PB}
+            if (j >= PB) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(pi), ((j - PB) / PB) & 1, flag))) {
+                    ok = false;
+                    break;
+                }
+            }
+            if (__any_sync(0xffffffffu, rescale)) {   // rows without a new maximum scale by 1
+                // O must hold blocks 0..j-1 exactly: PV_{j-1} complete (PV_j is not issued yet)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done((j - 1) % PB), ((j - 1) / PB) & 1, flag))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {   // rows without a new maximum scale by 1
 #pragma unroll 1
-                for (int k = 0; k < D / 32; ++k) {
+                for (int k = 0; k < D / 64; ++k) {
+                    const uint32_t col = L::O_COL + (D / 2) * hh + 32 * k;
                     float o[32];
-                    tmem_ld32(tmem + lanes + L::O_COL + 32 * k, o);
+                    tmem_ld32(tmem + lanes + col, o);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(tmem + lanes + L::O_COL + 32 * k, o);
+                    tmem_st32(tmem + lanes + col, o);
                 }
                 tmem_st_wait();
             }
-            // P row r, keys 0..127: 16 chunks of 8 keys; chunk ch lies in 64-key atom ch / 8 at
-            // 16-byte slot (ch % 8) ^ (r % 8) of the row (128-byte swizzle)
-            uint8_t* prow = gbase + L::OFF_P + r * 128;
+            // P row r, this warp's keys: 16-byte chunks ch (8 keys each) lie in 64-key atom ch / 8
+            // at slot (ch % 8) ^ (r % 8) of the row (128-byte swizzle)
+            uint8_t* prow = gbase + L::OFF_P + pi * L::P_BYTES + r * 128;
 #pragma unroll
-            for (int ch = 0; ch < kAttnK / 8; ++ch) {
-                uint4* dst = reinterpret_cast<uint4*>(prow + (ch >> 3) * L::REGION + (((ch & 7) ^ (r & 7)) << 4));
-                *dst = make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            for (int q = 0; q < HK / 8; ++q) {
+                const int ch = (HK / 8) * hh + q;
+                uint4* dst = reinterpret_cast<uint4*>(prow + (ch / 8) * L::Q_REGION + (((ch % 8) ^ (r & 7)) << 4));
+                *dst = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
             fence_async_smem();   // the generic-proxy P writes become visible to the tensor core
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(p_full(pi));
         }
-        if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(o_done, (nb - 1) & 1, flag))) {
+        const int last = nb - 1;
+        if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(o_done(last % PB), (last / PB) & 1, flag))) {
             tc_fence_after();
-            const float inv = 1.0f / l;
-            __nv_bfloat16* orow = a.O + static_cast<int64_t>(row0 + r) * D;
+            // the row sum is the sum of the two halves' partial sums; P is free now, so the
+            // softmax warps exchange them there (a bounded mbarrier wait, not a named barrier:
+            // a warp that gave up earlier must not leave its partner blocked)
+            float* lx = reinterpret_cast<float*>(gbase + L::OFF_P);
+            lx[hh * kAttnQ + r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_ready);
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(l_ready, 0, flag));
+            const float inv = 1.0f / (l + lx[(1 - hh) * kAttnQ + r]);
+            if (got) {
+                __nv_bfloat16* orow = a.O + static_cast<int64_t>(row0 + r) * D + (D / 2) * hh;
 #pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
-                float o[32];
-                tmem_ld32(tmem + lanes + L::O_COL + 32 * k, o);
-                tmem_ld_wait();
-                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+                for (int k = 0; k < D / 64; ++k) {
+                    float o[32];
+                    tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 32 * k, o);
+                    tmem_ld_wait();
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                            pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                            pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                            pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                }
             }
         }
     }
     tc_fence_before();
-    __syncthreads();
+    // no CTA leaves while its peer may still multicast into its shared memory or commit to its
+    // barriers
+    if (CL > 1) cluster_sync();
+    else __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
@@ -322,7 +417,7 @@ constexpr uint32_t attn_launch_smem() {
 }
 
 // Opt the kernel into its shared-memory size on the current device (once per device).
-template <int D>
+template <int D, int CL>
 int attn_attr() {
     static std::mutex mu;
     static bool done[64] = {false};
@@ -332,7 +427,7 @@ int attn_attr() {
     if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_fwd_kernel<D, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(attn_launch_smem<D>()));
         if (e != cudaSuccess) return record_cuda_error(e);
         done[dev] = true;
@@ -340,11 +435,31 @@ int attn_attr() {
     return FUSE_OK;
 }
 
-template <int D>
-int launch_attn(const void* q, const void* k, const void* v, void* o, int bh, int S, float scale,
-                cudaStream_t st) {
-    const int rc = attn_attr<D>();
+template <int D, int CL>
+int launch_attn(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
+                const AttnArgs& args, cudaStream_t st) {
+    const int rc = attn_attr<D, CL>();
     if (rc != FUSE_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ));
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = attn_launch_smem<D>();
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = CL;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, CL>, mQ, mK, mV, args);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    return check_launch();
+}
+
+template <int D>
+int run_attn(const void* q, const void* k, const void* v, void* o, int bh, int S, float scale,
+             cudaStream_t st) {
     const int64_t rows = static_cast<int64_t>(bh) * S;
     CUtensorMap mQ, mK, mV;
     if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mK, k, rows, D, 64, kAttnK, true) ||
@@ -352,10 +467,11 @@ int launch_attn(const void* q, const void* k, const void* v, void* o, int bh, in
         return FUSE_ECUDA;
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
-    AttnArgs args{bh, S, scale * 1.4426950408889634f, static_cast<__nv_bfloat16*>(o), flag};
-    const unsigned grid = static_cast<unsigned>(rows / kAttnQ);
-    attn_fwd_kernel<D><<<grid, kAttnThreads, attn_launch_smem<D>(), st>>>(mQ, mK, mV, args);
-    return check_launch();
+    const AttnArgs args{bh, S, scale * 1.4426950408889634f, static_cast<__nv_bfloat16*>(o), flag};
+    // pairs of adjacent query tiles share their key/value stream when the tiles pair up and the
+    // head splits into two halves of 64-wide swizzle atoms
+    if (D >= 128 && (S / kAttnQ) % 2 == 0) return launch_attn<D, 2>(mQ, mK, mV, args, st);
+    return launch_attn<D, 1>(mQ, mK, mV, args, st);
 }
 
 bool overlap(const void* a, const void* b, int64_t bytes) {
@@ -368,11 +484,13 @@ bool overlap(const void* a, const void* b, int64_t bytes) {
 int attn_report_count() { return 1; }
 int attn_report(int i, fuse_kernel_record* out) {
     if (i != 0) return FUSE_EINVAL;
-    const int rc = attn_attr<256>();
+    const int rc = attn_attr<256, 2>();
     if (rc != FUSE_OK) return rc;
-    return describe_kernel((const void*)attn_fwd_kernel<256>,
-                           "attn_fwd_kernel<D=256> (tcgen05, no score matrix)", kAttnThreads,
-                           static_cast<int>(attn_launch_smem<256>()), out);
+    const int r2 = describe_kernel((const void*)attn_fwd_kernel<256, 2>,
+                                   "attn_fwd_kernel<D=256> (tcgen05, 2-CTA K/V multicast)", kAttnThreads,
+                                   static_cast<int>(attn_launch_smem<256>()), out);
+    if (r2 == FUSE_OK) out->cluster_size = 2;
+    return r2;
 }
 
 }  // namespace fc
@@ -391,9 +509,9 @@ extern "C" int fuse_attention(const void* q, const void* k, const void* v, void*
     if (overlap(o, q, bytes) || overlap(o, k, bytes) || overlap(o, v, bytes)) return FUSE_EINVAL;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int B = static_cast<int>(bh), SS = static_cast<int>(S);
-    if (D == 64) return launch_attn<64>(q, k, v, o, B, SS, scale, st);
-    if (D == 128) return launch_attn<128>(q, k, v, o, B, SS, scale, st);
-    return launch_attn<256>(q, k, v, o, B, SS, scale, st);
+    if (D == 64) return run_attn<64>(q, k, v, o, B, SS, scale, st);
+    if (D == 128) return run_attn<128>(q, k, v, o, B, SS, scale, st);
+    return run_attn<256>(q, k, v, o, B, SS, scale, st);
 }
 
 extern "C" int64_t fuse_attention_bytes(int64_t bh, int64_t S, int64_t D) {
