@@ -114,12 +114,14 @@ __device__ __forceinline__ uint4 pack_h8(const float* f) {
 }
 
 // =============================================================================== main kernel
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4;
+// A CTA pair computes a 256 x BN output tile with M = 256 MMAs (cta_group::2): each CTA holds its
+// own 128 rows of A and one half (BN / 2 columns) of B per stage.
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 6;
 constexpr int kEpiWarps = 8;                   // two per TMEM lane quadrant
 constexpr int kMainThreads = 32 * (2 + kEpiWarps);
 constexpr uint32_t A_STAGE = BM * BK * 2;      // 16 KB
 constexpr uint32_t B_BOX = 64 * BK * 2;        // 8 KB: 64 N x 64 K
-constexpr uint32_t B_STAGE = BN * BK * 2;      // 32 KB
+constexpr uint32_t B_STAGE = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of the B tile
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_STAGE;
@@ -188,23 +190,28 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const int my_units = cid < total_units ? (total_units - cid + nclusters - 1) / nclusters : 0;
     const int total_kb = my_units * nk;
 
+    // The even CTA of the pair (rank 0) issues the MMAs.  Its full barriers count the bytes both
+    // CTAs load for a stage; every CTA's empty and accumulator-full barriers are signalled by the
+    // leader's commits (multicast); its accumulator-empty barriers collect the epilogue warps of
+    // both CTAs.
+    const bool leader = rank == 0;
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 2);  // freed by the MMAs of both CTAs of the pair
+            mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), kEpiWarps);
+            mbar_init(acce_bar(b), 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
         fence_mbar_init();
         prefetch_map(&mapA);
         prefetch_map(&mapB);
     }
-    if (warp == 1) tmem_alloc(holder, TMEM_COLS);
+    if (warp == 1) tmem_alloc_pair(holder, TMEM_COLS);
     tc_fence_before();
-    cluster_sync();  // both CTAs' barriers exist before either multicasts into the other
+    cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_HOLD);
 
@@ -220,27 +227,29 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
                 inflight &= ~(1u << stage);  // its previous load was consumed
                 if (lane == 0) {
-                    // this CTA's A rows; the pair's B tile is fetched once from L2: each CTA
-                    // multicasts every other 64-column box into both CTAs' shared memory
-                    mbar_arrive_expect_tx(full_bar(stage), A_STAGE + (w.bn / 64) * B_BOX);
-                    tma_load_2d(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, w.m0, full_bar(stage));
-                    for (int j = static_cast<int>(rank); j < w.bn / 64; j += 2)
-                        tma_load_2d_mc(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB, w.n0 + 64 * j,
-                                       kb * BK, full_bar(stage), 0x3);
+                    // this CTA's 128 rows of A and its half of the B tile's columns; both CTAs'
+                    // bytes complete on the leader's full barrier
+                    const int half_boxes = w.bn / 128;
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_STAGE + half_boxes * B_BOX));
+                    const uint32_t full_cl = mapa_shared(full_bar(stage), 0);
+                    tma_load_2d_pair(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, w.m0, full_cl);
+                    for (int j = 0; j < half_boxes; ++j)
+                        tma_load_2d_pair(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB,
+                                         w.n0 + static_cast<int>(rank) * (w.bn / 2) + 64 * j, kb * BK, full_cl);
                 }
                 inflight |= 1u << stage;
                 issue_par = (issue_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        if (!ok) {  // let loads in flight land before this CTA can exit
+        if (!ok && leader) {  // let both CTAs' loads in flight land before either can exit
             for (int s = 0; s < STAGES; ++s)
                 if ((inflight >> s) & 1u) (void)mbar_wait_drain(full_bar(s), (issue_par >> s) & 1u);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 && leader) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc_full = idesc_f16(BM, BN, false, true);
-        constexpr uint32_t idesc_half = idesc_f16(BM, BN / 2, false, true);
+        constexpr uint32_t idesc_full = idesc_f16(2 * BM, BN, false, true);
+        constexpr uint32_t idesc_half = idesc_f16(2 * BM, BN / 2, false, true);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true, issued = false;
@@ -261,13 +270,14 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                         // A: K-major rows of 128 B, 8-row groups 1024 B apart; +32 B per K=16 step
                         const uint64_t ad = smem_desc_sw128(a0 + 32u * k, 16u, 1024u);
                         // B: MN-major, 64-wide N boxes 8 KB apart (LBO), 8-row K groups 1024 B
-                        // apart (SBO); +16 rows (2048 B) per K=16 step
+                        // apart (SBO); +16 rows (2048 B) per K=16 step; the peer's half sits at
+                        // the same offsets in its shared memory
                         const uint64_t bd = smem_desc_sw128(b0 + 2048u * k, B_BOX, 1024u);
-                        tc_mma(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        tc_mma_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
                     }
                     // frees the stage in both CTAs once these MMAs are done -- unless no later load
-                    // uses it (then nothing may arrive after the peer could have left)
-                    if (kg + STAGES < total_kb) tc_commit_mc(empty_bar(stage), 0x3);
+                    // uses it
+                    if (kg + STAGES < total_kb) tc_commit_pair_mc(empty_bar(stage), 0x3);
                 }
                 ++kg;
                 issued = true;
@@ -275,16 +285,16 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) tc_commit(accf_bar(acc));
+            if (lane == 0) tc_commit_pair_mc(accf_bar(acc), 0x3);   // both CTAs' accumulators
             __syncwarp();
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
         if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
-            if (lane == 0) tc_commit(drain_bar);
+            if (lane == 0) tc_commit_pair(drain_bar);
             __syncwarp();
             (void)mbar_wait_drain(drain_bar, 0);
         }
-    } else {
+    } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (warps 2-9)
         // Warp w drains TMEM lane quadrant q = w % 4 (rows 32q..32q+31 of the unit) and one half
         // of the unit's 32-column chunks.  Each thread owns one row: it prefetches its residual
@@ -333,7 +343,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                 if (cc == per - 1) {  // this warp is done with the accumulator buffer
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acce_bar(acc));
+                    if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));   // the leader's
                 }
                 const int ncol0 = w.n0 + CH * c;
                 __half* yrow = args.Y + static_cast<int64_t>(row) * args.N + ncol0;
@@ -363,7 +373,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     tc_fence_before();
     cluster_sync();  // neither CTA leaves while its peer may still write into its shared memory
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, TMEM_COLS);
+    if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
 // =============================================================================== decode kernel
