@@ -6,25 +6,31 @@
 // arXiv:2205.14135), which also skips the masked half of the scores.  Per (batch, head) slice:
 //     O = softmax(scale Q K^T, keys j <= query i) V,   Q, K, V, O bf16 [S, D].
 //
-// GB300 design: one CTA per 128-row query tile, heaviest (most key blocks) tiles first; two CTAs
-// with adjacent tiles of one slice form a cluster and multicast the key/value blocks they share.
-// Keys go in blocks of 128 (the MMA re-reads the whole Q tile from shared memory for every block,
-// so longer blocks cost less shared-memory bandwidth per flop), which at a head size of 256 leaves
-// room for one K, one V and one P buffer (Q 64 KB + K 64 KB + V 64 KB + P 32 KB) and two score
-// buffers in TMEM (2 x 128 score columns + 256 O columns).  320 threads in three roles:
-//  * warp 0: lane 0 loads Q once and the K blocks, lane 1 the V blocks (TMA, 128-byte swizzle),
-//    each as soon as its buffer is free (K_j+1 once S_j is computed, V_j+1 once PV_j is);
-//  * warp 1 owns TMEM and issues the tcgen05 MMAs: S_j = Q K_j^T (M 128, N 128, bf16, K-major
-//    both) into score buffer j % 2, and O += P_j V_j (M 128, N D, P K-major, V MN-major), in the
-//    order S_0, S_1, PV_0, S_2, PV_1, ... so the next scores are computed while the softmax warps
-//    work on the current ones;
-//  * warps 2-9 (two per TMEM lane quadrant, one query row per thread, each warp half of a
-//    block's keys and half of O's columns) read the scores with tcgen05.ld, mask the diagonal
-//    blocks, keep the running row maximum m and sum l in base-2 units, write P = 2^(s c - m) as
-//    bf16 into shared memory in the MMA's swizzled layout, and rescale their half of the O
-//    accumulator in TMEM only when the maximum has grown by more than 2^8 since it was last
-//    applied (P stays <= 256, exact in the final O / l).  After the last block they divide O by
-//    l and store it.
+// GB300 design, two kernels sharing the softmax code:
+//  * attn_pair_kernel (D = 128, 256 with an even number of 128-row query tiles, the benchmarked
+//    case): two CTAs of a cluster run as one 2-SM MMA unit over a pair of adjacent query tiles;
+//    P goes from the softmax warps to the PV MMA through TMEM.  Described at the kernel.
+//  * attn_fwd_kernel (D = 64, or an odd tile count): one CTA per 128-row query tile.  Keys go in
+//    blocks of 128 (the MMA re-reads the whole Q tile from shared memory for every block, so longer
+//    blocks cost less shared-memory bandwidth per flop), which at a head size of 256 leaves room
+//    for one K, one V and one P buffer (Q 64 KB + K 64 KB + V 64 KB + P 32 KB) and two score
+//    buffers in TMEM (2 x 128 score columns + 256 O columns).  320 threads in three roles:
+//     - warp 0: lane 0 loads Q once and the K blocks, lane 1 the V blocks (TMA, 128-byte
+//       swizzle), each as soon as its buffer is free (K_j+1 once S_j is computed, V_j+1 once PV_j
+//       is);
+//     - warp 1 owns TMEM and issues the tcgen05 MMAs: S_j = Q K_j^T (M 128, N 128, bf16, K-major
+//       both) into score buffer j % 2, and O += P_j V_j (M 128, N D, P K-major, V MN-major), in
+//       the order S_0, S_1, PV_0, S_2, PV_1, ... so the next scores are computed while the softmax
+//       warps work on the current ones;
+//     - warps 2-9 (two per TMEM lane quadrant, one query row per thread, each warp half of a
+//       block's keys and half of O's columns) read the scores with tcgen05.ld, mask the diagonal
+//       block, keep the running row maximum m and sum l in base-2 units, write P = 2^(s c - m) as
+//       bf16 into shared memory in the MMA's swizzled layout, and rescale their half of the O
+//       accumulator in TMEM only when the maximum has grown by more than 2^8 since it was last
+//       applied (P stays <= 256, exact in the final O / l).  After the last block they divide O
+//       by l and store it.
+// Consecutive CTAs (pairs) take the tiles of one (batch, head) slice, heaviest first, so the
+// ones resident together share that slice's key and value blocks in L2.
 // All waits are bounded (watchdog); a CTA whose wait runs out drains its MMAs and copies and
 // frees its TMEM before it returns.
 #include <math.h>
@@ -90,7 +96,50 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return *reinterpret_cast<uint32_t*>(&h);
 }
 
-template <int D, int CL>
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+// Row maximum over this thread's HK scores s (keys k0 + k) and its partner warp's HK scores so
+// (keys ko + k); with MASK, keys past `lim` (the last visible key of the block) are left out.
+// Four independent chains of three-input maxima.
+template <int HK, bool MASK>
+__device__ __forceinline__ float block_row_max(const float (&s)[HK], const float (&so)[HK], int k0, int ko,
+                                               int lim) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+    for (int k = 0; k < HK; ++k) {
+        const float x = (MASK && k0 + k > lim) ? -INFINITY : s[k];
+        const float y = (MASK && ko + k > lim) ? -INFINITY : so[k];
+        m[k & 3] = max3f(m[k & 3], x, y);
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+// p = 2^(s c - m) for this thread's HK keys, two at a time, packed to bf16 pairs; with MASK,
+// keys past `lim` give p = 0.  Returns the (unrounded) sum of p as two partial sums.
+template <int HK, bool MASK>
+__device__ __forceinline__ float2 block_exp2(const float (&s)[HK], int k0, int lim, float c, float m,
+                                             uint32_t (&pk)[HK / 2]) {
+    const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+    float2 sum2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int k = 0; k < HK; k += 2) {
+        const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+        float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+        if (MASK) {
+            if (k0 + k > lim) p.x = 0.0f;
+            if (k0 + k + 1 > lim) p.y = 0.0f;
+        }
+        sum2 = __fadd2_rn(sum2, p);
+        pk[k / 2] = pack_bf16x2(p.x, p.y);
+    }
+    return sum2;
+}
+
+template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
@@ -115,30 +164,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     auto s_free = [&](int i) { return bar0 + 8u * (3 + 4 * KV + 2 * PB + SB + i); };
     int* flag = a.flag;
 
-    // CL = 2: the two CTAs of a cluster take adjacent query tiles 2u, 2u + 1 of one slice and
-    // share the key blocks both need: each loads half of every shared K and V block and
-    // multicasts it to both, halving the L2 traffic of the key/value stream.  Heaviest tiles first.
+    // Consecutive CTAs take the tiles of one (batch, head) slice, heaviest (most key blocks)
+    // first, so the CTAs resident together share their slice's key/value blocks in L2.
     const int ntile = a.S / kAttnQ;
-    const uint32_t rank = CL > 1 ? cluster_rank() : 0u;
-    const int group = blockIdx.x / CL;
-    const int u = ntile / CL - 1 - group / a.BH;
-    const int bh = group % a.BH;
-    const int qt = CL * u + static_cast<int>(rank);
+    const int bh = static_cast<int>(blockIdx.x) / ntile;
+    const int qt = ntile - 1 - static_cast<int>(blockIdx.x) % ntile;
     constexpr int kBlocksPerTile = kAttnQ / kAttnK;
     const int nb = (qt + 1) * kBlocksPerTile;             // key blocks up to the diagonal
-    const int nshared = (CL * u + 1) * kBlocksPerTile;    // needed by every CTA of the cluster
     const int row0 = bh * a.S + qt * kAttnQ;
     const int krow0 = bh * a.S;
-    constexpr uint16_t kAll = static_cast<uint16_t>((1u << CL) - 1u);
-    constexpr int kAtomsPerCta = L::ATOMS / CL;
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int i = 0; i < KV; ++i) {
             mbar_init(k_full(i), 1);
-            mbar_init(k_empty(i), CL);   // a shared block is free once every CTA is done with it
+            mbar_init(k_empty(i), 1);
             mbar_init(v_full(i), 1);
-            mbar_init(v_empty(i), CL);
+            mbar_init(v_empty(i), 1);
         }
         for (int i = 0; i < PB; ++i) {
             mbar_init(p_full(i), kAttnSoftmaxWarps);
@@ -154,8 +196,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     }
     if (warp == 1) tmem_alloc(base + L::OFF_HOLD, L::TMEM_COLS);
     tc_fence_before();
-    if (CL > 1) cluster_sync();   // the peer's multicast copies and commits find initialised barriers
-    else __syncthreads();
+    __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
 
@@ -183,12 +224,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
                 mbar_arrive_expect_tx(full, L::KV_BYTES);
                 const int y = krow0 + j * kAttnK;
                 const uint32_t dst = base + off + st * L::KV_BYTES;
-                if (CL > 1 && j < nshared) {
-                    for (int c = kAtomsPerCta * rank; c < kAtomsPerCta * (rank + 1); ++c)
-                        tma_load_2d_mc(dst + c * L::KV_REGION, map, 64 * c, y, full, kAll);
-                } else {
-                    for (int c = 0; c < L::ATOMS; ++c) tma_load_2d(dst + c * L::KV_REGION, map, 64 * c, y, full);
-                }
+                for (int c = 0; c < L::ATOMS; ++c) tma_load_2d(dst + c * L::KV_REGION, map, 64 * c, y, full);
                 ++loads;
             }
             if (loads < nb) {  // let the copies in flight land before the shared memory goes away
@@ -219,8 +255,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
                            smem_desc_sw128(kb + (s / 4) * L::KV_REGION + (s % 4) * 32, 16, 1024), idS,
                            s > 0 ? 1u : 0u);
                 tc_commit(s_full(sb));
-                if (CL > 1 && j < nshared) tc_commit_mc(k_empty(st), kAll);   // free in every CTA
-                else tc_commit(k_empty(st));
+                tc_commit(k_empty(st));
                 issued = true;
                 return true;
             };
@@ -237,8 +272,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
                            smem_desc_sw128(vb + s * 2048, L::KV_REGION, 1024), idO,
                            (j > 0 || s > 0) ? 1u : 0u);
                 tc_commit(o_done(pi));
-                if (CL > 1 && j < nshared) tc_commit_mc(v_empty(st), kAll);
-                else tc_commit(v_empty(st));
+                tc_commit(v_empty(st));
                 issued = true;
                 return true;
             };
@@ -291,17 +325,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
             if (lane == 0) mbar_arrive(s_free(sb));   // the score buffer may be overwritten now
 
             // keys with index > query index are masked (only in the blocks at the diagonal)
+            // keys with index > query index are masked: only in the blocks at and past the
+            // tile's diagonal (j >= qt), a condition uniform over the CTA
             const int lim = qrow - j * kAttnK;           // last visible key of this block
-            const bool masked = lim < kAttnK - 1;
+            const bool diag = j >= qt;
             const int k0 = HK * hh, ko = HK * (1 - hh);
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int k = 0; k < HK; ++k) {
-                const float x = (masked && k0 + k > lim) ? -INFINITY : s[k];
-                const float y = (masked && ko + k > lim) ? -INFINITY : so[k];
-                mx4[k & 3] = fmaxf(mx4[k & 3], fmaxf(x, y));
-            }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * c;
+            const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
+                                   : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
             float alpha = 1.0f;
             bool rescale = false;
             if (mx > m_used + kRescaleLog2) {   // always true for the first block (m_used = -inf)
@@ -311,21 +341,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
                 }
                 m_used = mx;
             }
-            // p = 2^(s c - m) for this warp's HK keys, two at a time
-            const float2 c2 = make_float2(c, c), nm2 = make_float2(-m_used, -m_used);
-            float2 sum2 = make_float2(0.0f, 0.0f);
+            // p = 2^(s c - m) for this warp's HK keys
             uint32_t pk[HK / 2];
-#pragma unroll
-            for (int k = 0; k < HK; k += 2) {
-                const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
-                float2 p = make_float2(ex2f(x.x), ex2f(x.y));
-                if (masked) {
-                    if (k0 + k > lim) p.x = 0.0f;
-                    if (k0 + k + 1 > lim) p.y = 0.0f;
-                }
-                sum2 = __fadd2_rn(sum2, p);
-                pk[k / 2] = pack_bf16x2(p.x, p.y);
-            }
+            const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
+                                     : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
             l = l * alpha + (sum2.x + sum2.y);
 
             // P buffer pi was last read by PV_{j-PB}
@@ -399,13 +418,340 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
         }
     }
     tc_fence_before();
-    // no CTA leaves while its peer may still multicast into its shared memory or commit to its
-    // barriers
-    if (CL > 1) cluster_sync();
-    else __syncthreads();
+    __syncthreads();
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, L::TMEM_COLS);
+    }
+}
+
+// ================================================================== 2-SM variant (D = 128, 256)
+// The two CTAs of a cluster hold adjacent query tiles 2u and 2u + 1 of one slice and act as one
+// MMA unit (tcgen05 .cta_group::2, M = 256): S = Q K^T takes rows 0-127 of Q from CTA 0 and rows
+// 128-255 from CTA 1 and keys 0-63 of the block from CTA 0, keys 64-127 from CTA 1; O += P V
+// takes P's rows the same way and V's columns 0..D/2-1 from CTA 0, D/2..D-1 from CTA 1.  Each CTA
+// so holds half of every key and value block: two K and two V stages fit next to Q at D = 256
+// (Q 64 KB + K 2 x 32 KB + V 2 x 32 KB), and the MMAs read half as many B-operand bytes per flop
+// from each CTA's shared memory.  P never touches shared memory: the softmax warps store it as
+// bf16 into TMEM and the PV MMA takes its A operand from there.  TMEM (512 columns per CTA):
+// S at 0-127 (one buffer: S_j+1 is computed as soon as both CTAs have read S_j), P at 128-255
+// (two buffers of 64 columns, 128 bf16 keys each), O at 256-511.  The pair walks key blocks
+// 0 .. 2u + 1 together (tile 2u finds block 2u + 1 fully masked).
+//  * warp 0 of each CTA: lane 0 loads the CTA's Q rows and its half of every K block, lane 1 its
+//    half of every V block; the bytes of both CTAs complete on CTA 0's barriers;
+//  * warp 1 of CTA 0 issues every MMA of the pair, in the order S_0, S_1, PV_0, S_2, PV_1, ...;
+//    commits signal both CTAs' barriers;
+//  * warps 2-9 of each CTA: the softmax of its own 128 query rows (two warps per TMEM lane
+//    quadrant, each exponentiating half of a block's keys and rescaling half of O's columns); they
+//    release S and publish P on CTA 0's barriers.
+constexpr int kPairKV = 2;   // K and V stages
+
+template <int D>
+struct PairLayout {
+    static constexpr int QATOMS = D / 64;                      // 64-column swizzle atoms of Q and K
+    static constexpr int VATOMS = D / 128;                     // atoms of this CTA's V columns
+    static constexpr uint32_t Q_REGION = kAttnQ * 128;         // one Q atom: 128 rows x 128 B
+    static constexpr uint32_t KH_REGION = (kAttnK / 2) * 128;  // one atom of a K half: 64 keys x 128 B
+    static constexpr uint32_t V_REGION = kAttnK * 128;         // one atom of a V half: 128 keys x 128 B
+    static constexpr uint32_t Q_BYTES = kAttnQ * D * 2;
+    static constexpr uint32_t KH_BYTES = (kAttnK / 2) * D * 2;
+    static constexpr uint32_t VH_BYTES = kAttnK * (D / 2) * 2;
+    static constexpr uint32_t OFF_Q = 0;
+    static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                 // + stage * KH_BYTES
+    static constexpr uint32_t OFF_V = OFF_K + kPairKV * KH_BYTES;      // + stage * VH_BYTES
+    static constexpr uint32_t OFF_LX = OFF_V + kPairKV * VH_BYTES;     // row-sum exchange, 2 x 128 fp32
+    static constexpr uint32_t OFF_BAR = OFF_LX + 2 * kAttnQ * 4;
+    // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KV], k_empty[KV],
+    // v_full[KV], v_empty[KV]
+    static constexpr int N_BARS = 9 + 4 * kPairKV;
+    static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
+    static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t S_COL = 0, P_COL = 128, O_COL = 256;
+    static_assert(D == 128 || D == 256, "2-SM attention handles D = 128 and 256");
+    static_assert(S_COL + kAttnK <= P_COL && P_COL + 2 * (kAttnK / 2) <= O_COL && O_COL + D <= TMEM_COLS,
+                  "TMEM budget");
+    static_assert(SMEM <= 232448, "shared-memory budget");
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
+    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
+    const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
+    using L = PairLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const uint32_t bar0 = base + L::OFF_BAR;
+    const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16, s_full = bar0 + 24,
+                   s_free = bar0 + 32;
+    constexpr int KV = kPairKV;
+    auto p_full = [&](int b) { return bar0 + 8u * (5 + b); };
+    auto o_done = [&](int b) { return bar0 + 8u * (7 + b); };
+    auto k_full = [&](int i) { return bar0 + 8u * (9 + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (9 + KV + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KV + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (9 + 3 * KV + i); };
+    int* flag = a.flag;
+
+    // Consecutive pairs take the tile pairs of one (batch, head) slice, heaviest first, so the
+    // pairs resident together share their slices' key/value blocks in L2.
+    const int ntile = a.S / kAttnQ;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int group = blockIdx.x / 2;
+    const int bh = group / (ntile / 2);
+    const int u = ntile / 2 - 1 - group % (ntile / 2);
+    const int qt = 2 * u + static_cast<int>(rank);
+    const int nb = (2 * u + 2) * (kAttnQ / kAttnK);   // key blocks up to the pair's last diagonal
+    const int row0 = bh * a.S + qt * kAttnQ;
+    const int krow0 = bh * a.S;
+
+    // Ring use: barrier x of a ring of n serves blocks j = x, x + n, ...; block j waits for
+    // completion number j / n, parity (j / n) & 1.
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(drain, 1);
+        mbar_init(l_ready, kAttnSoftmaxWarps);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 2 * kAttnSoftmaxWarps);   // both CTAs' softmax warps (CTA 0's copy)
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(p_full(b), 2 * kAttnSoftmaxWarps);
+            mbar_init(o_done(b), 1);
+        }
+        for (int i = 0; i < KV; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(base + L::OFF_HOLD, L::TMEM_COLS);
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
+
+    if (warp == 0) {
+        // ---------------------------------------------------------------- TMA producers
+        if (lane < 2) {
+            const bool is_k = lane == 0;
+            prefetch_map(is_k ? &mKh : &mV);
+            if (is_k) {
+                prefetch_map(&mQ);
+                if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+                const uint32_t qf = mapa_shared(q_full, 0);
+                for (int c = 0; c < L::QATOMS; ++c)
+                    tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
+            }
+            int loads = 0;
+            for (int j = 0; j < nb; ++j) {
+                const int st = j % KV;
+                const uint32_t full = is_k ? k_full(st) : v_full(st);
+                const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+                if (j >= KV && !mbar_wait_bounded(empty, ((j - KV) / KV) & 1, flag)) break;
+                if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
+                const uint32_t full_cl = mapa_shared(full, 0);
+                if (is_k) {
+                    const int y = krow0 + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2);
+                    for (int c = 0; c < L::QATOMS; ++c)
+                        tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
+                                         full_cl);
+                } else {
+                    const int y = krow0 + j * kAttnK;
+                    for (int c = 0; c < L::VATOMS; ++c)
+                        tma_load_2d_pair(base + L::OFF_V + st * L::VH_BYTES + c * L::V_REGION, &mV,
+                                         static_cast<int>(rank) * (D / 2) + 64 * c, y, full_cl);
+                }
+                ++loads;
+            }
+            if (loads < nb && leader) {  // both CTAs' copies in flight complete on CTA 0's barriers
+                if (is_k) (void)mbar_wait_drain(q_full, 0);
+                for (int j = loads - KV < 0 ? 0 : loads - KV; j < loads; ++j)
+                    (void)mbar_wait_drain(is_k ? k_full(j % KV) : v_full(j % KV), (j / KV) & 1);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer (CTA 0)
+        if (leader && lane == 0) {
+            constexpr uint32_t idS = idesc_f16(2 * kAttnQ, kAttnK, false, false, true);
+            constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
+            bool issued = false;
+            auto issue_s = [&](int j) -> bool {
+                const int st = j % KV;
+                if (!mbar_wait_bounded(k_full(st), (j / KV) & 1, flag)) return false;
+                // both CTAs have read S_{j-1} into registers
+                if (j >= 1 && !mbar_wait_bounded(s_free, (j - 1) & 1, flag)) return false;
+                tc_fence_after();
+                const uint32_t kb = base + L::OFF_K + st * L::KH_BYTES;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)   // K = 16 steps over the head: atom s / 4, 32 B apart
+                    tc_mma_pair(tmem + L::S_COL,
+                                smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
+                                smem_desc_sw128(kb + (s / 4) * L::KH_REGION + (s % 4) * 32, 16, 1024), idS,
+                                s > 0 ? 1u : 0u);
+                tc_commit_pair_mc(s_full, 0x3);
+                tc_commit_pair_mc(k_empty(st), 0x3);
+                issued = true;
+                return true;
+            };
+            auto issue_pv = [&](int j) -> bool {
+                const int st = j % KV, pb = j % 2;
+                if (!mbar_wait_bounded(p_full(pb), (j / 2) & 1, flag)) return false;
+                if (!mbar_wait_bounded(v_full(st), (j / KV) & 1, flag)) return false;
+                tc_fence_after();
+                const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
+#pragma unroll
+                for (int s = 0; s < kAttnK / 16; ++s)   // K = 16 keys: 8 TMEM columns of P; V rows 16 s..
+                    tc_mma_pair_ts(tmem + L::O_COL, tmem + L::P_COL + (kAttnK / 2) * pb + 8 * s,
+                                   smem_desc_sw128(vb + s * 2048, L::V_REGION, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+                tc_commit_pair_mc(o_done(pb), 0x3);
+                tc_commit_pair_mc(v_empty(st), 0x3);
+                issued = true;
+                return true;
+            };
+            bool ok = mbar_wait_bounded(q_full, 0, flag);
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < nb; ++j) {
+                if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
+                ok = issue_pv(j);
+            }
+            if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
+                tc_commit_pair(drain);
+                (void)mbar_wait_drain(drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        // Warp w serves TMEM lane quadrant w % 4 (query rows 32 (w % 4) + lane of this CTA's tile)
+        // and half hh of each block's keys and of O's columns.  Both warps of a quadrant read the
+        // whole score row, so they reach the same row maximum without exchanging it.
+        const int qd = warp % 4;
+        const int hh = (warp - 2) / 4;
+        const int r = 32 * qd + lane;
+        const int qrow = qt * kAttnQ + r;
+        const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
+        const float c = a.c;
+        const uint32_t s_free0 = mapa_shared(s_free, 0);
+        const uint32_t p_full_a = mapa_shared(p_full(0), 0), p_full_b = mapa_shared(p_full(1), 0);
+        float m_used = -INFINITY, l = 0.0f;
+        bool ok = true;
+        // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform before them
+        for (int j = 0; j < nb; ++j) {
+            const int pb = j % 2;
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, j & 1, flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            constexpr int HK = kAttnK / 2;
+            float s[HK], so[HK];
+            const uint32_t sbase = tmem + lanes + L::S_COL;
+#pragma unroll
+            for (int k = 0; k < HK / 32; ++k) {
+                tmem_ld32(sbase + HK * hh + 32 * k, s + 32 * k);
+                tmem_ld32(sbase + HK * (1 - hh) + 32 * k, so + 32 * k);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(s_free0);   // S may be overwritten by S_{j+1} now
+
+            // keys with index > query index are masked: only in the blocks at and past the
+            // tile's diagonal (j >= qt), a condition uniform over the CTA
+            const int lim = qrow - j * kAttnK;           // last visible key of this block
+            const bool diag = j >= qt;
+            const int k0 = HK * hh, ko = HK * (1 - hh);
+            const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
+                                   : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
+            float alpha = 1.0f;
+            bool rescale = false;
+            if (mx > m_used + kRescaleLog2) {   // always true for the first block (m_used = -inf)
+                if (j > 0) {
+                    alpha = ex2f(m_used - mx);
+                    rescale = true;
+                }
+                m_used = mx;
+            }
+            uint32_t pk[HK / 2];
+            const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
+                                     : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
+            l = l * alpha + (sum2.x + sum2.y);
+
+            // P buffer pb was last read by PV_{j-2}
+            if (j >= 2) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(pb), ((j - 2) / 2) & 1, flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {   // rows without a new maximum scale by 1
+                // O must hold blocks 0..j-1 exactly: PV_{j-1} complete (PV_j is not issued yet)
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done((j - 1) % 2), ((j - 1) / 2) & 1, flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+#pragma unroll 1
+                for (int k = 0; k < D / 64; ++k) {
+                    const uint32_t col = L::O_COL + (D / 2) * hh + 32 * k;
+                    float o[32];
+                    tmem_ld32(tmem + lanes + col, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                    tmem_st32(tmem + lanes + col, o);
+                }
+            }
+            // this warp's 64 keys of P row r: 32 columns of bf16 pairs
+            tmem_st32(tmem + lanes + L::P_COL + HK * pb + (HK / 2) * hh, reinterpret_cast<const float*>(pk));
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(pb ? p_full_b : p_full_a);
+        }
+        const int last = nb - 1;
+        if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(o_done(last % 2), (last / 2) & 1, flag))) {
+            tc_fence_after();
+            // the row sum is the sum of the two halves' partial sums, exchanged through shared
+            // memory (a bounded mbarrier wait, not a named barrier: a warp that gave up earlier
+            // must not leave its partner blocked)
+            float* lx = reinterpret_cast<float*>(gbase + L::OFF_LX);
+            lx[hh * kAttnQ + r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_ready);
+            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(l_ready, 0, flag));
+            const float inv = 1.0f / (l + lx[(1 - hh) * kAttnQ + r]);
+            if (got) {
+                __nv_bfloat16* orow = a.O + static_cast<int64_t>(row0 + r) * D + (D / 2) * hh;
+#pragma unroll 1
+                for (int k = 0; k < D / 64; ++k) {
+                    float o[32];
+                    tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 32 * k, o);
+                    tmem_ld_wait();
+                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                            pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                            pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                            pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    // neither CTA leaves while its peer may still read its shared memory or TMEM (MMA operands),
+    // write into it (copies) or signal its barriers
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, L::TMEM_COLS);
     }
 }
 
@@ -417,7 +763,7 @@ constexpr uint32_t attn_launch_smem() {
 }
 
 // Opt the kernel into its shared-memory size on the current device (once per device).
-template <int D, int CL>
+template <int D>
 int attn_attr() {
     static std::mutex mu;
     static bool done[64] = {false};
@@ -427,7 +773,7 @@ int attn_attr() {
     if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
     std::lock_guard<std::mutex> lock(mu);
     if (!done[dev]) {
-        e = cudaFuncSetAttribute(attn_fwd_kernel<D, CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(attn_launch_smem<D>()));
         if (e != cudaSuccess) return record_cuda_error(e);
         done[dev] = true;
@@ -435,24 +781,57 @@ int attn_attr() {
     return FUSE_OK;
 }
 
-template <int D, int CL>
+template <int D>
 int launch_attn(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap& mV,
                 const AttnArgs& args, cudaStream_t st) {
-    const int rc = attn_attr<D, CL>();
+    const int rc = attn_attr<D>();
     if (rc != FUSE_OK) return rc;
+    attn_fwd_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ), kAttnThreads,
+                         attn_launch_smem<D>(), st>>>(mQ, mK, mV, args);
+    return check_launch();
+}
+
+template <int D>
+int pair_attr() {
+    static std::mutex mu;
+    static bool done[64] = {false};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        e = cudaFuncSetAttribute(attn_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PairLayout<D>::SMEM));
+        if (e != cudaSuccess) return record_cuda_error(e);
+        done[dev] = true;
+    }
+    return FUSE_OK;
+}
+
+// 2-SM kernel: one cluster of two CTAs per pair of adjacent query tiles
+template <int D>
+int launch_pair(const void* q, const void* k, const void* v, const AttnArgs& args, cudaStream_t st) {
+    const int rc = pair_attr<D>();
+    if (rc != FUSE_OK) return rc;
+    const int64_t rows = static_cast<int64_t>(args.BH) * args.S;
+    CUtensorMap mQ, mKh, mV;
+    if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mKh, k, rows, D, 64, kAttnK / 2, true) ||
+        !make_map(&mV, v, rows, D, 64, kAttnK, true))
+        return FUSE_ECUDA;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ));
+    cfg.gridDim = dim3(static_cast<unsigned>(rows / kAttnQ));
     cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = attn_launch_smem<D>();
+    cfg.dynamicSmemBytes = PairLayout<D>::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attrs[1];
     attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = CL;
+    attrs[0].val.clusterDim.x = 2;
     attrs[0].val.clusterDim.y = 1;
     attrs[0].val.clusterDim.z = 1;
     cfg.attrs = attrs;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D, CL>, mQ, mK, mV, args);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_pair_kernel<D>, mQ, mKh, mV, args);
     if (e != cudaSuccess) return record_cuda_error(e);
     return check_launch();
 }
@@ -468,10 +847,12 @@ int run_attn(const void* q, const void* k, const void* v, void* o, int bh, int S
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     const AttnArgs args{bh, S, scale * 1.4426950408889634f, static_cast<__nv_bfloat16*>(o), flag};
-    // pairs of adjacent query tiles share their key/value stream when the tiles pair up and the
-    // head splits into two halves of 64-wide swizzle atoms
-    if (D >= 128 && (S / kAttnQ) % 2 == 0) return launch_attn<D, 2>(mQ, mK, mV, args, st);
-    return launch_attn<D, 1>(mQ, mK, mV, args, st);
+    // adjacent query tiles run as 2-SM pairs when they pair up and the head splits into two
+    // halves of 64-wide swizzle atoms
+    if constexpr (D >= 128) {
+        if ((S / kAttnQ) % 2 == 0) return launch_pair<D>(q, k, v, args, st);
+    }
+    return launch_attn<D>(mQ, mK, mV, args, st);
 }
 
 bool overlap(const void* a, const void* b, int64_t bytes) {
@@ -484,11 +865,11 @@ bool overlap(const void* a, const void* b, int64_t bytes) {
 int attn_report_count() { return 1; }
 int attn_report(int i, fuse_kernel_record* out) {
     if (i != 0) return FUSE_EINVAL;
-    const int rc = attn_attr<256, 2>();
+    const int rc = pair_attr<256>();
     if (rc != FUSE_OK) return rc;
-    const int r2 = describe_kernel((const void*)attn_fwd_kernel<256, 2>,
-                                   "attn_fwd_kernel<D=256> (tcgen05, 2-CTA K/V multicast)", kAttnThreads,
-                                   static_cast<int>(attn_launch_smem<256>()), out);
+    const int r2 = describe_kernel((const void*)attn_pair_kernel<256>,
+                                   "attn_pair_kernel<D=256> (tcgen05 2-SM, M=256)", kAttnThreads,
+                                   static_cast<int>(PairLayout<256>::SMEM), out);
     if (r2 == FUSE_OK) out->cluster_size = 2;
     return r2;
 }

@@ -28,20 +28,29 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// Suspend-time hint of one try_wait, in ns: a waiting thread is parked by the hardware until the
+// phase completes or this much time has passed, instead of spinning and taking issue slots from
+// the warps that do the work.
+constexpr uint32_t kTryWaitHintNs = 20000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(kTryWaitHintNs)
         : "memory");
     return ok != 0;
 }
 
 // Default budget of one bounded wait, in SM clock cycles (~1 s at 2 GHz).
 constexpr long long kWaitBudget = 2000000000LL;
+// A wait reads the watchdog flag (a global-memory load) only once it has lasted this many cycles
+// (~0.5 ms): a normal pipeline wait ends within microseconds and never pays for the load, which
+// would otherwise delay its noticing the phase change by a memory round trip.
+constexpr long long kFlagPollAfter = 1LL << 20;
 
 // Wait for phase `parity` of an mbarrier to complete, for at most `budget` SM cycles.  On expiry
 // (or when another thread already raised the watchdog flag) the flag is set and false is
@@ -52,9 +61,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     const long long t0 = clock64();
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (++spins % 64u == 0u) {
-            if (*reinterpret_cast<volatile int*>(flag) != 0) return false;
-            if (clock64() - t0 > budget) {
+        if (++spins % 8u == 0u) {
+            const long long dt = clock64() - t0;
+            if (dt > kFlagPollAfter && *reinterpret_cast<volatile int*>(flag) != 0) return false;
+            if (dt > budget) {
                 atomicExch(flag, 1);
                 return false;
             }
@@ -72,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity,
     const long long t0 = clock64();
     uint32_t spins = 0;
     while (!mbar_try_wait(bar, parity)) {
-        if (++spins % 64u == 0u && clock64() - t0 > budget) return false;
+        if (++spins % 8u == 0u && clock64() - t0 > budget) return false;
     }
     return true;
 }

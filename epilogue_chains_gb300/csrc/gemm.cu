@@ -398,20 +398,29 @@ struct DecodeLayout {
     static constexpr uint32_t A_ST = NM * BK * 2;
     static constexpr uint32_t OFF_BT = 0;
     static constexpr uint32_t OFF_AS = OFF_BT + STAGES * DEC_BT_STAGE;
-    static constexpr uint32_t OFF_P = OFF_AS + STAGES * A_ST;           // fp32 partial [NM][128]
+    // fp32 partials received from every CTA of the cluster for this CTA's column slice:
+    // [source rank][slice column][output row], DEC_SPLIT x (128 / DEC_SPLIT) x NM
+    static constexpr uint32_t OFF_P = OFF_AS + STAGES * A_ST;
     static constexpr uint32_t OFF_BAR = OFF_P + NM * 128 * 4;
-    static constexpr uint32_t N_BARS = 2 * STAGES + 2;               // full, empty, acc, drain
+    static constexpr uint32_t N_BARS = 2 * STAGES + 3;               // full, empty, acc, drain, recv
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
     static constexpr uint32_t TCOLS = NM <= 32 ? 32 : 64;
 };
 
-__device__ __forceinline__ float ld_dsmem_f32(uint32_t local_addr, uint32_t rank) {
-    uint32_t remote;
-    float v;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
-    return v;
+// Store four floats into the shared memory of a CTA of the cluster (`remote` and `remote_bar` are
+// shared::cluster addresses); the bytes count toward that CTA's mbarrier transaction.
+__device__ __forceinline__ void st_async_v4(uint32_t remote, float a, float b, float c, float d,
+                                            uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
+                 ::"r"(remote), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
+                 : "memory");
+}
+__device__ __forceinline__ void cluster_arrive() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 template <int NM>
@@ -433,8 +442,9 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     auto empty_bar = [&](int s) { return bar0 + 8u * (L::STAGES + s); };
     const uint32_t acc_bar = bar0 + 8u * (2 * L::STAGES);
     const uint32_t drain_bar = acc_bar + 8u;
+    const uint32_t recv_bar = drain_bar + 8u;
     const uint32_t holder = base + L::OFF_HOLD;
-    float* part = reinterpret_cast<float*>(gbase + L::OFF_P);  // [NM][128]
+    const float* recv = reinterpret_cast<const float*>(gbase + L::OFF_P);  // [DEC_SPLIT][COLS][NM]
     int* flag = args.flag;
 
     if (threadIdx.x == 0) {
@@ -444,7 +454,10 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
         }
         mbar_init(acc_bar, 1);
         mbar_init(drain_bar, 1);
+        mbar_init(recv_bar, 1);
         fence_mbar_init();
+        // every CTA of the cluster sends this CTA one slice of its partial (NM x COLS fp32)
+        mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(128 * NM * 4));
         prefetch_map(&mapA);
         prefetch_map(&mapB);
     }
@@ -452,8 +465,34 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // Peers may send into this CTA's shared memory only once its receive barrier exists: the
+    // cluster barrier is arrived at here and waited on just before the first send, so the wait
+    // overlaps the main loop.  Every thread reaches both on every path.
+    cluster_arrive();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
     bool ok = true;
+
+    // After the K reduction CTA `rank` finishes output columns [n0 + COLS*rank, +COLS) of all NM
+    // rows, in units of one column and four consecutive rows: unit idx = threadIdx.x +
+    // kDecThreads*u is slice column idx / (NM/4), rows 4*(idx % (NM/4)) .. +3.  Each thread loads
+    // the bias and residual values of its units now, so their latency hides under the main loop.
+    constexpr int COLS = 128 / DEC_SPLIT;  // 16
+    constexpr int UNITS = NM * COLS / 4;
+    constexpr int UPT = (UNITS + kDecThreads - 1) / kDecThreads;
+    float eb[UPT], er[UPT][4];
+#pragma unroll
+    for (int u = 0; u < UPT; ++u) {
+        const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
+        const int n = n0 + COLS * static_cast<int>(rank) + idx / (NM / 4);
+        const int m0 = 4 * (idx % (NM / 4));
+        const bool valid = idx < UNITS && n < args.N;
+        eb[u] = valid && args.epi >= 1 ? __half2float(__ldg(args.bias + n)) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            er[u][i] = valid && args.epi >= 3 && m0 + i < args.M
+                           ? __half2float(__ldcs(args.R + static_cast<int64_t>(m0 + i) * args.N + n))
+                           : 0.0f;
+    }
 
     if (warp == 0) {
         uint32_t inflight = 0, issue_par = 0, phase = 0;
@@ -509,7 +548,9 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
             (void)mbar_wait_drain(drain_bar, 0);
         }
     }
-    // all four warps: accumulator (TMEM lane = output column n0 + 32*warp + lane) -> smem partial
+    // All four warps: thread (warp, lane) holds output column n0 + 32*warp + lane of this CTA's
+    // partial (its TMEM lane) for all NM rows and sends it to the CTA that owns that column's slice,
+    // into row `rank` of that CTA's receive buffer.
     {
         const bool have = nk > 0;
         bool got = true;
@@ -523,34 +564,56 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
             tmem_ld_wait();
         } else {
 #pragma unroll
-            for (int c = 0; c < NM; ++c) v[c] = 0.0f;
+            for (int c = 0; c < NM; ++c) v[c] = 0.0f;   // after a failed wait: zeros, still sent
         }
+        const int col = 32 * warp + lane;
+        const uint32_t owner = static_cast<uint32_t>(col / COLS);
+        const uint32_t dst = mapa_shared(
+            smem_addr(recv) + 4u * static_cast<uint32_t>((static_cast<int>(rank) * COLS + col % COLS) * NM), owner);
+        const uint32_t dst_bar = mapa_shared(recv_bar, owner);
+        cluster_wait();   // every CTA of the cluster has initialised its receive barrier
 #pragma unroll
-        for (int c = 0; c < NM; ++c) part[c * 128 + 32 * warp + lane] = v[c];
+        for (int c = 0; c < NM; c += 4) st_async_v4(dst + 4u * c, v[c], v[c + 1], v[c + 2], v[c + 3], dst_bar);
     }
-    tc_fence_before();
-    cluster_sync();  // every CTA of the cluster has its partial in shared memory
 
-    // CTA `rank` reduces output columns [n0 + COLS*rank, n0 + COLS*rank + COLS) for all NM rows
-    {
-        constexpr int COLS = 128 / DEC_SPLIT;  // 16
-        const uint32_t part_addr = smem_addr(part);
-        for (int idx = threadIdx.x; idx < COLS * NM; idx += kDecThreads) {
-            const int m = idx / COLS;
-            const int nl = static_cast<int>(rank) * COLS + idx % COLS;
-            float s = 0.0f;
+    // This CTA's slice: the DEC_SPLIT partials summed in rank order, then the epilogue.  If the
+    // wait gives up (another wait of the launch failed), the peers still send their slices on every
+    // path: wait for them without the flag (bounded) so none lands after this CTA has exited.
+    const bool received = mbar_wait_bounded(recv_bar, 0, flag);
+    if (!received) (void)mbar_wait_drain(recv_bar, 0, kWaitBudget);
+    if (received) {
 #pragma unroll
-            for (int r = 0; r < DEC_SPLIT; ++r)
-                s += ld_dsmem_f32(part_addr + 4u * (m * 128 + nl), static_cast<uint32_t>(r));
-            const int n = n0 + nl;
-            if (m < args.M && n < args.N) {
-                const float b = args.epi >= 1 ? __half2float(args.bias[n]) : 0.0f;
-                const float rr = args.epi >= 3 ? __half2float(args.R[static_cast<int64_t>(m) * args.N + n]) : 0.0f;
-                args.Y[static_cast<int64_t>(m) * args.N + n] = __float2half_rn(apply_stages(s, 1, args.epi, b, rr));
+        for (int u = 0; u < UPT; ++u) {
+            const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
+            if (idx >= UNITS) break;
+            const int c = idx / (NM / 4);
+            const int m0 = 4 * (idx % (NM / 4));
+            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int r = 0; r < DEC_SPLIT; ++r) {
+                const float4 p = *reinterpret_cast<const float4*>(recv + (r * COLS + c) * NM + m0);
+                sum.x += p.x;
+                sum.y += p.y;
+                sum.z += p.z;
+                sum.w += p.w;
+            }
+            const int n = n0 + COLS * static_cast<int>(rank) + c;
+            if (n < args.N) {
+                const float2 lo = apply_stages2(make_float2(sum.x, sum.y), 1, args.epi, make_float2(eb[u], eb[u]),
+                                                make_float2(er[u][0], er[u][1]));
+                const float2 hi = apply_stages2(make_float2(sum.z, sum.w), 1, args.epi, make_float2(eb[u], eb[u]),
+                                                make_float2(er[u][2], er[u][3]));
+                const float o[4] = {lo.x, lo.y, hi.x, hi.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (m0 + i < args.M) args.Y[static_cast<int64_t>(m0 + i) * args.N + n] = __float2half_rn(o[i]);
             }
         }
     }
-    cluster_sync();  // no CTA leaves while another still reads its partial
+    // TMEM is freed once every thread's reads of it have completed.  No cluster barrier: a CTA's
+    // shared memory is written by its peers only until its own receive barrier completes.
+    tc_fence_before();
+    __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, L::TCOLS);
 }
@@ -607,6 +670,29 @@ int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs
     cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<NM>, mA, mB, a);
     if (e != cudaSuccess) return record_cuda_error(e);
     return check_launch();
+}
+
+// Clusters of the decode kernel that can be resident at once (0 if the query fails).
+template <int NM>
+int decode_max_active_clusters() {
+    using L = DecodeLayout<NM>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(DEC_SPLIT * 32));
+    cfg.blockDim = dim3(kDecThreads);
+    cfg.dynamicSmemBytes = L::SMEM;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeClusterDimension;
+    attrs[0].val.clusterDim.x = DEC_SPLIT;
+    attrs[0].val.clusterDim.y = 1;
+    attrs[0].val.clusterDim.z = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<NM>, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    return n;
 }
 
 bool main_attr_ok() {
@@ -742,7 +828,10 @@ int gemm_report(int i, fuse_kernel_record* out) {
             const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
                                            "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
                                            static_cast<int>(DecodeLayout<16>::SMEM), out);
-            if (rc == FUSE_OK) out->cluster_size = DEC_SPLIT;
+            if (rc == FUSE_OK) {
+                out->cluster_size = DEC_SPLIT;
+                out->max_active_clusters = decode_max_active_clusters<16>();
+            }
             return rc;
         }
         case 2: return describe_kernel((const void*)epi_tail_kernel, "epi_tail_kernel (unfused plans)", 256, 0, out);

@@ -48,7 +48,10 @@ def _check(o, ref, v, rows=None):
     assert np.sqrt(np.mean(err ** 2)) <= 2.0 ** -9 * np.sqrt(np.mean(vd ** 2))
 
 
-@pytest.mark.parametrize("shape", [(2, 256, 256), (1, 128, 64), (3, 384, 128), (2, 512, 256)])
+# (bh, S, D): an even number of 128-row query tiles at D = 128 / 256 runs the 2-SM kernel, an odd
+# number (or D = 64) the one-CTA kernel
+@pytest.mark.parametrize("shape", [(2, 256, 256), (1, 128, 64), (3, 384, 128), (2, 512, 256),
+                                   (1, 384, 256), (5, 256, 128), (2, 1024, 64)])
 def test_small_shapes_every_row(cuda_device, shape):
     bh, S, D = shape
     q, k, v = wl.attention_input(bh, S, D, salt=S + D)
@@ -86,10 +89,12 @@ def test_sharp_queries_select_exactly_one_value_row(cuda_device):
     assert np.array_equal(o, v[sel])
 
 
-def test_growing_scores_rescale_every_block(cuda_device):
+@pytest.mark.parametrize("D", [64, 128, 256])
+def test_growing_scores_rescale_every_block(cuda_device, D):
     """Scores that rise by 64 (natural units) per 128-key block force the O rescale in every block
-    of every row; large magnitudes also exercise the far tails of exp."""
-    S, D = 512, 64
+    of every row; large magnitudes also exercise the far tails of exp.  D = 64 runs the one-CTA
+    kernel, D = 128 and 256 the 2-SM kernel (four query tiles: two pairs)."""
+    S = 512
     k = np.zeros((S, D), np.float32)
     k[:, 0] = np.arange(S) / 2.0                      # rounded to bf16 below; both sides see it
     g = np.random.default_rng(24)
