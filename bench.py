@@ -6,17 +6,21 @@ function of K, on the pointwise chain x, y fp32 [16,777,216], K in {2, 3, 4, 6, 
 y = a_s y + b_s (a_s ~ U[0.9,1.1], b_s ~ U[-0.1,0.1]), ReLU on even s.
 
 One step = one pass over every row of the hot path on its own synthetic batch:
-  chain fused (K = 2,3,4,6,8) | chain unfused (same K) | fat probe (same K) |
-  RMSNorm [2048,4096] fused + unfused | causal softmax [8,16,2048,2048] fused (skip 0/64/128) +
-  unfused.
-Each row runs as a group: one untimed launch of the same kernels first, then the timed launches
-back to back over rotating buffers (4 input/output pairs, 512 MiB for the chain: larger than the
-126 MiB L2), so every timed launch pays for the dirty lines its predecessor of the same kind left
-in L2, as in a steady stream.  Every launch is bracketed by CUDA events on the launching stream.
+  chain fused (K = 2,3,4,6,8) | chain unfused (same K) | fat probe (K = 4) |
+  RMSNorm [2048,4096] fused + unfused | residual add + RMSNorm | SiLU*up |
+  causal softmax [8,16,2048,2048] fused (skip 0/64/128) + unfused | attention [128,2048,256] |
+  GEMM + bias + GELU + residual 4096^3 and 16x4096x4096, every cut plan.
+Each group is one kind of call: one untimed call first, then its timed calls back to back over
+rotating buffers (4 input/output pairs, 512 MiB for the chain: larger than the 126 MiB L2), so
+every timed call pays for the dirty lines its predecessor left in L2, as in a steady stream.  One
+pair of CUDA events on the launching stream brackets the group's timed calls, so a call's time is
+the group's time over its calls: the work of a stream of such calls, without an event between
+every two of them.  A separate pass after the timed region brackets single calls (rows.per_call).
 
-``value`` = fused-chain algorithmic bytes (2 N b per launch, N b read + N b written) / summed
-fused-chain device time.  ``e2e`` = the same bytes / time of pinned-host -> device copy, the
-C-ABI call and the device -> host copy of y, per K.
+``value`` = fused-chain algorithmic bytes (2 N b per call, N b read + N b written) / the fused
+chain groups' device time.  ``e2e`` = the same bytes / the time of the same chains run through
+the C ABI from pinned host memory: each call's x is copied in and its y copied out in chunks
+pipelined over three streams (copies in both directions overlap the kernels).
 
 ``--impl reference`` times the plain CPU oracle (the only other place this script runs it) on
 the same workload on the host cores, rank 0 only.
@@ -169,15 +173,17 @@ def committed_traffic(group: str, src_name: str):
 
 # ------------------------------------------------------------------------------ our arm
 class Group:
-    """One row of the hot path in a step: an untimed leading call, then timed calls.
+    """One kind of call in a step: an untimed leading call, then `n` timed calls back to back.
 
-    calls: list of (tag, fn, units) -- units are the call's algorithmic bytes (bound "hbm") or
-    flops (bound "tensor").  `kernel` names the single kernel the calls launch (None if a call
-    launches several kernels); `launches` is the number of our kernels one call launches."""
+    fn(): one call (rotating its buffers); units: the call's algorithmic bytes (bound "hbm") or
+    flops (bound "tensor"); kernel: the single kernel a call launches (None if it launches
+    several); launches: kernels of ours per call; family: groups of the same kernel that add up
+    to one roofline row."""
 
-    def __init__(self, name, calls, pre, bound, kernel, launches):
-        self.name, self.calls, self.pre = name, calls, pre
+    def __init__(self, name, fn, units, n, bound, kernel, launches, family=None):
+        self.name, self.fn, self.units, self.n = name, fn, units, n
         self.bound, self.kernel, self.launches = bound, kernel, launches
+        self.family = family or name
 
 
 def run_ours(args, rank, world, local):
@@ -229,17 +235,16 @@ def run_ours(args, rank, world, local):
             counter["launches"] += K if mode == fc.FUSE_UNFUSED else 1
         return fn
 
-    groups = [
-        Group("chain_fused", [(f"K{K}", chain(K, fc.FUSE_FUSED), chain_bytes) for K in KS],
-              chain(KS[0], fc.FUSE_FUSED), "hbm", "chain_fused_kernel<f32>", 1),
-        Group("chain_unfused", [(f"K{K}", chain(K, fc.FUSE_UNFUSED),
-                                 fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED)) for K in KS],
-              chain(KS[0], fc.FUSE_UNFUSED), "hbm", None, None),
-        # the fat probe is a fixed-point probe at K = 4 ([C05] §5: not part of the sweep)
-        Group("chain_fat", [("K4", chain(4, fc.FUSE_FAT), chain_bytes)], chain(4, fc.FUSE_FAT),
-              "hbm", "chain_fat_kernel<f32>", 1),
-    ]
+    groups = [Group(f"chain_fused_K{K}", chain(K, fc.FUSE_FUSED), chain_bytes, 4, "hbm",
+                    "chain_fused_kernel<f32>", 1, "chain_fused") for K in KS]
+    groups += [Group(f"chain_unfused_K{K}", chain(K, fc.FUSE_UNFUSED),
+                     fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED), 2, "hbm", None, K,
+                     "chain_unfused") for K in KS]
+    # the fat probe is a fixed-point probe at K = 4 ([C05] §5: not part of the sweep)
+    groups += [Group("chain_fat", chain(4, fc.FUSE_FAT), chain_bytes, 2, "hbm", "chain_fat_kernel<f32>", 1)]
 
+    plans = {"[4]": 0, "[1,3]": 1, "[2,2]": 2, "[1,1,1,1]": 7}
+    gemm_bufs = {}
     if args.rows == "all":
         # -------------------------------------------------------------- RMSNorm
         with torch.cuda.stream(stream):
@@ -260,10 +265,8 @@ def run_ours(args, rank, world, local):
             return fn
         rb = {m: fc.fuse_rmsnorm_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
         groups += [
-            Group("rmsnorm_fused", [("r", rms(fc.FUSE_FUSED), rb[fc.FUSE_FUSED])] * 2, rms(fc.FUSE_FUSED),
-                  "hbm", "rmsnorm_row_kernel", 1),
-            Group("rmsnorm_unfused", [("r", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED])] * 2,
-                  rms(fc.FUSE_UNFUSED), "hbm", None, None),
+            Group("rmsnorm_fused", rms(fc.FUSE_FUSED), rb[fc.FUSE_FUSED], 4, "hbm", "rmsnorm_row_kernel", 1),
+            Group("rmsnorm_unfused", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED], 2, "hbm", None, 4),
         ]
         # -------------------------------------------------------------- residual add + RMSNorm
         with torch.cuda.stream(stream):
@@ -301,14 +304,11 @@ def run_ours(args, rank, world, local):
             return fn
         sb = {m: fc.fuse_silu_mul_bytes(SR, SC, fc.FUSE_BF16, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
         groups += [
-            Group("add_rmsnorm_fused", [("r", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED])] * 2,
-                  addrms(fc.FUSE_FUSED), "hbm", "rmsnorm_row_kernel<+residual>", 1),
-            Group("add_rmsnorm_unfused", [("r", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED])] * 2,
-                  addrms(fc.FUSE_UNFUSED), "hbm", None, None),
-            Group("silu_mul_fused", [("s", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED])] * 2,
-                  silu(fc.FUSE_FUSED), "hbm", "silu_mul_vec_kernel<bf16>", 1),
-            Group("silu_mul_unfused", [("s", silu(fc.FUSE_UNFUSED), sb[fc.FUSE_UNFUSED])] * 2,
-                  silu(fc.FUSE_UNFUSED), "hbm", None, None),
+            Group("add_rmsnorm_fused", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED], 2, "hbm",
+                  "rmsnorm_row_kernel<+residual>", 1),
+            Group("add_rmsnorm_unfused", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED], 2, "hbm", None, 5),
+            Group("silu_mul_fused", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED], 2, "hbm", "silu_mul_vec_kernel<bf16>", 1),
+            Group("silu_mul_unfused", silu(fc.FUSE_UNFUSED), sb[fc.FUSE_UNFUSED], 2, "hbm", None, 2),
         ]
         # -------------------------------------------------------------- causal softmax
         bh, S = wl.SM_B * wl.SM_H, wl.SM_S
@@ -328,15 +328,11 @@ def run_ours(args, rank, world, local):
                       "fuse_causal_softmax")
                 counter["launches"] += 1 if mode == fc.FUSE_FUSED else 5
             return fn
-        groups += [
-            Group("softmax_fused", [(f"T{t}", sm(t, fc.FUSE_FUSED),
-                                     fc.fuse_causal_softmax_bytes(bh, S, t, fc.FUSE_BF16, fc.FUSE_FUSED))
-                                    for t in (0, 64, 128)], sm(0, fc.FUSE_FUSED), "hbm",
-                  "softmax_fused_kernel<bf16>", 1),
-            Group("softmax_unfused", [("T0", sm(0, fc.FUSE_UNFUSED),
-                                       fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED))],
-                  sm(0, fc.FUSE_UNFUSED), "hbm", None, None),
-        ]
+        groups += [Group(f"softmax_fused_T{t}", sm(t, fc.FUSE_FUSED),
+                         fc.fuse_causal_softmax_bytes(bh, S, t, fc.FUSE_BF16, fc.FUSE_FUSED), 2, "hbm",
+                         "softmax_fused_kernel<bf16>", 1, "softmax_fused") for t in (0, 64, 128)]
+        groups += [Group("softmax_unfused", sm(0, fc.FUSE_UNFUSED),
+                         fc.fuse_causal_softmax_bytes(bh, S, 0, fc.FUSE_BF16, fc.FUSE_UNFUSED), 1, "hbm", None, 5)]
         # -------------------------------------------------------------- attention, no score matrix
         with torch.cuda.stream(stream):
             aq, ak, av = wl.attention_input(device=dev, salt=rank)
@@ -345,18 +341,13 @@ def run_ours(args, rank, world, local):
         ABH, AS, AD = wl.ATT_BH, wl.ATT_S, wl.ATT_D
 
         def attn():
-            def fn():
-                check(lib.fuse_attention(aq.data_ptr(), ak.data_ptr(), av.data_ptr(), aos[orot()].data_ptr(),
-                                         ABH, AS, AD, wl.ATT_SCALE, sh), "fuse_attention")
-                counter["launches"] += 1
-            return fn
+            check(lib.fuse_attention(aq.data_ptr(), ak.data_ptr(), av.data_ptr(), aos[orot()].data_ptr(),
+                                     ABH, AS, AD, wl.ATT_SCALE, sh), "fuse_attention")
+            counter["launches"] += 1
         att_flops = fc.fuse_attention_flops(ABH, AS, AD)
-        groups += [Group("attention_fused", [("a", attn(), att_flops)] * 2, attn(), "tensor",
-                         "attn_fwd_kernel<D=256>", 1)]
+        groups += [Group("attention_fused", attn, att_flops, 2, "tensor", "attn_pair_kernel<D=256>", 1)]
         # -------------------------------------------------------------- GEMM epilogue chain
-        plans = {"[4]": 0, "[1,3]": 1, "[2,2]": 2, "[1,1,1,1]": 7}
         gN, gK = wl.GEMM_N, wl.GEMM_K
-        gemm_bufs = {}
         with torch.cuda.stream(stream):
             for M in wl.GEMM_MS:
                 A, B, bias, Rr = wl.gemm_input(M, device=dev, salt=rank)
@@ -375,30 +366,31 @@ def run_ours(args, rank, world, local):
                 counter["launches"] += 1 + bin(mask).count("1")
             return fn
         flops = {M: 2 * M * gN * gK for M in wl.GEMM_MS}
-        groups += [
-            Group("gemm_M4096_fused", [("[4]", gemm(4096, 0), flops[4096])], gemm(4096, 0), "tensor",
-                  "gemm_tc_kernel", 1),
-            Group("gemm_M4096_unfused", [(p_, gemm(4096, m_), flops[4096]) for p_, m_ in plans.items() if m_],
-                  gemm(4096, 7), "tensor", None, None),
-            Group("gemm_M16_fused", [("[4]", gemm(16, 0), fc.fuse_gemm_bytes(16, gN, gK, 0))], gemm(16, 0),
-                  "hbm", "gemm_decode_kernel<16>", 1),
-            Group("gemm_M16_unfused", [(p_, gemm(16, m_), fc.fuse_gemm_bytes(16, gN, gK, m_))
-                                       for p_, m_ in plans.items() if m_], gemm(16, 7), "hbm", None, None),
-        ]
+        for p_, m_ in plans.items():
+            groups.append(Group(f"gemm_M4096_{p_}", gemm(4096, m_), flops[4096], 2 if m_ == 0 else 1, "tensor",
+                                "gemm_tc_kernel" if m_ == 0 else None, 1 + bin(m_).count("1"),
+                                "gemm_M4096_fused" if m_ == 0 else "gemm_M4096_unfused"))
+        for p_, m_ in plans.items():
+            groups.append(Group(f"gemm_M16_{p_}", gemm(16, m_), fc.fuse_gemm_bytes(16, gN, gK, m_),
+                                4 if m_ == 0 else 2, "hbm", "gemm_decode_kernel<16>" if m_ == 0 else None,
+                                1 + bin(m_).count("1"), "gemm_M16_fused" if m_ == 0 else "gemm_M16_unfused"))
 
     def make_events():
-        # per group: the untimed leading call's events first, then one pair per timed call
+        # per group: the untimed leading call's pair, then one pair around the timed calls
         return {g.name: [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                         for _ in range(len(g.calls) + 1)] for g in groups}
+                         for _ in range(2)] for g in groups}
 
     def step(evs):
         with torch.cuda.stream(stream):
             for g in groups:
-                fns = [g.pre] + [fn for _, fn, _ in g.calls]
-                for fn, (e0, e1) in zip(fns, evs[g.name]):
-                    e0.record(stream)
-                    fn()
-                    e1.record(stream)
+                (l0, l1), (e0, e1) = evs[g.name]
+                l0.record(stream)
+                g.fn()
+                l1.record(stream)
+                e0.record(stream)
+                for _ in range(g.n):
+                    g.fn()
+                e1.record(stream)
 
     for _ in range(max(3, args.warmup)):      # warm-up steps (untimed)
         step(make_events())
@@ -419,23 +411,21 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
     t1 = time.time()
     clocks = summarize_clocks(sampler.stop(), t0, t1)
-    timed_launches = counter["launches"]   # every kernel of ours launched inside the timed region
+    # every kernel of ours launched inside the timed region, the untimed leading calls included
+    timed_launches = counter["launches"]
 
-    # ms per call: times[group][step][call] (timed calls); lead[group][step] (the untimed lead call)
-    times = {g.name: [[e0.elapsed_time(e1) for e0, e1 in evs[g.name][1:]] for evs in all_evs] for g in groups}
-    lead = {g.name: [evs[g.name][0][0].elapsed_time(evs[g.name][0][1]) for evs in all_evs] for g in groups}
     gmap = {g.name: g for g in groups}
+    # ms of a group's timed calls per step, and of its leading call
+    gms = {g.name: [evs[g.name][1][0].elapsed_time(evs[g.name][1][1]) for evs in all_evs] for g in groups}
+    lead = {g.name: [evs[g.name][0][0].elapsed_time(evs[g.name][0][1]) for evs in all_evs] for g in groups}
 
-    def mean_ms(name, idx):
-        return float(np.mean([st[idx] for st in times[name]]))
+    def call_ms(name):       # mean ms per call of a group
+        return float(np.mean(gms[name])) / gmap[name].n
 
-    def group_total_ms(name):
-        return float(np.mean([sum(st) for st in times[name]]))
-
-    fused_ms_total = sum(sum(st) for st in times["chain_fused"])
-    n_fused = args.steps * len(KS)
-    elapsed_s = fused_ms_total / 1e3
-    step_ms = float(np.mean([sum(sum(times[g][s_]) for g in times) for s_ in range(args.steps)]))
+    step_ms = float(np.mean([sum(gms[g][s_] for g in gms) for s_ in range(args.steps)]))
+    fused_groups = [g for g in groups if g.family == "chain_fused"]
+    elapsed_s = sum(sum(gms[g.name]) for g in fused_groups) / 1e3
+    n_fused = args.steps * sum(g.n for g in fused_groups)
     if world > 1:
         import torch.distributed as dist
         t = torch.tensor([elapsed_s, step_ms], dtype=torch.float64, device=dev)
@@ -447,92 +437,104 @@ def run_ours(args, rank, world, local):
                   "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm.cu",
                   "add_rmsnorm_fused": "rmsnorm.cu", "silu_mul_fused": "silu_mul.cu",
                   "attention_fused": "attention.cu"}
+    families = {}
+    for g in groups:
+        families.setdefault(g.family, []).append(g)
 
-    def roofline_of(name):
-        g = gmap[name]
-        tot_units = sum(u for _, _, u in g.calls)
-        tot_ms = group_total_ms(name)
-        if g.bound == "hbm":
+    def family_ms(fam):      # mean ms per step of a family's timed calls
+        return sum(float(np.mean(gms[g.name])) for g in families[fam])
+
+    def roofline_of(fam):
+        gs = families[fam]
+        calls = sum(g.n for g in gs)
+        tot_units = sum(g.units * g.n for g in gs)
+        tot_ms = family_ms(fam)
+        if gs[0].bound == "hbm":
             achieved, peak, unit = tot_units / tot_ms / 1e6, peaks["hbm_gbs"], "GB/s"
         else:
             achieved, peak, unit = tot_units / tot_ms / 1e9, peaks["bf16_tflops"], "TFLOP/s"
-        out = {"bound": g.bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
-               "frac": round(achieved / peak, 4), "kernel": g.kernel,
-               "units_per_launch": int(tot_units / len(g.calls)),
-               "avg_launch_us": round(tot_ms / len(g.calls) * 1e3, 2),
+        out = {"bound": gs[0].bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+               "frac": round(achieved / peak, 4), "kernel": gs[0].kernel,
+               "units_per_launch": int(tot_units / calls),
+               "avg_launch_us": round(tot_ms / calls * 1e3, 2),
                "step_share": round(tot_ms / step_ms, 4)}
-        if g.bound == "tensor":
+        if gs[0].bound == "tensor":
             out["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
         # DRAM bytes per launch from the committed ncu summary of this kernel source, else None
-        out["traffic"] = committed_traffic(name, kernel_src.get(name, ""))
+        out["traffic"] = committed_traffic(fam, kernel_src.get(fam, ""))
         return out
 
-    # dominant kernel: the single-kernel group with the largest share of the step
-    single = [g.name for g in groups if g.kernel is not None]
-    dominant = max(single, key=group_total_ms)
+    # dominant kernel: the single-kernel family with the largest share of the step
+    single = [f for f, gs in families.items() if gs[0].kernel is not None]
+    dominant = max(single, key=family_ms)
     roofline = roofline_of(dominant)
     roofline["peak_source"] = peak_src
 
-    rows = {"step_share": {g.name: round(group_total_ms(g.name) / step_ms, 4) for g in groups}}
+    rows = {"timing": "per group: one untimed call, then its timed calls back to back between one "
+                      "CUDA event pair; per-call figures are the group time over its calls",
+            "step_share": {f: round(family_ms(f) / step_ms, 4) for f in families}}
     # the same shares over every launch of the step, the untimed lead calls included: the figure an
     # ncu launch list of this command (all launches, serialised) can be compared with
-    all_ms = {g.name: group_total_ms(g.name) + float(np.mean(lead[g.name])) for g in groups}
+    all_ms = {f: sum(float(np.mean(gms[g.name])) + float(np.mean(lead[g.name])) for g in gs)
+              for f, gs in families.items()}
     rows["step_share_all_launches"] = {k: round(v / sum(all_ms.values()), 4) for k, v in all_ms.items()}
     per_k = {}
-    for j, K in enumerate(KS):
-        f = mean_ms("chain_fused", j)
-        u = mean_ms("chain_unfused", j)
+    for K in KS:
+        f = call_ms(f"chain_fused_K{K}")
+        u = call_ms(f"chain_unfused_K{K}")
         per_k[str(K)] = {"fused_us": round(f * 1e3, 2), "unfused_us": round(u * 1e3, 2),
                          "speedup_fused_vs_unfused": round(u / f, 3),
                          "fused_GBs": round(chain_bytes / (f / 1e3) / 1e9, 1),
                          "unfused_ledger_GBs": round(fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED)
                                                      / (u / 1e3) / 1e9, 1)}
-    fat = mean_ms("chain_fat", 0)
+    fat = call_ms("chain_fat")
     rows["chain"] = {"per_K": per_k, "roofline_fused": roofline_of("chain_fused"),
-                     "fat_K4": {"us": round(fat * 1e3, 2), "fat_over_fused": round(fat / mean_ms("chain_fused", KS.index(4)), 3)}}
+                     "fat_K4": {"us": round(fat * 1e3, 2), "fat_over_fused": round(fat / call_ms("chain_fused_K4"), 3)}}
     if args.rows == "all":
-        rf, ru = group_total_ms("rmsnorm_fused") / 2, group_total_ms("rmsnorm_unfused") / 2
+        rf, ru = call_ms("rmsnorm_fused"), call_ms("rmsnorm_unfused")
         rows["rmsnorm"] = {"fused_us": round(rf * 1e3, 2), "unfused_us": round(ru * 1e3, 2),
                            "speedup": round(ru / rf, 3), "roofline_fused": roofline_of("rmsnorm_fused")}
-        af, au = group_total_ms("add_rmsnorm_fused") / 2, group_total_ms("add_rmsnorm_unfused") / 2
+        af, au = call_ms("add_rmsnorm_fused"), call_ms("add_rmsnorm_unfused")
         rows["add_rmsnorm"] = {"fused_us": round(af * 1e3, 2), "unfused_us": round(au * 1e3, 2),
                                "speedup": round(au / af, 3),
                                "unfused_ledger_GBs": round(ab[fc.FUSE_UNFUSED] / au / 1e6, 1),
                                "roofline_fused": roofline_of("add_rmsnorm_fused")}
-        sf, su = group_total_ms("silu_mul_fused") / 2, group_total_ms("silu_mul_unfused") / 2
+        sf, su = call_ms("silu_mul_fused"), call_ms("silu_mul_unfused")
         rows["silu_mul"] = {"fused_us": round(sf * 1e3, 2), "unfused_us": round(su * 1e3, 2),
                             "speedup": round(su / sf, 3),
                             "unfused_ledger_GBs": round(sb[fc.FUSE_UNFUSED] / su / 1e6, 1),
                             "roofline_fused": roofline_of("silu_mul_fused")}
-        at = group_total_ms("attention_fused") / 2
+        at = call_ms("attention_fused")
         rows["attention"] = {"us": round(at * 1e3, 1), "flops": att_flops,
                              "TFLOPs": round(att_flops / at / 1e9, 1),
                              "bytes": fc.fuse_attention_bytes(ABH, AS, AD),
                              "roofline": roofline_of("attention_fused"),
-                             "softmax_alone_T0_us": round(mean_ms("softmax_fused", 0) * 1e3, 1),
-                             "vs_softmax_alone": round(mean_ms("softmax_fused", 0) / at, 3),
+                             "softmax_alone_T0_us": round(call_ms("softmax_fused_T0") * 1e3, 1),
+                             "vs_softmax_alone": round(call_ms("softmax_fused_T0") / at, 3),
                              "note": "the materialised path needs Q K^T and P V GEMMs besides the "
                                      "softmax over the 1 GiB score tensor; the softmax alone is its "
                                      "lower bound"}
         smr = {}
-        for j, t in enumerate((0, 64, 128)):
-            ms_ = mean_ms("softmax_fused", j)
-            b_ = gmap["softmax_fused"].calls[j][2]
+        for t in (0, 64, 128):
+            ms_ = call_ms(f"softmax_fused_T{t}")
+            b_ = gmap[f"softmax_fused_T{t}"].units
             smr[f"fused_T{t}"] = {"us": round(ms_ * 1e3, 1), "bytes": b_, "GBs": round(b_ / ms_ / 1e6, 1),
                                   "frac_hbm": round(b_ / ms_ / 1e6 / peaks["hbm_gbs"], 4)}
-        mu = mean_ms("softmax_unfused", 0)
-        bu = gmap["softmax_unfused"].calls[0][2]
+        mu = call_ms("softmax_unfused")
+        bu = gmap["softmax_unfused"].units
         smr["unfused"] = {"us": round(mu * 1e3, 1), "bytes": bu, "GBs": round(bu / mu / 1e6, 1)}
-        smr["speedup_fused_T0"] = round(mu / mean_ms("softmax_fused", 0), 3)
-        smr["speedup_fused_T64"] = round(mu / mean_ms("softmax_fused", 1), 3)
+        smr["speedup_fused_T0"] = round(mu / call_ms("softmax_fused_T0"), 3)
+        smr["speedup_fused_T64"] = round(mu / call_ms("softmax_fused_T64"), 3)
         rows["causal_softmax"] = smr
         gm = {}
         for M in wl.GEMM_MS:
-            fus = mean_ms(f"gemm_M{M}_fused", 0)
+            fus = call_ms(f"gemm_M{M}_[4]")
             ent = {"[4]_us": round(fus * 1e3, 2), "[4]_TFLOPs": round(flops[M] / fus / 1e9, 1),
                    "[4]_ledger_GBs": round(fc.fuse_gemm_bytes(M, gN, gK, 0) / fus / 1e6, 1)}
-            for j, (p_, _, _) in enumerate(gmap[f"gemm_M{M}_unfused"].calls):
-                u = mean_ms(f"gemm_M{M}_unfused", j)
+            for p_, m_ in plans.items():
+                if m_ == 0:
+                    continue
+                u = call_ms(f"gemm_M{M}_{p_}")
                 ent[f"{p_}_us"] = round(u * 1e3, 2)
                 ent[f"speedup_[4]_vs_{p_}"] = round(u / fus, 3)
             gm[f"M{M}"] = ent
@@ -541,26 +543,30 @@ def run_ours(args, rank, world, local):
         rows["gemm_epilogue"] = gm
         rows["launch_graph"] = launch_graph_rows(fc, lib, wl, torch, dev, gemm_bufs[16], check)
         rows["planner"] = planner_rows(fc, wl, peaks, rows["launch_graph"]["t_exec_queued_us"],
-                                       {M: {p_: (mean_ms(f"gemm_M{M}_fused", 0) if m_ == 0 else
-                                                 mean_ms(f"gemm_M{M}_unfused",
-                                                         [c[0] for c in gmap[f"gemm_M{M}_unfused"].calls].index(p_)))
-                                             for p_, m_ in plans.items()} for M in wl.GEMM_MS}, plans)
+                                       {M: {p_: call_ms(f"gemm_M{M}_{p_}") for p_ in plans} for M in wl.GEMM_MS},
+                                       plans)
+    rows["per_call"] = per_call_rows(torch, stream, {K: chain(K, fc.FUSE_FUSED) for K in KS},
+                                     {K: chain(K, fc.FUSE_UNFUSED) for K in KS})
 
     # same-size copy reference: cudaMemcpy D2D of one chain operand (64 MiB) -- the practical roof
-    # for a 2 x 64 MiB streaming kernel at this size (the measured peak is a 2 GiB copy)
-    cev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(20)]
+    # for a 2 x 64 MiB streaming kernel at this size (the measured peak is a 2 GiB copy), timed
+    # like the groups (back to back between one event pair)
     with torch.cuda.stream(stream):
         for i in range(5):
             ys[i % R].copy_(xs[(i + 1) % R])
-        for i, (e0, e1) in enumerate(cev):
+        cts = []
+        for rep in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            ys[i % R].copy_(xs[(i + 1) % R])
+            for i in range(4):
+                ys[i % R].copy_(xs[(i + 1) % R])
             e1.record(stream)
+            cts.append((e0, e1))
     torch.cuda.synchronize()
-    copy_us = float(np.median([e0.elapsed_time(e1) for e0, e1 in cev])) * 1e3
+    copy_us = float(np.median([e0.elapsed_time(e1) for e0, e1 in cts])) / 4 * 1e3
     rows["chain"]["copy_reference"] = {"us": round(copy_us, 2),
                                        "GBs": round(chain_bytes / copy_us / 1e3, 1),
-                                       "what": "cudaMemcpy D2D of 64 MiB, same rotation"}
+                                       "what": "cudaMemcpy D2D of 64 MiB, same rotation, back to back"}
 
     # register / occupancy report of every kernel variant ([K4] §③, [C05] §6.2)
     report_rows = []
@@ -611,6 +617,27 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return report
+
+
+def per_call_rows(torch, stream, fused, unfused, reps=10):
+    """The chain sweep with one CUDA event pair around every single call (after the timed region):
+    per K the median call time fused and unfused and their ratio.  An event between every two
+    calls adds the event's own cost to each call, so these times sit a little above the groups'."""
+    def med_us(fn):
+        with torch.cuda.stream(stream):
+            fn()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+        torch.cuda.synchronize()
+        return float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])) * 1e3
+    out = {}
+    for K in fused:
+        f, u = med_us(fused[K]), med_us(unfused[K])
+        out[str(K)] = {"fused_us": round(f, 2), "unfused_us": round(u, 2), "speedup": round(u / f, 3)}
+    return {"what": "chain sweep, one event pair per call, median of %d calls" % reps, "per_K": out}
 
 
 def launch_graph_rows(fc, lib, wl, torch, dev, gemm16, check):
@@ -758,24 +785,39 @@ def planner_rows(fc, wl, peaks, launch_us, measured_ms, plans):
     return out
 
 
-def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world):
-    """Per K: pinned host x -> device, the fused chain through the C ABI, device y -> pinned host."""
+def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world, chunks=8):
+    """Per K: the fused chain through the C ABI on x from pinned host memory, y back to pinned host
+    memory.  The chain is element-wise, so each call is issued as `chunks` calls on consecutive
+    slices, round-robin over three streams: a slice's host-to-device copy, its kernel and its
+    device-to-host copy queue on one stream, and the copy engines move other slices in both
+    directions meanwhile.  Bytes moved per step: x in and y out once per K."""
     import torch
     hx = torch.from_numpy(wl.chain_input(N, salt=7)).pin_memory()
     hy = torch.empty(N, dtype=torch.float32).pin_memory()
     dx = torch.empty(N, dtype=torch.float32, device=dev)
     dy = torch.empty(N, dtype=torch.float32, device=dev)
-    sh = stream.cuda_stream
+    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(2)]
+    csz = (N + chunks - 1) // chunks
 
     def one_step():
-        with torch.cuda.stream(stream):
-            for K in KS:
-                dx.copy_(hx, non_blocking=True)
-                rc = lib.fuse_chain_run(stage_sets[K], K, dx.data_ptr(), dy.data_ptr(), N,
-                                        fc.FUSE_F32, fc.FUSE_FUSED, sh)
-                if rc != 0:
-                    raise fc.FuseError(rc, "fuse_chain_run")
-                hy.copy_(dy, non_blocking=True)
+        for K in KS:
+            for c in range(chunks):
+                lo, hi = c * csz, min(N, (c + 1) * csz)
+                st = streams[c % len(streams)]   # a slice always on the same stream: in order
+                with torch.cuda.stream(st):
+                    dx[lo:hi].copy_(hx[lo:hi], non_blocking=True)
+                    rc = lib.fuse_chain_run(stage_sets[K], K, dx[lo:].data_ptr(), dy[lo:].data_ptr(), hi - lo,
+                                            fc.FUSE_F32, fc.FUSE_FUSED, st.cuda_stream)
+                    if rc != 0:
+                        raise fc.FuseError(rc, "fuse_chain_run")
+                    hy[lo:hi].copy_(dy[lo:hi], non_blocking=True)
+
+    def join():
+        # the first stream waits for the others, so one event on it closes the step
+        for st in streams[1:]:
+            ev = torch.cuda.Event()
+            ev.record(st)
+            stream.wait_event(ev)
 
     for _ in range(2):
         one_step()
@@ -783,10 +825,22 @@ def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, worl
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     steps = max(3, min(args.steps, 10))
     e0.record(stream)
+    for st in streams[1:]:
+        st.wait_stream(stream)
     for _ in range(steps):
         one_step()
+    join()
     e1.record(stream)
     torch.cuda.synchronize()
+    # the sliced, pipelined calls must give what one call on the whole vector gives
+    with torch.cuda.stream(stream):
+        rc = lib.fuse_chain_run(stage_sets[KS[-1]], KS[-1], dx.data_ptr(), dy.data_ptr(), N, fc.FUSE_F32,
+                                fc.FUSE_FUSED, stream.cuda_stream)
+        if rc != 0:
+            raise fc.FuseError(rc, "fuse_chain_run")
+    torch.cuda.synchronize()
+    if not torch.equal(hy.to(dev), dy):
+        raise RuntimeError("e2e: pipelined slices differ from the whole-vector call")
     elapsed = e0.elapsed_time(e1) / 1e3
     return {"_elapsed": elapsed, "_bytes": steps * len(KS) * chain_bytes,
             "h2d": len(KS) * N * 4, "d2h": len(KS) * N * 4}
