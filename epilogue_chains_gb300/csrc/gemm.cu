@@ -8,17 +8,20 @@
 // "epilogue fusion": the GEMM's output is written once, already in its final form.
 //
 // GB300 design.
-//  * M > 64: one persistent CTA per SM, warp-specialised.  Warp 0 drives TMA (128B-swizzled
-//    tiles, a 4-stage mbarrier ring); warp 1 owns TMEM and issues tcgen05.mma (M=128, N=256,
-//    K=16, fp16 in, fp32 accumulate), committing each stage back to the producer and each
-//    finished tile to the epilogue; warps 2-9 drain the accumulator with tcgen05.ld, 32 columns
-//    at a time, add bias, apply GELU(erf), add the residual (prefetched into registers one chunk
-//    ahead) and store fp16 Y straight from registers.  The accumulator is double-buffered in TMEM (2 x 256 columns), so
-//    the epilogue of tile i overlaps the main loop of tile i+1.  A is consumed K-major, B
-//    ([K,N], N contiguous) MN-major, both straight from their row-major layouts.
-//  * M <= 64 (decode): swap A and B so N fills the 128-row MMA dimension and M becomes the MMA's
-//    N (16..64); split K across an 8-CTA cluster, reduce the eight fp32 partial tiles through
-//    distributed shared memory (no global workspace) and apply the epilogue there.
+//  * M > 64: persistent 2-CTA clusters, one CTA per SM, warp-specialised.  The two CTAs of a
+//    cluster act as one MMA unit (tcgen05 .cta_group::2): each holds its own 128 rows of A and one
+//    half (128 columns) of the B tile per stage, and the even CTA issues M = 256, N = 256, K = 16
+//    MMAs (fp16 in, fp32 accumulate) whose rows 0-127 accumulate in its TMEM and rows 128-255 in
+//    its peer's.  Warp 0 drives TMA (128B-swizzled tiles, a 6-stage mbarrier ring, both CTAs'
+//    bytes completing on the even CTA's barriers); warp 1 of the even CTA issues the MMAs,
+//    committing each stage back to both producers and each finished tile to both epilogues;
+//    warps 2-9 of each CTA drain its accumulator with tcgen05.ld, 32 columns at a time, add bias,
+//    apply GELU(erf), add the residual (prefetched into registers one chunk ahead) and store fp16
+//    Y straight from registers.  The accumulator is double-buffered in TMEM (2 x 256 columns), so
+//    the epilogue of tile i overlaps the main loop of tile i+1; the last partial wave of tiles is
+//    split into 128-column halves.  A is consumed K-major, B ([K,N], N contiguous) MN-major,
+//    both straight from their row-major layouts.
+//  * M <= 64 (decode): gemm_decode.cu.
 //  * Cut plans: the GEMM kernel stops after the first stage segment and stores that fp16
 //    intermediate; a vectorised tail kernel applies each later segment in place in Y.
 //  * Every mbarrier wait is bounded; a wait that runs out raises the watchdog word, the CTA lets
@@ -31,87 +34,16 @@
 #include "fc_internal.cuh"
 #include "fc_ptx.cuh"
 #include "fc_tc.cuh"
+#include "gemm_epi.cuh"
 
 namespace fc {
+
+// the decode kernel (gemm_decode.cu)
+int launch_decode_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
+                       int64_t N, int64_t K, int epi, cudaStream_t st);
+int decode_report(fuse_kernel_record* out);
+
 namespace {
-
-// ------------------------------------------------------------------------------ epilogue math
-// Stages of the chain after the GEMM: 1 = +bias, 2 = GELU(erf), 3 = +residual.
-//
-// GELU(v) = v/2 (1 + erf(v/sqrt2)).  1 + erf(x) is evaluated as erfc(-x) for x < 0 and as
-// 2 - erfc(x) for x >= 0, so there is no cancellation for strongly negative v (where 1 + erf(x)
-// is tiny).  erfc(z), z >= 0, is the Chebyshev-fitted approximation "erfcc" of Press, Teukolsky,
-// Vetterling & Flannery, Numerical Recipes (2nd ed., §6.2): erfc(z) = t exp(-z^2 + P(t)),
-// t = 1/(1 + z/2), fractional error below 1.2e-7 for every z >= 0 -- far below the fp16 output
-// resolution.  Cost per element: one reciprocal and one ex2 (MUFU), the rest in packed fp32x2
-// instructions (sm_100+), which evaluate two elements per instruction.
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp_approx(float x) {
-    float y;
-    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
-
-// GELU of two values at once
-__device__ __forceinline__ float2 gelu_erf2(float2 v) {
-    const float2 z = __fmul2_rn(make_float2(fabsf(v.x), fabsf(v.y)), f2(0.70710678118654752f));
-    const float2 d = __ffma2_rn(f2(0.5f), z, f2(1.0f));
-    const float2 t = make_float2(rcp_approx(d.x), rcp_approx(d.y));
-    float2 p = f2(0.17087277f);
-    p = __ffma2_rn(p, t, f2(-0.82215223f));
-    p = __ffma2_rn(p, t, f2(1.48851587f));
-    p = __ffma2_rn(p, t, f2(-1.13520398f));
-    p = __ffma2_rn(p, t, f2(0.27886807f));
-    p = __ffma2_rn(p, t, f2(-0.18628806f));
-    p = __ffma2_rn(p, t, f2(0.09678418f));
-    p = __ffma2_rn(p, t, f2(0.37409196f));
-    p = __ffma2_rn(p, t, f2(1.00002368f));
-    p = __ffma2_rn(p, t, f2(-1.26551223f));
-    const float2 a = __fmul2_rn(__ffma2_rn(make_float2(-z.x, -z.y), z, p), f2(1.44269504088896341f));
-    const float2 e = __fmul2_rn(t, make_float2(ex2_approx(a.x), ex2_approx(a.y)));
-    const float2 s = make_float2(v.x >= 0.0f ? 2.0f - e.x : e.x, v.y >= 0.0f ? 2.0f - e.y : e.y);
-    return __fmul2_rn(__fmul2_rn(f2(0.5f), v), s);
-}
-__device__ __forceinline__ float gelu_erf(float v) { return gelu_erf2(make_float2(v, v)).x; }
-
-// apply stages first..last (inclusive, 1..3) to v
-__device__ __forceinline__ float apply_stages(float v, int first, int last, float b, float r) {
-    if (first <= 1 && last >= 1) v += b;
-    if (first <= 2 && last >= 2) v = gelu_erf(v);
-    if (first <= 3 && last >= 3) v += r;
-    return v;
-}
-// the same on two values
-__device__ __forceinline__ float2 apply_stages2(float2 v, int first, int last, float2 b, float2 r) {
-    if (first <= 1 && last >= 1) v = __fadd2_rn(v, b);
-    if (first <= 2 && last >= 2) v = gelu_erf2(v);
-    if (first <= 3 && last >= 3) v = __fadd2_rn(v, r);
-    return v;
-}
-
-__device__ __forceinline__ void unpack_h8(const uint4& u, float* f) {
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));
-        f[2 * i] = t.x;
-        f[2 * i + 1] = t.y;
-    }
-}
-__device__ __forceinline__ uint4 pack_h8(const float* f) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
-        w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
-}
 
 // =============================================================================== main kernel
 // A CTA pair computes a 256 x BN output tile with M = 256 MMAs (cta_group::2): each CTA holds its
@@ -376,248 +308,6 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     if (warp == 1) tmem_dealloc_pair(tmem_base, TMEM_COLS);
 }
 
-// =============================================================================== decode kernel
-// Y^T[N, M] = B^T[N, K] A^T[K, M] for M <= 64: MMA M = 128 rows of N, MMA N = NM >= M.
-constexpr int DEC_SPLIT = 8;    // K split = cluster size
-constexpr int kDecThreads = 128;
-constexpr uint32_t DEC_BT_STAGE = 128 * BK * 2;  // 16 KB: two 64-wide N boxes
-
-struct DecodeArgs {
-    int M, N, K;
-    int kb_per_split;   // k-blocks of 64 per CTA
-    int epi;
-    const __half* bias;
-    const __half* R;
-    __half* Y;
-    int* flag;
-};
-
-template <int NM>
-struct DecodeLayout {
-    static constexpr int STAGES = NM <= 32 ? 4 : 3;
-    static constexpr uint32_t A_ST = NM * BK * 2;
-    static constexpr uint32_t OFF_BT = 0;
-    static constexpr uint32_t OFF_AS = OFF_BT + STAGES * DEC_BT_STAGE;
-    // fp32 partials received from every CTA of the cluster for this CTA's column slice:
-    // [source rank][slice column][output row], DEC_SPLIT x (128 / DEC_SPLIT) x NM
-    static constexpr uint32_t OFF_P = OFF_AS + STAGES * A_ST;
-    static constexpr uint32_t OFF_BAR = OFF_P + NM * 128 * 4;
-    static constexpr uint32_t N_BARS = 2 * STAGES + 3;               // full, empty, acc, drain, recv
-    static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
-    static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
-    static constexpr uint32_t TCOLS = NM <= 32 ? 32 : 64;
-};
-
-// Store four floats into the shared memory of a CTA of the cluster (`remote` and `remote_bar` are
-// shared::cluster addresses); the bytes count toward that CTA's mbarrier transaction.
-__device__ __forceinline__ void st_async_v4(uint32_t remote, float a, float b, float c, float d,
-                                            uint32_t remote_bar) {
-    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];"
-                 ::"r"(remote), "f"(a), "f"(b), "f"(c), "f"(d), "r"(remote_bar)
-                 : "memory");
-}
-__device__ __forceinline__ void cluster_arrive() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-__device__ __forceinline__ void cluster_wait() {
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-template <int NM>
-__global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
-    const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
-    const __grid_constant__ DecodeArgs args) {
-    using L = DecodeLayout<NM>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t rank = cluster_rank();                  // K split index
-    const int n0 = (blockIdx.x / DEC_SPLIT) * 128;          // 128 output columns of Y
-    const int kb0 = static_cast<int>(rank) * args.kb_per_split;
-    const int nk_all = (args.K + BK - 1) / BK;
-    const int nk = max(0, min(args.kb_per_split, nk_all - kb0));
-    const uint32_t bar0 = base + L::OFF_BAR;
-    auto full_bar = [&](int s) { return bar0 + 8u * s; };
-    auto empty_bar = [&](int s) { return bar0 + 8u * (L::STAGES + s); };
-    const uint32_t acc_bar = bar0 + 8u * (2 * L::STAGES);
-    const uint32_t drain_bar = acc_bar + 8u;
-    const uint32_t recv_bar = drain_bar + 8u;
-    const uint32_t holder = base + L::OFF_HOLD;
-    const float* recv = reinterpret_cast<const float*>(gbase + L::OFF_P);  // [DEC_SPLIT][COLS][NM]
-    int* flag = args.flag;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < L::STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        mbar_init(acc_bar, 1);
-        mbar_init(drain_bar, 1);
-        mbar_init(recv_bar, 1);
-        fence_mbar_init();
-        // every CTA of the cluster sends this CTA one slice of its partial (NM x COLS fp32)
-        mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(128 * NM * 4));
-        prefetch_map(&mapA);
-        prefetch_map(&mapB);
-    }
-    if (warp == 1) tmem_alloc(holder, L::TCOLS);
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    // Peers may send into this CTA's shared memory only once its receive barrier exists: the
-    // cluster barrier is arrived at here and waited on just before the first send, so the wait
-    // overlaps the main loop.  Every thread reaches both on every path.
-    cluster_arrive();
-    const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
-    bool ok = true;
-
-    // After the K reduction CTA `rank` finishes output columns [n0 + COLS*rank, +COLS) of all NM
-    // rows, in units of one column and four consecutive rows: unit idx = threadIdx.x +
-    // kDecThreads*u is slice column idx / (NM/4), rows 4*(idx % (NM/4)) .. +3.  Each thread loads
-    // the bias and residual values of its units now, so their latency hides under the main loop.
-    constexpr int COLS = 128 / DEC_SPLIT;  // 16
-    constexpr int UNITS = NM * COLS / 4;
-    constexpr int UPT = (UNITS + kDecThreads - 1) / kDecThreads;
-    float eb[UPT], er[UPT][4];
-#pragma unroll
-    for (int u = 0; u < UPT; ++u) {
-        const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
-        const int n = n0 + COLS * static_cast<int>(rank) + idx / (NM / 4);
-        const int m0 = 4 * (idx % (NM / 4));
-        const bool valid = idx < UNITS && n < args.N;
-        eb[u] = valid && args.epi >= 1 ? __half2float(__ldg(args.bias + n)) : 0.0f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            er[u][i] = valid && args.epi >= 3 && m0 + i < args.M
-                           ? __half2float(__ldcs(args.R + static_cast<int64_t>(m0 + i) * args.N + n))
-                           : 0.0f;
-    }
-
-    if (warp == 0) {
-        uint32_t inflight = 0, issue_par = 0, phase = 0;
-        int stage = 0;
-        for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
-            inflight &= ~(1u << stage);
-            if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(stage), DEC_BT_STAGE + L::A_ST);
-                const int k = (kb0 + kb) * BK;
-                tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE, &mapB, n0, k, full_bar(stage));
-                tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE + B_BOX, &mapB, n0 + 64, k, full_bar(stage));
-                tma_load_2d(base + L::OFF_AS + stage * L::A_ST, &mapA, k, 0, full_bar(stage));
-            }
-            inflight |= 1u << stage;
-            issue_par = (issue_par & ~(1u << stage)) | (phase << stage);
-            if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
-        }
-        if (!ok)
-            for (int s = 0; s < L::STAGES; ++s)
-                if ((inflight >> s) & 1u) (void)mbar_wait_drain(full_bar(s), (issue_par >> s) & 1u);
-    } else if (warp == 1) {
-        constexpr uint32_t idesc = idesc_f16(128, NM, true, false);
-        uint32_t phase = 0;
-        int stage = 0;
-        bool issued = false;
-        for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait_bounded(full_bar(stage), phase, flag)) { ok = false; break; }
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t bt0 = base + L::OFF_BT + stage * DEC_BT_STAGE;
-                const uint32_t a0 = base + L::OFF_AS + stage * L::A_ST;
-#pragma unroll
-                for (int k = 0; k < BK / 16; ++k) {
-                    // MMA A = B^T tile: MN-major (N contiguous), N boxes of 64 are 8 KB apart
-                    const uint64_t ad = smem_desc_sw128(bt0 + 2048u * k, B_BOX, 1024u);
-                    // MMA B = A rows: K-major, NM rows of 128 B
-                    const uint64_t bd = smem_desc_sw128(a0 + 32u * k, 16u, 1024u);
-                    tc_mma(tmem_base, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
-                }
-                tc_commit(empty_bar(stage));
-            }
-            issued = true;
-            __syncwarp();
-            if (++stage == L::STAGES) { stage = 0; phase ^= 1u; }
-        }
-        if (ok) {
-            if (lane == 0) tc_commit(acc_bar);
-            __syncwarp();
-        } else if (issued) {
-            if (lane == 0) tc_commit(drain_bar);
-            __syncwarp();
-            (void)mbar_wait_drain(drain_bar, 0);
-        }
-    }
-    // All four warps: thread (warp, lane) holds output column n0 + 32*warp + lane of this CTA's
-    // partial (its TMEM lane) for all NM rows and sends it to the CTA that owns that column's slice,
-    // into row `rank` of that CTA's receive buffer.
-    {
-        const bool have = nk > 0;
-        bool got = true;
-        if (have) got = mbar_wait_bounded(acc_bar, 0, flag);
-        tc_fence_after();
-        float v[NM];
-        if (have && got) {
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * warp) << 16);
-#pragma unroll
-            for (int c = 0; c < NM; c += 16) tmem_ld16(taddr + c, v + c);
-            tmem_ld_wait();
-        } else {
-#pragma unroll
-            for (int c = 0; c < NM; ++c) v[c] = 0.0f;   // after a failed wait: zeros, still sent
-        }
-        const int col = 32 * warp + lane;
-        const uint32_t owner = static_cast<uint32_t>(col / COLS);
-        const uint32_t dst = mapa_shared(
-            smem_addr(recv) + 4u * static_cast<uint32_t>((static_cast<int>(rank) * COLS + col % COLS) * NM), owner);
-        const uint32_t dst_bar = mapa_shared(recv_bar, owner);
-        cluster_wait();   // every CTA of the cluster has initialised its receive barrier
-#pragma unroll
-        for (int c = 0; c < NM; c += 4) st_async_v4(dst + 4u * c, v[c], v[c + 1], v[c + 2], v[c + 3], dst_bar);
-    }
-
-    // This CTA's slice: the DEC_SPLIT partials summed in rank order, then the epilogue.  If the
-    // wait gives up (another wait of the launch failed), the peers still send their slices on every
-    // path: wait for them without the flag (bounded) so none lands after this CTA has exited.
-    const bool received = mbar_wait_bounded(recv_bar, 0, flag);
-    if (!received) (void)mbar_wait_drain(recv_bar, 0, kWaitBudget);
-    if (received) {
-#pragma unroll
-        for (int u = 0; u < UPT; ++u) {
-            const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
-            if (idx >= UNITS) break;
-            const int c = idx / (NM / 4);
-            const int m0 = 4 * (idx % (NM / 4));
-            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-            for (int r = 0; r < DEC_SPLIT; ++r) {
-                const float4 p = *reinterpret_cast<const float4*>(recv + (r * COLS + c) * NM + m0);
-                sum.x += p.x;
-                sum.y += p.y;
-                sum.z += p.z;
-                sum.w += p.w;
-            }
-            const int n = n0 + COLS * static_cast<int>(rank) + c;
-            if (n < args.N) {
-                const float2 lo = apply_stages2(make_float2(sum.x, sum.y), 1, args.epi, make_float2(eb[u], eb[u]),
-                                                make_float2(er[u][0], er[u][1]));
-                const float2 hi = apply_stages2(make_float2(sum.z, sum.w), 1, args.epi, make_float2(eb[u], eb[u]),
-                                                make_float2(er[u][2], er[u][3]));
-                const float o[4] = {lo.x, lo.y, hi.x, hi.y};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (m0 + i < args.M) args.Y[static_cast<int64_t>(m0 + i) * args.N + n] = __float2half_rn(o[i]);
-            }
-        }
-    }
-    // TMEM is freed once every thread's reads of it have completed.  No cluster barrier: a CTA's
-    // shared memory is written by its peers only until its own receive barrier completes.
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, L::TCOLS);
-}
-
 // =============================================================================== tail kernel
 // Y <- h(stages first..last applied to Y), 8 halves per thread (N % 8 == 0).
 __global__ void __launch_bounds__(256) epi_tail_kernel(__half* __restrict__ Y, const __half* __restrict__ bias,
@@ -642,57 +332,6 @@ __global__ void __launch_bounds__(256) epi_tail_kernel(__half* __restrict__ Y, c
 bool overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
     const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return x < y + static_cast<uintptr_t>(bbytes) && y < x + static_cast<uintptr_t>(abytes);
-}
-
-template <int NM>
-int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs& a, cudaStream_t st) {
-    using L = DecodeLayout<NM>;
-    // all of an SM's shared memory as shared (not L1) lets two decode CTAs share an SM, so the
-    // whole grid (ceil(N/128) x 8 CTAs) is resident in one wave
-    static const bool attr =
-        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(L::SMEM)) == cudaSuccess &&
-        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
-    if (!attr) return check_launch();
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.N, 128) * DEC_SPLIT));
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = L::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = DEC_SPLIT;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<NM>, mA, mB, a);
-    if (e != cudaSuccess) return record_cuda_error(e);
-    return check_launch();
-}
-
-// Clusters of the decode kernel that can be resident at once (0 if the query fails).
-template <int NM>
-int decode_max_active_clusters() {
-    using L = DecodeLayout<NM>;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(DEC_SPLIT * 32));
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = L::SMEM;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = DEC_SPLIT;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_decode_kernel<NM>, &cfg) != cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    return n;
 }
 
 bool main_attr_ok() {
@@ -740,24 +379,7 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     CUtensorMap mA, mB;
-    if (M <= 64) {
-        const int NM = M <= 16 ? 16 : (M <= 32 ? 32 : 64);
-        if (!make_map(&mA, A, M, K, 64, NM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
-        DecodeArgs a;
-        a.M = static_cast<int>(M);
-        a.N = static_cast<int>(N);
-        a.K = static_cast<int>(K);
-        const int nk = static_cast<int>(ceil_div(K, BK));
-        a.kb_per_split = static_cast<int>(ceil_div(nk, DEC_SPLIT));
-        a.epi = epi;
-        a.bias = static_cast<const __half*>(bias);
-        a.R = static_cast<const __half*>(R);
-        a.Y = static_cast<__half*>(Y);
-        a.flag = flag;
-        if (NM == 16) return launch_decode<16>(mA, mB, a, st);
-        if (NM == 32) return launch_decode<32>(mA, mB, a, st);
-        return launch_decode<64>(mA, mB, a, st);
-    }
+    if (M <= 64) return launch_decode_gemm(A, B, bias, R, Y, M, N, K, epi, st);
     if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
     if (!main_attr_ok()) return check_launch();
     MainArgs a;
@@ -820,20 +442,7 @@ int gemm_report(int i, fuse_kernel_record* out) {
             }
             return rc;
         }
-        case 1: {
-            (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       static_cast<int>(DecodeLayout<16>::SMEM));
-            (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       static_cast<int>(cudaSharedmemCarveoutMaxShared));
-            const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
-                                           "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
-                                           static_cast<int>(DecodeLayout<16>::SMEM), out);
-            if (rc == FUSE_OK) {
-                out->cluster_size = DEC_SPLIT;
-                out->max_active_clusters = decode_max_active_clusters<16>();
-            }
-            return rc;
-        }
+        case 1: return decode_report(out);
         case 2: return describe_kernel((const void*)epi_tail_kernel, "epi_tail_kernel (unfused plans)", 256, 0, out);
         default: return FUSE_EINVAL;
     }

@@ -25,7 +25,6 @@ namespace {
 constexpr int kWarpsPerBlock = 8;
 constexpr int kSmBlock = 32 * kWarpsPerBlock;
 constexpr int kEwBlock = 256;
-constexpr float kLog2e = 1.4426950408889634f;
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
