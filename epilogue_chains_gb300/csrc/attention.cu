@@ -143,6 +143,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     using L = AttnLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -478,6 +479,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     using L = PairLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -786,9 +788,7 @@ int launch_attn(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap&
                 const AttnArgs& args, cudaStream_t st) {
     const int rc = attn_attr<D>();
     if (rc != FUSE_OK) return rc;
-    attn_fwd_kernel<D><<<static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ), kAttnThreads,
-                         attn_launch_smem<D>(), st>>>(mQ, mK, mV, args);
-    return check_launch();
+    return launch_pdl(attn_fwd_kernel<D>, dim3(static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ)), dim3(kAttnThreads), attn_launch_smem<D>(), st, 1, mQ, mK, mV, args);
 }
 
 template <int D>
@@ -819,21 +819,7 @@ int launch_pair(const void* q, const void* k, const void* v, const AttnArgs& arg
     if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mKh, k, rows, D, 64, kAttnK / 2, true) ||
         !make_map(&mV, v, rows, D, 64, kAttnK, true))
         return FUSE_ECUDA;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(rows / kAttnQ));
-    cfg.blockDim = dim3(kAttnThreads);
-    cfg.dynamicSmemBytes = PairLayout<D>::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = 2;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, attn_pair_kernel<D>, mQ, mKh, mV, args);
-    if (e != cudaSuccess) return record_cuda_error(e);
-    return check_launch();
+    return launch_pdl(attn_pair_kernel<D>, dim3(static_cast<unsigned>(rows / kAttnQ)), dim3(kAttnThreads), PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, args);
 }
 
 template <int D>

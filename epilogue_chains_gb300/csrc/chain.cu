@@ -81,11 +81,13 @@ __device__ __forceinline__ void chain_body(const ChainParams& p) {
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_fused_kernel(const __grid_constant__ ChainParams p) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     chain_body<T, false>(p);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_stage_kernel(const __grid_constant__ ChainParams p) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     chain_body<T, true>(p);
 }
 
@@ -121,6 +123,7 @@ __device__ __forceinline__ float fat_group(float (&v)[E], const ChainParams& p) 
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock, 1) chain_fat_kernel(const __grid_constant__ ChainParams p) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const T* x = static_cast<const T*>(p.x);
     T* y = static_cast<T*>(p.y);
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -200,16 +203,14 @@ int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
     ChainParams p = base;
     partition<T>(p, p.x, p.y);
     if (mode == FUSE_FUSED) {
-        chain_fused_kernel<T><<<exact_grid<T>(p), kBlock, 0, stream>>>(p);
-        return check_launch();
+        return launch_pdl(chain_fused_kernel<T>, dim3(exact_grid<T>(p)), dim3(kBlock), 0, stream, 1, p);
     }
     if (mode == FUSE_FAT) {
         static const int occ = blocks_per_sm(chain_fat_kernel<T>, kBlock);
         const int64_t want = ceil_div(ceil_div(p.n, 4), kBlock);
         const int64_t cap = static_cast<int64_t>(sm_count()) * occ;
         const unsigned grid = static_cast<unsigned>(want < 1 ? 1 : (want < cap ? want : cap));
-        chain_fat_kernel<T><<<grid, kBlock, 0, stream>>>(p);
-        return check_launch();
+        return launch_pdl(chain_fat_kernel<T>, dim3(grid), dim3(kBlock), 0, stream, 1, p);
     }
     // FUSE_UNFUSED: stage s is its own launch; stage 0 reads x, every later stage reads and
     // rewrites y in place, so each intermediate makes a full round trip through global memory.
@@ -221,8 +222,7 @@ int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
         q.relu_mask = (base.relu_mask >> s) & 1u;
         if (s > 0) q.x = base.y;
         partition<T>(q, q.x, q.y);
-        chain_stage_kernel<T><<<exact_grid<T>(q), kBlock, 0, stream>>>(q);
-        const int rc = check_launch();
+        const int rc = launch_pdl(chain_stage_kernel<T>, dim3(exact_grid<T>(q)), dim3(kBlock), 0, stream, 1, q);
         if (rc != FUSE_OK) return rc;
     }
     return FUSE_OK;

@@ -20,6 +20,48 @@ inline int check_launch() {
     return e == cudaSuccess ? FUSE_OK : record_cuda_error(e);
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+// Every kernel of this library is launched with programmatic stream serialization allowed: it may
+// be scheduled while the kernel before it on the stream is still finishing, which hides the launch
+// latency between back-to-back kernels.  In exchange every kernel calls pdl_begin() before it
+// touches global memory: griddepcontrol.wait returns once the preceding grid has completed and its
+// writes are visible (at once if there is no such grid), so stream order is kept for every byte.
+// launch_dependents lets the next kernel be scheduled as soon as every CTA of this one has started.
+__device__ __forceinline__ void pdl_begin() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Launch `kernel` on `grid` x `block` threads with `smem` bytes of dynamic shared memory on `st`,
+// programmatic serialization allowed, as clusters of `cluster_x` CTAs when cluster_x > 1.
+// FUSE_OK, or FUSE_ECUDA with the error recorded.
+template <typename... KArgs, typename... Args>
+int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, int cluster_x,
+               Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute at[2];
+    unsigned n = 0;
+    at[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+    if (cluster_x > 1) {
+        at[n].id = cudaLaunchAttributeClusterDimension;
+        at[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        at[n].val.clusterDim.y = 1;
+        at[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = at;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    return check_launch();
+}
+
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 

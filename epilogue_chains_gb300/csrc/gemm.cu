@@ -101,6 +101,7 @@ __device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank)
 __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
     const __grid_constant__ MainArgs args) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
@@ -313,6 +314,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
 __global__ void __launch_bounds__(256) epi_tail_kernel(__half* __restrict__ Y, const __half* __restrict__ bias,
                                                        const __half* __restrict__ R, int64_t M, int N,
                                                        int first, int last) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t total = M * N / 8;
     if (g >= total) return;
@@ -400,30 +402,16 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     const int tail = tiles % clusters;
     a.full_units = (tail != 0 && 2 * tail <= clusters) ? tiles - tail : tiles;
     a.units = a.full_units + 2 * (tiles - a.full_units);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
-    cfg.blockDim = dim3(kMainThreads);
-    cfg.dynamicSmemBytes = MAIN_SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = 2;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_tc_kernel, mA, mB, a);
-    if (e != cudaSuccess) return record_cuda_error(e);
-    return check_launch();
+    return launch_pdl(gemm_tc_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kMainThreads), MAIN_SMEM, st,
+                      2, mA, mB, a);
 }
 
 int launch_tail(void* Y, const void* bias, const void* R, int64_t M, int64_t N, int first, int last,
                 cudaStream_t st) {
     const int64_t units = M * N / 8;
-    epi_tail_kernel<<<static_cast<unsigned>(ceil_div(units, 256)), 256, 0, st>>>(
-        static_cast<__half*>(Y), static_cast<const __half*>(bias), static_cast<const __half*>(R), M,
-        static_cast<int>(N), first, last);
-    return check_launch();
+    return launch_pdl(epi_tail_kernel, dim3(static_cast<unsigned>(ceil_div(units, 256))), dim3(256), 0, st, 1,
+                      static_cast<__half*>(Y), static_cast<const __half*>(bias), static_cast<const __half*>(R), M,
+                      static_cast<int>(N), first, last);
 }
 
 }  // namespace

@@ -75,6 +75,7 @@ template <int NM>
 __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
     const __grid_constant__ DecodeArgs args) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     using L = DecodeLayout<NM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -277,21 +278,7 @@ int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs
         cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributePreferredSharedMemoryCarveout,
                              static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
     if (!attr) return check_launch();
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(a.N, 128) * DEC_SPLIT));
-    cfg.blockDim = dim3(kDecThreads);
-    cfg.dynamicSmemBytes = L::SMEM;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeClusterDimension;
-    attrs[0].val.clusterDim.x = DEC_SPLIT;
-    attrs[0].val.clusterDim.y = 1;
-    attrs[0].val.clusterDim.z = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, gemm_decode_kernel<NM>, mA, mB, a);
-    if (e != cudaSuccess) return record_cuda_error(e);
-    return check_launch();
+    return launch_pdl(gemm_decode_kernel<NM>, dim3(static_cast<unsigned>(ceil_div(a.N, 128) * DEC_SPLIT)), dim3(kDecThreads), L::SMEM, st, DEC_SPLIT, mA, mB, a);
 }
 
 // Clusters of the decode kernel that can be resident at once (0 if the query fails).

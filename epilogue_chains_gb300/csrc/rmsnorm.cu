@@ -48,6 +48,7 @@ template <int THR, int VPT, bool ADD>
 __global__ void __launch_bounds__(THR) rmsnorm_row_kernel(const float* x, const float* res,
                                                           const float* __restrict__ w, float* h,
                                                           float* __restrict__ y, int hidden, float eps) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     __shared__ float red[THR / 32];
     const int64_t row = blockIdx.x;
     const int nv = hidden / 4;
@@ -100,6 +101,7 @@ template <int EPT, bool ADD>
 __global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel(
     const float* x, const float* res, const float* __restrict__ w, float* h, float* __restrict__ y,
     int hidden, float eps) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     __shared__ float red[kRowThreadsScalar / 32];
     const int64_t row = blockIdx.x;
     const float* xr = x + row * hidden;
@@ -129,6 +131,7 @@ __global__ void __launch_bounds__(kRowThreadsScalar) rmsnorm_fused_scalar_kernel
 // (0, residual form only) h = x + res
 __global__ void __launch_bounds__(kEwBlock) residual_add_kernel(const float* x, const float* res,
                                                                 float* h, int64_t n, bool vec) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t done = 0;
@@ -150,6 +153,7 @@ __global__ void __launch_bounds__(kEwBlock) residual_add_kernel(const float* x, 
 __global__ void __launch_bounds__(kEwBlock) rms_square_kernel(const float* __restrict__ x,
                                                               float* __restrict__ y, int64_t n,
                                                               bool vec) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t done = 0;
@@ -168,6 +172,7 @@ __global__ void __launch_bounds__(kEwBlock) rms_square_kernel(const float* __res
 
 __global__ void __launch_bounds__(kRowThreadsScalar) rms_rowmean_kernel(
     const float* __restrict__ sq, float* __restrict__ ms, int hidden) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     __shared__ float red[kRowThreadsScalar / 32];
     const int64_t row = blockIdx.x;
     const float* r = sq + row * hidden;
@@ -181,6 +186,7 @@ __global__ void __launch_bounds__(kEwBlock) rms_scale_kernel(const float* __rest
                                                              const float* __restrict__ ms,
                                                              float* __restrict__ y, int64_t n,
                                                              int hidden, float eps, bool vec) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec) {  // hidden % 4 == 0: a vector never straddles two rows
@@ -201,6 +207,7 @@ __global__ void __launch_bounds__(kEwBlock) rms_scale_kernel(const float* __rest
 __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict__ y,
                                                               const float* __restrict__ w,
                                                               int64_t n, int hidden, bool vec) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t tid = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t nthr = static_cast<int64_t>(gridDim.x) * blockDim.x;
     if (vec) {
@@ -221,17 +228,13 @@ __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict_
 template <int THR, int VPT, bool ADD>
 int launch_fused_vec(const float* x, const float* res, const float* w, float* h, float* y,
                      int64_t rows, int hidden, float eps, cudaStream_t st) {
-    rmsnorm_row_kernel<THR, VPT, ADD><<<static_cast<unsigned>(rows), THR, 0, st>>>(x, res, w, h, y,
-                                                                                 hidden, eps);
-    return check_launch();
+    return launch_pdl(rmsnorm_row_kernel<THR, VPT, ADD>, dim3(static_cast<unsigned>(rows)), dim3(THR), 0, st, 1, x, res, w, h, y, hidden, eps);
 }
 
 template <int EPT, bool ADD>
 int launch_fused_scalar(const float* x, const float* res, const float* w, float* h, float* y,
                         int64_t rows, int hidden, float eps, cudaStream_t st) {
-    rmsnorm_fused_scalar_kernel<EPT, ADD><<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(
-        x, res, w, h, y, hidden, eps);
-    return check_launch();
+    return launch_pdl(rmsnorm_fused_scalar_kernel<EPT, ADD>, dim3(static_cast<unsigned>(rows)), dim3(kRowThreadsScalar), 0, st, 1, x, res, w, h, y, hidden, eps);
 }
 
 // The fused form for hidden <= 16384: the row lives in registers (VPT float4 or EPT floats per
@@ -271,15 +274,11 @@ int unfused_steps(const float* x, const float* w, float* y, float* ms, int64_t r
                   float eps, bool vec, cudaStream_t st) {
     const int64_t n = rows * H;
     const bool fvec = is_aligned(x, 16) && is_aligned(y, 16);
-    rms_square_kernel<<<ew_grid(fvec ? n / 4 : n), kEwBlock, 0, st>>>(x, y, n, fvec);
-    int rc = check_launch();
+    int rc = launch_pdl(rms_square_kernel, dim3(ew_grid(fvec ? n / 4 : n)), dim3(kEwBlock), 0, st, 1, x, y, n, fvec);
     if (rc) return rc;
-    rms_rowmean_kernel<<<static_cast<unsigned>(rows), kRowThreadsScalar, 0, st>>>(y, ms, H);
-    if ((rc = check_launch())) return rc;
-    rms_scale_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(x, ms, y, n, H, eps, vec);
-    if ((rc = check_launch())) return rc;
-    rms_weight_kernel<<<ew_grid(vec ? n / 4 : n), kEwBlock, 0, st>>>(y, w, n, H, vec);
-    return check_launch();
+    if ((rc = launch_pdl(rms_rowmean_kernel, dim3(static_cast<unsigned>(rows)), dim3(kRowThreadsScalar), 0, st, 1, y, ms, H))) return rc;
+    if ((rc = launch_pdl(rms_scale_kernel, dim3(ew_grid(vec ? n / 4 : n)), dim3(kEwBlock), 0, st, 1, x, ms, y, n, H, eps, vec))) return rc;
+    return launch_pdl(rms_weight_kernel, dim3(ew_grid(vec ? n / 4 : n)), dim3(kEwBlock), 0, st, 1, y, w, n, H, vec);
 }
 
 int rmsnorm_report_count() { return 4; }
@@ -353,8 +352,7 @@ extern "C" int fuse_add_rmsnorm(const float* x, const float* r, const float* w, 
     if (!is_aligned(workspace, 4)) return FUSE_EALIGN;
     const int64_t n = rows * hidden;
     const bool avec = is_aligned(x, 16) && is_aligned(r, 16) && is_aligned(h, 16);
-    residual_add_kernel<<<ew_grid(avec ? n / 4 : n), kEwBlock, 0, st>>>(x, r, h, n, avec);
-    const int rc = check_launch();
+    const int rc = launch_pdl(residual_add_kernel, dim3(ew_grid(avec ? n / 4 : n)), dim3(kEwBlock), 0, st, 1, x, r, h, n, avec);
     if (rc) return rc;
     return unfused_steps(h, w, y, static_cast<float*>(workspace), rows, H, eps, vec, st);
 }

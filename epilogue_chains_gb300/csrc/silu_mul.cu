@@ -60,6 +60,7 @@ __device__ __forceinline__ float apply(float gv, float uv, float yv) {
 
 template <typename T, int STEP>
 __global__ void __launch_bounds__(kBlock) silu_mul_vec_kernel(const __grid_constant__ SiluParams p) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     using V = Vec32<T>;
     constexpr int E = V::N;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kBlock) silu_mul_vec_kernel(const __grid_const
 // Element-wise variant for shapes or pointers the 32-byte vectors do not fit.
 template <typename T, int STEP>
 __global__ void __launch_bounds__(kBlock) silu_mul_scalar_kernel(const __grid_constant__ SiluParams p) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t n = p.rows * p.cols;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     const T* g = static_cast<const T*>(p.g);
@@ -105,14 +107,14 @@ int launch(const SiluParams& p, bool vec, cudaStream_t st) {
     if (vec) {
         const int64_t grid = ceil_div(p.nvec, kBlock);
         if (grid > 0x7fffffffLL) return FUSE_EUNSUPPORTED;
-        silu_mul_vec_kernel<T, STEP><<<static_cast<unsigned>(grid), kBlock, 0, st>>>(p);
+        return launch_pdl(silu_mul_vec_kernel<T, STEP>, dim3(static_cast<unsigned>(grid)), dim3(kBlock), 0, st, 1, p);
     } else {
         int64_t grid = ceil_div(p.rows * p.cols, kBlock);
         const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kBlock) * 4;
         if (grid > cap) grid = cap;
-        silu_mul_scalar_kernel<T, STEP><<<static_cast<unsigned>(grid), kBlock, 0, st>>>(p);
+        return launch_pdl(silu_mul_scalar_kernel<T, STEP>, dim3(static_cast<unsigned>(grid)), dim3(kBlock), 0, st,
+                          1, p);
     }
-    return check_launch();
 }
 
 template <typename T>

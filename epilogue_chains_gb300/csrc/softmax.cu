@@ -128,6 +128,7 @@ template <int VPL, typename OutT>
 __global__ void __launch_bounds__(kSmBlock, 2) softmax_fused_kernel(
     const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float c,
     int skip_tile, int* flag) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const uint32_t rowbytes = static_cast<uint32_t>(S) * 2;
@@ -250,6 +251,7 @@ template <typename OutT>
 __global__ void __launch_bounds__(kSmBlock) softmax_fused_generic_kernel(
     const __nv_bfloat16* __restrict__ s, OutT* __restrict__ p, int64_t rows, int S, float c,
     int skip_tile) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int lane = threadIdx.x % 32;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
     if (row >= rows) return;
@@ -284,6 +286,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kSmBlock) sm_rowmax_kernel(const __nv_bfloat16* __restrict__ s,
                                                              float* __restrict__ m, int64_t rows,
                                                              int S, float scale) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int lane = threadIdx.x % 32;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
     if (row >= rows) return;
@@ -315,6 +318,7 @@ __global__ void __launch_bounds__(kEwBlock) sm_sub_kernel(const __nv_bfloat16* _
                                                           const float* __restrict__ m,
                                                           __nv_bfloat16* __restrict__ d,
                                                           int64_t n, int S, float scale) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (VEC) {
         const int64_t vpr = S / 16;
@@ -347,6 +351,7 @@ __global__ void __launch_bounds__(kEwBlock) sm_sub_kernel(const __nv_bfloat16* _
 
 template <bool VEC>
 __global__ void __launch_bounds__(kEwBlock) sm_exp_kernel(__nv_bfloat16* __restrict__ d, int64_t n) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (VEC) {
         if (g >= n / 16) return;
@@ -369,6 +374,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kSmBlock) sm_rowsum_kernel(const __nv_bfloat16* __restrict__ e,
                                                              float* __restrict__ l, int64_t rows,
                                                              int S) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int lane = threadIdx.x % 32;
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + threadIdx.x / 32;
     if (row >= rows) return;
@@ -394,6 +400,7 @@ template <bool VEC>
 __global__ void __launch_bounds__(kEwBlock) sm_div_kernel(__nv_bfloat16* __restrict__ e,
                                                           const float* __restrict__ l, int64_t n,
                                                           int S) {
+    pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (VEC) {
         if (g >= n / 16) return;
@@ -432,9 +439,7 @@ int launch_vec(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float c, in
     int64_t grid = ceil_div(rows, kWarpsPerBlock);
     const int64_t cap = static_cast<int64_t>(sm_count()) * occ;
     if (grid > cap) grid = cap;
-    softmax_fused_kernel<VPL, OutT><<<static_cast<unsigned>(grid), kSmBlock, smem, st>>>(
-        s, p, rows, S, c, tile, flag);
-    return check_launch();
+    return launch_pdl(softmax_fused_kernel<VPL, OutT>, dim3(static_cast<unsigned>(grid)), dim3(kSmBlock), smem, st, 1, s, p, rows, S, c, tile, flag);
 }
 
 template <typename OutT>
@@ -446,8 +451,7 @@ int launch_fused(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float c, 
         if (vpl <= 2) return launch_vec<2, OutT>(s, p, rows, S, c, tile, st);
         return launch_vec<4, OutT>(s, p, rows, S, c, tile, st);
     }
-    softmax_fused_generic_kernel<OutT><<<grid_for(rows, kWarpsPerBlock), kSmBlock, 0, st>>>(s, p, rows, S, c, tile);
-    return check_launch();
+    return launch_pdl(softmax_fused_generic_kernel<OutT>, dim3(grid_for(rows, kWarpsPerBlock)), dim3(kSmBlock), 0, st, 1, s, p, rows, S, c, tile);
 }
 
 template <bool VEC>
@@ -457,16 +461,11 @@ int launch_unfused(const __nv_bfloat16* s, __nv_bfloat16* d, float* m, float* l,
     const int64_t units = VEC ? n / 16 : n;
     const unsigned rgrid = grid_for(rows, kWarpsPerBlock);
     int rc;
-    sm_rowmax_kernel<VEC><<<rgrid, kSmBlock, 0, st>>>(s, m, rows, S, scale);
-    if ((rc = check_launch())) return rc;
-    sm_sub_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(s, m, d, n, S, scale);
-    if ((rc = check_launch())) return rc;
-    sm_exp_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(d, n);
-    if ((rc = check_launch())) return rc;
-    sm_rowsum_kernel<VEC><<<rgrid, kSmBlock, 0, st>>>(d, l, rows, S);
-    if ((rc = check_launch())) return rc;
-    sm_div_kernel<VEC><<<grid_for(units, kEwBlock), kEwBlock, 0, st>>>(d, l, n, S);
-    return check_launch();
+    if ((rc = launch_pdl(sm_rowmax_kernel<VEC>, dim3(rgrid), dim3(kSmBlock), 0, st, 1, s, m, rows, S, scale))) return rc;
+    if ((rc = launch_pdl(sm_sub_kernel<VEC>, dim3(grid_for(units, kEwBlock)), dim3(kEwBlock), 0, st, 1, s, m, d, n, S, scale))) return rc;
+    if ((rc = launch_pdl(sm_exp_kernel<VEC>, dim3(grid_for(units, kEwBlock)), dim3(kEwBlock), 0, st, 1, d, n))) return rc;
+    if ((rc = launch_pdl(sm_rowsum_kernel<VEC>, dim3(rgrid), dim3(kSmBlock), 0, st, 1, d, l, rows, S))) return rc;
+    return launch_pdl(sm_div_kernel<VEC>, dim3(grid_for(units, kEwBlock)), dim3(kEwBlock), 0, st, 1, d, l, n, S);
 }
 
 }  // namespace
