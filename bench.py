@@ -249,11 +249,11 @@ def run_ours(args, rank, world, local):
         # -------------------------------------------------------------- RMSNorm
         with torch.cuda.stream(stream):
             rx, rw = wl.rmsnorm_input(device=dev, salt=rank)
-            rxs = [rx] + [rx.clone() for _ in range(3)]   # 4 x/y pairs: 256 MiB, twice the L2
-            rys = [torch.empty_like(rx) for _ in range(4)]
+            rxs = [rx] + [rx.clone() for _ in range(7)]   # 8 x/y pairs: 512 MiB, four times the L2
+            rys = [torch.empty_like(rx) for _ in range(8)]
             rws = torch.empty(fc.fuse_rmsnorm_workspace_bytes(wl.RMS_ROWS, wl.RMS_HIDDEN, fc.FUSE_UNFUSED),
                               dtype=torch.uint8, device=dev)
-        rrot = rotating(4)
+        rrot = rotating(8)
 
         def rms(mode):
             def fn():
@@ -271,10 +271,10 @@ def run_ours(args, rank, world, local):
         # -------------------------------------------------------------- residual add + RMSNorm
         with torch.cuda.stream(stream):
             ax, ar, aw = wl.add_rmsnorm_input(device=dev, salt=rank)
-            axs, ars = [ax, ax.clone()], [ar, ar.clone()]
-            ahs = [torch.empty_like(ax) for _ in range(2)]
-            ays = [torch.empty_like(ax) for _ in range(2)]
-        arot = rotating(2)
+            axs, ars = [ax] + [ax.clone() for _ in range(3)], [ar] + [ar.clone() for _ in range(3)]
+            ahs = [torch.empty_like(ax) for _ in range(4)]   # 4 sets of x, r, h, y: 512 MiB
+            ays = [torch.empty_like(ax) for _ in range(4)]
+        arot = rotating(4)
         AR, AH = wl.ADDRMS_ROWS, wl.ADDRMS_HIDDEN
 
         def addrms(mode):
@@ -601,8 +601,9 @@ def run_ours(args, rank, world, local):
                        "N": N, "K": list(KS),
                        "step": "all rows" if args.rows == "all" else "chain rows",
                        "l2": "inputs larger than L2 or rotated (chain: 4 x/y pairs = 512 MiB; RMSNorm: "
-                             "4 pairs = 256 MiB; decode GEMM: 4 weight copies); each row group led by "
-                             "an untimed same-kind call",
+                             "8 pairs = 512 MiB; residual add + RMSNorm: 4 sets = 512 MiB; decode GEMM: "
+                             "4 weight copies); each group led by an untimed same-kind call; timed calls "
+                             "back to back between one CUDA event pair",
                        "parallelism": f"replicas x{world}"},
             "frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
             "roofline": roofline,
@@ -931,12 +932,12 @@ def run_profile(args):
         rows = args.size or wl.RMS_ROWS
         mode = fc.FUSE_FUSED if name == "rmsnorm_fused" else fc.FUSE_UNFUSED
         x0, w = wl.rmsnorm_input(rows, wl.RMS_HIDDEN, device=dev)
-        xs = [x0] + [x0.clone() for _ in range(3)]
-        ys = [torch.empty_like(x0) for _ in range(4)]
+        xs = [x0] + [x0.clone() for _ in range(7)]
+        ys = [torch.empty_like(x0) for _ in range(8)]
         ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.RMS_HIDDEN, mode)),
                          dtype=torch.uint8, device=dev)
         for i in range(L):
-            rc = lib.fuse_rmsnorm(xs[i % 4].data_ptr(), w.data_ptr(), ys[i % 4].data_ptr(), rows,
+            rc = lib.fuse_rmsnorm(xs[i % 8].data_ptr(), w.data_ptr(), ys[i % 8].data_ptr(), rows,
                                   wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)
@@ -944,13 +945,13 @@ def run_profile(args):
         rows = args.size or wl.ADDRMS_ROWS
         mode = fc.FUSE_FUSED if name == "add_rmsnorm_fused" else fc.FUSE_UNFUSED
         x, r, w = wl.add_rmsnorm_input(rows, wl.ADDRMS_HIDDEN, device=dev)
-        xs, rs = [x, x.clone()], [r, r.clone()]
-        hs, ys = [torch.empty_like(x) for _ in range(2)], [torch.empty_like(x) for _ in range(2)]
+        xs, rs = [x] + [x.clone() for _ in range(3)], [r] + [r.clone() for _ in range(3)]
+        hs, ys = [torch.empty_like(x) for _ in range(4)], [torch.empty_like(x) for _ in range(4)]
         ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.ADDRMS_HIDDEN, mode)),
                          dtype=torch.uint8, device=dev)
         for i in range(L):
-            rc = lib.fuse_add_rmsnorm(xs[i % 2].data_ptr(), rs[i % 2].data_ptr(), w.data_ptr(),
-                                      hs[i % 2].data_ptr(), ys[i % 2].data_ptr(), rows, wl.ADDRMS_HIDDEN,
+            rc = lib.fuse_add_rmsnorm(xs[i % 4].data_ptr(), rs[i % 4].data_ptr(), w.data_ptr(),
+                                      hs[i % 4].data_ptr(), ys[i % 4].data_ptr(), rows, wl.ADDRMS_HIDDEN,
                                       wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_add_rmsnorm_bytes(rows, wl.ADDRMS_HIDDEN, mode)
