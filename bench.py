@@ -69,6 +69,25 @@ def parse_args():
     return ap.parse_args()
 
 
+def max_over_ranks(values, world, device):
+    """Each value's maximum over all ranks (one all_reduce of the vector), or the values as they
+    are with a single rank.  The timed region of every rank is bracketed by a barrier, so the
+    slowest rank's time is the job's time."""
+    if world == 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def weak_scaling_gbs(bytes_per_rank, world, elapsed_s):
+    """Whole-job throughput of a weak-scaling run: every rank moved `bytes_per_rank`, the job took
+    the slowest rank's `elapsed_s`."""
+    return bytes_per_rank * world / elapsed_s / 1e9
+
+
 def dist_env():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -426,12 +445,8 @@ def run_ours(args, rank, world, local):
     fused_groups = [g for g in groups if g.family == "chain_fused"]
     elapsed_s = sum(sum(gms[g.name]) for g in fused_groups) / 1e3
     n_fused = args.steps * sum(g.n for g in fused_groups)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_s, step_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_s, step_ms = float(t[0]), float(t[1])
-    value = n_fused * chain_bytes * world / elapsed_s / 1e9
+    elapsed_s, step_ms = max_over_ranks([elapsed_s, step_ms], world, dev)
+    value = weak_scaling_gbs(n_fused * chain_bytes, world, elapsed_s)
 
     kernel_src = {"softmax_fused": "softmax.cu", "chain_fused": "chain.cu", "gemm_M4096_fused": "gemm.cu",
                   "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm_decode.cu",
@@ -579,12 +594,8 @@ def run_ours(args, rank, world, local):
 
     # ---------------------------------------------------------------- e2e through host buffers
     e2e = run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e["_elapsed"]], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e["_elapsed"] = float(t[0])
-    e2e_value = e2e["_bytes"] * world / e2e["_elapsed"] / 1e9
+    e2e["_elapsed"] = max_over_ranks([e2e["_elapsed"]], world, dev)[0]
+    e2e_value = weak_scaling_gbs(e2e["_bytes"], world, e2e["_elapsed"])
 
     report = None
     if rank == 0:
