@@ -14,15 +14,15 @@
 //    blocks of 128 (the MMA re-reads the whole Q tile from shared memory for every block, so longer
 //    blocks cost less shared-memory bandwidth per flop), which at a head size of 256 leaves room
 //    for one K, one V and one P buffer (Q 64 KB + K 64 KB + V 64 KB + P 32 KB) and two score
-//    buffers in TMEM (2 x 128 score columns + 256 O columns).  320 threads in three roles:
-//     - warp 0: lane 0 loads Q once and the K blocks, lane 1 the V blocks (TMA, 128-byte
-//       swizzle), each as soon as its buffer is free (K_j+1 once S_j is computed, V_j+1 once PV_j
-//       is);
+//    buffers in TMEM (2 x 128 score columns + 256 O columns).  352 threads in four roles:
+//     - warps 0 and 2: lane 0 of warp 0 loads Q once and the K blocks, lane 0 of warp 2 the V
+//       blocks (TMA, 128-byte swizzle), each as soon as its buffer is free (K_j+1 once S_j is
+//       computed, V_j+1 once PV_j is);
 //     - warp 1 owns TMEM and issues the tcgen05 MMAs: S_j = Q K_j^T (M 128, N 128, bf16, K-major
 //       both) into score buffer j % 2, and O += P_j V_j (M 128, N D, P K-major, V MN-major), in
 //       the order S_0, S_1, PV_0, S_2, PV_1, ... so the next scores are computed while the softmax
 //       warps work on the current ones;
-//     - warps 2-9 (two per TMEM lane quadrant, one query row per thread, each warp half of a
+//     - warps 3-10 (two per TMEM lane quadrant, one query row per thread, each warp half of a
 //       block's keys and half of O's columns) read the scores with tcgen05.ld, mask the diagonal
 //       block, keep the running row maximum m and sum l in base-2 units, write P = 2^(s c - m) as
 //       bf16 into shared memory in the MMA's swizzled layout, and rescale their half of the O
@@ -49,7 +49,9 @@ constexpr int kAttnK = 128;          // keys per block
 constexpr int kKVStages = 1;         // K and V buffers (each a ring of this many blocks)
 constexpr int kPBuf = 1;             // P buffers in shared memory
 constexpr int kAttnSoftmaxWarps = 8; // two per TMEM lane quadrant, each exponentiating 32 keys
-constexpr int kAttnThreads = 32 * (2 + kAttnSoftmaxWarps);
+// warp 0: Q and K loads; warp 1: MMA issue; warp 2: V loads; warps 3-10: softmax.  Every
+// producer and the MMA issuer own a warp: a thread parked in an mbarrier wait parks its whole warp.
+constexpr int kAttnThreads = 32 * (3 + kAttnSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.0f; // rescale O only when the row maximum grew by more than this
 constexpr int kSBuf = 2;             // score buffers in TMEM: S_j+kSBuf-1 is computed before PV_j
 
@@ -201,12 +203,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
         // ---------------------------------------------------------------- TMA producers
-        // lane 0 loads Q and the K blocks, lane 1 the V blocks, each into a two-stage ring: block
-        // j + 2 streams in while blocks j and j + 1 are being used
-        if (lane < 2) {
-            const bool is_k = lane == 0;
+        // warp 0 loads Q and the K blocks, warp 2 the V blocks (lane 0 of each), each into its ring
+        if (lane == 0) {
+            const bool is_k = warp == 0;
             const CUtensorMap* map = is_k ? &mK : &mV;
             const uint32_t off = is_k ? L::OFF_K : L::OFF_V;
             prefetch_map(map);
@@ -296,7 +297,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
         // they reach the same row maximum without exchanging it; each exponentiates and writes its
         // 32 keys of P and keeps the partial row sum of its own keys.
         const int qd = warp % 4;
-        const int hh = (warp - 2) / 4;
+        const int hh = (warp - 3) / 4;
         const int r = 32 * qd + lane;                        // query row within the tile
         const int qrow = qt * kAttnQ + r;                    // query index within the slice
         const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
@@ -438,14 +439,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
 // S at 0-127 (one buffer: S_j+1 is computed as soon as both CTAs have read S_j), P at 128-255
 // (two buffers of 64 columns, 128 bf16 keys each), O at 256-511.  The pair walks key blocks
 // 0 .. 2u + 1 together (tile 2u finds block 2u + 1 fully masked).
-//  * warp 0 of each CTA: lane 0 loads the CTA's Q rows and its half of every K block, lane 1 its
-//    half of every V block; the bytes of both CTAs complete on CTA 0's barriers;
+//  * warps 0 and 2 of each CTA: lane 0 of warp 0 loads the CTA's Q rows and its half of every K
+//    block, lane 0 of warp 2 its half of every V block; the bytes of both CTAs complete on CTA 0's
+//    barriers;
 //  * warp 1 of CTA 0 issues every MMA of the pair, in the order S_0, S_1, PV_0, S_2, PV_1, ...;
 //    commits signal both CTAs' barriers;
-//  * warps 2-9 of each CTA: the softmax of its own 128 query rows (two warps per TMEM lane
+//  * warps 3-10 of each CTA: the softmax of its own 128 query rows (two warps per TMEM lane
 //    quadrant, each exponentiating half of a block's keys and rescaling half of O's columns); they
 //    release S and publish P on CTA 0's barriers.
-constexpr int kPairKV = 2;   // K and V stages
+// K and V ring depths (K_j+2 is loaded once S_j has completed, V_j+2 once PV_j has).
+constexpr int kPairK = 2, kPairV = 2;
 
 template <int D>
 struct PairLayout {
@@ -459,12 +462,12 @@ struct PairLayout {
     static constexpr uint32_t VH_BYTES = kAttnK * (D / 2) * 2;
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                 // + stage * KH_BYTES
-    static constexpr uint32_t OFF_V = OFF_K + kPairKV * KH_BYTES;      // + stage * VH_BYTES
-    static constexpr uint32_t OFF_LX = OFF_V + kPairKV * VH_BYTES;     // row-sum exchange, 2 x 128 fp32
+    static constexpr uint32_t OFF_V = OFF_K + kPairK * KH_BYTES;       // + stage * VH_BYTES
+    static constexpr uint32_t OFF_LX = OFF_V + kPairV * VH_BYTES;      // row-sum exchange, 2 x 128 fp32
     static constexpr uint32_t OFF_BAR = OFF_LX + 2 * kAttnQ * 4;
-    // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KV], k_empty[KV],
-    // v_full[KV], v_empty[KV]
-    static constexpr int N_BARS = 9 + 4 * kPairKV;
+    // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KS], k_empty[KS],
+    // v_full[VS], v_empty[VS]
+    static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV;
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -488,13 +491,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     const uint32_t bar0 = base + L::OFF_BAR;
     const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16, s_full = bar0 + 24,
                    s_free = bar0 + 32;
-    constexpr int KV = kPairKV;
+    constexpr int KS = kPairK, VS = kPairV;
     auto p_full = [&](int b) { return bar0 + 8u * (5 + b); };
     auto o_done = [&](int b) { return bar0 + 8u * (7 + b); };
     auto k_full = [&](int i) { return bar0 + 8u * (9 + i); };
-    auto k_empty = [&](int i) { return bar0 + 8u * (9 + KV + i); };
-    auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KV + i); };
-    auto v_empty = [&](int i) { return bar0 + 8u * (9 + 3 * KV + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (9 + KS + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KS + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (9 + 2 * KS + VS + i); };
     int* flag = a.flag;
 
     // Consecutive pairs take the tile pairs of one (batch, head) slice, heaviest first, so the
@@ -522,9 +525,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
             mbar_init(p_full(b), 2 * kAttnSoftmaxWarps);
             mbar_init(o_done(b), 1);
         }
-        for (int i = 0; i < KV; ++i) {
+        for (int i = 0; i < KS; ++i) {
             mbar_init(k_full(i), 1);
             mbar_init(k_empty(i), 1);
+        }
+        for (int i = 0; i < VS; ++i) {
             mbar_init(v_full(i), 1);
             mbar_init(v_empty(i), 1);
         }
@@ -536,10 +541,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
 
-    if (warp == 0) {
+    if (warp == 0 || warp == 2) {
         // ---------------------------------------------------------------- TMA producers
-        if (lane < 2) {
-            const bool is_k = lane == 0;
+        // warp 0 loads this CTA's Q rows and K halves, warp 2 its V halves (lane 0 of each)
+        if (lane == 0) {
+            const bool is_k = warp == 0;
             prefetch_map(is_k ? &mKh : &mV);
             if (is_k) {
                 prefetch_map(&mQ);
@@ -548,12 +554,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
                 for (int c = 0; c < L::QATOMS; ++c)
                     tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
             }
+            const int R = is_k ? KS : VS;   // ring depth
             int loads = 0;
             for (int j = 0; j < nb; ++j) {
-                const int st = j % KV;
+                const int st = j % R;
                 const uint32_t full = is_k ? k_full(st) : v_full(st);
                 const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
-                if (j >= KV && !mbar_wait_bounded(empty, ((j - KV) / KV) & 1, flag)) break;
+                if (j >= R && !mbar_wait_bounded(empty, ((j - R) / R) & 1, flag)) break;
                 if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
                 const uint32_t full_cl = mapa_shared(full, 0);
                 if (is_k) {
@@ -571,8 +578,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
             }
             if (loads < nb && leader) {  // both CTAs' copies in flight complete on CTA 0's barriers
                 if (is_k) (void)mbar_wait_drain(q_full, 0);
-                for (int j = loads - KV < 0 ? 0 : loads - KV; j < loads; ++j)
-                    (void)mbar_wait_drain(is_k ? k_full(j % KV) : v_full(j % KV), (j / KV) & 1);
+                for (int j = loads - R < 0 ? 0 : loads - R; j < loads; ++j)
+                    (void)mbar_wait_drain(is_k ? k_full(j % R) : v_full(j % R), (j / R) & 1);
             }
         }
         __syncwarp();
@@ -583,8 +590,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
             constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
             bool issued = false;
             auto issue_s = [&](int j) -> bool {
-                const int st = j % KV;
-                if (!mbar_wait_bounded(k_full(st), (j / KV) & 1, flag)) return false;
+                const int st = j % KS;
+                if (!mbar_wait_bounded(k_full(st), (j / KS) & 1, flag)) return false;
                 // both CTAs have read S_{j-1} into registers
                 if (j >= 1 && !mbar_wait_bounded(s_free, (j - 1) & 1, flag)) return false;
                 tc_fence_after();
@@ -601,9 +608,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
                 return true;
             };
             auto issue_pv = [&](int j) -> bool {
-                const int st = j % KV, pb = j % 2;
+                const int st = j % VS, pb = j % 2;
                 if (!mbar_wait_bounded(p_full(pb), (j / 2) & 1, flag)) return false;
-                if (!mbar_wait_bounded(v_full(st), (j / KV) & 1, flag)) return false;
+                if (!mbar_wait_bounded(v_full(st), (j / VS) & 1, flag)) return false;
                 tc_fence_after();
                 const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
 #pragma unroll
@@ -633,7 +640,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
         // and half hh of each block's keys and of O's columns.  Both warps of a quadrant read the
         // whole score row, so they reach the same row maximum without exchanging it.
         const int qd = warp % 4;
-        const int hh = (warp - 2) / 4;
+        const int hh = (warp - 3) / 4;
         const int r = 32 * qd + lane;
         const int qrow = qt * kAttnQ + r;
         const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
