@@ -19,8 +19,9 @@ every two of them.  A separate pass after the timed region brackets single calls
 
 ``value`` = fused-chain algorithmic bytes (2 N b per call, N b read + N b written) / the fused
 chain groups' device time.  ``e2e`` = the same bytes / the time of the same chains run through
-the C ABI from pinned host memory: each call's x is copied in and its y copied out in chunks
-pipelined over three streams (copies in both directions overlap the kernels).
+the C ABI from pinned host memory: each call's x is copied in and its y copied out in slices, the
+copies in on one stream, the kernels on a second, the copies out on a third (ordered by events),
+so both copy directions overlap the kernels.
 
 ``--impl reference`` times the plain CPU oracle (the only other place this script runs it) on
 the same workload on the host cores, rank 0 only.
@@ -797,52 +798,66 @@ def planner_rows(fc, wl, peaks, launch_us, measured_ms, plans):
     return out
 
 
-def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world, chunks=8):
+def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world, chunks=4):
     """Per K: the fused chain through the C ABI on x from pinned host memory, y back to pinned host
     memory.  The chain is element-wise, so each call is issued as `chunks` calls on consecutive
-    slices, round-robin over three streams: a slice's host-to-device copy, its kernel and its
-    device-to-host copy queue on one stream, and the copy engines move other slices in both
-    directions meanwhile.  Bytes moved per step: x in and y out once per K."""
+    slices.  Host-to-device copies run back to back on one stream, the kernels on a second and
+    device-to-host copies on a third, ordered by events (a slice's kernel after its copy in and
+    after the previous read-out of its y slice; its copy in after the previous kernel on that
+    slice), so both copy directions stay busy while the kernels run.  Bytes moved per step: x in
+    and y out once per K."""
     import torch
     hx = torch.from_numpy(wl.chain_input(N, salt=7)).pin_memory()
     hy = torch.empty(N, dtype=torch.float32).pin_memory()
     dx = torch.empty(N, dtype=torch.float32, device=dev)
     dy = torch.empty(N, dtype=torch.float32, device=dev)
-    streams = [stream] + [torch.cuda.Stream(device=dev) for _ in range(2)]
+    s_in, s_run, s_out = stream, torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     csz = (N + chunks - 1) // chunks
+    ev = {k: [torch.cuda.Event() for _ in range(chunks)] for k in ("in", "run", "out")}
+    started = [False] * chunks
 
     def one_step():
         for K in KS:
             for c in range(chunks):
                 lo, hi = c * csz, min(N, (c + 1) * csz)
-                st = streams[c % len(streams)]   # a slice always on the same stream: in order
-                with torch.cuda.stream(st):
+                if started[c]:
+                    s_in.wait_event(ev["run"][c])          # the last kernel on this slice has read dx
+                with torch.cuda.stream(s_in):
                     dx[lo:hi].copy_(hx[lo:hi], non_blocking=True)
-                    rc = lib.fuse_chain_run(stage_sets[K], K, dx[lo:].data_ptr(), dy[lo:].data_ptr(), hi - lo,
-                                            fc.FUSE_F32, fc.FUSE_FUSED, st.cuda_stream)
-                    if rc != 0:
-                        raise fc.FuseError(rc, "fuse_chain_run")
+                ev["in"][c].record(s_in)
+                s_run.wait_event(ev["in"][c])
+                if started[c]:
+                    s_run.wait_event(ev["out"][c])         # the last read-out of this dy slice is done
+                rc = lib.fuse_chain_run(stage_sets[K], K, dx[lo:].data_ptr(), dy[lo:].data_ptr(), hi - lo,
+                                        fc.FUSE_F32, fc.FUSE_FUSED, s_run.cuda_stream)
+                if rc != 0:
+                    raise fc.FuseError(rc, "fuse_chain_run")
+                ev["run"][c].record(s_run)
+                s_out.wait_event(ev["run"][c])
+                with torch.cuda.stream(s_out):
                     hy[lo:hi].copy_(dy[lo:hi], non_blocking=True)
+                ev["out"][c].record(s_out)
+                started[c] = True
 
     def join():
         # the first stream waits for the others, so one event on it closes the step
-        for st in streams[1:]:
-            ev = torch.cuda.Event()
-            ev.record(st)
-            stream.wait_event(ev)
+        for st in (s_run, s_out):
+            e = torch.cuda.Event()
+            e.record(st)
+            s_in.wait_event(e)
 
     for _ in range(2):
         one_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     steps = max(3, min(args.steps, 10))
-    e0.record(stream)
-    for st in streams[1:]:
-        st.wait_stream(stream)
+    e0.record(s_in)
+    for st in (s_run, s_out):
+        st.wait_stream(s_in)
     for _ in range(steps):
         one_step()
     join()
-    e1.record(stream)
+    e1.record(s_in)
     torch.cuda.synchronize()
     # the sliced, pipelined calls must give what one call on the whole vector gives
     with torch.cuda.stream(stream):
