@@ -145,7 +145,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
     using L = AttnLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
+    pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     if (warp == 0 || warp == 2) {
         // ---------------------------------------------------------------- TMA producers
@@ -482,7 +483,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
     const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
     using L = PairLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -540,6 +541,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
+    pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     if (warp == 0 || warp == 2) {
         // ---------------------------------------------------------------- TMA producers

@@ -27,10 +27,15 @@ inline int check_launch() {
 // touches global memory: griddepcontrol.wait returns once the preceding grid has completed and its
 // writes are visible (at once if there is no such grid), so stream order is kept for every byte.
 // launch_dependents lets the next kernel be scheduled as soon as every CTA of this one has started.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_begin() {
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    pdl_trigger();
+    pdl_wait();
 }
+// Kernels with a set-up phase that touches no global memory (mbarrier init, TMEM allocation,
+// tensor-map prefetch) call pdl_trigger() at entry and pdl_wait() after the set-up, so the set-up
+// overlaps the end of the preceding kernel.
 
 // Launch `kernel` on `grid` x `block` threads with `smem` bytes of dynamic shared memory on `st`,
 // programmatic serialization allowed, as clusters of `cluster_x` CTAs when cluster_x > 1.

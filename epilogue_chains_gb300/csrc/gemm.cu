@@ -101,7 +101,7 @@ __device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank)
 __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
     const __grid_constant__ MainArgs args) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
@@ -147,6 +147,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     cluster_sync();  // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + OFF_HOLD);
+    pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer

@@ -75,7 +75,7 @@ template <int NM>
 __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     const __grid_constant__ CUtensorMap mapA, const __grid_constant__ CUtensorMap mapB,
     const __grid_constant__ DecodeArgs args) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
     using L = DecodeLayout<NM>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
@@ -120,6 +120,7 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     cluster_arrive();
     const uint32_t tmem_base = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
     bool ok = true;
+    pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     // After the K reduction CTA `rank` finishes output columns [n0 + COLS*rank, +COLS) of all NM
     // rows, in units of one column and four consecutive rows: unit idx = threadIdx.x +
