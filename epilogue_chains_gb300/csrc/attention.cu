@@ -29,8 +29,8 @@
 //       accumulator in TMEM only when the maximum has grown by more than 2^8 since it was last
 //       applied (P stays <= 256, exact in the final O / l).  After the last block they divide O
 //       by l and store it.
-// Consecutive CTAs (pairs) take the tiles of one (batch, head) slice, heaviest first, so the
-// ones resident together share that slice's key and value blocks in L2.
+// CTAs (pairs) run in groups of 16 (batch, head) slices, heaviest tiles first within a group, so
+// the ones resident together share their slices' key and value blocks in L2 (order_item()).
 // All waits are bounded (watchdog); a CTA whose wait runs out drains its MMAs and copies and
 // frees its TMEM before it returns.
 #include <math.h>
@@ -96,6 +96,21 @@ __device__ __forceinline__ float ex2f(float x) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Work order: item i of `per_head` items per (batch, head) slice, heaviest item (index 0 of a
+// slice) ... lightest.  Slices go in groups of kOrderGroup: within a group the items run heaviest
+// first across all of the group's slices, then the next group.  The group's key/value blocks
+// (kOrderGroup x 2 x S x D x 2 B: 32 MiB at S = 2048, D = 256) stay in L2 while its items run, and
+// every group ends with its lightest items, so the grid ends with short work instead of with the
+// heaviest items of the last slices.
+constexpr int kOrderGroup = 16;
+__device__ __forceinline__ void order_item(int i, int per_head, int BH, int& bh, int& heavy_rank) {
+    const int g = i / (kOrderGroup * per_head);
+    const int gs = min(kOrderGroup, BH - g * kOrderGroup);   // slices in this group
+    const int r = i - g * kOrderGroup * per_head;
+    heavy_rank = r / gs;                                       // 0 = heaviest
+    bh = g * kOrderGroup + r % gs;
 }
 
 __device__ __forceinline__ float max3f(float a, float b, float c) {
@@ -167,11 +182,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     auto s_free = [&](int i) { return bar0 + 8u * (3 + 4 * KV + 2 * PB + SB + i); };
     int* flag = a.flag;
 
-    // Consecutive CTAs take the tiles of one (batch, head) slice, heaviest (most key blocks)
-    // first, so the CTAs resident together share their slice's key/value blocks in L2.
     const int ntile = a.S / kAttnQ;
-    const int bh = static_cast<int>(blockIdx.x) / ntile;
-    const int qt = ntile - 1 - static_cast<int>(blockIdx.x) % ntile;
+    int bh, heavy;
+    order_item(static_cast<int>(blockIdx.x), ntile, a.BH, bh, heavy);
+    const int qt = ntile - 1 - heavy;
     constexpr int kBlocksPerTile = kAttnQ / kAttnK;
     const int nb = (qt + 1) * kBlocksPerTile;             // key blocks up to the diagonal
     const int row0 = bh * a.S + qt * kAttnQ;
@@ -467,8 +481,8 @@ struct PairLayout {
     static constexpr uint32_t OFF_LX = OFF_V + kPairV * VH_BYTES;      // row-sum exchange, 2 x 128 fp32
     static constexpr uint32_t OFF_BAR = OFF_LX + 2 * kAttnQ * 4;
     // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KS], k_empty[KS],
-    // v_full[VS], v_empty[VS]
-    static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV;
+    // v_full[VS], v_empty[VS], and q_empty, o_free (persistent kernel only)
+    static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV + 2;
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -501,14 +515,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     auto v_empty = [&](int i) { return bar0 + 8u * (9 + 2 * KS + VS + i); };
     int* flag = a.flag;
 
-    // Consecutive pairs take the tile pairs of one (batch, head) slice, heaviest first, so the
-    // pairs resident together share their slices' key/value blocks in L2.
+    // Pairs in the grouped, heaviest-first order of order_item().
     const int ntile = a.S / kAttnQ;
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
-    const int group = blockIdx.x / 2;
-    const int bh = group / (ntile / 2);
-    const int u = ntile / 2 - 1 - group % (ntile / 2);
+    int bh, heavy;
+    order_item(static_cast<int>(blockIdx.x / 2), ntile / 2, a.BH, bh, heavy);
+    const int u = ntile / 2 - 1 - heavy;
     const int qt = 2 * u + static_cast<int>(rank);
     const int nb = (2 * u + 2) * (kAttnQ / kAttnK);   // key blocks up to the pair's last diagonal
     const int row0 = bh * a.S + qt * kAttnQ;
@@ -766,6 +779,362 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
     }
 }
 
+// ================================================================== persistent 2-SM variant
+// attn_pair_kernel's pipeline, but each cluster stays resident and walks a list of tile pairs
+// (items c, c + C, c + 2C, ... of the order_item() order for cluster c of C), so the set-up (TMEM
+// allocation, barriers) happens once and every ring (K, V, S, P) runs on across items: the next
+// item's Q, K and V stream in while the current item finishes, its first scores are computed
+// while the softmax warps store the current item's output.  A fourth producer warp loads Q: the
+// next item's Q may only overwrite the current one once the current item's last S has completed
+// (q_empty), and the K and V rings must not wait for that.  Roles (384 threads):
+//   warp 0: K halves; warp 1 (CTA 0): every MMA; warp 2: V halves; warp 3: Q;
+//   warps 4-11: softmax and output of this CTA's 128 query rows.
+// At an item boundary the softmax warps first turn the next item's S_0 into P_0 (so its S_1 can
+// start at once), then read out and store the previous item's O and arrive on o_free; the next
+// item's PV_0, which overwrites O (accumulate off), waits for o_free.
+constexpr int kPersistThreads = 32 * (4 + kAttnSoftmaxWarps);
+
+template <int D>
+__global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
+    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
+    const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
+    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
+    using L = PairLayout<D>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    // barriers: the pair kernel's set (q_full, drain, l_ready, s_full, s_free, p_full[2],
+    // o_done[2], K ring, V ring) plus q_empty after them
+    const uint32_t bar0 = base + L::OFF_BAR;
+    const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16, s_full = bar0 + 24,
+                   s_free = bar0 + 32;
+    constexpr int KS = kPairK, VS = kPairV;
+    auto p_full = [&](int b) { return bar0 + 8u * (5 + b); };
+    auto o_done = [&](int b) { return bar0 + 8u * (7 + b); };
+    auto k_full = [&](int i) { return bar0 + 8u * (9 + i); };
+    auto k_empty = [&](int i) { return bar0 + 8u * (9 + KS + i); };
+    auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KS + i); };
+    auto v_empty = [&](int i) { return bar0 + 8u * (9 + 2 * KS + VS + i); };
+    const uint32_t q_empty = bar0 + 8u * (L::N_BARS - 2), o_free = bar0 + 8u * (L::N_BARS - 1);
+    int* flag = a.flag;
+
+    const int ntile = a.S / kAttnQ;
+    const int per_head = ntile / 2;
+    const int n_items = a.BH * per_head;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    const int cid = blockIdx.x / 2, ncl = gridDim.x / 2;
+    const int my_items = cid < n_items ? (n_items - cid + ncl - 1) / ncl : 0;
+    // item t of this cluster -> slice, pair index u, key blocks, first query row
+    auto item = [&](int t, int& bh, int& u, int& nb) {
+        int heavy;
+        order_item(cid + t * ncl, per_head, a.BH, bh, heavy);
+        u = per_head - 1 - heavy;
+        nb = (2 * u + 2) * (kAttnQ / kAttnK);
+    };
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
+        mbar_init(o_free, 2 * kAttnSoftmaxWarps);   // both CTAs' softmax warps (CTA 0's copy)
+        mbar_init(drain, 1);
+        mbar_init(l_ready, kAttnSoftmaxWarps);
+        mbar_init(s_full, 1);
+        mbar_init(s_free, 2 * kAttnSoftmaxWarps);   // both CTAs' softmax warps (CTA 0's copy)
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(p_full(b), 2 * kAttnSoftmaxWarps);
+            mbar_init(o_done(b), 1);
+        }
+        for (int i = 0; i < KS; ++i) {
+            mbar_init(k_full(i), 1);
+            mbar_init(k_empty(i), 1);
+        }
+        for (int i = 0; i < VS; ++i) {
+            mbar_init(v_full(i), 1);
+            mbar_init(v_empty(i), 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc_pair(base + L::OFF_HOLD, L::TMEM_COLS);
+    tc_fence_before();
+    cluster_sync();   // both CTAs' barriers exist before either signals the other
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
+    pdl_wait();  // the preceding kernel has completed: global memory may be touched
+
+    if (warp == 0 || warp == 2) {
+        // ---------------------------------------------------------------- K / V producers
+        if (lane == 0) {
+            const bool is_k = warp == 0;
+            prefetch_map(is_k ? &mKh : &mV);
+            const int R = is_k ? KS : VS;
+            int g = 0;   // blocks loaded so far, over all items
+            bool ok = true;
+            for (int t = 0; ok && t < my_items; ++t) {
+                int bh, u, nb;
+                item(t, bh, u, nb);
+                const int krow0 = bh * a.S;
+                for (int j = 0; j < nb; ++j, ++g) {
+                    const int st = g % R;
+                    const uint32_t full = is_k ? k_full(st) : v_full(st);
+                    const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+                    if (g >= R && !mbar_wait_bounded(empty, ((g - R) / R) & 1, flag)) { ok = false; break; }
+                    if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
+                    const uint32_t full_cl = mapa_shared(full, 0);
+                    if (is_k) {
+                        const int y = krow0 + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2);
+                        for (int c = 0; c < L::QATOMS; ++c)
+                            tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
+                                             full_cl);
+                    } else {
+                        const int y = krow0 + j * kAttnK;
+                        for (int c = 0; c < L::VATOMS; ++c)
+                            tma_load_2d_pair(base + L::OFF_V + st * L::VH_BYTES + c * L::V_REGION, &mV,
+                                             static_cast<int>(rank) * (D / 2) + 64 * c, y, full_cl);
+                    }
+                }
+            }
+            if (!ok && leader)   // both CTAs' copies in flight complete on CTA 0's barriers
+                for (int h = g - R < 0 ? 0 : g - R; h < g; ++h)
+                    (void)mbar_wait_drain(is_k ? k_full(h % R) : v_full(h % R), (h / R) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 3) {
+        // ---------------------------------------------------------------- Q producer
+        if (lane == 0) {
+            prefetch_map(&mQ);
+            const uint32_t qf = mapa_shared(q_full, 0);
+            int t = 0;
+            for (; t < my_items; ++t) {
+                // the previous item's last S has completed in both CTAs
+                if (t >= 1 && !mbar_wait_bounded(q_empty, (t - 1) & 1, flag)) break;
+                int bh, u, nb;
+                item(t, bh, u, nb);
+                const int row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
+                if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+                for (int c = 0; c < L::QATOMS; ++c)
+                    tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
+            }
+            if (t < my_items && t >= 1 && leader) (void)mbar_wait_drain(q_full, (t - 1) & 1);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ---------------------------------------------------------------- MMA issuer (CTA 0)
+        if (leader && lane == 0) {
+            constexpr uint32_t idS = idesc_f16(2 * kAttnQ, kAttnK, false, false, true);
+            constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
+            bool issued = false;
+            // S_j and PV_j of item t are global block g = (blocks of earlier items) + j
+            auto issue_s = [&](int t, int j, int g, int nb) -> bool {
+                const int st = g % KS;
+                if (j == 0 && !mbar_wait_bounded(q_full, t & 1, flag)) return false;
+                if (!mbar_wait_bounded(k_full(st), (g / KS) & 1, flag)) return false;
+                // both CTAs have read the previous S into registers
+                if (g >= 1 && !mbar_wait_bounded(s_free, (g - 1) & 1, flag)) return false;
+                tc_fence_after();
+                const uint32_t kb = base + L::OFF_K + st * L::KH_BYTES;
+#pragma unroll
+                for (int s = 0; s < D / 16; ++s)
+                    tc_mma_pair(tmem + L::S_COL,
+                                smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
+                                smem_desc_sw128(kb + (s / 4) * L::KH_REGION + (s % 4) * 32, 16, 1024), idS,
+                                s > 0 ? 1u : 0u);
+                tc_commit_pair_mc(s_full, 0x3);
+                tc_commit_pair_mc(k_empty(st), 0x3);
+                if (j == nb - 1) tc_commit_pair_mc(q_empty, 0x3);   // the item's Q is no longer read
+                issued = true;
+                return true;
+            };
+            auto issue_pv = [&](int t, int j, int g) -> bool {
+                const int st = g % VS, pb = g % 2;
+                if (!mbar_wait_bounded(p_full(pb), (g / 2) & 1, flag)) return false;
+                // the previous item's O has been read out by both CTAs
+                if (j == 0 && t >= 1 && !mbar_wait_bounded(o_free, (t - 1) & 1, flag)) return false;
+                if (!mbar_wait_bounded(v_full(st), (g / VS) & 1, flag)) return false;
+                tc_fence_after();
+                const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
+#pragma unroll
+                for (int s = 0; s < kAttnK / 16; ++s)
+                    tc_mma_pair_ts(tmem + L::O_COL, tmem + L::P_COL + (kAttnK / 2) * pb + 8 * s,
+                                   smem_desc_sw128(vb + s * 2048, L::V_REGION, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
+                tc_commit_pair_mc(o_done(pb), 0x3);
+                tc_commit_pair_mc(v_empty(st), 0x3);
+                issued = true;
+                return true;
+            };
+            // per item: S_0, then S_j+1 before PV_j (the next scores are computed while the
+            // softmax warps work on the current ones); an item's last PV precedes the next item's
+            // S_0, which waits for the next Q
+            bool ok = true;
+            int g = 0;
+            for (int t = 0; ok && t < my_items; ++t) {
+                int bh, u, nb;
+                item(t, bh, u, nb);
+                ok = issue_s(t, 0, g, nb);
+                for (int j = 0; ok && j < nb; ++j) {
+                    if (j + 1 < nb && !issue_s(t, j + 1, g + j + 1, nb)) { ok = false; break; }
+                    ok = issue_pv(t, j, g + j);
+                }
+                g += nb;
+            }
+            if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
+                tc_commit_pair(drain);
+                (void)mbar_wait_drain(drain, 0);
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        // Warp w serves TMEM lane quadrant w % 4 (query rows 32 (w % 4) + lane of this CTA's tile)
+        // and half hh of each block's keys and of O's columns.
+        const int qd = warp % 4;
+        const int hh = (warp - 4) / 4;
+        const int r = 32 * qd + lane;
+        const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
+        const float c = a.c;
+        const uint32_t s_free0 = mapa_shared(s_free, 0);
+        const uint32_t p_full_a = mapa_shared(p_full(0), 0), p_full_b = mapa_shared(p_full(1), 0);
+        float* lx = reinterpret_cast<float*>(gbase + L::OFF_LX);
+        const uint32_t o_free0 = mapa_shared(o_free, 0);
+        // Read out item e's O (its last PV is global block g_last): O / l, this warp's 32 rows and
+        // half of the columns.  The row sum is the sum of the two halves' partial sums, exchanged
+        // through shared memory (a bounded mbarrier wait, not a named barrier: a warp that gave
+        // up earlier must not leave its partner blocked).  The partner cannot overwrite its slot
+        // for item e + 1 before this warp has read it: it writes that slot only after item
+        // e + 1's last PV, which follows that item's PV_0, which waits on this warp's o_free
+        // arrival at the end of this read-out.
+        auto epilogue = [&](int e, int bh_e, int qt_e, float l_e, int g_last) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(g_last % 2), (g_last / 2) & 1, flag)))
+                return false;
+            tc_fence_after();
+            lx[hh * kAttnQ + r] = l_e;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_ready);
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(l_ready, e & 1, flag))) return false;
+            const float inv = 1.0f / (l_e + lx[(1 - hh) * kAttnQ + r]);
+            __nv_bfloat16* orow = a.O + static_cast<int64_t>(bh_e * a.S + qt_e * kAttnQ + r) * D + (D / 2) * hh;
+#pragma unroll 1
+            for (int k = 0; k < D / 64; ++k) {
+                float o[32];
+                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 32 * k, o);
+                tmem_ld_wait();
+                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(o_free0);   // the next item's PV_0 may overwrite O
+            return true;
+        };
+        bool ok = true;
+        int g = 0;   // global block index
+        int bh_p = 0, qt_p = 0;   // the previous item, whose O is read out at the next item's block 0
+        float l_p = 0.0f;
+        for (int t = 0; ok && t < my_items; ++t) {
+            int bh, u, nb;
+            item(t, bh, u, nb);
+            const int qt = 2 * u + static_cast<int>(rank);
+            const int qrow = qt * kAttnQ + r;
+            float m_used = -INFINITY, l = 0.0f;
+            // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform before them
+            for (int j = 0; j < nb; ++j, ++g) {
+                const int pb = g % 2;
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, g & 1, flag))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                constexpr int HK = kAttnK / 2;
+                float s[HK], so[HK];
+                const uint32_t sbase = tmem + lanes + L::S_COL;
+#pragma unroll
+                for (int k = 0; k < HK / 32; ++k) {
+                    tmem_ld32(sbase + HK * hh + 32 * k, s + 32 * k);
+                    tmem_ld32(sbase + HK * (1 - hh) + 32 * k, so + 32 * k);
+                }
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(s_free0);   // S may be overwritten now
+
+                const int lim = qrow - j * kAttnK;           // last visible key of this block
+                const bool diag = j >= qt;
+                const int k0 = HK * hh, ko = HK * (1 - hh);
+                const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
+                                       : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
+                float alpha = 1.0f;
+                bool rescale = false;
+                if (mx > m_used + kRescaleLog2) {
+                    if (j > 0) {
+                        alpha = ex2f(m_used - mx);
+                        rescale = true;
+                    }
+                    m_used = mx;
+                }
+                uint32_t pk[HK / 2];
+                const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
+                                         : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
+                l = l * alpha + (sum2.x + sum2.y);
+
+                // P buffer pb was last read by PV of global block g - 2
+                if (g >= 2) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(pb), ((g - 2) / 2) & 1, flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+                    // O must hold blocks 0..j-1 of this item exactly: PV of block g - 1 complete
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done((g - 1) % 2), ((g - 1) / 2) & 1, flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int k = 0; k < D / 64; ++k) {
+                        const uint32_t col = L::O_COL + (D / 2) * hh + 32 * k;
+                        float o[32];
+                        tmem_ld32(tmem + lanes + col, o);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= alpha;
+                        tmem_st32(tmem + lanes + col, o);
+                    }
+                }
+                tmem_st32(tmem + lanes + L::P_COL + HK * pb + (HK / 2) * hh, reinterpret_cast<const float*>(pk));
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(pb ? p_full_b : p_full_a);
+                // the previous item's output, now that this item's S_1 can run
+                if (j == 0 && t >= 1 && !epilogue(t - 1, bh_p, qt_p, l_p, g - 1)) {
+                    ok = false;
+                    break;
+                }
+            }
+            bh_p = bh;
+            qt_p = qt;
+            l_p = l;
+        }
+        if (ok && my_items > 0) (void)epilogue(my_items - 1, bh_p, qt_p, l_p, g - 1);
+    }
+    tc_fence_before();
+    // neither CTA leaves while its peer may still read its shared memory or TMEM (MMA operands),
+    // write into it (copies) or signal its barriers
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, L::TMEM_COLS);
+    }
+}
+
 // Dynamic shared memory of a launch: the layout's, but at least 120 KB so that one CTA runs per SM
 // for every D (each CTA allocates all 512 TMEM columns).
 template <int D>
@@ -831,6 +1200,51 @@ int launch_pair(const void* q, const void* k, const void* v, const AttnArgs& arg
     return launch_pdl(attn_pair_kernel<D>, dim3(static_cast<unsigned>(rows / kAttnQ)), dim3(kAttnThreads), PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, args);
 }
 
+// Persistent 2-SM kernel: as many clusters as can be resident (at most one per tile pair).
+template <int D>
+int launch_persist(const void* q, const void* k, const void* v, const AttnArgs& args, cudaStream_t st) {
+    static std::mutex mu;
+    static int clusters[64] = {0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (clusters[dev] == 0) {
+            e = cudaFuncSetAttribute(attn_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(PairLayout<D>::SMEM));
+            if (e != cudaSuccess) return record_cuda_error(e);
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
+            cfg.blockDim = dim3(kPersistThreads);
+            cfg.dynamicSmemBytes = PairLayout<D>::SMEM;
+            cudaLaunchAttribute attrs[1];
+            attrs[0].id = cudaLaunchAttributeClusterDimension;
+            attrs[0].val.clusterDim.x = 2;
+            attrs[0].val.clusterDim.y = 1;
+            attrs[0].val.clusterDim.z = 1;
+            cfg.attrs = attrs;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, attn_persist_kernel<D>, &cfg) != cudaSuccess || n < 1) {
+                (void)cudaGetLastError();
+                n = sm_count() / 2;
+            }
+            clusters[dev] = n;
+        }
+    }
+    const int64_t rows = static_cast<int64_t>(args.BH) * args.S;
+    const int64_t items = rows / kAttnQ / 2;
+    const int ncl = static_cast<int>(items < clusters[dev] ? items : clusters[dev]);
+    CUtensorMap mQ, mKh, mV;
+    if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mKh, k, rows, D, 64, kAttnK / 2, true) ||
+        !make_map(&mV, v, rows, D, 64, kAttnK, true))
+        return FUSE_ECUDA;
+    return launch_pdl(attn_persist_kernel<D>, dim3(2 * static_cast<unsigned>(ncl)), dim3(kPersistThreads),
+                      PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, args);
+}
+
 template <int D>
 int run_attn(const void* q, const void* k, const void* v, void* o, int bh, int S, float scale,
              cudaStream_t st) {
@@ -845,7 +1259,7 @@ int run_attn(const void* q, const void* k, const void* v, void* o, int bh, int S
     // adjacent query tiles run as 2-SM pairs when they pair up and the head splits into two
     // halves of 64-wide swizzle atoms
     if constexpr (D >= 128) {
-        if ((S / kAttnQ) % 2 == 0) return launch_pair<D>(q, k, v, args, st);
+        if ((S / kAttnQ) % 2 == 0) return launch_persist<D>(q, k, v, args, st);
     }
     return launch_attn<D>(mQ, mK, mV, args, st);
 }
