@@ -365,7 +365,7 @@ def run_ours(args, rank, world, local):
                                      ABH, AS, AD, wl.ATT_SCALE, sh), "fuse_attention")
             counter["launches"] += 1
         att_flops = fc.fuse_attention_flops(ABH, AS, AD)
-        groups += [Group("attention_fused", attn, att_flops, 2, "tensor", "attn_pair_kernel<D=256>", 1)]
+        groups += [Group("attention_fused", attn, att_flops, 2, "tensor", "attn_persist_kernel<D=256>", 1)]
         # -------------------------------------------------------------- GEMM epilogue chain
         gN, gK = wl.GEMM_N, wl.GEMM_K
         with torch.cuda.stream(stream):

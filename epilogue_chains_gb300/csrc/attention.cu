@@ -7,9 +7,10 @@
 //     O = softmax(scale Q K^T, keys j <= query i) V,   Q, K, V, O bf16 [S, D].
 //
 // GB300 design, two kernels sharing the softmax code:
-//  * attn_pair_kernel (D = 128, 256 with an even number of 128-row query tiles, the benchmarked
-//    case): two CTAs of a cluster run as one 2-SM MMA unit over a pair of adjacent query tiles;
-//    P goes from the softmax warps to the PV MMA through TMEM.  Described at the kernel.
+//  * attn_persist_kernel (D = 128, 256 with an even number of 128-row query tiles, the
+//    benchmarked case): two CTAs of a cluster run as one 2-SM MMA unit over a pair of adjacent
+//    query tiles, P goes from the softmax warps to the PV MMA through TMEM, and each cluster stays
+//    resident over a list of tile pairs.  Described at the kernel.
 //  * attn_fwd_kernel (D = 64, or an odd tile count): one CTA per 128-row query tile.  Keys go in
 //    blocks of 128 (the MMA re-reads the whole Q tile from shared memory for every block, so longer
 //    blocks cost less shared-memory bandwidth per flop), which at a head size of 256 leaves room
@@ -454,14 +455,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
 // S at 0-127 (one buffer: S_j+1 is computed as soon as both CTAs have read S_j), P at 128-255
 // (two buffers of 64 columns, 128 bf16 keys each), O at 256-511.  The pair walks key blocks
 // 0 .. 2u + 1 together (tile 2u finds block 2u + 1 fully masked).
-//  * warps 0 and 2 of each CTA: lane 0 of warp 0 loads the CTA's Q rows and its half of every K
-//    block, lane 0 of warp 2 its half of every V block; the bytes of both CTAs complete on CTA 0's
-//    barriers;
-//  * warp 1 of CTA 0 issues every MMA of the pair, in the order S_0, S_1, PV_0, S_2, PV_1, ...;
-//    commits signal both CTAs' barriers;
-//  * warps 3-10 of each CTA: the softmax of its own 128 query rows (two warps per TMEM lane
-//    quadrant, each exponentiating half of a block's keys and rescaling half of O's columns); they
-//    release S and publish P on CTA 0's barriers.
+// Warp roles are given at the persistent kernel below, the only kernel on this layout.
 // K and V ring depths (K_j+2 is loaded once S_j has completed, V_j+2 once PV_j has).
 constexpr int kPairK = 2, kPairV = 2;
 
@@ -478,10 +472,14 @@ struct PairLayout {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                 // + stage * KH_BYTES
     static constexpr uint32_t OFF_V = OFF_K + kPairK * KH_BYTES;       // + stage * VH_BYTES
-    static constexpr uint32_t OFF_LX = OFF_V + kPairV * VH_BYTES;      // row-sum exchange, 2 x 128 fp32
+    // output staging: per softmax warp 32 rows x 64 columns of bf16 (one 128-byte-swizzled box of
+    // the O tensor map), written to global memory by a TMA store
+    static constexpr uint32_t ST_WARP = 32 * 128;
+    static constexpr uint32_t OFF_ST = OFF_V + kPairV * VH_BYTES;
+    static constexpr uint32_t OFF_LX = OFF_ST + kAttnSoftmaxWarps * ST_WARP;   // row-sum exchange, 2 x 128 fp32
     static constexpr uint32_t OFF_BAR = OFF_LX + 2 * kAttnQ * 4;
     // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KS], k_empty[KS],
-    // v_full[VS], v_empty[VS], and q_empty, o_free (persistent kernel only)
+    // v_full[VS], v_empty[VS], q_empty, o_free
     static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV + 2;
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
@@ -493,302 +491,21 @@ struct PairLayout {
     static_assert(SMEM <= 232448, "shared-memory budget");
 };
 
-template <int D>
-__global__ void __launch_bounds__(kAttnThreads, 1) attn_pair_kernel(
-    const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
-    const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
-    pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
-    using L = PairLayout<D>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
-    uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const uint32_t bar0 = base + L::OFF_BAR;
-    const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16, s_full = bar0 + 24,
-                   s_free = bar0 + 32;
-    constexpr int KS = kPairK, VS = kPairV;
-    auto p_full = [&](int b) { return bar0 + 8u * (5 + b); };
-    auto o_done = [&](int b) { return bar0 + 8u * (7 + b); };
-    auto k_full = [&](int i) { return bar0 + 8u * (9 + i); };
-    auto k_empty = [&](int i) { return bar0 + 8u * (9 + KS + i); };
-    auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KS + i); };
-    auto v_empty = [&](int i) { return bar0 + 8u * (9 + 2 * KS + VS + i); };
-    int* flag = a.flag;
-
-    // Pairs in the grouped, heaviest-first order of order_item().
-    const int ntile = a.S / kAttnQ;
-    const uint32_t rank = cluster_rank();
-    const bool leader = rank == 0;
-    int bh, heavy;
-    order_item(static_cast<int>(blockIdx.x / 2), ntile / 2, a.BH, bh, heavy);
-    const int u = ntile / 2 - 1 - heavy;
-    const int qt = 2 * u + static_cast<int>(rank);
-    const int nb = (2 * u + 2) * (kAttnQ / kAttnK);   // key blocks up to the pair's last diagonal
-    const int row0 = bh * a.S + qt * kAttnQ;
-    const int krow0 = bh * a.S;
-
-    // Ring use: barrier x of a ring of n serves blocks j = x, x + n, ...; block j waits for
-    // completion number j / n, parity (j / n) & 1.
-    if (threadIdx.x == 0) {
-        mbar_init(q_full, 1);
-        mbar_init(drain, 1);
-        mbar_init(l_ready, kAttnSoftmaxWarps);
-        mbar_init(s_full, 1);
-        mbar_init(s_free, 2 * kAttnSoftmaxWarps);   // both CTAs' softmax warps (CTA 0's copy)
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(p_full(b), 2 * kAttnSoftmaxWarps);
-            mbar_init(o_done(b), 1);
-        }
-        for (int i = 0; i < KS; ++i) {
-            mbar_init(k_full(i), 1);
-            mbar_init(k_empty(i), 1);
-        }
-        for (int i = 0; i < VS; ++i) {
-            mbar_init(v_full(i), 1);
-            mbar_init(v_empty(i), 1);
-        }
-        fence_mbar_init();
-    }
-    if (warp == 1) tmem_alloc_pair(base + L::OFF_HOLD, L::TMEM_COLS);
-    tc_fence_before();
-    cluster_sync();   // both CTAs' barriers exist before either signals the other
-    tc_fence_after();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
-    pdl_wait();  // the preceding kernel has completed: global memory may be touched
-
-    if (warp == 0 || warp == 2) {
-        // ---------------------------------------------------------------- TMA producers
-        // warp 0 loads this CTA's Q rows and K halves, warp 2 its V halves (lane 0 of each)
-        if (lane == 0) {
-            const bool is_k = warp == 0;
-            prefetch_map(is_k ? &mKh : &mV);
-            if (is_k) {
-                prefetch_map(&mQ);
-                if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
-                const uint32_t qf = mapa_shared(q_full, 0);
-                for (int c = 0; c < L::QATOMS; ++c)
-                    tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
-            }
-            const int R = is_k ? KS : VS;   // ring depth
-            int loads = 0;
-            for (int j = 0; j < nb; ++j) {
-                const int st = j % R;
-                const uint32_t full = is_k ? k_full(st) : v_full(st);
-                const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
-                if (j >= R && !mbar_wait_bounded(empty, ((j - R) / R) & 1, flag)) break;
-                if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
-                const uint32_t full_cl = mapa_shared(full, 0);
-                if (is_k) {
-                    const int y = krow0 + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2);
-                    for (int c = 0; c < L::QATOMS; ++c)
-                        tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
-                                         full_cl);
-                } else {
-                    const int y = krow0 + j * kAttnK;
-                    for (int c = 0; c < L::VATOMS; ++c)
-                        tma_load_2d_pair(base + L::OFF_V + st * L::VH_BYTES + c * L::V_REGION, &mV,
-                                         static_cast<int>(rank) * (D / 2) + 64 * c, y, full_cl);
-                }
-                ++loads;
-            }
-            if (loads < nb && leader) {  // both CTAs' copies in flight complete on CTA 0's barriers
-                if (is_k) (void)mbar_wait_drain(q_full, 0);
-                for (int j = loads - R < 0 ? 0 : loads - R; j < loads; ++j)
-                    (void)mbar_wait_drain(is_k ? k_full(j % R) : v_full(j % R), (j / R) & 1);
-            }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer (CTA 0)
-        if (leader && lane == 0) {
-            constexpr uint32_t idS = idesc_f16(2 * kAttnQ, kAttnK, false, false, true);
-            constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
-            bool issued = false;
-            auto issue_s = [&](int j) -> bool {
-                const int st = j % KS;
-                if (!mbar_wait_bounded(k_full(st), (j / KS) & 1, flag)) return false;
-                // both CTAs have read S_{j-1} into registers
-                if (j >= 1 && !mbar_wait_bounded(s_free, (j - 1) & 1, flag)) return false;
-                tc_fence_after();
-                const uint32_t kb = base + L::OFF_K + st * L::KH_BYTES;
-#pragma unroll
-                for (int s = 0; s < D / 16; ++s)   // K = 16 steps over the head: atom s / 4, 32 B apart
-                    tc_mma_pair(tmem + L::S_COL,
-                                smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
-                                smem_desc_sw128(kb + (s / 4) * L::KH_REGION + (s % 4) * 32, 16, 1024), idS,
-                                s > 0 ? 1u : 0u);
-                tc_commit_pair_mc(s_full, 0x3);
-                tc_commit_pair_mc(k_empty(st), 0x3);
-                issued = true;
-                return true;
-            };
-            auto issue_pv = [&](int j) -> bool {
-                const int st = j % VS, pb = j % 2;
-                if (!mbar_wait_bounded(p_full(pb), (j / 2) & 1, flag)) return false;
-                if (!mbar_wait_bounded(v_full(st), (j / VS) & 1, flag)) return false;
-                tc_fence_after();
-                const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
-#pragma unroll
-                for (int s = 0; s < kAttnK / 16; ++s)   // K = 16 keys: 8 TMEM columns of P; V rows 16 s..
-                    tc_mma_pair_ts(tmem + L::O_COL, tmem + L::P_COL + (kAttnK / 2) * pb + 8 * s,
-                                   smem_desc_sw128(vb + s * 2048, L::V_REGION, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
-                tc_commit_pair_mc(o_done(pb), 0x3);
-                tc_commit_pair_mc(v_empty(st), 0x3);
-                issued = true;
-                return true;
-            };
-            bool ok = mbar_wait_bounded(q_full, 0, flag);
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < nb; ++j) {
-                if (j + 1 < nb && !issue_s(j + 1)) { ok = false; break; }
-                ok = issue_pv(j);
-            }
-            if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
-                tc_commit_pair(drain);
-                (void)mbar_wait_drain(drain, 0);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ---------------------------------------------------------------- softmax warps
-        // Warp w serves TMEM lane quadrant w % 4 (query rows 32 (w % 4) + lane of this CTA's tile)
-        // and half hh of each block's keys and of O's columns.  Both warps of a quadrant read the
-        // whole score row, so they reach the same row maximum without exchanging it.
-        const int qd = warp % 4;
-        const int hh = (warp - 3) / 4;
-        const int r = 32 * qd + lane;
-        const int qrow = qt * kAttnQ + r;
-        const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
-        const float c = a.c;
-        const uint32_t s_free0 = mapa_shared(s_free, 0);
-        const uint32_t p_full_a = mapa_shared(p_full(0), 0), p_full_b = mapa_shared(p_full(1), 0);
-        float m_used = -INFINITY, l = 0.0f;
-        bool ok = true;
-        // tcgen05.ld/st are warp-collective: every wait outcome is made warp-uniform before them
-        for (int j = 0; j < nb; ++j) {
-            const int pb = j % 2;
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(s_full, j & 1, flag))) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            constexpr int HK = kAttnK / 2;
-            float s[HK], so[HK];
-            const uint32_t sbase = tmem + lanes + L::S_COL;
-#pragma unroll
-            for (int k = 0; k < HK / 32; ++k) {
-                tmem_ld32(sbase + HK * hh + 32 * k, s + 32 * k);
-                tmem_ld32(sbase + HK * (1 - hh) + 32 * k, so + 32 * k);
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(s_free0);   // S may be overwritten by S_{j+1} now
-
-            // keys with index > query index are masked: only in the blocks at and past the
-            // tile's diagonal (j >= qt), a condition uniform over the CTA
-            const int lim = qrow - j * kAttnK;           // last visible key of this block
-            const bool diag = j >= qt;
-            const int k0 = HK * hh, ko = HK * (1 - hh);
-            const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
-                                   : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
-            float alpha = 1.0f;
-            bool rescale = false;
-            if (mx > m_used + kRescaleLog2) {   // always true for the first block (m_used = -inf)
-                if (j > 0) {
-                    alpha = ex2f(m_used - mx);
-                    rescale = true;
-                }
-                m_used = mx;
-            }
-            uint32_t pk[HK / 2];
-            const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
-                                     : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
-            l = l * alpha + (sum2.x + sum2.y);
-
-            // P buffer pb was last read by PV_{j-2}
-            if (j >= 2) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(pb), ((j - 2) / 2) & 1, flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-            }
-            if (__any_sync(0xffffffffu, rescale)) {   // rows without a new maximum scale by 1
-                // O must hold blocks 0..j-1 exactly: PV_{j-1} complete (PV_j is not issued yet)
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done((j - 1) % 2), ((j - 1) / 2) & 1, flag))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-#pragma unroll 1
-                for (int k = 0; k < D / 64; ++k) {
-                    const uint32_t col = L::O_COL + (D / 2) * hh + 32 * k;
-                    float o[32];
-                    tmem_ld32(tmem + lanes + col, o);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] *= alpha;
-                    tmem_st32(tmem + lanes + col, o);
-                }
-            }
-            // this warp's 64 keys of P row r: 32 columns of bf16 pairs
-            tmem_st32(tmem + lanes + L::P_COL + HK * pb + (HK / 2) * hh, reinterpret_cast<const float*>(pk));
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(pb ? p_full_b : p_full_a);
-        }
-        const int last = nb - 1;
-        if (ok && __all_sync(0xffffffffu, mbar_wait_bounded(o_done(last % 2), (last / 2) & 1, flag))) {
-            tc_fence_after();
-            // the row sum is the sum of the two halves' partial sums, exchanged through shared
-            // memory (a bounded mbarrier wait, not a named barrier: a warp that gave up earlier
-            // must not leave its partner blocked)
-            float* lx = reinterpret_cast<float*>(gbase + L::OFF_LX);
-            lx[hh * kAttnQ + r] = l;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(l_ready);
-            const bool got = __all_sync(0xffffffffu, mbar_wait_bounded(l_ready, 0, flag));
-            const float inv = 1.0f / (l + lx[(1 - hh) * kAttnQ + r]);
-            if (got) {
-                __nv_bfloat16* orow = a.O + static_cast<int64_t>(row0 + r) * D + (D / 2) * hh;
-#pragma unroll 1
-                for (int k = 0; k < D / 64; ++k) {
-                    float o[32];
-                    tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 32 * k, o);
-                    tmem_ld_wait();
-                    uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                            pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                            pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                            pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
-                }
-            }
-        }
-    }
-    tc_fence_before();
-    // neither CTA leaves while its peer may still read its shared memory or TMEM (MMA operands),
-    // write into it (copies) or signal its barriers
-    cluster_sync();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem, L::TMEM_COLS);
-    }
-}
-
 // ================================================================== persistent 2-SM variant
-// attn_pair_kernel's pipeline, but each cluster stays resident and walks a list of tile pairs
-// (items c, c + C, c + 2C, ... of the order_item() order for cluster c of C), so the set-up (TMEM
-// allocation, barriers) happens once and every ring (K, V, S, P) runs on across items: the next
-// item's Q, K and V stream in while the current item finishes, its first scores are computed
-// while the softmax warps store the current item's output.  A fourth producer warp loads Q: the
-// next item's Q may only overwrite the current one once the current item's last S has completed
-// (q_empty), and the K and V rings must not wait for that.  Roles (384 threads):
-//   warp 0: K halves; warp 1 (CTA 0): every MMA; warp 2: V halves; warp 3: Q;
-//   warps 4-11: softmax and output of this CTA's 128 query rows.
+// The 2-SM pipeline above in a persistent kernel: each cluster stays resident and walks a list of
+// tile pairs (items c, c + C, c + 2C, ... of the order_item() order for cluster c of C), so the
+// set-up (TMEM allocation, barriers) happens once and every ring (K, V, S, P) runs on across
+// items: the next item's Q, K and V stream in while the current item finishes.  Roles (384
+// threads per CTA):
+//   warp 0, lane 0: this CTA's half of every K block (TMA); warp 2, lane 0: its half of every V
+//     block; warp 3, lane 0: its 128 Q rows.  The bytes of both CTAs complete on CTA 0's barriers.
+//     Q gets a warp of its own because the next item's Q may only overwrite the current one once
+//     the current item's last S has completed (q_empty), and the K and V rings must not wait.
+//   warp 1 of CTA 0: every MMA of the pair, per item in the order S_0, S_1, PV_0, S_2, PV_1, ...;
+//     its commits signal both CTAs' barriers.
+//   warps 4-11: softmax and output of this CTA's 128 query rows (two warps per TMEM lane
+//     quadrant, each exponentiating half of a block's keys and rescaling half of O's columns);
+//     they release S and publish P on CTA 0's barriers.
 // At an item boundary the softmax warps first turn the next item's S_0 into P_0 (so its S_1 can
 // start at once), then read out and store the previous item's O and arrive on o_free; the next
 // item's PV_0, which overwrites O (accumulate off), waits for o_free.
@@ -797,15 +514,16 @@ constexpr int kPersistThreads = 32 * (4 + kAttnSoftmaxWarps);
 template <int D>
 __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mKh,
-    const __grid_constant__ CUtensorMap mV, const __grid_constant__ AttnArgs a) {
+    const __grid_constant__ CUtensorMap mV,
+    const __grid_constant__ CUtensorMap mO, const __grid_constant__ AttnArgs a) {
     pdl_trigger();  // the set-up below touches no global memory; pdl_wait() follows it
     using L = PairLayout<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t base = (smem_addr(smem_raw) + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - smem_addr(smem_raw));
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // barriers: the pair kernel's set (q_full, drain, l_ready, s_full, s_free, p_full[2],
-    // o_done[2], K ring, V ring) plus q_empty after them
+    // barriers: q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], K ring, V ring,
+    // then q_empty and o_free
     const uint32_t bar0 = base + L::OFF_BAR;
     const uint32_t q_full = bar0, drain = bar0 + 8, l_ready = bar0 + 16, s_full = bar0 + 24,
                    s_free = bar0 + 32;
@@ -915,6 +633,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                 if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
                 for (int c = 0; c < L::QATOMS; ++c)
                     tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
+                // the next item's Q into L2 now, so that its load (after this item's last S) is short
+                if (t + 1 < my_items) {
+                    item(t + 1, bh, u, nb);
+                    const int row1 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
+                    for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, row1);
+                }
             }
             if (t < my_items && t >= 1 && leader) (void)mbar_wait_drain(q_full, (t - 1) & 1);
         }
@@ -963,20 +687,32 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                 issued = true;
                 return true;
             };
-            // per item: S_0, then S_j+1 before PV_j (the next scores are computed while the
-            // softmax warps work on the current ones); an item's last PV precedes the next item's
-            // S_0, which waits for the next Q
-            bool ok = true;
-            int g = 0;
-            for (int t = 0; ok && t < my_items; ++t) {
-                int bh, u, nb;
-                item(t, bh, u, nb);
-                ok = issue_s(t, 0, g, nb);
-                for (int j = 0; ok && j < nb; ++j) {
-                    if (j + 1 < nb && !issue_s(t, j + 1, g + j + 1, nb)) { ok = false; break; }
-                    ok = issue_pv(t, j, g + j);
+            // S_0, then for every block g (over all items) S_g+1 before PV_g: the next scores are
+            // computed while the softmax warps work on the current ones, across item boundaries
+            // too (the next item's S_0 precedes the current item's last PV)
+            bool ok = my_items > 0;
+            int ts = 0, js = 0, nbs = 0, tp = 0, jp = 0, nbp = 0, bh_, u_;
+            if (ok) {
+                item(0, bh_, u_, nbs);
+                nbp = nbs;
+                ok = issue_s(0, 0, 0, nbs);
+                js = 1;
+            }
+            for (int g = 0; ok && tp < my_items; ++g) {
+                if (js == nbs && ts + 1 < my_items) {   // the S cursor moves to the next item
+                    ++ts;
+                    js = 0;
+                    item(ts, bh_, u_, nbs);
                 }
-                g += nb;
+                if (js < nbs) {
+                    if (!issue_s(ts, js, g + 1, nbs)) { ok = false; break; }
+                    ++js;
+                }
+                if (!issue_pv(tp, jp, g)) { ok = false; break; }
+                if (++jp == nbp && ++tp < my_items) {
+                    jp = 0;
+                    item(tp, bh_, u_, nbp);
+                }
             }
             if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
                 tc_commit_pair(drain);
@@ -997,6 +733,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
         const uint32_t p_full_a = mapa_shared(p_full(0), 0), p_full_b = mapa_shared(p_full(1), 0);
         float* lx = reinterpret_cast<float*>(gbase + L::OFF_LX);
         const uint32_t o_free0 = mapa_shared(o_free, 0);
+        uint8_t* stage = gbase + L::OFF_ST + (warp - 4) * L::ST_WARP;
+        const uint32_t stage_s = base + L::OFF_ST + (warp - 4) * L::ST_WARP;
         // Read out item e's O (its last PV is global block g_last): O / l, this warp's 32 rows and
         // half of the columns.  The row sum is the sum of the two halves' partial sums, exchanged
         // through shared memory (a bounded mbarrier wait, not a named barrier: a warp that gave
@@ -1013,19 +751,32 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
             if (lane == 0) mbar_arrive(l_ready);
             if (!__all_sync(0xffffffffu, mbar_wait_bounded(l_ready, e & 1, flag))) return false;
             const float inv = 1.0f / (l_e + lx[(1 - hh) * kAttnQ + r]);
-            __nv_bfloat16* orow = a.O + static_cast<int64_t>(bh_e * a.S + qt_e * kAttnQ + r) * D + (D / 2) * hh;
+            // 64 columns at a time: TMEM -> registers -> this warp's staging box (row = lane, 16-byte
+            // chunks in the 128-byte swizzle of the O tensor map) -> TMA store.  A store instruction
+            // per lane and row would touch 32 rows per warp instruction; the box store writes whole
+            // 128-byte lines.
+            const int orow0 = bh_e * a.S + qt_e * kAttnQ + 32 * qd;
 #pragma unroll 1
-            for (int k = 0; k < D / 64; ++k) {
-                float o[32];
-                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 32 * k, o);
+            for (int k = 0; k < D / 128; ++k) {
+                float o[64];
+                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 64 * k, o);
+                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 64 * k + 32, o + 32);
                 tmem_ld_wait();
-                uint4* dst = reinterpret_cast<uint4*>(orow + 32 * k);
+                if (lane == 0) bulk_wait_read0();   // the previous box has left the staging buffer
+                __syncwarp();
 #pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                        pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                        pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                        pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                for (int v = 0; v < 8; ++v)
+                    *reinterpret_cast<uint4*>(stage + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+                        make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
+                                   pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
+                                   pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
+                                   pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
+                fence_async_smem();   // generic-proxy writes become visible to the TMA engine
+                __syncwarp();
+                if (lane == 0) {
+                    tma_store_2d(&mO, (D / 2) * hh + 64 * k, orow0, stage_s);
+                    bulk_commit();
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -1124,6 +875,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
             l_p = l;
         }
         if (ok && my_items > 0) (void)epilogue(my_items - 1, bh_p, qt_p, l_p, g - 1);
+        if (lane == 0) bulk_wait0();   // the output stores have completed
+        __syncwarp();
     }
     tc_fence_before();
     // neither CTA leaves while its peer may still read its shared memory or TMEM (MMA operands),
@@ -1169,80 +922,58 @@ int launch_attn(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap&
     return launch_pdl(attn_fwd_kernel<D>, dim3(static_cast<unsigned>(static_cast<int64_t>(args.BH) * args.S / kAttnQ)), dim3(kAttnThreads), attn_launch_smem<D>(), st, 1, mQ, mK, mV, args);
 }
 
+// Sets the persistent kernel's shared-memory attribute once per device and returns (through *n)
+// how many of its clusters can be resident at once.
 template <int D>
-int pair_attr() {
-    static std::mutex mu;
-    static bool done[64] = {false};
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return record_cuda_error(e);
-    if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
-    std::lock_guard<std::mutex> lock(mu);
-    if (!done[dev]) {
-        e = cudaFuncSetAttribute(attn_pair_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(PairLayout<D>::SMEM));
-        if (e != cudaSuccess) return record_cuda_error(e);
-        done[dev] = true;
-    }
-    return FUSE_OK;
-}
-
-// 2-SM kernel: one cluster of two CTAs per pair of adjacent query tiles
-template <int D>
-int launch_pair(const void* q, const void* k, const void* v, const AttnArgs& args, cudaStream_t st) {
-    const int rc = pair_attr<D>();
-    if (rc != FUSE_OK) return rc;
-    const int64_t rows = static_cast<int64_t>(args.BH) * args.S;
-    CUtensorMap mQ, mKh, mV;
-    if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mKh, k, rows, D, 64, kAttnK / 2, true) ||
-        !make_map(&mV, v, rows, D, 64, kAttnK, true))
-        return FUSE_ECUDA;
-    return launch_pdl(attn_pair_kernel<D>, dim3(static_cast<unsigned>(rows / kAttnQ)), dim3(kAttnThreads), PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, args);
-}
-
-// Persistent 2-SM kernel: as many clusters as can be resident (at most one per tile pair).
-template <int D>
-int launch_persist(const void* q, const void* k, const void* v, const AttnArgs& args, cudaStream_t st) {
+int persist_setup(int* n_out) {
     static std::mutex mu;
     static int clusters[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return record_cuda_error(e);
     if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
-    {
-        std::lock_guard<std::mutex> lock(mu);
-        if (clusters[dev] == 0) {
-            e = cudaFuncSetAttribute(attn_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     static_cast<int>(PairLayout<D>::SMEM));
-            if (e != cudaSuccess) return record_cuda_error(e);
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
-            cfg.blockDim = dim3(kPersistThreads);
-            cfg.dynamicSmemBytes = PairLayout<D>::SMEM;
-            cudaLaunchAttribute attrs[1];
-            attrs[0].id = cudaLaunchAttributeClusterDimension;
-            attrs[0].val.clusterDim.x = 2;
-            attrs[0].val.clusterDim.y = 1;
-            attrs[0].val.clusterDim.z = 1;
-            cfg.attrs = attrs;
-            cfg.numAttrs = 1;
-            int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, attn_persist_kernel<D>, &cfg) != cudaSuccess || n < 1) {
-                (void)cudaGetLastError();
-                n = sm_count() / 2;
-            }
-            clusters[dev] = n;
+    std::lock_guard<std::mutex> lock(mu);
+    if (clusters[dev] == 0) {
+        e = cudaFuncSetAttribute(attn_persist_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(PairLayout<D>::SMEM));
+        if (e != cudaSuccess) return record_cuda_error(e);
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
+        cfg.blockDim = dim3(kPersistThreads);
+        cfg.dynamicSmemBytes = PairLayout<D>::SMEM;
+        cudaLaunchAttribute attrs[1];
+        attrs[0].id = cudaLaunchAttributeClusterDimension;
+        attrs[0].val.clusterDim.x = 2;
+        attrs[0].val.clusterDim.y = 1;
+        attrs[0].val.clusterDim.z = 1;
+        cfg.attrs = attrs;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, attn_persist_kernel<D>, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = sm_count() / 2;
         }
+        clusters[dev] = n;
     }
+    *n_out = clusters[dev];
+    return FUSE_OK;
+}
+
+// Persistent 2-SM kernel: as many clusters as can be resident (at most one per tile pair).
+template <int D>
+int launch_persist(const void* q, const void* k, const void* v, const AttnArgs& args, cudaStream_t st) {
+    int resident = 0;
+    const int rc = persist_setup<D>(&resident);
+    if (rc != FUSE_OK) return rc;
     const int64_t rows = static_cast<int64_t>(args.BH) * args.S;
     const int64_t items = rows / kAttnQ / 2;
-    const int ncl = static_cast<int>(items < clusters[dev] ? items : clusters[dev]);
-    CUtensorMap mQ, mKh, mV;
+    const int ncl = static_cast<int>(items < resident ? items : resident);
+    CUtensorMap mQ, mKh, mV, mO;
     if (!make_map(&mQ, q, rows, D, 64, kAttnQ, true) || !make_map(&mKh, k, rows, D, 64, kAttnK / 2, true) ||
-        !make_map(&mV, v, rows, D, 64, kAttnK, true))
+        !make_map(&mV, v, rows, D, 64, kAttnK, true) || !make_map(&mO, args.O, rows, D, 64, 32, true))
         return FUSE_ECUDA;
     return launch_pdl(attn_persist_kernel<D>, dim3(2 * static_cast<unsigned>(ncl)), dim3(kPersistThreads),
-                      PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, args);
+                      PairLayout<D>::SMEM, st, 2, mQ, mKh, mV, mO, args);
 }
 
 template <int D>
@@ -1274,11 +1005,12 @@ bool overlap(const void* a, const void* b, int64_t bytes) {
 int attn_report_count() { return 1; }
 int attn_report(int i, fuse_kernel_record* out) {
     if (i != 0) return FUSE_EINVAL;
-    const int rc = pair_attr<256>();
+    int resident = 0;
+    const int rc = persist_setup<256>(&resident);
     if (rc != FUSE_OK) return rc;
-    const int r2 = describe_kernel((const void*)attn_pair_kernel<256>,
-                                   "attn_pair_kernel<D=256> (tcgen05 2-SM, M=256)", kAttnThreads,
-                                   static_cast<int>(PairLayout<256>::SMEM), out);
+    const int r2 = describe_kernel((const void*)attn_persist_kernel<256>,
+                                   "attn_persist_kernel<D=256> (tcgen05 2-SM, M=256, persistent)",
+                                   kPersistThreads, static_cast<int>(PairLayout<256>::SMEM), out);
     if (r2 == FUSE_OK) out->cluster_size = 2;
     return r2;
 }

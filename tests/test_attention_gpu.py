@@ -61,6 +61,21 @@ def test_small_shapes_every_row(cuda_device, shape):
     assert np.array_equal(o[:, 0], v[:, 0])
 
 
+@pytest.mark.parametrize("shape", [(160, 256, 128), (97, 512, 256)])
+def test_more_tile_pairs_than_resident_clusters(cuda_device, shape):
+    """More (slice, tile pair) items than clusters fit on the GPU (~74): each cluster walks
+    several items of different lengths, and the counts per cluster are uneven.  The first, second
+    and last rows of every 128-row tile and a few random rows are checked in every slice."""
+    bh, S, D = shape
+    q, k, v = wl.attention_input(bh, S, D, salt=7 * S + D)
+    scale = 1.0 / np.sqrt(D)
+    o = _run(q, k, v, scale)
+    t0 = np.arange(0, S, 128)
+    rows = np.unique(np.concatenate([t0, t0 + 1, t0 + 127, np.random.default_rng(S).integers(0, S, 4)]))
+    _check(o[:, rows], oracle.attention(q, k, v, scale, rows=rows), v, rows)
+    assert np.array_equal(o[:, 0], v[:, 0])
+
+
 def test_full_size_sampled_rows(cuda_device):
     """[128, 2048, 256] as benchmarked: the GPU computes all of O; rows at tile edges, first,
     last and random are compared in every slice."""
