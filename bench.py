@@ -374,15 +374,18 @@ def run_ours(args, rank, world, local):
                 nb = 4 if M < 128 else 1   # decode: rotate 4 weight copies (128 MiB > L2 share)
                 Bs = [B] + [B.clone() for _ in range(nb - 1)]
                 Ys = [torch.empty(M, gN, dtype=torch.float16, device=dev) for _ in range(2)]
-                gemm_bufs[M] = (A, Bs, bias, Rr, Ys, rotating(nb), rotating(2))
+                # split-K workspace for the last wave of tiles (zero-filled once, reused)
+                gws = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, gN, gK)), dtype=torch.uint8, device=dev)
+                gemm_bufs[M] = (A, Bs, bias, Rr, Ys, rotating(nb), rotating(2), gws)
 
         def gemm(M, mask):
-            A, Bs, bias, Rr, Ys, brot, yrot = gemm_bufs[M]
+            A, Bs, bias, Rr, Ys, brot, yrot, gws = gemm_bufs[M]
 
             def fn():
                 b, y = Bs[brot()], Ys[yrot()]
-                check(lib.fuse_gemm_epilogue_plan(A.data_ptr(), b.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
-                                                  y.data_ptr(), M, gN, gK, mask, sh), "fuse_gemm_epilogue_plan")
+                check(lib.fuse_gemm_epilogue_ws(A.data_ptr(), b.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
+                                                y.data_ptr(), M, gN, gK, mask, gws.data_ptr(), gws.numel(), sh),
+                      "fuse_gemm_epilogue_ws")
                 counter["launches"] += 1 + bin(mask).count("1")
             return fn
         flops = {M: 2 * M * gN * gK for M in wl.GEMM_MS}
@@ -667,7 +670,7 @@ def launch_graph_rows(fc, lib, wl, torch, dev, gemm16, check):
     K, n = len(a), x0.size
     x = torch.from_numpy(x0).to(dev)
     y = torch.empty_like(x)
-    A, Bs, bias, Rr, Ys, _, _ = gemm16
+    A, Bs, bias, Rr, Ys, _, _, _ = gemm16
 
     def chain(mode, xx=x, yy=y):
         return lambda: check(lib.fuse_chain_run(st, K, xx.data_ptr(), yy.data_ptr(), n, fc.FUSE_F32,
@@ -1006,9 +1009,12 @@ def run_profile(args):
         M = args.size or 4096
         A, B, bias, Rr = wl.gemm_input(M, device=dev)
         Ys = [torch.empty(M, wl.GEMM_N, dtype=torch.float16, device=dev) for _ in range(2)]
+        gws = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, wl.GEMM_N, wl.GEMM_K)), dtype=torch.uint8,
+                          device=dev)
         for i in range(L):
-            rc = lib.fuse_gemm_epilogue_plan(A.data_ptr(), B.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
-                                             Ys[i % 2].data_ptr(), M, wl.GEMM_N, wl.GEMM_K, args.mask, stream)
+            rc = lib.fuse_gemm_epilogue_ws(A.data_ptr(), B.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
+                                           Ys[i % 2].data_ptr(), M, wl.GEMM_N, wl.GEMM_K, args.mask,
+                                           gws.data_ptr(), gws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_gemm_bytes(M, wl.GEMM_N, wl.GEMM_K, args.mask)
     else:

@@ -68,6 +68,8 @@ SIGNATURES = {
     "fuse_causal_softmax_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "fuse_gemm_epilogue": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _P], _I32),
     "fuse_gemm_epilogue_plan": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P], _I32),
+    "fuse_gemm_epilogue_ws": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I32),
+    "fuse_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "fuse_gemm_bytes": ([_I64, _I64, _I64, _U32], _I64),
     "fuse_ledger": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_ledger_t)], _I32),
     "fuse_plan_time": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_cost_model),
@@ -271,16 +273,24 @@ def fuse_causal_softmax(s, p, scale: float, skip_tile: int = 0, mode: int = FUSE
                                    _stream(stream)), "fuse_causal_softmax")
 
 
-def fuse_gemm_epilogue(A, B, bias, R, Y, cut_mask: int = 0, stream=None) -> None:
+def fuse_gemm_epilogue(A, B, bias, R, Y, cut_mask: int = 0, workspace=None, stream=None) -> None:
     """Y = fp16(GELU(A @ B + bias) + R) for fp16 A [M,K], B [K,N], bias [N], R, Y [M,N]; cut_mask
-    selects the plan (0 = fully fused [4]; 7 = [1,1,1,1])."""
+    selects the plan (0 = fully fused [4]; 7 = [1,1,1,1]).  workspace: optional zero-filled device
+    tensor of fuse_gemm_workspace_bytes(M, N, K) bytes (see fuse_gemm_epilogue_ws in the header),
+    reused across calls on one stream."""
     _need_device(A, B, bias, R, Y)
     M, K = A.shape
     K2, N = B.shape
     if K != K2 or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N) or bias.numel() != N:
         raise ValueError("shape mismatch")
-    _check(_load().fuse_gemm_epilogue_plan(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(Y), M, N, K,
-                                           int(cut_mask), _stream(stream)), "fuse_gemm_epilogue")
+    ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(_load().fuse_gemm_epilogue_ws(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(Y), M, N, K,
+                                         int(cut_mask), _ptr(workspace), ws_size, _stream(stream)),
+           "fuse_gemm_epilogue")
+
+
+def fuse_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
+    return _load().fuse_gemm_workspace_bytes(M, N, K)
 
 
 def fuse_gemm_bytes(M: int, N: int, K: int, cut_mask: int) -> int:

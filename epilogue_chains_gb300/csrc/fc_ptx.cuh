@@ -73,6 +73,43 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     return true;
 }
 
+// Global-memory flags between CTAs of one grid (all co-resident): a release store after the
+// writer's data, an acquire load before the reader's.
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_gpu(const int* p) {
+    int v;
+    asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// Wait until *p == want, for at most `budget` SM cycles (then the watchdog flag is set and false
+// returned, as for mbar_wait_bounded).  Spins on the load: the waits it serves last microseconds,
+// below the wake-up granularity of a sleep.
+__device__ __forceinline__ bool flag_wait_bounded(const int* p, int want, int* flag,
+                                                  long long budget = kWaitBudget) {
+    if (ld_acquire_gpu(p) == want) return true;
+    const long long t0 = clock64();
+    uint32_t spins = 0;
+    while (ld_relaxed_gpu(p) != want) {
+        if (++spins % 8u != 0u) continue;
+        const long long dt = clock64() - t0;
+        if (dt > kFlagPollAfter && *reinterpret_cast<volatile int*>(flag) != 0) return false;
+        if (dt > budget) {
+            atomicExch(flag, 1);
+            return false;
+        }
+    }
+    fence_acq_rel_gpu();   // with the relaxed load that saw `want`: an acquire of the writer's release
+    return true;
+}
+
 // Drain wait after a failure: the copies or MMAs this CTA already issued must land before its
 // shared memory and TMEM are released, whatever other CTAs reported, so the watchdog flag is not
 // consulted; only the time budget bounds the wait.  Returns false if it ran out.

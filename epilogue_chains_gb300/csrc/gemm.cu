@@ -29,6 +29,7 @@
 #include <cudaTypedefs.h>
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "fc_internal.cuh"
@@ -57,44 +58,66 @@ constexpr uint32_t B_STAGE = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of th
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_STAGE;
-// barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain[1]
-constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 1;
+// barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], part_written, part_read, drain
+constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 2 + 1;
 constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
-constexpr uint32_t MAIN_SMEM = OFF_HOLD + 16 + 1024;  // + alignment slack
+// epilogue staging: per epilogue warp one 32-row x 128-byte tile (16-byte chunk j of row r at
+// slot j ^ (r % 8)), through which it transposes between its row-per-lane TMEM layout and
+// coalesced global accesses
+constexpr uint32_t STAGE_WARP = 32 * 128;
+constexpr uint32_t OFF_STAGE = (OFF_HOLD + 16 + 127) / 128 * 128;
+constexpr uint32_t MAIN_SMEM = OFF_STAGE + kEpiWarps * STAGE_WARP + 1024;  // + alignment slack
+static_assert(MAIN_SMEM <= 232448, "shared-memory budget");
 constexpr uint32_t TMEM_COLS = 2 * BN;
 
 struct MainArgs {
     int M, N, K;
     int pair_rows;       // ceil(tiles_m / 2): a CTA pair covers two adjacent 128-row tiles
     int tiles_n;
-    int full_units;      // pair tiles processed whole; each later one is split into 128-wide halves
-    int units;           // full_units + 2 * (pair tiles - full_units)
+    int full_units;      // pair tiles computed over the whole K by one pair
+    int units;           // full_units + 2 * (split tiles): each later tile is split over K in two
+    int nk_split;        // first k-block of the second K half of a split tile
     int epi;             // last stage applied in this kernel: 0 (C), 1 (C'), 2 (C''), 3 (Y)
     const __half* bias;
     const __half* R;
     __half* Y;
+    float* part;         // split tiles: exchanged fp32 partial sums, [slot][rank] x 128 x 256
+    int* ready;          // split tiles: [slot][rank][column half] = epoch once that half is written
+    int epoch;           // this call's tag for `ready` (never 0)
     int* flag;
 };
 
 // Work unit u of a CTA pair -> output rows [m0, m0+128) of this CTA (rank r of the pair takes the
-// r-th of two adjacent 128-row tiles), columns [n0, n0+bn) shared by the pair.  The first
-// full_units units are whole 256-wide pair tiles; the pair tiles of the last, partial wave are
-// split into 128-wide halves so that the wave spreads over more SMs (wave quantisation: 256 pair
-// tiles on 76 pairs would otherwise leave a third of the SMs idle for the last tile time).
+// r-th of two adjacent 128-row tiles), columns [n0, n0+256) shared by the pair, k-blocks
+// [kb0, kb1).  The first full_units units are whole pair tiles; the pair tiles of the last,
+// partial wave are split over K into two units (part 0: the first half of K, part 1: the second),
+// which exchange fp32 partial sums through global memory, each finishing one column half of the
+// tile (part p adds the other part's sums of columns 128p..128p+127 and applies the epilogue
+// there, with all eight epilogue warps), so that the wave spreads over twice as many SMs (wave quantisation: 256 pair tiles on 76 pairs
+// would otherwise leave two thirds of the SMs idle for the last tile time).  Splitting N instead
+// does not help: an M = 256, N = 128 MMA takes as long as an N = 256 one on this hardware.
 struct Unit {
-    int m0, n0, bn;
+    int m0, n0, kb0, kb1;
+    int part;   // -1: whole tile; 0 or 1: K half of a split tile
+    int slot;   // split tile index
 };
-__device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank) {
+__device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank, int nk) {
     Unit r;
     int t = u;
-    int half = -1;
+    r.part = -1;
+    r.slot = 0;
+    r.kb0 = 0;
+    r.kb1 = nk;
     if (u >= a.full_units) {
-        t = a.full_units + (u - a.full_units) / 2;
-        half = (u - a.full_units) % 2;
+        const int s = u - a.full_units;
+        t = a.full_units + s / 2;
+        r.slot = s / 2;
+        r.part = s % 2;
+        r.kb0 = r.part ? a.nk_split : 0;
+        r.kb1 = r.part ? nk : a.nk_split;
     }
     r.m0 = (2 * (t % a.pair_rows) + static_cast<int>(rank)) * BM;
-    r.n0 = (t / a.pair_rows) * BN + (half > 0 ? BN / 2 : 0);
-    r.bn = half < 0 ? BN : BN / 2;
+    r.n0 = (t / a.pair_rows) * BN;
     return r;
 }
 
@@ -112,6 +135,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (N_BARS - 1);
+    // the eight epilogue warps of a split unit have written (read) the exchanged partial sums
+    const uint32_t part_written = bar0 + 8u * (N_BARS - 3), part_read = bar0 + 8u * (N_BARS - 2);
     const uint32_t holder = base + OFF_HOLD;
     const int total_units = args.units;
     const int nk = (args.K + BK - 1) / BK;
@@ -120,8 +145,11 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     const int cid = blockIdx.x / 2;            // CTA pair (cluster) index
     const int nclusters = gridDim.x / 2;
     // k-blocks this pair runs in all (both CTAs run the same sequence)
-    const int my_units = cid < total_units ? (total_units - cid + nclusters - 1) / nclusters : 0;
-    const int total_kb = my_units * nk;
+    int total_kb = 0;
+    for (int u = cid; u < total_units; u += nclusters) {
+        const Unit w = unit_of(u, args, rank, nk);
+        total_kb += w.kb1 - w.kb0;
+    }
 
     // The even CTA of the pair (rank 0) issues the MMAs.  Its full barriers count the bytes both
     // CTAs load for a stage; every CTA's empty and accumulator-full barriers are signalled by the
@@ -138,6 +166,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
             mbar_init(acce_bar(b), 2 * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(part_written, kEpiWarps);
+        mbar_init(part_read, kEpiWarps);
         fence_mbar_init();
         prefetch_map(&mapA);
         prefetch_map(&mapB);
@@ -155,21 +185,20 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         uint32_t phase = 0, inflight = 0, issue_par = 0;
         bool ok = true;
         for (int u = cid; u < total_units && ok; u += nclusters) {
-            const Unit w = unit_of(u, args, rank);
-            for (int kb = 0; kb < nk; ++kb) {
+            const Unit w = unit_of(u, args, rank, nk);
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 // the stage is free in both CTAs (each MMA commit arrives on both empty barriers)
                 if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
                 inflight &= ~(1u << stage);  // its previous load was consumed
                 if (lane == 0) {
                     // this CTA's 128 rows of A and its half of the B tile's columns; both CTAs'
                     // bytes complete on the leader's full barrier
-                    const int half_boxes = w.bn / 128;
-                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_STAGE + half_boxes * B_BOX));
+                    if (leader) mbar_arrive_expect_tx(full_bar(stage), 2 * (A_STAGE + B_STAGE));
                     const uint32_t full_cl = mapa_shared(full_bar(stage), 0);
                     tma_load_2d_pair(base + OFF_A + stage * A_STAGE, &mapA, kb * BK, w.m0, full_cl);
-                    for (int j = 0; j < half_boxes; ++j)
+                    for (int j = 0; j < B_STAGE / B_BOX; ++j)
                         tma_load_2d_pair(base + OFF_B + stage * B_STAGE + j * B_BOX, &mapB,
-                                         w.n0 + static_cast<int>(rank) * (w.bn / 2) + 64 * j, kb * BK, full_cl);
+                                         w.n0 + static_cast<int>(rank) * (BN / 2) + 64 * j, kb * BK, full_cl);
                 }
                 inflight |= 1u << stage;
                 issue_par = (issue_par & ~(1u << stage)) | (phase << stage);
@@ -182,18 +211,17 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         }
     } else if (warp == 1 && leader) {
         // ------------------------------------------------------------ MMA issuer
-        constexpr uint32_t idesc_full = idesc_f16(2 * BM, BN, false, true);
-        constexpr uint32_t idesc_half = idesc_f16(2 * BM, BN / 2, false, true);
+        constexpr uint32_t idesc = idesc_f16(2 * BM, BN, false, true);
         int stage = 0, acc = 0;
         uint32_t phase = 0, acc_phase = 0;
         bool ok = true, issued = false;
         int kg = 0;  // k-blocks issued so far by this CTA (the same sequence in both CTAs)
         for (int u = cid; u < total_units && ok; u += nclusters) {
-            const uint32_t idesc = unit_of(u, args, rank).bn == BN ? idesc_full : idesc_half;
+            const Unit w = unit_of(u, args, rank, nk);
             if (!mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, flag)) { ok = false; break; }
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + acc * BN;
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = w.kb0; kb < w.kb1; ++kb) {
                 if (!mbar_wait_bounded(full_bar(stage), phase, flag)) { ok = false; break; }
                 tc_fence_after();
                 if (lane == 0) {
@@ -207,7 +235,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                         // apart (SBO); +16 rows (2048 B) per K=16 step; the peer's half sits at
                         // the same offsets in its shared memory
                         const uint64_t bd = smem_desc_sw128(b0 + 2048u * k, B_BOX, 1024u);
-                        tc_mma_pair(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        tc_mma_pair(d_tmem, ad, bd, idesc, (kb > w.kb0 || k > 0) ? 1u : 0u);
                     }
                     // frees the stage in both CTAs once these MMAs are done -- unless no later load
                     // uses it
@@ -231,73 +259,187 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     } else if (warp >= 2) {
         // ------------------------------------------------------------ epilogue (warps 2-9)
         // Warp w drains TMEM lane quadrant q = w % 4 (rows 32q..32q+31 of the unit) and one half
-        // of the unit's 32-column chunks.  Each thread owns one row: it prefetches its residual
-        // row segment for the next chunk into registers while it computes the current one, and
-        // writes its 32 fp16 results with 16-byte stores straight from registers (no shared
-        // memory staging, so no store read-back or load round trip sits between chunks).
-        constexpr int CH = 32;
+        // of the unit's 64-column chunks; after tcgen05.ld each thread holds one row.  Global
+        // memory is accessed coalesced (8 lanes per 128-byte row segment, 4 rows per instruction)
+        // and transposed through the warp's staging tile: the residual chunk is loaded that way
+        // one chunk ahead, written to the tile and read back by rows; the fp16 results are
+        // written to the tile by rows and stored by row segments.
+        // Split tiles: the first K half stores its raw fp32 sums (`part`) the same way and
+        // publishes them with a release store of the call's epoch into `ready`; the second K half
+        // waits for that epoch (acquire), adds the partial sums and applies the epilogue, then
+        // clears `ready` for the next call.
+        constexpr int CH = 64;
+        constexpr int PER = (BN / CH) / 2;   // chunks of each warp per unit
         const int q = warp % 4;
         const int h = (warp - 2) / 4;
         const bool need_r = args.epi >= 3;
+        uint8_t* stage = gbase + OFF_STAGE + (warp - 2) * STAGE_WARP;
+        const int cr = lane / 8, cj = lane % 8;   // coalesced layout: row cr + 4 i, 16-byte chunk cj
+        auto st_row = [&](int r, int j, const uint4& v) {
+            *reinterpret_cast<uint4*>(stage + r * 128 + ((j ^ (r & 7)) * 16)) = v;
+        };
+        auto ld_row = [&](int r, int j) {
+            return *reinterpret_cast<const uint4*>(stage + r * 128 + ((j ^ (r & 7)) * 16));
+        };
         int acc = 0;
         uint32_t acc_phase = 0;
         bool ok = true;
-        uint4 rnext[CH / 8];
-        auto load_r = [&](int u, int cc) {  // this thread's residual segment of chunk cc of unit u
-            const Unit w = unit_of(u, args, rank);
-            const int per = (w.bn / CH) / 2;
-            const int row = w.m0 + 32 * q + lane;
-            const int col = w.n0 + CH * (h * per + cc);
+        uint4 rnext[8];
+        // The chunks of a unit this warp handles, in order: whole tiles: 2h and 2h + 1 (both
+        // finished here); split tiles (part p): first chunk 2(1 - p) + h, whose raw sums it hands
+        // to the other part, then chunk 2p + h, which it finishes with the other part's sums --
+        // so all eight warps of both pairs share the split tile's epilogue.
+        auto chunk_of = [&](const Unit& w, int cc) {
+            return w.part < 0 ? h * PER + cc : (cc == 0 ? 2 * (1 - w.part) + h : 2 * w.part + h);
+        };
+        auto first_r_chunk = [&](const Unit& w) { return w.part < 0 ? h * PER : 2 * w.part + h; };
+        auto load_r = [&](int u, int c) {  // residual chunk c of unit u, coalesced layout
+            const Unit w = unit_of(u, args, rank, nk);
+            const int col = w.n0 + CH * c + 8 * cj;
 #pragma unroll
-            for (int j = 0; j < CH / 8; ++j) {
-                rnext[j] = make_uint4(0, 0, 0, 0);
-                if (row < args.M && col + 8 * j < args.N)
-                    rnext[j] = __ldcs(reinterpret_cast<const uint4*>(args.R + static_cast<int64_t>(row) * args.N + col + 8 * j));
+            for (int i = 0; i < 8; ++i) {
+                const int row = w.m0 + 32 * q + cr + 4 * i;
+                rnext[i] = make_uint4(0, 0, 0, 0);
+                if (row < args.M && col < args.N)
+                    rnext[i] = __ldcs(reinterpret_cast<const uint4*>(args.R + static_cast<int64_t>(row) * args.N + col));
             }
         };
-        if (need_r && cid < total_units) load_r(cid, 0);
+        // Partial-sum tile of a split unit (one per slot and CTA rank, 128 x 256 fp32), laid out
+        // for rows held one per lane: float4 j (columns 4j..4j+3) of 32-column group g of this
+        // warp's row `lane` sits at [q][g][j][lane], so a warp instruction covers 512 contiguous
+        // bytes both when one part writes it and when the other reads it.
+        auto part_at = [&](const Unit& w, int g, int j) {
+            return reinterpret_cast<float4*>(args.part) +
+                   (((static_cast<int64_t>(w.slot * 2 + static_cast<int>(rank)) * 4 + q) * 8 + g) * 8 + j) * 32 + lane;
+        };
+        // ready word of column half x of a split tile: set by the part that writes that half
+        auto ready_word = [&](const Unit& w, int x) {
+            return args.ready + (w.slot * 2 + static_cast<int>(rank)) * 2 + x;
+        };
+        if (need_r && cid < total_units) load_r(cid, first_r_chunk(unit_of(cid, args, rank, nk)));
         for (int u = cid; u < total_units && ok; u += nclusters) {
-            const Unit w = unit_of(u, args, rank);
-            const int per = (w.bn / CH) / 2;   // chunks of this warp: 4 (full unit) or 2 (half)
+            const Unit w = unit_of(u, args, rank, nk);
+            const bool split = w.part >= 0;
+            // the bias values of the chunks this warp finishes, four per lane (lanes 16k..16k+15:
+            // its k-th finished chunk), fetched while the unit's MMAs run and handed to every lane
+            // by shuffles, so no load latency sits in the element loop
+            uint2 bl = make_uint2(0, 0);
+            {
+                const int k = lane / 16;
+                const int c = split ? 2 * w.part + h : h * PER + k;
+                const int col = w.n0 + CH * c + 4 * (lane % 16);
+                if (args.epi >= 1 && (!split || k == 0) && col < args.N)
+                    bl = __ldg(reinterpret_cast<const uint2*>(args.bias + col));
+            }
             if (!mbar_wait_bounded(accf_bar(acc), acc_phase, flag)) { ok = false; break; }
             tc_fence_after();
-            const int row = w.m0 + 32 * q + lane;
-            for (int cc = 0; cc < per; ++cc) {
-                const int c = h * per + cc;
-                uint4 rcur[CH / 8];
-#pragma unroll
-                for (int j = 0; j < CH / 8; ++j) rcur[j] = rnext[j];
-                if (need_r) {  // next chunk of this warp: same unit, or the first of the next unit
-                    if (cc + 1 < per) load_r(u, cc + 1);
-                    else if (u + nclusters < total_units) load_r(u + nclusters, 0);
-                }
-                float v[CH];
-                tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c, v);
-                tmem_ld_wait();
-                if (cc == per - 1) {  // this warp is done with the accumulator buffer
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));   // the leader's
-                }
+            for (int cc = 0; cc < PER; ++cc) {
+                const int c = chunk_of(w, cc);
+                const bool writer = split && cc == 0;   // hands this chunk's sums to the other part
+                const bool reader = split && cc == 1;   // adds the other part's sums of this chunk
+                const int bslot = split ? 0 : cc;       // which 16 lanes hold this chunk's bias
                 const int ncol0 = w.n0 + CH * c;
-                __half* yrow = args.Y + static_cast<int64_t>(row) * args.N + ncol0;
+                if (writer) {
+                    // raw partial sums of the chunk for the other part; then publish this half
+                    // once all eight warps have written theirs
+#pragma unroll 1
+                    for (int g = 0; g < 2; ++g) {
+                        float v[32];
+                        tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
+                        tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < CH / 8; ++j) {
-                    float bv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    const bool in_n = ncol0 + 8 * j < args.N;
-                    if (args.epi >= 1 && in_n)
-                        unpack_h8(__ldg(reinterpret_cast<const uint4*>(args.bias + ncol0 + 8 * j)), bv);
-                    float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                    if (need_r) unpack_h8(rcur[j], rv);
-                    float o[8];
-#pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const float2 r2 = apply_stages2(make_float2(v[8 * j + e], v[8 * j + e + 1]), 1, args.epi,
-                                                        make_float2(bv[e], bv[e + 1]), make_float2(rv[e], rv[e + 1]));
-                        o[e] = r2.x;
-                        o[e + 1] = r2.y;
+                        for (int j = 0; j < 8; ++j)
+                            __stcg(part_at(w, 2 * c + g, j), make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
                     }
-                    if (row < args.M && in_n) __stcs(reinterpret_cast<uint4*>(yrow + 8 * j), pack_h8(o));
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(part_written);
+                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_written, 0, flag)) {
+                        __threadfence();
+                        st_release_gpu(ready_word(w, 1 - w.part), args.epoch);
+                    }
+                    __syncwarp();
+                    continue;
+                }
+                if (reader) {   // the other part's sums of this column half are complete
+                    if (!__all_sync(0xffffffffu, flag_wait_bounded(ready_word(w, w.part), args.epoch, flag))) {
+                        ok = false;
+                        break;
+                    }
+                }
+                // the residual chunk into the staging tile (each thread then reads its own row's
+                // segments there and overwrites each with its result); then the next chunk's load
+                if (need_r) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) st_row(cr + 4 * i, cj, rnext[i]);
+                    __syncwarp();
+                    if (!split && cc + 1 < PER) load_r(u, chunk_of(w, cc + 1));
+                    else if (u + nclusters < total_units) load_r(u + nclusters, first_r_chunk(unit_of(u + nclusters, args, rank, nk)));
+                }
+                // two 32-column halves of the chunk, one tcgen05.ld each
+#pragma unroll 1
+                for (int g = 0; g < 2; ++g) {
+                    float v[32];
+                    tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
+                    tmem_ld_wait();
+                    if (cc == PER - 1 && g == 1) {  // this warp is done with the accumulator buffer
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));   // the leader's
+                    }
+                    if (reader) {   // add the other part's partial sums
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) {
+                            const float4 t = __ldcg(part_at(w, 2 * c + g, j));
+                            v[4 * j] += t.x;
+                            v[4 * j + 1] += t.y;
+                            v[4 * j + 2] += t.z;
+                            v[4 * j + 3] += t.w;
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float bv[8];
+                        {
+                            const int src = 16 * bslot + (32 * g + 8 * j) / 4;   // lane holding these columns
+                            uint4 b8;
+                            b8.x = __shfl_sync(0xffffffffu, bl.x, src);
+                            b8.y = __shfl_sync(0xffffffffu, bl.y, src);
+                            b8.z = __shfl_sync(0xffffffffu, bl.x, src + 1);
+                            b8.w = __shfl_sync(0xffffffffu, bl.y, src + 1);
+                            unpack_h8(b8, bv);
+                        }
+                        float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if (need_r) unpack_h8(ld_row(lane, 4 * g + j), rv);
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 r2 = apply_stages2(make_float2(v[8 * j + e], v[8 * j + e + 1]), 1, args.epi,
+                                                            make_float2(bv[e], bv[e + 1]), make_float2(rv[e], rv[e + 1]));
+                            o[e] = r2.x;
+                            o[e + 1] = r2.y;
+                        }
+                        st_row(lane, 4 * g + j, pack_h8(o));
+                    }
+                }
+                __syncwarp();
+                {
+                    const int col = ncol0 + 8 * cj;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const int row = w.m0 + 32 * q + cr + 4 * i;
+                        const uint4 t = ld_row(cr + 4 * i, cj);
+                        if (row < args.M && col < args.N)
+                            __stcs(reinterpret_cast<uint4*>(args.Y + static_cast<int64_t>(row) * args.N + col), t);
+                    }
+                }
+                __syncwarp();
+                if (reader) {
+                    // all eight warps have read the other part's sums: clear the word for the
+                    // next call.  A split unit is the last unit of its pair and each pair gets at
+                    // most one, so part_written and part_read each complete their phase 0 once.
+                    if (lane == 0) mbar_arrive(part_read);
+                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_read, 0, flag)) *ready_word(w, w.part) = 0;
+                    __syncwarp();
                 }
             }
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
@@ -376,9 +518,29 @@ int max_active_pairs() {
     return cached[dev] > 0 ? cached[dev] : sm_count() / 2;
 }
 
-// GEMM + the stages 1..epi, fp16 result into Y
+// Split-K workspace: the ready words (one per split tile, CTA rank and column half, padded to
+// 1 KB), then the exchanged fp32 partial sums of the split tiles, 128 x 256 per CTA.
+constexpr int kSplitMaxTiles = 64;
+constexpr int64_t kSplitHeader = 1024;
+constexpr int64_t kSplitTileBytes = 2LL * BM * BN * 4;
+static_assert(2 * 2 * kSplitMaxTiles * 4 <= kSplitHeader, "ready words fit the header");
+
+int64_t split_ws_bytes(int tiles) {
+    const int t = tiles < kSplitMaxTiles ? tiles : kSplitMaxTiles;
+    return kSplitHeader + t * kSplitTileBytes;
+}
+
+// Tag of one call for the ready words: never 0, different from the tags of recent calls.
+int next_epoch() {
+    static std::atomic<unsigned> counter{0};
+    unsigned e = counter.fetch_add(1, std::memory_order_relaxed) % 0x7fffffffu;
+    return static_cast<int>(e) + 1;
+}
+
+// GEMM + the stages 1..epi, fp16 result into Y.  `ws` (ws_bytes, zero-filled before its first use)
+// lets the last, partial wave of tiles be split over K; without it that wave runs whole tiles.
 int launch_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
-                int64_t N, int64_t K, int epi, cudaStream_t st) {
+                int64_t N, int64_t K, int epi, void* ws, size_t ws_bytes, cudaStream_t st) {
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     CUtensorMap mA, mB;
@@ -398,11 +560,20 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     a.flag = flag;
     const int tiles = a.pair_rows * a.tiles_n;             // pair tiles (256 rows x 256 cols)
     const int pairs = max_active_pairs();
+    const int nk = static_cast<int>(ceil_div(K, BK));
+    // split the last, partial wave over K when its halves still fit in one wave (each pair then
+    // runs at most one split unit, its last) and the caller gave room for the partial sums
+    const int tail = tiles % pairs;
+    const bool split = tiles > pairs && tail != 0 && 2 * tail <= pairs && tail <= kSplitMaxTiles && nk >= 2 &&
+                       ws != nullptr && is_aligned(ws, 256) &&
+                       static_cast<int64_t>(ws_bytes) >= kSplitHeader + tail * kSplitTileBytes;
     const int clusters = tiles < pairs ? tiles : pairs;
-    // split the last, partial wave into half tiles when the halves still fit in one wave
-    const int tail = tiles % clusters;
-    a.full_units = (tail != 0 && 2 * tail <= clusters) ? tiles - tail : tiles;
+    a.full_units = split ? tiles - tail : tiles;
     a.units = a.full_units + 2 * (tiles - a.full_units);
+    a.nk_split = nk / 2;
+    a.ready = split ? static_cast<int*>(ws) : nullptr;
+    a.part = split ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSplitHeader) : nullptr;
+    a.epoch = split ? next_epoch() : 1;
     return launch_pdl(gemm_tc_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kMainThreads), MAIN_SMEM, st,
                       2, mA, mB, a);
 }
@@ -439,9 +610,9 @@ int gemm_report(int i, fuse_kernel_record* out) {
 
 }  // namespace fc
 
-extern "C" int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, const void* R,
-                                       void* Y, int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask,
-                                       fuse_stream_t stream) {
+extern "C" int fuse_gemm_epilogue_ws(const void* A, const void* B, const void* bias, const void* R, void* Y,
+                                     int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask, void* workspace,
+                                     size_t ws_bytes, fuse_stream_t stream) {
     using namespace fc;
     if (M < 0 || N < 0 || Kdim < 0 || cut_mask > 7u) return FUSE_EINVAL;
     if (M == 0 || N == 0) return FUSE_OK;
@@ -456,13 +627,20 @@ extern "C" int fuse_gemm_epilogue_plan(const void* A, const void* B, const void*
     if (overlap(Y, ybytes, A, M * Kdim * 2) || overlap(Y, ybytes, B, Kdim * N * 2) ||
         overlap(Y, ybytes, bias, N * 2) || overlap(Y, ybytes, R, M * N * 2))
         return FUSE_EINVAL;
+    if (workspace && ws_bytes > 0) {
+        const int64_t wb = static_cast<int64_t>(ws_bytes);
+        if (overlap(workspace, wb, Y, ybytes) || overlap(workspace, wb, A, M * Kdim * 2) ||
+            overlap(workspace, wb, B, Kdim * N * 2) || overlap(workspace, wb, bias, N * 2) ||
+            overlap(workspace, wb, R, M * N * 2))
+            return FUSE_EINVAL;
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // segments of the chain (stage 0 = mm, 1 = bias, 2 = gelu, 3 = residual)
     int first = 0;
     while (first < 4) {
         int last = first;
         while (last < 3 && !((cut_mask >> last) & 1u)) ++last;
-        const int rc = first == 0 ? launch_gemm(A, B, bias, R, Y, M, N, Kdim, last, st)
+        const int rc = first == 0 ? launch_gemm(A, B, bias, R, Y, M, N, Kdim, last, workspace, ws_bytes, st)
                                   : launch_tail(Y, bias, R, M, N, first, last, st);
         if (rc != FUSE_OK) return rc;
         first = last + 1;
@@ -470,9 +648,22 @@ extern "C" int fuse_gemm_epilogue_plan(const void* A, const void* B, const void*
     return FUSE_OK;
 }
 
+extern "C" int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, const void* R,
+                                       void* Y, int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask,
+                                       fuse_stream_t stream) {
+    return fuse_gemm_epilogue_ws(A, B, bias, R, Y, M, N, Kdim, cut_mask, nullptr, 0, stream);
+}
+
 extern "C" int fuse_gemm_epilogue(const void* A, const void* B, const void* bias, const void* R, void* Y,
                                   int64_t M, int64_t N, int64_t Kdim, fuse_stream_t stream) {
-    return fuse_gemm_epilogue_plan(A, B, bias, R, Y, M, N, Kdim, 0u, stream);
+    return fuse_gemm_epilogue_ws(A, B, bias, R, Y, M, N, Kdim, 0u, nullptr, 0, stream);
+}
+
+extern "C" size_t fuse_gemm_workspace_bytes(int64_t M, int64_t N, int64_t Kdim) {
+    using namespace fc;
+    if (M <= 64 || N <= 0 || Kdim <= 0) return 0;   // the decode kernel needs none
+    const int64_t tiles = ceil_div(ceil_div(M, BM), 2) * ceil_div(N, BN);
+    return static_cast<size_t>(split_ws_bytes(tiles > kSplitMaxTiles ? kSplitMaxTiles : static_cast<int>(tiles)));
 }
 
 extern "C" int64_t fuse_gemm_bytes(int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask) {

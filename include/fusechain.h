@@ -229,13 +229,29 @@ size_t fuse_causal_softmax_workspace_bytes(int64_t batch_heads, int64_t S, int m
  * (0 = mm, 1 = +bias, 2 = GELU): [1,1,1,1] = 7, [1,3] = 1, [2,2] = 2, [4] = 0; all 8 masks
  * are accepted.  Each cut stores the intermediate (C, C', C'') as fp16 in Y and the next kernel
  * reads it back in place, so the plan's DRAM traffic is fuse_gemm_bytes() and its numerics round
- * to fp16 exactly at the cuts.  No workspace is needed.
+ * to fp16 exactly at the cuts.  No workspace is needed (fuse_gemm_epilogue_ws() takes an optional
+ * one that balances the last wave of tiles).
  */
 int fuse_gemm_epilogue(const void* A, const void* B, const void* bias, const void* R, void* Y,
                        int64_t M, int64_t N, int64_t Kdim, fuse_stream_t stream);
 int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, const void* R, void* Y,
                             int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask,
                             fuse_stream_t stream);
+/* The same with a caller workspace (the library allocates nothing).  With it, when the tiles do
+ * not fill a whole number of waves of the persistent kernel and the last, partial wave would leave
+ * at least half of the SM pairs idle, each tile of that wave is split over K between two SM pairs,
+ * which exchange fp32 partial sums through the workspace and each apply the epilogue to one half of
+ * the tile's columns.  Results equal the unsplit kernel's up to fp32 summation order.
+ *   workspace  device memory of at least fuse_gemm_workspace_bytes(M, N, Kdim) bytes, 256-byte
+ *              aligned, zero-filled before its first use (every completed call leaves it so);
+ *              not shared with a call that may run at the same time.  NULL, or smaller, or
+ *              misaligned: no split (still correct).  Must not overlap any operand (FUSE_EINVAL).
+ */
+int fuse_gemm_epilogue_ws(const void* A, const void* B, const void* bias, const void* R, void* Y,
+                          int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask, void* workspace,
+                          size_t ws_bytes, fuse_stream_t stream);
+/* Workspace bytes for fuse_gemm_epilogue_ws (0 when no split can apply, e.g. M <= 64). */
+size_t fuse_gemm_workspace_bytes(int64_t M, int64_t N, int64_t Kdim);
 /* [K4] §① traffic of a plan, in bytes: 2 * (M*K + K*N + N + 2*M*N + 2*cuts*M*N). */
 int64_t fuse_gemm_bytes(int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask);
 

@@ -64,14 +64,21 @@ def _dev(bits, shape=None):
     return t if shape is None else t.view(*shape)
 
 
-def _run(A, B, bias, R, mask):
+def _run(A, B, bias, R, mask, ws=False, workspace=None):
+    """ws: pass a zero-filled split-K workspace (or `workspace`, reused); its ready words must be
+    zero again after the call."""
     import torch
     M, K = A.shape
     N = B.shape[1]
     Y = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
-    fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y, cut_mask=mask)
+    if ws and workspace is None:
+        workspace = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device="cuda")
+    fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y, cut_mask=mask,
+                          workspace=workspace if ws else None)
     torch.cuda.synchronize()
     assert fc.fuse_check() == fc.FUSE_OK
+    if ws and workspace.numel() >= 1024:
+        assert int(workspace[:1024].count_nonzero()) == 0
     return Y.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
@@ -104,12 +111,41 @@ def test_ragged_shapes(cuda_device, shape, mask):
     _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
 
 
-@pytest.mark.parametrize("shape", [(2560, 2048, 128), (2500, 2040, 200)])
+@pytest.mark.parametrize("shape", [(2560, 2048, 128), (2500, 2040, 200), (2560, 2048, 72)])
 @pytest.mark.parametrize("mask", [0, 7])
-def test_last_wave_split_into_half_tiles(cuda_device, shape, mask):
-    """160 tiles on 152 SMs: the last 8 tiles run as 16 half tiles (128 x 128 units)."""
+@pytest.mark.parametrize("ws", [False, True])
+def test_last_wave_split_over_k(cuda_device, shape, mask, ws):
+    """80 pair tiles on 76 SM pairs: with a workspace the last 4 tiles are split over K between
+    two pairs each, which exchange partial sums through global memory and finish one column half
+    each; K = 72 leaves a ragged second half."""
     A, B, bias, R = wl.gemm_input(*shape, salt=9, std=1.0 / 8.0)
-    _check(_run(A, B, bias, R, mask), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+    _check(_run(A, B, bias, R, mask, ws=ws), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+def test_split_workspace_reused_across_calls(cuda_device):
+    """One workspace for consecutive calls: each call finds the ready words cleared by the one
+    before, and the results are identical."""
+    import torch
+    A, B, bias, R = wl.gemm_input(2560, 2048, 256, salt=10, std=1.0 / 8.0)
+    wsb = torch.zeros(fc.fuse_gemm_workspace_bytes(2560, 2048, 256), dtype=torch.uint8, device="cuda")
+    y0 = _run(A, B, bias, R, 0, ws=True, workspace=wsb)
+    _check(y0, oracle.gemm_epilogue(A, B, bias, R, 0), 0, A, B)
+    for _ in range(3):
+        assert np.array_equal(_run(A, B, bias, R, 0, ws=True, workspace=wsb), y0)
+
+
+def test_workspace_size_and_overlap(cuda_device):
+    import torch
+    assert fc.fuse_gemm_workspace_bytes(16, 4096, 4096) == 0            # decode: no split
+    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 1024 + 64 * 2 * 128 * 256 * 4
+    A = torch.zeros(256, 64, dtype=torch.float16, device="cuda")
+    B = torch.zeros(64, 256, dtype=torch.float16, device="cuda")
+    b = torch.zeros(256, dtype=torch.float16, device="cuda")
+    R = torch.zeros(256, 256, dtype=torch.float16, device="cuda")
+    Y = torch.zeros(256, 256, dtype=torch.float16, device="cuda")
+    with pytest.raises(fc.FuseError):
+        fc.fuse_gemm_epilogue(A, B, b, R, Y, workspace=Y.view(torch.uint8))   # workspace aliases Y
+    fc.fuse_gemm_epilogue(A, B, b, R, Y, workspace=torch.zeros(8, dtype=torch.uint8, device="cuda"))
 
 
 @pytest.mark.parametrize("M", [16, 256])
@@ -153,11 +189,13 @@ def test_decode_full_size_every_plan(cuda_device, plan):
 
 
 @pytest.mark.parametrize("plan", list(PLANS))
-def test_full_size_sampled_rows(cuda_device, plan):
-    """M = N = K = 4096 as benchmarked: the GPU computes all of Y, 40 rows (tile edges, first,
-    last, random) are compared element by element with the oracle."""
+@pytest.mark.parametrize("ws", [False, True])
+def test_full_size_sampled_rows(cuda_device, plan, ws):
+    """M = N = K = 4096 as benchmarked (with the split-K workspace, as the benchmark runs it, and
+    without): the GPU computes all of Y, 40 rows (tile edges, first, last, random) are compared
+    element by element with the oracle; every row crosses the split tiles' column strips."""
     A, B, bias, R = wl.gemm_input(4096)
-    Y = _run(A, B, bias, R, PLANS[plan])
+    Y = _run(A, B, bias, R, PLANS[plan], ws=ws)
     g = np.random.default_rng(6)
     rows = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 2047, 2048, 4094, 4095],
                                      g.integers(0, 4096, 30)]))
