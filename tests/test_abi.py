@@ -184,3 +184,13 @@ def test_gemm_host_validation():
     assert lib.fuse_gemm_epilogue_plan(0x1008, 0x2000, 0x3000, 0x4000, 0x9000, 64, 64, 64, 0,
                                        None) == fc.FUSE_EALIGN      # A not 16-byte aligned
     assert lib.fuse_gemm_epilogue_plan(None, None, None, None, None, 0, 64, 64, 0, None) == fc.FUSE_OK
+
+
+def test_gemm_workspace_bytes_is_host_arithmetic():
+    """The split-K workspace size needs no GPU: a 1 KB header of ready words plus one 256 KB fp32
+    partial tile per CTA pair tile, for at most 64 tiles; none for the decode shapes."""
+    assert fc.fuse_gemm_workspace_bytes(16, 4096, 4096) == 0
+    assert fc.fuse_gemm_workspace_bytes(64, 4096, 4096) == 0
+    assert fc.fuse_gemm_workspace_bytes(256, 256, 64) == 1024 + 1 * 2 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(2560, 2048, 128) == 1024 + 64 * 2 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 1024 + 64 * 2 * 128 * 256 * 4
