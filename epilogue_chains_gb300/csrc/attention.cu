@@ -30,8 +30,9 @@
 //       accumulator in TMEM only when the maximum has grown by more than 2^8 since it was last
 //       applied (P stays <= 256, exact in the final O / l).  After the last block they divide O
 //       by l and store it.
-// CTAs (pairs) run in groups of 16 (batch, head) slices, heaviest tiles first within a group, so
-// the ones resident together share their slices' key and value blocks in L2 (order_item()).
+// Work runs in groups of 16 (batch, head) slices, heaviest tiles first within a group, so the
+// tiles in flight together share their slices' key and value blocks in L2 (order_item()); the
+// persistent kernel's clusters take that order through host-balanced item lists (build_sched()).
 // All waits are bounded (watchdog); a CTA whose wait runs out drains its MMAs and copies and
 // frees its TMEM before it returns.
 #include <math.h>
@@ -49,16 +50,17 @@ constexpr int kAttnQ = 128;          // query rows per CTA
 constexpr int kAttnK = 128;          // keys per block
 constexpr int kKVStages = 1;         // K and V buffers (each a ring of this many blocks)
 constexpr int kPBuf = 1;             // P buffers in shared memory
-constexpr int kAttnSoftmaxWarps = 8; // two per TMEM lane quadrant, each exponentiating 32 keys
-// warp 0: Q and K loads; warp 1: MMA issue; warp 2: V loads; warps 3-10: softmax.  Every
-// producer and the MMA issuer own a warp: a thread parked in an mbarrier wait parks its whole warp.
+constexpr int kAttnSoftmaxWarps = 8; // two per TMEM lane quadrant, each exponentiating half a block's keys
+// One-CTA kernel: warp 0: Q and K loads; warp 1: MMA issue; warp 2: V loads; warps 3-10: softmax.
+// Every producer and the MMA issuer own a warp: a thread parked in an mbarrier wait parks its
+// whole warp.
 constexpr int kAttnThreads = 32 * (3 + kAttnSoftmaxWarps);
 constexpr float kRescaleLog2 = 8.0f; // rescale O only when the row maximum grew by more than this
 constexpr int kSBuf = 2;             // score buffers in TMEM: S_j+kSBuf-1 is computed before PV_j
 
-// Shared memory: Q (128 x D), two K and two V stages (64 keys x D each) and two P buffers
-// (128 x 64 bf16), all in 128-byte-swizzled 64-column atoms.  TMEM: two 64-column score buffers
-// and the D-column O accumulator.
+// One-CTA kernel.  Shared memory: Q (128 x D), kKVStages K and V blocks (128 keys x D each) and
+// kPBuf P buffers (128 x 128 bf16), all in 128-byte-swizzled 64-column atoms.  TMEM: kSBuf
+// 128-column score buffers and the D-column O accumulator.
 template <int D>
 struct AttnLayout {
     static constexpr int ATOMS = D / 64;                   // 128-byte swizzle atoms along D
