@@ -109,6 +109,15 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
         mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(128 * NM * 4));
         prefetch_map(&mapA);
         prefetch_map(&mapB);
+        // Start this CTA's whole weight slice on its way into L2 while the preceding kernel may
+        // still run: an L2 prefetch returns nothing to the SM, and L2 is where that kernel's
+        // writes land, so the loads after pdl_wait() read current data, only sooner.
+        for (int kb = 0; kb < nk; ++kb) {
+            const int k = (kb0 + kb) * BK;
+            tma_prefetch_2d(&mapB, n0, k);
+            tma_prefetch_2d(&mapB, n0 + 64, k);
+            tma_prefetch_2d(&mapA, k, 0);
+        }
     }
     if (warp == 1) tmem_alloc(holder, L::TCOLS);
     tc_fence_before();
