@@ -396,29 +396,41 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                             v[4 * j + 3] += t.w;
                         }
                     }
+                    // the 32 columns' stages in one branch-free block per stage count (the count
+                    // is uniform per launch), so the 16 independent GELU chains interleave
+                    auto finish = [&](auto last_c) {
+                        constexpr int LAST = decltype(last_c)::value;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        float bv[8];
-                        {
-                            const int src = 16 * bslot + (32 * g + 8 * j) / 4;   // lane holding these columns
-                            uint4 b8;
-                            b8.x = __shfl_sync(0xffffffffu, bl.x, src);
-                            b8.y = __shfl_sync(0xffffffffu, bl.y, src);
-                            b8.z = __shfl_sync(0xffffffffu, bl.x, src + 1);
-                            b8.w = __shfl_sync(0xffffffffu, bl.y, src + 1);
-                            unpack_h8(b8, bv);
-                        }
-                        float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                        if (need_r) unpack_h8(ld_row(lane, 4 * g + j), rv);
-                        float o[8];
+                        for (int j = 0; j < 4; ++j) {
+                            float bv[8];
+                            {
+                                const int src = 16 * bslot + (32 * g + 8 * j) / 4;   // lane holding these columns
+                                uint4 b8;
+                                b8.x = __shfl_sync(0xffffffffu, bl.x, src);
+                                b8.y = __shfl_sync(0xffffffffu, bl.y, src);
+                                b8.z = __shfl_sync(0xffffffffu, bl.x, src + 1);
+                                b8.w = __shfl_sync(0xffffffffu, bl.y, src + 1);
+                                unpack_h8(b8, bv);
+                            }
+                            float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                            if constexpr (LAST >= 3) unpack_h8(ld_row(lane, 4 * g + j), rv);
+                            float o[8];
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {
-                            const float2 r2 = apply_stages2(make_float2(v[8 * j + e], v[8 * j + e + 1]), 1, args.epi,
-                                                            make_float2(bv[e], bv[e + 1]), make_float2(rv[e], rv[e + 1]));
-                            o[e] = r2.x;
-                            o[e + 1] = r2.y;
+                            for (int e = 0; e < 8; e += 2) {
+                                const float2 r2 = apply_stages2_upto<LAST>(make_float2(v[8 * j + e], v[8 * j + e + 1]),
+                                                                           make_float2(bv[e], bv[e + 1]),
+                                                                           make_float2(rv[e], rv[e + 1]));
+                                o[e] = r2.x;
+                                o[e + 1] = r2.y;
+                            }
+                            st_row(lane, 4 * g + j, pack_h8(o));
                         }
-                        st_row(lane, 4 * g + j, pack_h8(o));
+                    };
+                    switch (args.epi) {
+                        case 3: finish(IntC<3>{}); break;
+                        case 2: finish(IntC<2>{}); break;
+                        case 1: finish(IntC<1>{}); break;
+                        default: finish(IntC<0>{}); break;
                     }
                 }
                 __syncwarp();

@@ -67,6 +67,20 @@ __device__ __forceinline__ float2 apply_stages2(float2 v, int first, int last, f
     return v;
 }
 
+// the same with the last stage fixed at compile time (stages 1..LAST), so that a loop over many
+// values is one branch-free block whose independent GELU chains the compiler can interleave
+template <int LAST>
+__device__ __forceinline__ float2 apply_stages2_upto(float2 v, float2 b, float2 r) {
+    if constexpr (LAST >= 1) v = __fadd2_rn(v, b);
+    if constexpr (LAST >= 2) v = gelu_erf2(v);
+    if constexpr (LAST >= 3) v = __fadd2_rn(v, r);
+    return v;
+}
+template <int N>
+struct IntC {
+    static constexpr int value = N;
+};
+
 __device__ __forceinline__ void unpack_h8(const uint4& u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
