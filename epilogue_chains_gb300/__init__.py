@@ -71,6 +71,7 @@ SIGNATURES = {
     "fuse_gemm_epilogue_ws": ([_P, _P, _P, _P, _P, _I64, _I64, _I64, _U32, _P, _SZ, _P], _I32),
     "fuse_gemm_workspace_bytes": ([_I64, _I64, _I64], _SZ),
     "fuse_gemm_bytes": ([_I64, _I64, _I64, _U32], _I64),
+    "fuse_attention_schedule": ([_I64, _I64, _I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], _I64),
     "fuse_ledger": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_ledger_t)], _I32),
     "fuse_plan_time": ([ctypes.POINTER(fuse_stage), _I32, _U32, _I32, ctypes.POINTER(fuse_cost_model),
                         ctypes.POINTER(ctypes.c_double)], _I32),
@@ -291,6 +292,16 @@ def fuse_gemm_epilogue(A, B, bias, R, Y, cut_mask: int = 0, workspace=None, stre
 
 def fuse_gemm_workspace_bytes(M: int, N: int, K: int) -> int:
     return _load().fuse_gemm_workspace_bytes(M, N, K)
+
+
+def fuse_attention_schedule(bh: int, S: int, clusters: int):
+    """Per-cluster item lists of the persistent attention kernel: (first [clusters + 1], items)."""
+    n = bh * S // 256
+    first = (ctypes.c_int32 * (clusters + 1))()
+    items = (ctypes.c_int32 * max(1, n))()
+    rc = _load().fuse_attention_schedule(bh, S, clusters, first, items)
+    _check(rc if rc < 0 else 0, "fuse_attention_schedule")
+    return list(first), list(items[:rc])
 
 
 def fuse_gemm_bytes(M: int, N: int, K: int, cut_mask: int) -> int:

@@ -1117,6 +1117,20 @@ extern "C" int64_t fuse_attention_bytes(int64_t bh, int64_t S, int64_t D) {
     return 4 * bh * S * D * 2;   // read Q, K, V once, write O once (bf16)
 }
 
+extern "C" int64_t fuse_attention_schedule(int64_t bh, int64_t S, int clusters, int32_t* first,
+                                           int32_t* items) {
+    using namespace fc;
+    if (bh < 1 || S < 2 * kAttnQ || S % (2 * kAttnQ) != 0 || clusters < 1 || !first || !items) return FUSE_EINVAL;
+    const int64_t per_head = S / (2 * kAttnQ);
+    if (clusters > kSchedClusters || bh * per_head > kSchedItems) return FUSE_EUNSUPPORTED;
+    static thread_local AttnSched sch;
+    build_sched(static_cast<int>(bh), static_cast<int>(per_head), clusters, &sch);
+    if (sch.n == 0) return FUSE_EUNSUPPORTED;
+    for (int c = 0; c <= clusters; ++c) first[c] = sch.first[c];
+    for (int i = 0; i < sch.n; ++i) items[i] = sch.item[i];
+    return sch.n;
+}
+
 extern "C" int64_t fuse_attention_flops(int64_t bh, int64_t S, int64_t D) {
     if (bh < 0 || S < 0 || D < 1) return FUSE_EINVAL;
     // Q K^T and P V over the visible (i, j <= i) pairs: 2 * 2 * D flops per pair

@@ -273,6 +273,17 @@ int fuse_attention(const void* q, const void* k, const void* v, void* o, int64_t
  * visible query-key pair: 2 D bh S (S + 1)) of one fuse_attention() call. */
 int64_t fuse_attention_bytes(int64_t bh, int64_t S, int64_t D);
 int64_t fuse_attention_flops(int64_t bh, int64_t S, int64_t D);
+/* The work lists of the persistent 2-SM attention kernel (host arithmetic, no GPU needed).  Its
+ * items are pairs of adjacent 128-row query tiles: item i of bh * (S / 256) covers slice and tile
+ * pair as ordered in groups of 16 slices, heaviest pair first within a group; an item with pair
+ * index u reads 2u + 2 key blocks.  Items go, in that order, to the cluster with the earliest
+ * estimated finish (10 per key block + 14 per item).  Cluster c runs items[first[c]] ..
+ * items[first[c + 1] - 1].
+ *   first   host int32 [clusters + 1];  items  host int32 [bh * S / 256]
+ *   S a multiple of 256; 1 <= clusters <= 96; bh * S / 256 <= 4096 (the kernel falls back to a
+ *   round-robin assignment beyond these, and so does this call: FUSE_EUNSUPPORTED).
+ * Returns the number of items, or a negative FUSE_E* code. */
+int64_t fuse_attention_schedule(int64_t bh, int64_t S, int clusters, int32_t* first, int32_t* items);
 
 /* ===================================================================== ledgers
  * [K4] §① traffic(): a cut plan splits the K stages into consecutive kernels (cut_mask bit i =
