@@ -274,19 +274,49 @@ def fuse_causal_softmax(s, p, scale: float, skip_tile: int = 0, mode: int = FUSE
                                    _stream(stream)), "fuse_causal_softmax")
 
 
+# split-K workspaces handed out by fuse_gemm_epilogue(workspace=None): one zero-filled buffer per
+# (device, stream), reused (every completed call leaves it zero-filled), never freed
+_GEMM_WS = {}
+
+
+def _gemm_workspace(M: int, N: int, K: int, dev, stream_handle):
+    import torch
+    need = fuse_gemm_workspace_bytes(M, N, K)
+    if need == 0:
+        return None
+    key = (dev.index, stream_handle)
+    ws = _GEMM_WS.get(key)
+    if ws is not None and ws.numel() >= need:
+        return ws
+    # allocate only on torch's current stream and outside graph capture; otherwise the call
+    # runs unsplit
+    if torch.cuda.is_current_stream_capturing() or stream_handle != torch.cuda.current_stream(dev).cuda_stream:
+        return None
+    ws = torch.zeros(need, dtype=torch.uint8, device=dev)
+    torch.cuda.current_stream(dev).synchronize()   # zero-filled before any stream uses it
+    _GEMM_WS[key] = ws
+    return ws
+
+
 def fuse_gemm_epilogue(A, B, bias, R, Y, cut_mask: int = 0, workspace=None, stream=None) -> None:
     """Y = fp16(GELU(A @ B + bias) + R) for fp16 A [M,K], B [K,N], bias [N], R, Y [M,N]; cut_mask
-    selects the plan (0 = fully fused [4]; 7 = [1,1,1,1]).  workspace: optional zero-filled device
-    tensor of fuse_gemm_workspace_bytes(M, N, K) bytes (see fuse_gemm_epilogue_ws in the header),
-    reused across calls on one stream."""
+    selects the plan (0 = fully fused [4]; 7 = [1,1,1,1]).  workspace: a zero-filled device tensor
+    of fuse_gemm_workspace_bytes(M, N, K) bytes (see fuse_gemm_epilogue_ws in the header), reused
+    across calls on one stream; None: a buffer of that kind kept by this module per device and
+    stream; False: none (the last wave of tiles is not split over K)."""
     _need_device(A, B, bias, R, Y)
     M, K = A.shape
     K2, N = B.shape
     if K != K2 or tuple(R.shape) != (M, N) or tuple(Y.shape) != (M, N) or bias.numel() != N:
         raise ValueError("shape mismatch")
+    sh = _stream(stream)
+    if workspace is None:
+        workspace = _gemm_workspace(M, N, K, A.device, sh)
+    elif workspace is False:
+        workspace = None
     ws_size = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(_load().fuse_gemm_epilogue_ws(_ptr(A), _ptr(B), _ptr(bias), _ptr(R), _ptr(Y), M, N, K,
-                                         int(cut_mask), _ptr(workspace), ws_size, _stream(stream)),
+                                         int(cut_mask), _ptr(workspace), ws_size, sh),
            "fuse_gemm_epilogue")
 
 

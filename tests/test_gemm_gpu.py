@@ -74,7 +74,7 @@ def _run(A, B, bias, R, mask, ws=False, workspace=None):
     if ws and workspace is None:
         workspace = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, N, K)), dtype=torch.uint8, device="cuda")
     fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y, cut_mask=mask,
-                          workspace=workspace if ws else None)
+                          workspace=workspace if ws else False)
     torch.cuda.synchronize()
     assert fc.fuse_check() == fc.FUSE_OK
     if ws and workspace.numel() >= 1024:
@@ -145,6 +145,22 @@ def test_split_and_unsplit_agree(cuda_device, shape):
     diff = np.abs(y1 - y0)
     assert np.all(diff <= _ulp16(np.maximum(np.abs(y0), np.abs(y1))) + 1e-12)
     assert np.mean(diff > 0) < 0.02
+
+
+def test_module_workspace_by_default(cuda_device):
+    """workspace=None: the module's zero-filled per-stream buffer is used (split tail) and left
+    zero-filled; the result equals an explicit workspace's."""
+    import torch
+    A, B, bias, R = wl.gemm_input(2560, 2048, 128, salt=12, std=1.0 / 8.0)
+    Y = torch.empty(2560, 2048, dtype=torch.float16, device="cuda")
+    fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y)
+    torch.cuda.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    key = (torch.device("cuda").index or 0, torch.cuda.current_stream().cuda_stream)
+    ws = [v for k, v in fc._GEMM_WS.items() if k[1] == key[1]]
+    assert ws and int(ws[0][:1024].count_nonzero()) == 0
+    y_auto = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(y_auto, _run(A, B, bias, R, 0, ws=True))
 
 
 def test_workspace_size_and_overlap(cuda_device):
