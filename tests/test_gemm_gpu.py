@@ -137,13 +137,14 @@ def test_split_workspace_reused_across_calls(cuda_device):
 @pytest.mark.parametrize("shape", [(2560, 2048, 256), (4096, 4096, 4096)])
 def test_split_and_unsplit_agree(cuda_device, shape):
     """The split-K tail changes only the fp32 summation order of its tiles' accumulators: the two
-    results agree element by element to within one fp16 rounding step, and almost everywhere
-    exactly."""
+    results agree element by element to within one fp16 rounding step plus the reassociation error
+    carried through GELU and the residual (a few 1e-6 here, bounded by 2^-16 absolute, which
+    matters only where GELU(v) + R cancels to a tiny value), and almost everywhere exactly."""
     A, B, bias, R = wl.gemm_input(*shape, salt=11)
     y0 = _run(A, B, bias, R, 0).view(np.float16).astype(np.float64)
     y1 = _run(A, B, bias, R, 0, ws=True).view(np.float16).astype(np.float64)
     diff = np.abs(y1 - y0)
-    assert np.all(diff <= _ulp16(np.maximum(np.abs(y0), np.abs(y1))) + 1e-12)
+    assert np.all(diff <= _ulp16(np.maximum(np.abs(y0), np.abs(y1))) + 2.0 ** -16)
     assert np.mean(diff > 0) < 0.02
 
 
