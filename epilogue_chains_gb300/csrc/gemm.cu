@@ -466,9 +466,9 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
 
 // =============================================================================== tail kernel
 // Y <- h(stages first..last applied to Y), 8 halves per thread (N % 8 == 0).
+template <int FIRST, int LAST>
 __global__ void __launch_bounds__(256) epi_tail_kernel(__half* __restrict__ Y, const __half* __restrict__ bias,
-                                                       const __half* __restrict__ R, int64_t M, int N,
-                                                       int first, int last) {
+                                                       const __half* __restrict__ R, int64_t M, int N) {
     pdl_begin();  // before any global-memory access (programmatic dependent launch)
     const int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     const int64_t total = M * N / 8;
@@ -477,10 +477,18 @@ __global__ void __launch_bounds__(256) epi_tail_kernel(__half* __restrict__ Y, c
     float v[8], bv[8] = {0, 0, 0, 0, 0, 0, 0, 0}, rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     uint4* yp = reinterpret_cast<uint4*>(Y) + g;
     unpack_h8(*yp, v);
-    if (first <= 1 && last >= 1) unpack_h8(__ldg(reinterpret_cast<const uint4*>(bias + n)), bv);
-    if (last >= 3) unpack_h8(__ldcs(reinterpret_cast<const uint4*>(R) + g), rv);
+    if constexpr (FIRST <= 1 && LAST >= 1) unpack_h8(__ldg(reinterpret_cast<const uint4*>(bias + n)), bv);
+    if constexpr (LAST >= 3) unpack_h8(__ldcs(reinterpret_cast<const uint4*>(R) + g), rv);
+    // stages FIRST..LAST fixed at compile time: one branch-free block for the eight values
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = apply_stages(v[e], first, last, bv[e], rv[e]);
+    for (int e = 0; e < 8; e += 2) {
+        float2 x = make_float2(v[e], v[e + 1]);
+        if constexpr (FIRST <= 1 && LAST >= 1) x = __fadd2_rn(x, make_float2(bv[e], bv[e + 1]));
+        if constexpr (FIRST <= 2 && LAST >= 2) x = gelu_erf2(x);
+        if constexpr (LAST >= 3) x = __fadd2_rn(x, make_float2(rv[e], rv[e + 1]));
+        v[e] = x.x;
+        v[e + 1] = x.y;
+    }
     *yp = pack_h8(v);
 }
 
@@ -593,9 +601,20 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
 int launch_tail(void* Y, const void* bias, const void* R, int64_t M, int64_t N, int first, int last,
                 cudaStream_t st) {
     const int64_t units = M * N / 8;
-    return launch_pdl(epi_tail_kernel, dim3(static_cast<unsigned>(ceil_div(units, 256))), dim3(256), 0, st, 1,
-                      static_cast<__half*>(Y), static_cast<const __half*>(bias), static_cast<const __half*>(R), M,
-                      static_cast<int>(N), first, last);
+    const dim3 grid(static_cast<unsigned>(ceil_div(units, 256)));
+    __half* y = static_cast<__half*>(Y);
+    const __half* b = static_cast<const __half*>(bias);
+    const __half* r = static_cast<const __half*>(R);
+    const int n = static_cast<int>(N);
+    switch (first * 4 + last) {   // segments of the chain after a cut: stages first..last
+        case 1 * 4 + 1: return launch_pdl(epi_tail_kernel<1, 1>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        case 1 * 4 + 2: return launch_pdl(epi_tail_kernel<1, 2>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        case 1 * 4 + 3: return launch_pdl(epi_tail_kernel<1, 3>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        case 2 * 4 + 2: return launch_pdl(epi_tail_kernel<2, 2>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        case 2 * 4 + 3: return launch_pdl(epi_tail_kernel<2, 3>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        case 3 * 4 + 3: return launch_pdl(epi_tail_kernel<3, 3>, grid, dim3(256), 0, st, 1, y, b, r, M, n);
+        default: return FUSE_EINVAL;
+    }
 }
 
 }  // namespace
@@ -615,7 +634,7 @@ int gemm_report(int i, fuse_kernel_record* out) {
             return rc;
         }
         case 1: return decode_report(out);
-        case 2: return describe_kernel((const void*)epi_tail_kernel, "epi_tail_kernel (unfused plans)", 256, 0, out);
+        case 2: return describe_kernel((const void*)epi_tail_kernel<1, 3>, "epi_tail_kernel<1,3> (unfused plans)", 256, 0, out);
         default: return FUSE_EINVAL;
     }
 }
