@@ -15,15 +15,18 @@
 //    its peer's.  Warp 0 drives TMA (128B-swizzled tiles, a 6-stage mbarrier ring, both CTAs'
 //    bytes completing on the even CTA's barriers); warp 1 of the even CTA issues the MMAs,
 //    committing each stage back to both producers and each finished tile to both epilogues;
-//    warps 2-9 of each CTA drain its accumulator with tcgen05.ld, 32 columns at a time, add bias,
-//    apply GELU(erf), add the residual (prefetched into registers one chunk ahead) and store fp16
-//    Y straight from registers.  The accumulator is double-buffered in TMEM (2 x 256 columns), so
-//    the epilogue of tile i overlaps the main loop of tile i+1; the last partial wave of tiles is
-//    split into 128-column halves.  A is consumed K-major, B ([K,N], N contiguous) MN-major,
-//    both straight from their row-major layouts.
+//    warps 2-9 of each CTA drain its accumulator with tcgen05.ld, 32 columns at a time, add bias
+//    (handed out by shuffles), apply GELU(erf) and add the residual (prefetched one 64-column chunk
+//    ahead), with global loads and stores coalesced through a small shared-memory tile per warp.
+//    The accumulator is double-buffered in TMEM (2 x 256 columns), so the epilogue of tile i
+//    overlaps the main loop of tile i+1.  With a caller workspace the tiles of the last, partial
+//    wave are split over K between two pairs that exchange partial sums (described at unit_of).
+//    A is consumed K-major, B ([K,N], N contiguous) MN-major, both straight from their row-major
+//    layouts.
 //  * M <= 64 (decode): gemm_decode.cu.
 //  * Cut plans: the GEMM kernel stops after the first stage segment and stores that fp16
-//    intermediate; a vectorised tail kernel applies each later segment in place in Y.
+//    intermediate; a vectorised tail kernel (the segment's stages a template parameter) applies
+//    each later segment in place in Y.
 //  * Every mbarrier wait is bounded; a wait that runs out raises the watchdog word, the CTA lets
 //    its copies and MMAs in flight finish (bounded), frees its TMEM and returns.
 #include <cudaTypedefs.h>
@@ -93,8 +96,9 @@ struct MainArgs {
 // partial wave are split over K into two units (part 0: the first half of K, part 1: the second),
 // which exchange fp32 partial sums through global memory, each finishing one column half of the
 // tile (part p adds the other part's sums of columns 128p..128p+127 and applies the epilogue
-// there, with all eight epilogue warps), so that the wave spreads over twice as many SMs (wave quantisation: 256 pair tiles on 76 pairs
-// would otherwise leave two thirds of the SMs idle for the last tile time).  Splitting N instead
+// there, with all eight epilogue warps), so that the wave spreads over twice as many SMs (wave
+// quantisation: 256 pair tiles on 76 pairs would otherwise leave two thirds of the SMs idle for
+// the last tile time).  Splitting N instead
 // does not help: an M = 256, N = 128 MMA takes as long as an N = 256 one on this hardware.
 struct Unit {
     int m0, n0, kb0, kb1;
