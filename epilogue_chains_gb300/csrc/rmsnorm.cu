@@ -17,6 +17,8 @@
 // to its last, partial round of rows; for RMSNorm alone (32 MiB each way) both run at the speed of
 // a cudaMemcpy of the same 32 MiB (about 16 us), the fixed cost of filling and draining the memory
 // pipeline dominating at that size.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "fc_internal.cuh"
@@ -384,7 +386,36 @@ extern "C" int64_t fuse_rmsnorm_bytes(int64_t rows, int64_t hidden, int mode) {
 namespace {
 constexpr int64_t kStaticMaxRows = 65536;  // 256 KiB of fp32 row statistics
 __device__ __align__(256) float g_rms_static_ms[kStaticMaxRows];
+
+// The driver's process-unique id of the calling thread's current context (0 if there is none
+// or the driver entry points are missing).  Driver calls are reached through the runtime's entry
+// point query, so the library needs no link against libcuda.
+unsigned long long current_context_id() {
+    using GetCurrentFn = CUresult (*)(CUcontext*);
+    using GetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+    static GetCurrentFn get_current = nullptr;
+    static GetIdFn get_id = nullptr;
+    static bool looked = false;
+    if (!looked) {  // called under the entry point's mutex
+        looked = true;
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<GetCurrentFn>(p);
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<GetIdFn>(p);
+        (void)cudaGetLastError();
+    }
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 }  // namespace
+
 
 extern "C" int fuse_rmsnorm_unfused_static(const float* x, const float* w, float* y, int64_t rows,
                                            int64_t hidden, float eps, fuse_stream_t stream) {
@@ -396,9 +427,13 @@ extern "C" int fuse_rmsnorm_unfused_static(const float* x, const float* w, float
     if (!is_aligned(x, 4) || !is_aligned(w, 4) || !is_aligned(y, 4)) return FUSE_EALIGN;
 
     // Host code cannot use the array's name as a device address: look the address up once per
-    // device, with that device current.
+    // device, with that device current, and keep it for as long as that device's context lives.
+    // The cache is keyed by the driver's unique context id, so after cudaDeviceReset() (a new
+    // primary context, into which the module is loaded again, maybe at another address) the next
+    // call looks the address up afresh instead of launching on a stale pointer.
     static std::mutex mu;
     static float* dev_ms[64] = {nullptr};
+    static unsigned long long dev_ctx[64] = {0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return record_cuda_error(e);
@@ -406,11 +441,13 @@ extern "C" int fuse_rmsnorm_unfused_static(const float* x, const float* w, float
     float* ms = nullptr;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (!dev_ms[dev]) {
+        unsigned long long ctx = current_context_id();
+        if (!dev_ms[dev] || ctx == 0 || ctx != dev_ctx[dev]) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_rms_static_ms);
             if (e != cudaSuccess) return record_cuda_error(e);
             dev_ms[dev] = static_cast<float*>(p);
+            dev_ctx[dev] = current_context_id();  // the lookup made the device's context current
         }
         ms = dev_ms[dev];
     }

@@ -138,7 +138,9 @@ size_t fuse_rmsnorm_workspace_bytes(int64_t rows, int64_t hidden, int mode);
  * Same arithmetic, kernels and output as fuse_rmsnorm(..., FUSE_UNFUSED, ...).
  *   rows > FUSE_RMSNORM_STATIC_MAX_ROWS -> FUSE_EUNSUPPORTED (nothing launched); y != x.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress) with
- * that device current; make that first call before any stream capture.  All calls share the
+ * that device current; make that first call before any stream capture.  The address is kept per
+ * device context: after cudaDeviceReset() the next call on that device (a new context) looks it
+ * up again, so make that call before any capture too.  All calls share the
  * array and it keeps the last call's contents, so calls that may overlap on the GPU (different
  * streams, or different host threads on one device) race; serialize them.
  */

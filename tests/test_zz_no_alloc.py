@@ -6,7 +6,8 @@ keeps its row statistics in one fixed array owned by the library instead of a ca
 Its output must match the regular entry point, fuse_rmsnorm(..., FUSE_UNFUSED, workspace), within
 the RMSNorm tolerance of the other tests (1e-5 relative per element), on two calls in a row with
 different shapes, so that nothing left in the shared array by the first call leaks into the
-second.  This file is collected last on purpose.
+second.  The output is also compared with the CPU oracle directly.  This file is collected
+last on purpose.
 """
 import ctypes
 
@@ -14,6 +15,7 @@ import numpy as np
 import pytest
 
 import epilogue_chains_gb300 as fc
+import oracle
 from epilogue_chains_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -53,14 +55,22 @@ def test_static_scratch_matches_workspace_entry_point_twice(cuda_device):
         ref = _regular(lib, x, w, wl.RMS_EPS, stream)
         torch.cuda.synchronize()
         assert lib.fuse_check(stream) == fc.FUSE_OK
-        _close(y.cpu().numpy(), ref.cpu().numpy())
+        got = y.cpu().numpy()
+        _close(got, ref.cpu().numpy())
+        _close(got, oracle.rmsnorm(xh, wh, wl.RMS_EPS))
 
 
 def test_static_scratch_rejects_rows_beyond_its_size(cuda_device):
+    # Every buffer is valid for the full over-limit shape, so a call that got past the size check
+    # would return a status or a result, never touch memory outside its buffers.
     import torch
     lib = fc._load()
-    x = torch.zeros(1, 8, device="cuda")
-    rows = fc.FUSE_RMSNORM_STATIC_MAX_ROWS + 1
-    rc = lib.fuse_rmsnorm_unfused_static(x.data_ptr(), x.data_ptr(), x.data_ptr() + 64, rows, 8,
+    rows, hidden = fc.FUSE_RMSNORM_STATIC_MAX_ROWS + 1, 8
+    x = torch.ones(rows, hidden, device="cuda")
+    w = torch.ones(hidden, device="cuda")
+    y = torch.full_like(x, 7.0)
+    rc = lib.fuse_rmsnorm_unfused_static(x.data_ptr(), w.data_ptr(), y.data_ptr(), rows, hidden,
                                          ctypes.c_float(1e-6), None)
+    torch.cuda.synchronize()
     assert rc == fc.FUSE_EUNSUPPORTED
+    assert bool(torch.all(y == 7.0))   # nothing was launched
