@@ -260,6 +260,29 @@ def run_ours(args, rank, world, local):
     groups += [Group(f"chain_unfused_K{K}", chain(K, fc.FUSE_UNFUSED),
                      fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED), 2, "hbm", None, K,
                      "chain_unfused") for K in KS]
+    # The same sweep at N = 2^26 (256 MiB per operand, twice the L2): an unfused stage's 256 MiB
+    # intermediate cannot stay in L2, so every stage moves its 2 N b through DRAM as the ledger
+    # prices it, where at N = 2^24 the 64 MiB intermediate is partly served from L2.
+    NB, RB = 4 * N, 2
+    with torch.cuda.stream(stream):
+        xbs = [wl.chain_input(NB, device=dev, salt=r + 7 + 100 * rank) for r in range(RB)]
+        ybs = [torch.empty_like(xbs[0]) for _ in range(RB)]
+    brot = rotating(RB)
+    chain_bytes_big = fc.fuse_chain_bytes(1, NB, fc.FUSE_F32, fc.FUSE_FUSED)
+
+    def chain_big(K, mode):
+        def fn():
+            i = brot()
+            check(lib.fuse_chain_run(stage_sets[K], K, xbs[i].data_ptr(), ybs[i].data_ptr(), NB,
+                                     fc.FUSE_F32, mode, sh), "fuse_chain_run")
+            counter["launches"] += K if mode == fc.FUSE_UNFUSED else 1
+        return fn
+
+    groups += [Group(f"chain26_fused_K{K}", chain_big(K, fc.FUSE_FUSED), chain_bytes_big, 2, "hbm",
+                     "chain_fused_kernel<f32>", 1, "chain26_fused") for K in KS]
+    groups += [Group(f"chain26_unfused_K{K}", chain_big(K, fc.FUSE_UNFUSED),
+                     fc.fuse_chain_bytes(K, NB, fc.FUSE_F32, fc.FUSE_UNFUSED), 2, "hbm", None, K,
+                     "chain26_unfused") for K in KS]
     # the fat probe is a fixed-point probe at K = 4 ([C05] §5: not part of the sweep)
     groups += [Group("chain_fat", chain(4, fc.FUSE_FAT), chain_bytes, 2, "hbm", "chain_fat_kernel<f32>", 1)]
 
@@ -483,6 +506,8 @@ def run_ours(args, rank, world, local):
                "step_share": round(tot_ms / step_ms, 4)}
         if gs[0].bound == "tensor":
             out["frac_of_sustained"] = round(achieved / peaks["bf16_tflops_sustained"], 4)
+        else:
+            out["frac_of_nominal"] = round(achieved / NOMINAL_HBM_GBS, 4)
         # DRAM bytes per launch from the committed ncu summary of this kernel source, else None
         out["traffic"] = committed_traffic(fam, kernel_src.get(fam, ""))
         return out
@@ -510,8 +535,20 @@ def run_ours(args, rank, world, local):
                          "fused_GBs": round(chain_bytes / (f / 1e3) / 1e9, 1),
                          "unfused_ledger_GBs": round(fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED)
                                                      / (u / 1e3) / 1e9, 1)}
+    per_k26 = {}
+    for K in KS:
+        f = call_ms(f"chain26_fused_K{K}")
+        u = call_ms(f"chain26_unfused_K{K}")
+        per_k26[str(K)] = {"fused_us": round(f * 1e3, 2), "unfused_us": round(u * 1e3, 2),
+                           "speedup_fused_vs_unfused": round(u / f, 3),
+                           "fused_GBs": round(chain_bytes_big / (f / 1e3) / 1e9, 1),
+                           "unfused_ledger_GBs": round(fc.fuse_chain_bytes(K, NB, fc.FUSE_F32, fc.FUSE_UNFUSED)
+                                                       / (u / 1e3) / 1e9, 1)}
     fat = call_ms("chain_fat")
     rows["chain"] = {"per_K": per_k, "roofline_fused": roofline_of("chain_fused"),
+                     "per_K_N2^26": per_k26, "roofline_fused_N2^26": roofline_of("chain26_fused"),
+                     "note_N2^26": "operands of 256 MiB, twice the L2: every unfused stage's "
+                                   "intermediate goes through DRAM, as the 2KNb ledger prices it",
                      "fat_K4": {"us": round(fat * 1e3, 2), "fat_over_fused": round(fat / call_ms("chain_fused_K4"), 3)}}
     if args.rows == "all":
         rf, ru = call_ms("rmsnorm_fused"), call_ms("rmsnorm_unfused")
@@ -591,13 +628,24 @@ def run_ours(args, rank, world, local):
                                        "GBs": round(chain_bytes / copy_us / 1e3, 1),
                                        "what": "cudaMemcpy D2D of 64 MiB, same rotation, back to back"}
 
+    # dense fp16 and bf16 tensor peaks measured in this run the way the pool's bf16 figure was
+    # (cuBLAS through torch.matmul, 8192^3, best of 10): the GEMM chain computes in fp16
+    if args.rows == "all":
+        tp = tensor_peaks(torch, dev, stream)
+        rows["tensor_peaks_in_run"] = tp
+        for key in ("M4096",):
+            r4 = rows["gemm_epilogue"][key]["roofline"]
+            r4["frac_of_fp16_in_run"] = round(r4["achieved"] / tp["fp16_tflops"], 4)
+            r4["fp16_peak_in_run"] = tp["fp16_tflops"]
+
     # register / occupancy report of every kernel variant ([K4] §③, [C05] §6.2)
     report_rows = []
     for i in range(fc.fuse_kernel_count()):
         r_ = fc.fuse_kernel_report(i)
         report_rows.append({k: r_[k] for k in ("name", "regs_per_thread", "local_bytes_per_thread",
                                                "dynamic_smem_bytes", "block_threads", "blocks_per_sm",
-                                               "cluster_size", "max_active_clusters")})
+                                               "cluster_size", "max_active_clusters", "ptxas_registers",
+                                               "stack_bytes", "spill_store_bytes", "spill_load_bytes")})
     rows["kernel_report"] = report_rows
 
     # ---------------------------------------------------------------- e2e through host buffers
@@ -610,6 +658,8 @@ def run_ours(args, rank, world, local):
         cpu = None
         if not args.no_cpu_baseline and world == 1:
             cpu = cpu_baseline(wl, seconds=10.0)
+            if args.rows == "all":
+                rows["cpu_baselines"] = cpu_baselines_per_config(wl)
         report = {
             "metric": "fused-chain HBM GB/s and % of GB300 peak; fused/unfused speedup vs K",
             "value": round(value, 1), "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -625,6 +675,8 @@ def run_ours(args, rank, world, local):
                              "back to back between one CUDA event pair",
                        "parallelism": f"replicas x{world}"},
             "frac_of_peak": round(value / world / peaks["hbm_gbs"], 4),
+            "frac_of_nominal": round(value / world / NOMINAL_HBM_GBS, 4),
+            "nominal_hbm_gbs": NOMINAL_HBM_GBS,
             "roofline": roofline,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
                     "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
@@ -637,6 +689,28 @@ def run_ours(args, rank, world, local):
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
     return report
+
+
+def tensor_peaks(torch, dev, stream, n=8192, reps=10):
+    """Dense fp16 and bf16 GEMM throughput of cuBLAS (torch.matmul, n^3, best of `reps`)."""
+    out = {"what": f"torch.matmul {n}^3 (cuBLAS), best of {reps}, CUDA events on the launching stream"}
+    with torch.cuda.stream(stream):
+        for name, dt in (("fp16", torch.float16), ("bf16", torch.bfloat16)):
+            a = torch.randn(n, n, device=dev, dtype=dt)
+            b = torch.randn(n, n, device=dev, dtype=dt)
+            for _ in range(3):
+                torch.matmul(a, b)
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for e0, e1 in ev:
+                e0.record(stream)
+                torch.matmul(a, b)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            best = min(e0.elapsed_time(e1) for e0, e1 in ev) / 1e3
+            out[f"{name}_tflops"] = round(2 * n ** 3 / best / 1e12, 1)
+            del a, b
+    out["fp16_over_bf16"] = round(out["fp16_tflops"] / out["bf16_tflops"], 4)
+    return out
 
 
 def per_call_rows(torch, stream, fused, unfused, reps=10):
@@ -897,8 +971,67 @@ def cpu_baseline(wl, seconds=10.0):
             nbytes += 2 * wl.CHAIN_N * 4
         sweeps += 1
     return {"value": round(nbytes / t_total / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "host_cores_available": _host_cores(),
             "sample": f"{sweeps} full K-sweeps (K=2,3,4,6,8) over N=16,777,216 fp32, single thread, "
                       f"{t_total:.1f} s"}
+
+
+def _host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baselines_per_config(wl, seconds=2.0):
+    """Every other config's oracle, as it stands (single thread), on a bounded sample of its
+    workload, each rate in its row's own unit.  A baseline, not a target."""
+    import oracle
+
+    def timed(fn):
+        n, t = 0, 0.0
+        while t < seconds or n == 0:
+            t0 = time.perf_counter()
+            fn()
+            t += time.perf_counter() - t0
+            n += 1
+        return n, t
+
+    def row(value, unit, sample):
+        return {"value": value, "unit": unit, "cores": 1, "kind": "oracle", "sample": sample}
+
+    out = {"host_cores_available": _host_cores(), "threads_used": 1}
+    x, w = wl.rmsnorm_input()
+    n, t = timed(lambda: oracle.rmsnorm(x, w, wl.RMS_EPS))
+    b = 2 * x.size * 4 + x.shape[1] * 4
+    out["rmsnorm"] = row(round(b * n / t / 1e9, 3), "GB/s",
+                         f"{n} calls on the full [{x.shape[0]}, {x.shape[1]}] fp32, {t:.1f} s")
+    sl, S = 2, wl.SM_S
+    s_ = wl.softmax_input(sl, S)
+    n, t = timed(lambda: oracle.causal_softmax(s_, wl.SM_SCALE))
+    b = sl * 2 * S * S * 2
+    out["causal_softmax"] = row(round(b * n / t / 1e9, 3), "GB/s",
+                                f"{n} calls on {sl} of the 128 [{S}, {S}] bf16 slices (fused ledger "
+                                f"2 N b, no skip), {t:.1f} s")
+    A, B, bias, R = wl.gemm_input(16)
+    n, t = timed(lambda: oracle.gemm_epilogue(A, B, bias, R, 0))
+    out["gemm_M16"] = row(round(2 * 16 * wl.GEMM_N * wl.GEMM_K * n / t / 1e12, 6), "TFLOP/s",
+                          f"{n} calls of the full 16 x 4096 x 4096 plan [4], {t:.1f} s")
+    A, B, bias, R = wl.gemm_input(4096)
+    rows_ = np.arange(0, 4096, 512)
+    n, t = timed(lambda: oracle.gemm_epilogue(A, B, bias, R, 0, rows=rows_))
+    per_row = t / n / rows_.size
+    out["gemm_M4096"] = row(round(2 * rows_.size * wl.GEMM_N * wl.GEMM_K * n / t / 1e12, 6), "TFLOP/s",
+                            f"{n} calls on {rows_.size} of the 4096 rows of 4096^3 plan [4], {t:.1f} s; "
+                            f"the whole problem would take {per_row * 4096:.0f} s")
+    q, k, v = wl.attention_input(1, wl.ATT_S, wl.ATT_D)
+    arows = np.arange(0, wl.ATT_S, 128) + 127
+    n, t = timed(lambda: oracle.attention(q, k, v, wl.ATT_SCALE, rows=arows))
+    fl = int(sum(4 * wl.ATT_D * (int(i) + 1) for i in arows))
+    out["attention"] = row(round(fl * n / t / 1e12, 6), "TFLOP/s",
+                           f"{n} calls on {arows.size} query rows of one [{wl.ATT_S}, {wl.ATT_D}] slice, "
+                           f"{t:.1f} s")
+    return out
 
 
 def run_reference(args, rank, world):

@@ -53,7 +53,16 @@ class fuse_kernel_record(ctypes.Structure):
                 ("local_bytes_per_thread", ctypes.c_int32), ("static_smem_bytes", ctypes.c_int32),
                 ("dynamic_smem_bytes", ctypes.c_int32), ("block_threads", ctypes.c_int32),
                 ("blocks_per_sm", ctypes.c_int32), ("max_threads_per_block", ctypes.c_int32),
-                ("cluster_size", ctypes.c_int32), ("max_active_clusters", ctypes.c_int32)]
+                ("cluster_size", ctypes.c_int32), ("max_active_clusters", ctypes.c_int32),
+                ("ptxas_registers", ctypes.c_int32), ("stack_bytes", ctypes.c_int32),
+                ("spill_store_bytes", ctypes.c_int32), ("spill_load_bytes", ctypes.c_int32),
+                ("symbol", ctypes.c_char * 256)]
+
+
+class fuse_ptxas_record(ctypes.Structure):
+    _fields_ = [("symbol", ctypes.c_char * 256), ("registers", ctypes.c_int32),
+                ("stack_bytes", ctypes.c_int32), ("spill_store_bytes", ctypes.c_int32),
+                ("spill_load_bytes", ctypes.c_int32)]
 
 
 _P, _I32, _I64, _U32, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
@@ -92,6 +101,8 @@ SIGNATURES = {
     "fuse_causal_softmax_bytes": ([_I64, _I64, _I32, _I32, _I32], _I64),
     "fuse_kernel_count": ([], _I32),
     "fuse_kernel_report": ([_I32, ctypes.POINTER(fuse_kernel_record)], _I32),
+    "fuse_ptxas_count": ([], _I32),
+    "fuse_ptxas_entry": ([_I32, ctypes.POINTER(fuse_ptxas_record)], _I32),
     "fuse_strerror": ([_I32], ctypes.c_char_p),
     "fuse_last_cuda_error": ([], ctypes.c_char_p),
     "fuse_check": ([_P], _I32),
@@ -423,8 +434,20 @@ def fuse_kernel_count() -> int:
 def fuse_kernel_report(index: int) -> dict:
     rec = fuse_kernel_record()
     _check(_load().fuse_kernel_report(index, ctypes.byref(rec)), "fuse_kernel_report")
-    return {f: (getattr(rec, f).decode() if f == "name" else getattr(rec, f))
+    return {f: (getattr(rec, f).decode() if f in ("name", "symbol") else getattr(rec, f))
             for f, _ in fuse_kernel_record._fields_}
+
+
+def fuse_ptxas_table() -> list[dict]:
+    """The ptxas -v record of every kernel compiled into the library (host only)."""
+    lib = _load()
+    out = []
+    for i in range(lib.fuse_ptxas_count()):
+        rec = fuse_ptxas_record()
+        _check(lib.fuse_ptxas_entry(i, ctypes.byref(rec)), "fuse_ptxas_entry")
+        out.append({f: (getattr(rec, f).decode() if f == "symbol" else getattr(rec, f))
+                    for f, _ in fuse_ptxas_record._fields_})
+    return out
 
 
 def fuse_check(stream=None) -> int:

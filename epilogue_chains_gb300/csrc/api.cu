@@ -58,11 +58,30 @@ int sm_count() {
     return cached[dev];
 }
 
+// The ptxas -v table of this build (generated from the build's own ptxas output and linked in).
+extern const fuse_ptxas_record kPtxasTable[];
+extern const int kPtxasCount;
+
 int describe_kernel(const void* kernel, const char* name, int block, int dyn_smem,
                     fuse_kernel_record* out) {
     if (!out) return FUSE_EINVAL;
     memset(out, 0, sizeof(*out));
     snprintf(out->name, sizeof(out->name), "%s", name);
+    out->ptxas_registers = out->stack_bytes = out->spill_store_bytes = out->spill_load_bytes = -1;
+    const char* sym = nullptr;
+    if (cudaFuncGetName(&sym, kernel) == cudaSuccess && sym) {
+        snprintf(out->symbol, sizeof(out->symbol), "%s", sym);
+        for (int i = 0; i < kPtxasCount; ++i) {
+            if (strcmp(kPtxasTable[i].symbol, out->symbol) != 0) continue;
+            out->ptxas_registers = kPtxasTable[i].registers;
+            out->stack_bytes = kPtxasTable[i].stack_bytes;
+            out->spill_store_bytes = kPtxasTable[i].spill_store_bytes;
+            out->spill_load_bytes = kPtxasTable[i].spill_load_bytes;
+            break;
+        }
+    } else {
+        (void)cudaGetLastError();
+    }
     cudaFuncAttributes a;
     cudaError_t e = cudaFuncGetAttributes(&a, kernel);
     if (e != cudaSuccess) return record_cuda_error(e);
@@ -145,6 +164,14 @@ extern "C" int fuse_kernel_report(int index, fuse_kernel_record* out) {
         index -= c;
     }
     return FUSE_EINVAL;
+}
+
+extern "C" int fuse_ptxas_count(void) { return fc::kPtxasCount; }
+
+extern "C" int fuse_ptxas_entry(int index, fuse_ptxas_record* out) {
+    if (!out || index < 0 || index >= fc::kPtxasCount) return FUSE_EINVAL;
+    *out = fc::kPtxasTable[index];
+    return FUSE_OK;
 }
 
 extern "C" const char* fuse_strerror(int status) {

@@ -355,7 +355,30 @@ typedef struct {
     int32_t max_threads_per_block;
     int32_t cluster_size;             /* CTAs per thread-block cluster as launched (1 = none)    */
     int32_t max_active_clusters;      /* clusters resident at once on the GPU (0 if no cluster)  */
+    /* What ptxas -v printed for this kernel when the library was built (the same figures as
+     * fuse_ptxas_entry(); -1 each if the build kept no record of the kernel):                   */
+    int32_t ptxas_registers;
+    int32_t stack_bytes;              /* per-thread stack frame                                  */
+    int32_t spill_store_bytes;        /* bytes of register spill stores per thread               */
+    int32_t spill_load_bytes;         /* bytes of register spill loads per thread                */
+    char symbol[256];                 /* mangled device symbol ("" if the runtime cannot name it) */
 } fuse_kernel_record;
+
+/* The ptxas -v record of every kernel entry compiled into this library ([K4] §③ and [C05] §6.2:
+ * a fused kernel that needs more registers than the SM grants spills, and the spill traffic is
+ * the cost that decides against fusing).  The build parses its own ptxas output into a table
+ * linked into the library, so these two calls are host only and need no GPU.
+ *   fuse_ptxas_count() = number of entries; fuse_ptxas_entry(i, out) fills *out for entry i
+ *   (FUSE_EINVAL if out is NULL or i is out of range). */
+typedef struct {
+    char symbol[256];                 /* mangled entry name as ptxas printed it                 */
+    int32_t registers;
+    int32_t stack_bytes;
+    int32_t spill_store_bytes;
+    int32_t spill_load_bytes;
+} fuse_ptxas_record;
+int fuse_ptxas_count(void);
+int fuse_ptxas_entry(int index, fuse_ptxas_record* out);
 
 /* Number of kernel variants fuse_kernel_report() knows (index 0 .. count-1). */
 int fuse_kernel_count(void);

@@ -63,6 +63,51 @@ def test_host_side_validation_needs_no_gpu():
     assert fc.fuse_strerror(fc.FUSE_ETIMEOUT).startswith("bounded device wait")
 
 
+# ------------------------------------------------------------------------------ ptxas table
+def _entries(table, stem):
+    return [r for r in table if stem in r["symbol"]]
+
+
+def test_ptxas_table_covers_every_kernel_family_without_spills():
+    """[K4] §③ / [C05] §6.2: spill bytes are the signal that a fused kernel has outgrown the
+    register file.  The table is the build's own ptxas -v output, read without a GPU."""
+    table = fc.fuse_ptxas_table()
+    assert len(table) == fc._load().fuse_ptxas_count() > 0
+    for stem in ("chain_fused_kernel", "chain_stage_kernel", "chain_fat_kernel", "rmsnorm_row_kernel",
+                 "rms_square_kernel", "rms_rowmean_kernel", "rms_scale_kernel", "rms_weight_kernel",
+                 "softmax_fused_kernel", "sm_rowmax_kernel", "sm_sub_kernel", "sm_exp_kernel",
+                 "sm_rowsum_kernel", "sm_div_kernel", "gemm_tc_kernel", "gemm_decode_kernel",
+                 "epi_tail_kernel", "attn_persist_kernel", "silu_mul_vec_kernel", "residual_add_kernel"):
+        rows = _entries(table, stem)
+        assert rows, stem
+        for r in rows:
+            assert r["registers"] > 0, r
+            assert r["spill_store_bytes"] == 0 and r["spill_load_bytes"] == 0, r
+            assert r["stack_bytes"] == 0, r
+    with pytest.raises(fc.FuseError):
+        fc._check(fc._load().fuse_ptxas_entry(len(table), ctypes.byref(fc.fuse_ptxas_record())), "entry")
+    assert fc._load().fuse_ptxas_entry(0, None) == fc.FUSE_EINVAL
+
+
+def _blocks_per_sm_by_registers(regs, threads=256):
+    # registers are granted per warp in units of 256 (a per-thread count rounded up to 8); 64 Ki
+    # registers, 2048 threads and 32 blocks per SM
+    per_warp = -(-regs * 32 // 256) * 256
+    return min(65536 // (per_warp * (threads // 32)), 2048 // threads, 32)
+
+
+def test_fat_probe_collapses_occupancy_in_the_ptxas_figures():
+    """[C05] §6.2: 48 live temporaries per element push the fat kernel's registers so high that
+    one 256-thread block fits an SM, where the thin fused kernel keeps the SM full."""
+    table = fc.fuse_ptxas_table()
+    fat = [r for r in _entries(table, "chain_fat_kernel") if "kernelIf" in r["symbol"]]
+    fused = [r for r in _entries(table, "chain_fused_kernel") if "kernelIf" in r["symbol"]]
+    assert len(fat) == 1 and len(fused) == 1
+    assert fat[0]["registers"] >= 192
+    assert _blocks_per_sm_by_registers(fat[0]["registers"]) == 1
+    assert _blocks_per_sm_by_registers(fused[0]["registers"]) == 8
+
+
 # ------------------------------------------------------------------------------ ledgers
 def mlp_epilogue_stages(M, N, K):
     """[K4] §① chain_mlp_epilogue: mm -> +bias -> GELU -> +residual."""

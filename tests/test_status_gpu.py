@@ -36,3 +36,16 @@ def test_kernel_report_covers_every_variant(cuda_device):
         assert r["regs_per_thread"] > 0 and r["blocks_per_sm"] >= 1, r
     with pytest.raises(fc.FuseError):
         fc.fuse_kernel_report(n)
+
+
+def test_kernel_report_carries_the_ptxas_figures_of_its_build(cuda_device):
+    """Every reported kernel is found, by its device symbol, in the ptxas -v table the build
+    linked in; ptxas's register count is the one the runtime reports; no kernel spills."""
+    table = {r["symbol"]: r for r in fc.fuse_ptxas_table()}
+    for i in range(fc.fuse_kernel_count()):
+        r = fc.fuse_kernel_report(i)
+        assert r["symbol"] in table, r["name"]
+        t = table[r["symbol"]]
+        assert r["ptxas_registers"] == t["registers"] == r["regs_per_thread"], r["name"]
+        assert r["spill_store_bytes"] == 0 and r["spill_load_bytes"] == 0, r["name"]
+        assert r["stack_bytes"] == 0 and r["local_bytes_per_thread"] == 0, r["name"]
