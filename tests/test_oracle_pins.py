@@ -360,6 +360,90 @@ def test_softmax_unfused_oracle_tracks_fused_within_4_ulp():
     assert np.all(b[:, iu[0], iu[1]] == 0) and np.all(b[:, 0, 0] == 0x3F80)
 
 
+def _bf16_round_signed(q: Fraction) -> Fraction:
+    """Nearest-even bf16 value of a rational of normal magnitude (or zero), by integer steps."""
+    if q == 0:
+        return Fraction(0)
+    v = Fraction(oracle.bf16_value(_bf16_round_fraction(abs(q))))
+    return v if q > 0 else -v
+
+
+# The reference below takes [OFCG] fusion_lab [E]'s five steps one at a time, each stored before
+# the next, in an arithmetic of its own (numpy fp32 scalars for the fp32 steps, exact fractions
+# for the sum and the division, integer nearest-even rounding to bf16).  `mutation` drops or moves
+# one rounding point, to show that each one is seen by the comparison.
+_SOFTMAX_MUTATIONS = ("no_d_round", "no_e_round", "d_exact_then_bf16", "z_in_double",
+                      "z_rounded_to_bf16", "sum_of_unrounded_e", "numerator_unrounded_e")
+
+
+def _unfused_softmax_reference(vals, scale, mutation=None):
+    S = vals.shape[0]
+    out = np.zeros((S, S), dtype=object)
+    sc = np.float32(scale)
+    for i in range(S):
+        if mutation == "z_in_double":
+            z = [Fraction(float(vals[i, j])) * Fraction(float(scale)) for j in range(i + 1)]
+        else:
+            z = [Fraction(float(np.float32(np.float32(vals[i, j]) * sc))) for j in range(i + 1)]
+            if mutation == "z_rounded_to_bf16":
+                z = [_bf16_round_signed(t) for t in z]
+        m = max(z)                                                  # step 1: row max
+        e, e_raw = [], []
+        for j in range(i + 1):                                      # step 2: subtract, stored bf16
+            if mutation in ("z_in_double", "d_exact_then_bf16"):
+                d = z[j] - m
+            else:
+                d = Fraction(float(np.float32(np.float32(float(z[j])) - np.float32(float(m)))))
+            dq = d if mutation == "no_d_round" else _bf16_round_signed(d)
+            x = Fraction(math.exp(float(dq)))                       # step 3: exp, stored bf16
+            e_raw.append(x)
+            e.append(x if mutation == "no_e_round" else _bf16_round_signed(x))
+        l = sum(e_raw if mutation == "sum_of_unrounded_e" else e, Fraction(0))   # step 4: row sum
+        for j in range(i + 1):                                      # step 5: divide
+            num = e_raw[j] if mutation == "numerator_unrounded_e" else e[j]
+            out[i, j] = num / l
+    return out
+
+
+@pytest.mark.parametrize("scale", [1.0 / 16.0, 0.3])
+def test_softmax_unfused_rounding_points_brute_force(scale):
+    """orc_causal_softmax_unfused against the five stored steps done by hand, bit for bit, at the
+    workload's scale (1/16, exact in fp32) and at 0.3 (where the fp32 steps round)."""
+    BH, S = 16, 8
+    s = wl.softmax_input(BH, S, salt=11)
+    got = oracle.causal_softmax(s, scale, unfused=True)
+    got32 = oracle.causal_softmax(s, scale, out="f32", unfused=True)
+    for bh in range(BH):
+        vals = np.array([[oracle.bf16_value(h) for h in row] for row in s[bh]])
+        ref = _unfused_softmax_reference(vals, scale)
+        for i in range(S):
+            for j in range(S):
+                if j > i:
+                    assert got[bh, i, j] == 0 and got32[bh, i, j] == 0
+                    continue
+                assert got[bh, i, j] == _bf16_round_fraction(ref[i, j]), (bh, i, j)
+                assert got32[bh, i, j] == np.float32(float(ref[i, j])), (bh, i, j)
+
+
+def test_softmax_unfused_pin_sees_every_rounding_point():
+    """Each mutation of the hand reference (one rounding dropped or moved) changes at least one
+    output bit on the inputs the brute-force pin uses, so an oracle with that mistake fails it."""
+    BH, S = 16, 8
+    s = wl.softmax_input(BH, S, salt=11)
+    seen = {m: False for m in _SOFTMAX_MUTATIONS}
+    for scale in (1.0 / 16.0, 0.3):
+        for bh in range(BH):
+            vals = np.array([[oracle.bf16_value(h) for h in row] for row in s[bh]])
+            ref = _unfused_softmax_reference(vals, scale)
+            for mut in _SOFTMAX_MUTATIONS:
+                if seen[mut]:
+                    continue
+                bad = _unfused_softmax_reference(vals, scale, mut)
+                seen[mut] = any(_bf16_round_fraction(bad[i, j]) != _bf16_round_fraction(ref[i, j])
+                                for i in range(S) for j in range(i + 1))
+    assert all(seen.values()), seen
+
+
 # ============================================================== O5 GEMM epilogue
 PHI = {1.0: 0.8413447460685429, 2.0: 0.9772498680518208, -1.0: 0.15865525393145705,
        0.5: 0.6914624612740131, 3.0: 0.9986501019683699, 0.0: 0.5, -2.0: 0.022750131948179195}
