@@ -19,9 +19,8 @@ every two of them.  A separate pass after the timed region brackets single calls
 
 ``value`` = fused-chain algorithmic bytes (2 N b per call, N b read + N b written) / the fused
 chain groups' device time.  ``e2e`` = the same bytes / the time of the same chains run through
-the C ABI from pinned host memory: each call's x is copied in and its y copied out in slices, the
-copies in on one stream, the kernels on a second, the copies out on a third (ordered by events),
-so both copy directions overlap the kernels.
+the C ABI's host-buffer entry point (fuse_chain_run_host) from pinned host memory: each call
+copies its x in and its y out in slices whose copies overlap the kernels.
 
 ``--impl reference`` times the plain CPU oracle (the only other place this script runs it) on
 the same workload on the host cores, rank 0 only.
@@ -644,7 +643,8 @@ def run_ours(args, rank, world, local):
         r_ = fc.fuse_kernel_report(i)
         report_rows.append({k: r_[k] for k in ("name", "regs_per_thread", "local_bytes_per_thread",
                                                "dynamic_smem_bytes", "block_threads", "blocks_per_sm",
-                                               "cluster_size", "max_active_clusters", "ptxas_registers",
+                                               "cluster_size", "max_active_clusters", "blocks_per_sm_api",
+                                               "tmem_cols", "ptxas_registers",
                                                "stack_bytes", "spill_store_bytes", "spill_load_bytes")})
     rows["kernel_report"] = report_rows
 
@@ -679,7 +679,8 @@ def run_ours(args, rank, world, local):
             "nominal_hbm_gbs": NOMINAL_HBM_GBS,
             "roofline": roofline,
             "e2e": {"value": round(e2e_value, 1), "unit": "GB/s",
-                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"]},
+                    "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+                    "path": f"fuse_chain_run_host (C ABI, pinned host x and y, {e2e['slices']} slices per call)"},
             "gpu_launches": timed_launches,
             "clocks": clocks,
             "rows": rows,
@@ -879,79 +880,48 @@ def planner_rows(fc, wl, peaks, launch_us, measured_ms, plans):
     return out
 
 
-def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world, chunks=4):
-    """Per K: the fused chain through the C ABI on x from pinned host memory, y back to pinned host
-    memory.  The chain is element-wise, so each call is issued as `chunks` calls on consecutive
-    slices.  Host-to-device copies run back to back on one stream, the kernels on a second and
-    device-to-host copies on a third, ordered by events (a slice's kernel after its copy in and
-    after the previous read-out of its y slice; its copy in after the previous kernel on that
-    slice), so both copy directions stay busy while the kernels run.  Bytes moved per step: x in
-    and y out once per K."""
+def run_e2e(args, fc, lib, wl, stage_sets, N, KS, chain_bytes, dev, stream, world, slices=8):
+    """Per K: the fused chain through the C ABI's host-buffer entry point, fuse_chain_run_host():
+    x from pinned host memory, y back to pinned host memory, through device scratch the caller
+    owns.  The library cuts each call into `slices` pieces whose copies in (one helper stream),
+    kernels (the caller's stream) and copies out (a second helper stream) overlap.  Bytes moved
+    per step: x in and y out once per K."""
     import torch
     hx = torch.from_numpy(wl.chain_input(N, salt=7)).pin_memory()
     hy = torch.empty(N, dtype=torch.float32).pin_memory()
     dx = torch.empty(N, dtype=torch.float32, device=dev)
     dy = torch.empty(N, dtype=torch.float32, device=dev)
-    s_in, s_run, s_out = stream, torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-    csz = (N + chunks - 1) // chunks
-    ev = {k: [torch.cuda.Event() for _ in range(chunks)] for k in ("in", "run", "out")}
-    started = [False] * chunks
+    sh = stream.cuda_stream
 
     def one_step():
         for K in KS:
-            for c in range(chunks):
-                lo, hi = c * csz, min(N, (c + 1) * csz)
-                if started[c]:
-                    s_in.wait_event(ev["run"][c])          # the last kernel on this slice has read dx
-                with torch.cuda.stream(s_in):
-                    dx[lo:hi].copy_(hx[lo:hi], non_blocking=True)
-                ev["in"][c].record(s_in)
-                s_run.wait_event(ev["in"][c])
-                if started[c]:
-                    s_run.wait_event(ev["out"][c])         # the last read-out of this dy slice is done
-                rc = lib.fuse_chain_run(stage_sets[K], K, dx[lo:].data_ptr(), dy[lo:].data_ptr(), hi - lo,
-                                        fc.FUSE_F32, fc.FUSE_FUSED, s_run.cuda_stream)
-                if rc != 0:
-                    raise fc.FuseError(rc, "fuse_chain_run")
-                ev["run"][c].record(s_run)
-                s_out.wait_event(ev["run"][c])
-                with torch.cuda.stream(s_out):
-                    hy[lo:hi].copy_(dy[lo:hi], non_blocking=True)
-                ev["out"][c].record(s_out)
-                started[c] = True
-
-    def join():
-        # the first stream waits for the others, so one event on it closes the step
-        for st in (s_run, s_out):
-            e = torch.cuda.Event()
-            e.record(st)
-            s_in.wait_event(e)
+            rc = lib.fuse_chain_run_host(stage_sets[K], K, hx.data_ptr(), hy.data_ptr(), N, fc.FUSE_F32,
+                                         fc.FUSE_FUSED, dx.data_ptr(), dy.data_ptr(), slices, sh)
+            if rc != 0:
+                raise fc.FuseError(rc, "fuse_chain_run_host")
 
     for _ in range(2):
         one_step()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     steps = max(3, min(args.steps, 10))
-    e0.record(s_in)
-    for st in (s_run, s_out):
-        st.wait_stream(s_in)
+    e0.record(stream)
     for _ in range(steps):
         one_step()
-    join()
-    e1.record(s_in)
+    e1.record(stream)
     torch.cuda.synchronize()
-    # the sliced, pipelined calls must give what one call on the whole vector gives
+    # the sliced, pipelined call must give what one device call on the whole vector gives
     with torch.cuda.stream(stream):
         rc = lib.fuse_chain_run(stage_sets[KS[-1]], KS[-1], dx.data_ptr(), dy.data_ptr(), N, fc.FUSE_F32,
-                                fc.FUSE_FUSED, stream.cuda_stream)
+                                fc.FUSE_FUSED, sh)
         if rc != 0:
             raise fc.FuseError(rc, "fuse_chain_run")
     torch.cuda.synchronize()
     if not torch.equal(hy.to(dev), dy):
-        raise RuntimeError("e2e: pipelined slices differ from the whole-vector call")
+        raise RuntimeError("e2e: the host-buffer call differs from the whole-vector device call")
     elapsed = e0.elapsed_time(e1) / 1e3
     return {"_elapsed": elapsed, "_bytes": steps * len(KS) * chain_bytes,
-            "h2d": len(KS) * N * 4, "d2h": len(KS) * N * 4}
+            "h2d": len(KS) * N * 4, "d2h": len(KS) * N * 4, "slices": slices}
 
 
 # ------------------------------------------------------------------------------ oracle arms
@@ -1098,12 +1068,13 @@ def run_profile(args):
         rows = args.size or wl.RMS_ROWS
         mode = fc.FUSE_FUSED if name == "rmsnorm_fused" else fc.FUSE_UNFUSED
         x0, w = wl.rmsnorm_input(rows, wl.RMS_HIDDEN, device=dev)
-        xs = [x0] + [x0.clone() for _ in range(7)]
-        ys = [torch.empty_like(x0) for _ in range(8)]
+        npairs = 8 if rows <= 4096 else 2     # large sizes: 2 pairs already exceed L2
+        xs = [x0] + [x0.clone() for _ in range(npairs - 1)]
+        ys = [torch.empty_like(x0) for _ in range(npairs)]
         ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.RMS_HIDDEN, mode)),
                          dtype=torch.uint8, device=dev)
         for i in range(L):
-            rc = lib.fuse_rmsnorm(xs[i % 8].data_ptr(), w.data_ptr(), ys[i % 8].data_ptr(), rows,
+            rc = lib.fuse_rmsnorm(xs[i % npairs].data_ptr(), w.data_ptr(), ys[i % npairs].data_ptr(), rows,
                                   wl.RMS_HIDDEN, wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_rmsnorm_bytes(rows, wl.RMS_HIDDEN, mode)
@@ -1111,13 +1082,14 @@ def run_profile(args):
         rows = args.size or wl.ADDRMS_ROWS
         mode = fc.FUSE_FUSED if name == "add_rmsnorm_fused" else fc.FUSE_UNFUSED
         x, r, w = wl.add_rmsnorm_input(rows, wl.ADDRMS_HIDDEN, device=dev)
-        xs, rs = [x] + [x.clone() for _ in range(3)], [r] + [r.clone() for _ in range(3)]
-        hs, ys = [torch.empty_like(x) for _ in range(4)], [torch.empty_like(x) for _ in range(4)]
+        ns = 4 if rows <= 4096 else 2
+        xs, rs = [x] + [x.clone() for _ in range(ns - 1)], [r] + [r.clone() for _ in range(ns - 1)]
+        hs, ys = [torch.empty_like(x) for _ in range(ns)], [torch.empty_like(x) for _ in range(ns)]
         ws = torch.empty(max(1, fc.fuse_rmsnorm_workspace_bytes(rows, wl.ADDRMS_HIDDEN, mode)),
                          dtype=torch.uint8, device=dev)
         for i in range(L):
-            rc = lib.fuse_add_rmsnorm(xs[i % 4].data_ptr(), rs[i % 4].data_ptr(), w.data_ptr(),
-                                      hs[i % 4].data_ptr(), ys[i % 4].data_ptr(), rows, wl.ADDRMS_HIDDEN,
+            rc = lib.fuse_add_rmsnorm(xs[i % ns].data_ptr(), rs[i % ns].data_ptr(), w.data_ptr(),
+                                      hs[i % ns].data_ptr(), ys[i % ns].data_ptr(), rows, wl.ADDRMS_HIDDEN,
                                       wl.RMS_EPS, mode, ws.data_ptr(), ws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_add_rmsnorm_bytes(rows, wl.ADDRMS_HIDDEN, mode)

@@ -54,6 +54,7 @@ class fuse_kernel_record(ctypes.Structure):
                 ("dynamic_smem_bytes", ctypes.c_int32), ("block_threads", ctypes.c_int32),
                 ("blocks_per_sm", ctypes.c_int32), ("max_threads_per_block", ctypes.c_int32),
                 ("cluster_size", ctypes.c_int32), ("max_active_clusters", ctypes.c_int32),
+                ("blocks_per_sm_api", ctypes.c_int32), ("tmem_cols", ctypes.c_int32),
                 ("ptxas_registers", ctypes.c_int32), ("stack_bytes", ctypes.c_int32),
                 ("spill_store_bytes", ctypes.c_int32), ("spill_load_bytes", ctypes.c_int32),
                 ("symbol", ctypes.c_char * 256)]
@@ -70,6 +71,7 @@ _P, _I32, _I64, _U32, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64
 # every symbol the header declares, with its C signature
 SIGNATURES = {
     "fuse_chain_run": ([ctypes.POINTER(fuse_stage), _I32, _P, _P, _I64, _I32, _I32, _P], _I32),
+    "fuse_chain_run_host": ([ctypes.POINTER(fuse_stage), _I32, _P, _P, _I64, _I32, _I32, _P, _P, _I32, _P], _I32),
     "fuse_rmsnorm": ([_P, _P, _P, _I64, _I64, _F32, _I32, _P, _SZ, _P], _I32),
     "fuse_rmsnorm_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "fuse_rmsnorm_unfused_static": ([_P, _P, _P, _I64, _I64, _F32, _P], _I32),
@@ -107,6 +109,7 @@ SIGNATURES = {
     "fuse_last_cuda_error": ([], ctypes.c_char_p),
     "fuse_check": ([_P], _I32),
     "fuse_debug_expire_wait": ([_I64, _P], _I32),
+    "fuse_debug_split_window": ([_I64], _I32),
     "fuse_graph_begin": ([_P], _I32),
     "fuse_graph_end": ([_P, ctypes.POINTER(ctypes.c_void_p)], _I32),
     "fuse_graph_launch": ([_P, _P], _I32),
@@ -199,6 +202,24 @@ def fuse_chain_run(stages, x, y, mode: int = FUSE_FUSED, stream=None) -> None:
     st = _stages(stages)
     _check(_load().fuse_chain_run(st, len(st), _ptr(x), _ptr(y), x.numel(), _dtype_code(x), mode,
                                   _stream(stream)), "fuse_chain_run")
+
+
+def fuse_chain_run_host(stages, x_host, y_host, x_dev, y_dev, mode: int = FUSE_FUSED, slices: int = 8,
+                        stream=None) -> None:
+    """The chain on host tensors (x_host in, y_host out; pinned for asynchronous copies) through
+    the caller's device scratch x_dev, y_dev (same dtype and element count); see fusechain.h.
+    y_host is valid after the stream is synchronized."""
+    _need_device(x_dev, y_dev)
+    for t in (x_host, y_host):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("x_host and y_host must be contiguous host tensors")
+    n = x_host.numel()
+    if any(t.numel() != n or t.dtype != x_host.dtype for t in (y_host, x_dev, y_dev)):
+        raise ValueError("all four tensors must have the same dtype and element count")
+    st = _stages(stages)
+    _check(_load().fuse_chain_run_host(st, len(st), _ptr(x_host), _ptr(y_host), n, _dtype_code(x_host),
+                                       mode, _ptr(x_dev), _ptr(y_dev), int(slices), _stream(stream)),
+           "fuse_chain_run_host")
 
 
 def fuse_rmsnorm(x, w, y, eps: float, mode: int = FUSE_FUSED, workspace=None, stream=None) -> None:

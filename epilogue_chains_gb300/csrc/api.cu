@@ -63,7 +63,7 @@ extern const fuse_ptxas_record kPtxasTable[];
 extern const int kPtxasCount;
 
 int describe_kernel(const void* kernel, const char* name, int block, int dyn_smem,
-                    fuse_kernel_record* out) {
+                    fuse_kernel_record* out, int tmem_cols) {
     if (!out) return FUSE_EINVAL;
     memset(out, 0, sizeof(*out));
     snprintf(out->name, sizeof(out->name), "%s", name);
@@ -91,10 +91,30 @@ int describe_kernel(const void* kernel, const char* name, int block, int dyn_sme
     out->dynamic_smem_bytes = dyn_smem;
     out->block_threads = block;
     out->max_threads_per_block = a.maxThreadsPerBlock;
+    out->tmem_cols = tmem_cols;
     int b = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, dyn_smem);
     if (e != cudaSuccess) return record_cuda_error(e);
-    out->blocks_per_sm = b;
+    out->blocks_per_sm_api = b;
+    // residency from the SM's own limits: threads, blocks, registers (allocated per warp in units
+    // of 256), shared memory (each CTA also reserves some) and the 512 tensor-memory columns
+    int dev = 0, thr = 0, blk = 0, regs = 0, smem = 0, rsv = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&thr, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&blk, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&regs, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&rsv, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess)
+        return record_cuda_error(e);
+    const int warps = (block + 31) / 32;
+    const int regs_per_warp = (a.numRegs * 32 + 255) / 256 * 256;
+    int n = blk;
+    n = n < thr / block ? n : thr / block;
+    if (regs_per_warp > 0) n = n < regs / (regs_per_warp * warps) ? n : regs / (regs_per_warp * warps);
+    const int per_cta = dyn_smem + static_cast<int>(a.sharedSizeBytes) + rsv;
+    n = n < smem / per_cta ? n : smem / per_cta;
+    if (tmem_cols > 0) n = n < 512 / tmem_cols ? n : 512 / tmem_cols;
+    out->blocks_per_sm = n;
     out->cluster_size = 1;
     out->max_active_clusters = 0;
     return FUSE_OK;

@@ -1086,7 +1086,8 @@ int attn_report(int i, fuse_kernel_record* out) {
     if (rc != FUSE_OK) return rc;
     const int r2 = describe_kernel((const void*)attn_persist_kernel<256>,
                                    "attn_persist_kernel<D=256> (tcgen05 2-SM, M=256, persistent)",
-                                   kPersistThreads, static_cast<int>(PairLayout<256>::SMEM), out);
+                                   kPersistThreads, static_cast<int>(PairLayout<256>::SMEM), out,
+                                   static_cast<int>(PairLayout<256>::TMEM_COLS));
     if (r2 == FUSE_OK) out->cluster_size = 2;
     return r2;
 }

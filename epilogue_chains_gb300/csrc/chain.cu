@@ -12,6 +12,8 @@
 // ld/st.global.cs, sm_100+), an exact grid of many short CTAs (measured on GB300 to match
 // cudaMemcpy at this size, where persistent grid-stride loops and TMA bulk-copy pipelines were
 // slower), and stage coefficients in a __grid_constant__ parameter read from the constant bank.
+#include <mutex>
+
 #include "fc_internal.cuh"
 
 namespace fc {
@@ -27,6 +29,7 @@ struct ChainParams {
     int64_t nvec;   // 32-byte vectors in the body (fused/unfused); the fat probe reads the same
                     // body in groups of 4 elements
     int K;
+    int prefetch;   // 1: start this CTA's input on its way into L2 before the grid-dependency wait
     uint32_t relu_mask;
     float a[FUSE_MAX_STAGES];
     float b[FUSE_MAX_STAGES];
@@ -79,15 +82,33 @@ __device__ __forceinline__ void chain_body(const ChainParams& p) {
     }
 }
 
+// This CTA's share of the 32-byte-aligned body on its way into L2 while the preceding kernel may
+// still run, then the grid-dependency wait (before any global-memory load or store).  Not for an
+// unfused stage after the first: its input is the intermediate the preceding stage is writing,
+// already in L2 or about to be overwritten, and fetching it from DRAM early only adds traffic
+// (measured: the K = 8 unfused chain at N = 2^24 went from 104 to 113 us with it).
+template <typename T>
+__device__ __forceinline__ void prefetch_then_wait(const ChainParams& p) {
+    pdl_trigger();
+    if (p.prefetch && threadIdx.x == 0) {
+        const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kBlock;
+        const int64_t nv = p.nvec - v0 < kBlock ? p.nvec - v0 : kBlock;
+        if (nv > 0)
+            prefetch_l2_bulk(static_cast<const T*>(p.x) + p.head + v0 * Vec32<T>::N,
+                             static_cast<uint32_t>(nv) * 32u);
+    }
+    pdl_wait();
+}
+
 template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_fused_kernel(const __grid_constant__ ChainParams p) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    prefetch_then_wait<T>(p);
     chain_body<T, false>(p);
 }
 
 template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_stage_kernel(const __grid_constant__ ChainParams p) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    prefetch_then_wait<T>(p);
     chain_body<T, true>(p);
 }
 
@@ -201,6 +222,7 @@ unsigned exact_grid(const ChainParams& p) {
 template <typename T>
 int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
     ChainParams p = base;
+    p.prefetch = 1;
     partition<T>(p, p.x, p.y);
     if (mode == FUSE_FUSED) {
         return launch_pdl(chain_fused_kernel<T>, dim3(exact_grid<T>(p)), dim3(kBlock), 0, stream, 1, p);
@@ -221,6 +243,7 @@ int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
         q.b[0] = base.b[s];
         q.relu_mask = (base.relu_mask >> s) & 1u;
         if (s > 0) q.x = base.y;
+        q.prefetch = s == 0;
         partition<T>(q, q.x, q.y);
         const int rc = launch_pdl(chain_stage_kernel<T>, dim3(exact_grid<T>(q)), dim3(kBlock), 0, stream, 1, q);
         if (rc != FUSE_OK) return rc;
@@ -282,6 +305,84 @@ extern "C" int fuse_chain_run(const fuse_stage* stages, int K, const void* x, vo
         case FUSE_F16: return launch_chain<__half>(p, mode, st);
         default: return launch_chain<__nv_bfloat16>(p, mode, st);
     }
+}
+
+namespace fc {
+namespace {
+// Per-device helper streams and events of fuse_chain_run_host(), created at the first call on a
+// device and kept for the life of the process.
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t entry = nullptr, in = nullptr, run = nullptr, out = nullptr;
+};
+HostPipe g_pipes[64];
+
+int host_pipe_init(HostPipe& hp) {
+    if (hp.ready) return FUSE_OK;
+    cudaError_t e;
+    if ((e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.entry, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.in, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.run, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&hp.out, cudaEventDisableTiming)) != cudaSuccess)
+        return record_cuda_error(e);
+    hp.ready = true;
+    return FUSE_OK;
+}
+}  // namespace
+}  // namespace fc
+
+extern "C" int fuse_chain_run_host(const fuse_stage* stages, int K, const void* x_host, void* y_host,
+                                   int64_t n, int dtype, int mode, void* x_dev, void* y_dev, int slices,
+                                   fuse_stream_t stream) {
+    using namespace fc;
+    if (!stages || K < 1 || K > FUSE_MAX_STAGES || n < 0 || slices < 1 || slices > 64) return FUSE_EINVAL;
+    if (dtype != FUSE_F32 && dtype != FUSE_F16 && dtype != FUSE_BF16) return FUSE_EINVAL;
+    if (mode != FUSE_FUSED && mode != FUSE_UNFUSED && mode != FUSE_FAT) return FUSE_EINVAL;
+    if (n == 0) return FUSE_OK;
+    if (!x_host || !y_host || !x_dev || !y_dev) return FUSE_EINVAL;
+    const int64_t eb = dtype == FUSE_F32 ? 4 : 2;
+    const uintptr_t xa = reinterpret_cast<uintptr_t>(x_dev), ya = reinterpret_cast<uintptr_t>(y_dev);
+    const uintptr_t bytes = static_cast<uintptr_t>(n * eb);
+    if (xa != ya && xa < ya + bytes && ya < xa + bytes) return FUSE_EINVAL;  // partial overlap
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    if (dev < 0 || dev >= 64) return FUSE_EUNSUPPORTED;
+    HostPipe& hp = g_pipes[dev];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    int rc = host_pipe_init(hp);
+    if (rc != FUSE_OK) return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // slices of whole 32-byte vectors, so each slice keeps the vector path of the whole call
+    int64_t per = (n + slices - 1) / slices;
+    per = (per + 31) / 32 * 32;
+    auto ok = [&](cudaError_t err) { return err == cudaSuccess ? FUSE_OK : record_cuda_error(err); };
+    // the copies start after the work already queued on `stream`
+    if ((rc = ok(cudaEventRecord(hp.entry, st))) || (rc = ok(cudaStreamWaitEvent(hp.s_in, hp.entry, 0))) ||
+        (rc = ok(cudaStreamWaitEvent(hp.s_out, hp.entry, 0))))
+        return rc;
+    for (int64_t lo = 0; lo < n; lo += per) {
+        const int64_t cnt = n - lo < per ? n - lo : per;
+        const size_t off = static_cast<size_t>(lo * eb), len = static_cast<size_t>(cnt * eb);
+        if ((rc = ok(cudaMemcpyAsync(static_cast<char*>(x_dev) + off, static_cast<const char*>(x_host) + off, len,
+                                     cudaMemcpyHostToDevice, hp.s_in))) ||
+            (rc = ok(cudaEventRecord(hp.in, hp.s_in))) || (rc = ok(cudaStreamWaitEvent(st, hp.in, 0))))
+            return rc;
+        if ((rc = fuse_chain_run(stages, K, static_cast<const char*>(x_dev) + off, static_cast<char*>(y_dev) + off,
+                                 cnt, dtype, mode, stream)))
+            return rc;
+        if ((rc = ok(cudaEventRecord(hp.run, st))) || (rc = ok(cudaStreamWaitEvent(hp.s_out, hp.run, 0))) ||
+            (rc = ok(cudaMemcpyAsync(static_cast<char*>(y_host) + off, static_cast<const char*>(y_dev) + off, len,
+                                     cudaMemcpyDeviceToHost, hp.s_out))))
+            return rc;
+    }
+    // `stream` resumes once the last slice is back in host memory
+    if ((rc = ok(cudaEventRecord(hp.out, hp.s_out))) || (rc = ok(cudaStreamWaitEvent(st, hp.out, 0)))) return rc;
+    return FUSE_OK;
 }
 
 extern "C" int64_t fuse_chain_bytes(int K, int64_t n, int dtype, int mode) {

@@ -33,6 +33,13 @@ __device__ __forceinline__ void pdl_begin() {
     pdl_trigger();
     pdl_wait();
 }
+// Start `bytes` of global memory at `ptr` on their way into L2 (both 16-byte aligned; nothing to
+// wait for).  Issued before pdl_wait(), it overlaps a kernel's first DRAM reads with the end of
+// the preceding kernel: L2 is the point of coherence of the device's memory, so the loads after
+// pdl_wait() still return what the preceding kernel wrote, only sooner.
+__device__ __forceinline__ void prefetch_l2_bulk(const void* ptr, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
 // Kernels with a set-up phase that touches no global memory (mbarrier init, TMEM allocation,
 // tensor-map prefetch) call pdl_trigger() at entry and pdl_wait() after the set-up, so the set-up
 // overlaps the end of the preceding kernel.
@@ -85,9 +92,10 @@ int blocks_per_sm(K kernel, int block, size_t dyn_smem = 0) {
     return b > 0 ? b : 1;
 }
 
-// Fill a kernel record from the runtime's attributes of `kernel` launched with (block, dyn_smem).
+// Fill a kernel record from the runtime's attributes of `kernel` launched with (block, dyn_smem),
+// each CTA allocating `tmem_cols` tensor-memory columns.
 int describe_kernel(const void* kernel, const char* name, int block, int dyn_smem,
-                    fuse_kernel_record* out);
+                    fuse_kernel_record* out, int tmem_cols = 0);
 
 inline bool is_aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 

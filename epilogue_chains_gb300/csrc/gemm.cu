@@ -61,9 +61,11 @@ constexpr uint32_t B_STAGE = (BN / 2) * BK * 2;  // 16 KB: this CTA's half of th
 constexpr uint32_t OFF_A = 0;
 constexpr uint32_t OFF_B = OFF_A + STAGES * A_STAGE;
 constexpr uint32_t OFF_BAR = OFF_B + STAGES * B_STAGE;
-// barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], part_written, part_read, drain
-constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 2 + 1;
-constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
+// barriers: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], part_written, part_read, drain,
+// role
+constexpr uint32_t N_BARS = STAGES * 2 + 2 + 2 + 2 + 1 + 1;
+constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;   // TMEM address (4 bytes)
+constexpr uint32_t OFF_ROLE = OFF_HOLD + 4;           // split tile: this CTA's ticket role
 // epilogue staging: per epilogue warp one 32-row x 128-byte tile (16-byte chunk j of row r at
 // slot j ^ (r % 8)), through which it transposes between its row-per-lane TMEM layout and
 // coalesced global accesses
@@ -84,9 +86,11 @@ struct MainArgs {
     const __half* bias;
     const __half* R;
     __half* Y;
-    float* part;         // split tiles: exchanged fp32 partial sums, [slot][rank] x 128 x 256
-    int* ready;          // split tiles: [slot][rank][column half] = epoch once that half is written
-    int epoch;           // this call's tag for `ready` (never 0)
+    float* part;         // split tiles: raw fp32 sums, [slot][K half][rank] x 128 x 256
+    unsigned long long* ticket;   // split tiles: [slot][rank] ticket word, (epoch << 32) | count
+    int* full;           // split tiles: [slot][rank] = epoch once a leaving part's sums are complete
+    int epoch;           // this call's tag for the ticket and full words (never 0)
+    long long partner_window;   // SM cycles a first part waits for the other's ticket
     int* flag;
 };
 
@@ -94,17 +98,20 @@ struct MainArgs {
 // r-th of two adjacent 128-row tiles), columns [n0, n0+256) shared by the pair, k-blocks
 // [kb0, kb1).  The first full_units units are whole pair tiles; the pair tiles of the last,
 // partial wave are split over K into two units (part 0: the first half of K, part 1: the second),
-// which exchange fp32 partial sums through global memory, each finishing one column half of the
+// so that the wave spreads over twice as many SMs (wave quantisation: 256 pair tiles on 76 pairs
+// would otherwise leave two thirds of the SMs idle for the last tile time).  The two parts
+// exchange fp32 partial sums through global memory; normally each finishes one column half of the
 // tile (part p adds the other part's sums of columns 128p..128p+127 and applies the epilogue
-// there, with all eight epilogue warps), so that the wave spreads over twice as many SMs (wave
-// quantisation: 256 pair tiles on 76 pairs would otherwise leave two thirds of the SMs idle for
-// the last tile time).  Splitting N instead
-// does not help: an M = 256, N = 128 MMA takes as long as an N = 256 one on this hardware.
+// there, with all eight epilogue warps).  Which part finishes what is settled by a ticket
+// (split_ticket) so that neither part ever waits for one that has not started: the parts need
+// not be resident at the same time.  Splitting N instead does not help: an M = 256, N = 128 MMA
+// takes as long as an N = 256 one on this hardware.
 struct Unit {
     int m0, n0, kb0, kb1;
     int part;   // -1: whole tile; 0 or 1: K half of a split tile
     int slot;   // split tile index
 };
+constexpr int kGroupRows = 16;   // pair rows per band of the tile order
 __device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank, int nk) {
     Unit r;
     int t = u;
@@ -120,9 +127,75 @@ __device__ __forceinline__ Unit unit_of(int u, const MainArgs& a, uint32_t rank,
         r.kb0 = r.part ? a.nk_split : 0;
         r.kb1 = r.part ? nk : a.nk_split;
     }
-    r.m0 = (2 * (t % a.pair_rows) + static_cast<int>(rank)) * BM;
-    r.n0 = (t / a.pair_rows) * BN;
+    // Tiles run in groups of kGroupRows pair rows, column by column within a group, so that the
+    // tiles in flight share a band of A that stays in L2 (16 x 256 rows of A at K = 4096 are
+    // 32 MB) while B is streamed once per band; with one band (M <= 4096) this is plain
+    // column-major order.  Walking all of M per column instead re-reads A from DRAM for every
+    // column of tiles once A outgrows L2 (measured at M = 32768: 5.7x the ledger's bytes).
+    const int per_group = kGroupRows * a.tiles_n;
+    const int g = t / per_group, first = g * kGroupRows;
+    const int rows = a.pair_rows - first < kGroupRows ? a.pair_rows - first : kGroupRows;
+    const int i = t - g * per_group;
+    r.m0 = (2 * (first + i % rows) + static_cast<int>(rank)) * BM;
+    r.n0 = (i / rows) * BN;
     return r;
+}
+
+// Roles of the two parts of a split tile, per CTA rank, from its ticket word (epoch << 32 | count;
+// any other epoch reads as count 0).  Each part first publishes the raw sums of the other part's
+// column half, then takes its ticket:
+//  * count 2: the other part took its ticket first and published its sums before: both finish
+//    their own column half (kRoleNormal);
+//  * count 1: first.  The other part may not have started (it need not be resident), so this one
+//    waits for it a bounded while (kPartnerWindow); if it takes its ticket meanwhile, kRoleNormal.
+//    Otherwise the first claims the word (count kLeft) and leaves the whole tile to the other:
+//    it publishes its sums of its own half too, then the full word (kRoleLeft);
+//  * count kLeft + 1: the other part left: wait for its full word (it is running, so the wait
+//    ends) and finish both halves (kRoleAlone).
+// Nobody waits for a party that has not taken its ticket, so no pair of clusters needs to be
+// co-resident.  The party that sees the final count resets the word to 0 (the full word is reset
+// by its reader), so a completed call leaves the workspace as it found it: a CUDA graph replay,
+// which reuses its epoch, starts from zeros.
+constexpr int kRoleFailed = 0, kRoleNormal = 1, kRoleLeft = 2, kRoleAlone = 3;
+constexpr unsigned long long kLeft = 0x100;
+constexpr long long kPartnerWindow = 100000;   // SM cycles, ~50 us (default)
+
+__device__ __forceinline__ unsigned long long ld_relaxed_gpu_u64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ int split_ticket(unsigned long long* tw, int epoch, long long window) {
+    const unsigned long long E = static_cast<unsigned long long>(static_cast<unsigned>(epoch)) << 32;
+    unsigned long long old = ld_relaxed_gpu_u64(tw), nw;
+    for (;;) {
+        nw = (old & 0xffffffff00000000ull) == E ? old + 1 : (E | 1ull);
+        const unsigned long long prev = atomicCAS(tw, old, nw);
+        if (prev == old) break;
+        old = prev;
+    }
+    const unsigned long long cnt = nw & 0xffffffffull;
+    if (cnt == 2) return kRoleNormal;
+    if (cnt == kLeft + 1) {
+        atomicExch(tw, 0ull);
+        return kRoleAlone;
+    }
+    if (cnt != 1) return kRoleFailed;
+    const long long t0 = clock64();
+    while (clock64() - t0 < window) {
+        if (ld_relaxed_gpu_u64(tw) == (E | 2ull)) {
+            atomicExch(tw, 0ull);
+            return kRoleNormal;
+        }
+    }
+    const unsigned long long prev = atomicCAS(tw, E | 1ull, E | kLeft);
+    if (prev == (E | 1ull)) return kRoleLeft;
+    if (prev == (E | 2ull)) {
+        atomicExch(tw, 0ull);
+        return kRoleNormal;
+    }
+    return kRoleFailed;
 }
 
 __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
@@ -138,9 +211,10 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
     auto empty_bar = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bar0 + 8u * (N_BARS - 1);
+    const uint32_t drain_bar = bar0 + 8u * (N_BARS - 2);
     // the eight epilogue warps of a split unit have written (read) the exchanged partial sums
-    const uint32_t part_written = bar0 + 8u * (N_BARS - 3), part_read = bar0 + 8u * (N_BARS - 2);
+    const uint32_t part_written = bar0 + 8u * (N_BARS - 4), part_read = bar0 + 8u * (N_BARS - 3);
+    const uint32_t role_bar = bar0 + 8u * (N_BARS - 1);
     const uint32_t holder = base + OFF_HOLD;
     const int total_units = args.units;
     const int nk = (args.K + BK - 1) / BK;
@@ -172,6 +246,7 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         mbar_init(drain_bar, 1);
         mbar_init(part_written, kEpiWarps);
         mbar_init(part_read, kEpiWarps);
+        mbar_init(role_bar, 1);
         fence_mbar_init();
         prefetch_map(&mapA);
         prefetch_map(&mapB);
@@ -268,10 +343,8 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         // and transposed through the warp's staging tile: the residual chunk is loaded that way
         // one chunk ahead, written to the tile and read back by rows; the fp16 results are
         // written to the tile by rows and stored by row segments.
-        // Split tiles: the first K half stores its raw fp32 sums (`part`) the same way and
-        // publishes them with a release store of the call's epoch into `ready`; the second K half
-        // waits for that epoch (acquire), adds the partial sums and applies the epilogue, then
-        // clears `ready` for the next call.
+        // Split tiles exchange raw fp32 sums through the caller's workspace; which part finishes
+        // which columns is settled by a ticket (split_ticket).
         constexpr int CH = 64;
         constexpr int PER = (BN / CH) / 2;   // chunks of each warp per unit
         const int q = warp % 4;
@@ -289,13 +362,10 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
         uint32_t acc_phase = 0;
         bool ok = true;
         uint4 rnext[8];
-        // The chunks of a unit this warp handles, in order: whole tiles: 2h and 2h + 1 (both
-        // finished here); split tiles (part p): first chunk 2(1 - p) + h, whose raw sums it hands
-        // to the other part, then chunk 2p + h, which it finishes with the other part's sums --
-        // so all eight warps of both pairs share the split tile's epilogue.
-        auto chunk_of = [&](const Unit& w, int cc) {
-            return w.part < 0 ? h * PER + cc : (cc == 0 ? 2 * (1 - w.part) + h : 2 * w.part + h);
-        };
+        // Whole tiles: this warp finishes chunks h*PER and h*PER + 1.  Split tiles (part p): the
+        // warp owns chunk c1 = 2p + h of this part's column half and chunk c0 = 2(1 - p) + h of
+        // the other's; it first stores its raw sums of c0 for the other part, then finishes c1
+        // with the other part's sums of it (and c0 too when this part finishes the tile alone).
         auto first_r_chunk = [&](const Unit& w) { return w.part < 0 ? h * PER : 2 * w.part + h; };
         auto load_r = [&](int u, int c) {  // residual chunk c of unit u, coalesced layout
             const Unit w = unit_of(u, args, rank, nk);
@@ -308,153 +378,187 @@ __global__ void __launch_bounds__(kMainThreads, 1) gemm_tc_kernel(
                     rnext[i] = __ldcs(reinterpret_cast<const uint4*>(args.R + static_cast<int64_t>(row) * args.N + col));
             }
         };
-        // Partial-sum tile of a split unit (one per slot and CTA rank, 128 x 256 fp32), laid out
-        // for rows held one per lane: float4 j (columns 4j..4j+3) of 32-column group g of this
-        // warp's row `lane` sits at [q][g][j][lane], so a warp instruction covers 512 contiguous
-        // bytes both when one part writes it and when the other reads it.
-        auto part_at = [&](const Unit& w, int g, int j) {
+        // Raw partial sums of a split unit, one region per slot, K half and CTA rank (128 x 256
+        // fp32), laid out for rows held one per lane: float4 j (columns 4j..4j+3) of 32-column
+        // group g of this warp's row `lane` sits at [q][g][j][lane], so a warp instruction covers
+        // 512 contiguous bytes both when one part writes it and when the other reads it.
+        auto part_at = [&](const Unit& w, int part, int g, int j) {
             return reinterpret_cast<float4*>(args.part) +
-                   (((static_cast<int64_t>(w.slot * 2 + static_cast<int>(rank)) * 4 + q) * 8 + g) * 8 + j) * 32 + lane;
+                   ((((static_cast<int64_t>(w.slot * 2 + part) * 2 + static_cast<int>(rank)) * 4 + q) * 8 + g) * 8 + j) * 32 + lane;
         };
-        // ready word of column half x of a split tile: set by the part that writes that half
-        auto ready_word = [&](const Unit& w, int x) {
-            return args.ready + (w.slot * 2 + static_cast<int>(rank)) * 2 + x;
+        auto ticket_word = [&](const Unit& w) { return args.ticket + w.slot * 2 + static_cast<int>(rank); };
+        auto full_word = [&](const Unit& w) { return args.full + w.slot * 2 + static_cast<int>(rank); };
+        // This warp is done reading accumulator buffer `acc`: hand it back to the MMA issuer.
+        auto release_acc = [&]() {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));   // the leader's
+        };
+        // The raw fp32 sums of chunk c into this part's region.
+        auto store_raw = [&](const Unit& w, int c, bool release) {
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                float v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
+                tmem_ld_wait();
+                if (release && g == 1) release_acc();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    __stcg(part_at(w, w.part, 2 * c + g, j), make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            }
+        };
+        // Finish chunk c of unit w: accumulator (+ the other part's sums of it when `other` >= 0),
+        // then the stages with bias (lanes 16*bslot.. hold it) and the residual (staged from rnext,
+        // which holds this chunk's residual on entry; the residual chunk (nu, nc) is loaded next,
+        // none if nu < 0), stored to Y.  `release`: hand the accumulator back after the last read.
+        auto finish_chunk = [&](const Unit& w, int c, int bslot, int other, bool release, int nu, int nc,
+                                const uint2& bl) {
+            const int ncol0 = w.n0 + CH * c;
+            // the residual chunk into the staging tile (each thread then reads its own row's
+            // segments there and overwrites each with its result); then the next chunk's load
+            if (need_r) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) st_row(cr + 4 * i, cj, rnext[i]);
+                __syncwarp();
+                if (nu >= 0) load_r(nu, nc);
+            }
+            // two 32-column halves of the chunk, one tcgen05.ld each
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {
+                float v[32];
+                tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
+                tmem_ld_wait();
+                if (release && g == 1) release_acc();
+                if (other >= 0) {   // add the other part's partial sums
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const float4 t = __ldcg(part_at(w, other, 2 * c + g, j));
+                        v[4 * j] += t.x;
+                        v[4 * j + 1] += t.y;
+                        v[4 * j + 2] += t.z;
+                        v[4 * j + 3] += t.w;
+                    }
+                }
+                // the 32 columns' stages in one branch-free block per stage count (the count
+                // is uniform per launch), so the 16 independent GELU chains interleave
+                auto finish = [&](auto last_c) {
+                    constexpr int LAST = decltype(last_c)::value;
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        float bv[8];
+                        {
+                            const int src = 16 * bslot + (32 * g + 8 * j) / 4;   // lane holding these columns
+                            uint4 b8;
+                            b8.x = __shfl_sync(0xffffffffu, bl.x, src);
+                            b8.y = __shfl_sync(0xffffffffu, bl.y, src);
+                            b8.z = __shfl_sync(0xffffffffu, bl.x, src + 1);
+                            b8.w = __shfl_sync(0xffffffffu, bl.y, src + 1);
+                            unpack_h8(b8, bv);
+                        }
+                        float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+                        if constexpr (LAST >= 3) unpack_h8(ld_row(lane, 4 * g + j), rv);
+                        float o[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 r2 = apply_stages2_upto<LAST>(make_float2(v[8 * j + e], v[8 * j + e + 1]),
+                                                                       make_float2(bv[e], bv[e + 1]),
+                                                                       make_float2(rv[e], rv[e + 1]));
+                            o[e] = r2.x;
+                            o[e + 1] = r2.y;
+                        }
+                        st_row(lane, 4 * g + j, pack_h8(o));
+                    }
+                };
+                switch (args.epi) {
+                    case 3: finish(IntC<3>{}); break;
+                    case 2: finish(IntC<2>{}); break;
+                    case 1: finish(IntC<1>{}); break;
+                    default: finish(IntC<0>{}); break;
+                }
+            }
+            __syncwarp();
+            {
+                const int col = ncol0 + 8 * cj;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int row = w.m0 + 32 * q + cr + 4 * i;
+                    const uint4 t = ld_row(cr + 4 * i, cj);
+                    if (row < args.M && col < args.N)
+                        __stcs(reinterpret_cast<uint4*>(args.Y + static_cast<int64_t>(row) * args.N + col), t);
+                }
+            }
+            __syncwarp();
         };
         if (need_r && cid < total_units) load_r(cid, first_r_chunk(unit_of(cid, args, rank, nk)));
         for (int u = cid; u < total_units && ok; u += nclusters) {
             const Unit w = unit_of(u, args, rank, nk);
             const bool split = w.part >= 0;
-            // the bias values of the chunks this warp finishes, four per lane (lanes 16k..16k+15:
-            // its k-th finished chunk), fetched while the unit's MMAs run and handed to every lane
-            // by shuffles, so no load latency sits in the element loop
+            const int nu = u + nclusters < total_units ? u + nclusters : -1;     // next unit
+            const int nc = nu >= 0 ? first_r_chunk(unit_of(nu, args, rank, nk)) : 0;
+            // the bias values of this warp's two chunks, four per lane (lanes 16k..16k+15: its
+            // k-th chunk; split units: k = 0 for c1, k = 1 for c0), fetched while the unit's MMAs
+            // run and handed to every lane by shuffles, so no load latency sits in the element loop
             uint2 bl = make_uint2(0, 0);
             {
                 const int k = lane / 16;
-                const int c = split ? 2 * w.part + h : h * PER + k;
+                const int c = split ? (k == 0 ? 2 * w.part + h : 2 * (1 - w.part) + h) : h * PER + k;
                 const int col = w.n0 + CH * c + 4 * (lane % 16);
-                if (args.epi >= 1 && (!split || k == 0) && col < args.N)
-                    bl = __ldg(reinterpret_cast<const uint2*>(args.bias + col));
+                if (args.epi >= 1 && col < args.N) bl = __ldg(reinterpret_cast<const uint2*>(args.bias + col));
             }
             if (!mbar_wait_bounded(accf_bar(acc), acc_phase, flag)) { ok = false; break; }
             tc_fence_after();
-            for (int cc = 0; cc < PER; ++cc) {
-                const int c = chunk_of(w, cc);
-                const bool writer = split && cc == 0;   // hands this chunk's sums to the other part
-                const bool reader = split && cc == 1;   // adds the other part's sums of this chunk
-                const int bslot = split ? 0 : cc;       // which 16 lanes hold this chunk's bias
-                const int ncol0 = w.n0 + CH * c;
-                if (writer) {
-                    // raw partial sums of the chunk for the other part; then publish this half
-                    // once all eight warps have written theirs
-#pragma unroll 1
-                    for (int g = 0; g < 2; ++g) {
-                        float v[32];
-                        tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            __stcg(part_at(w, 2 * c + g, j), make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
-                    }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(part_written);
-                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_written, 0, flag)) {
-                        __threadfence();
-                        st_release_gpu(ready_word(w, 1 - w.part), args.epoch);
-                    }
-                    __syncwarp();
-                    continue;
+            if (!split) {
+                for (int cc = 0; cc < PER; ++cc) {
+                    const bool last = cc + 1 == PER;
+                    finish_chunk(w, h * PER + cc, cc, -1, last, last ? nu : u, last ? nc : h * PER + cc + 1, bl);
                 }
-                if (reader) {   // the other part's sums of this column half are complete
-                    if (!__all_sync(0xffffffffu, flag_wait_bounded(ready_word(w, w.part), args.epoch, flag))) {
+            } else {
+                const int p = w.part;
+                const int c0 = 2 * (1 - p) + h, c1 = 2 * p + h;
+                // (1) the other part's column half: raw sums into this part's region
+                store_raw(w, c0, false);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(part_written);
+                // (2) one thread takes the tile's ticket once all eight warps have written; the
+                // ticket decides who finishes what, and nobody waits on a party that has not taken
+                // its ticket yet (which might not even be resident)
+                if (warp == 2 && lane == 0) {
+                    int role = kRoleFailed;
+                    if (mbar_wait_bounded(part_written, 0, flag)) {
+                        __threadfence();
+                        role = split_ticket(ticket_word(w), args.epoch, args.partner_window);
+                        __threadfence();
+                    }
+                    *reinterpret_cast<volatile int*>(gbase + OFF_ROLE) = role;
+                    mbar_arrive(role_bar);
+                }
+                if (!mbar_wait_bounded(role_bar, 0, flag)) { ok = false; break; }
+                const int role = *reinterpret_cast<volatile int*>(gbase + OFF_ROLE);
+                if (role == kRoleFailed) { ok = false; break; }
+                fence_acq_rel_gpu();   // the other part's sums, published before its ticket
+                if (role == kRoleLeft) {
+                    // the other part finishes the whole tile: leave it this part's other half too
+                    store_raw(w, c1, true);
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(part_read);
+                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_read, 0, flag)) {
+                        __threadfence();
+                        st_release_gpu(full_word(w), args.epoch);
+                    }
+                    __syncwarp();
+                } else if (role == kRoleNormal) {
+                    finish_chunk(w, c1, 0, 1 - p, true, nu, nc, bl);
+                } else {   // kRoleAlone: the other part left both halves of its sums
+                    if (!__all_sync(0xffffffffu, flag_wait_bounded(full_word(w), args.epoch, flag))) {
                         ok = false;
                         break;
                     }
-                }
-                // the residual chunk into the staging tile (each thread then reads its own row's
-                // segments there and overwrites each with its result); then the next chunk's load
-                if (need_r) {
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) st_row(cr + 4 * i, cj, rnext[i]);
-                    __syncwarp();
-                    if (!split && cc + 1 < PER) load_r(u, chunk_of(w, cc + 1));
-                    else if (u + nclusters < total_units) load_r(u + nclusters, first_r_chunk(unit_of(u + nclusters, args, rank, nk)));
-                }
-                // two 32-column halves of the chunk, one tcgen05.ld each
-#pragma unroll 1
-                for (int g = 0; g < 2; ++g) {
-                    float v[32];
-                    tmem_ld32(tmem_base + (static_cast<uint32_t>(32 * q) << 16) + acc * BN + CH * c + 32 * g, v);
-                    tmem_ld_wait();
-                    if (cc == PER - 1 && g == 1) {  // this warp is done with the accumulator buffer
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(mapa_shared(acce_bar(acc), 0));   // the leader's
-                    }
-                    if (reader) {   // add the other part's partial sums
-#pragma unroll
-                        for (int j = 0; j < 8; ++j) {
-                            const float4 t = __ldcg(part_at(w, 2 * c + g, j));
-                            v[4 * j] += t.x;
-                            v[4 * j + 1] += t.y;
-                            v[4 * j + 2] += t.z;
-                            v[4 * j + 3] += t.w;
-                        }
-                    }
-                    // the 32 columns' stages in one branch-free block per stage count (the count
-                    // is uniform per launch), so the 16 independent GELU chains interleave
-                    auto finish = [&](auto last_c) {
-                        constexpr int LAST = decltype(last_c)::value;
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            float bv[8];
-                            {
-                                const int src = 16 * bslot + (32 * g + 8 * j) / 4;   // lane holding these columns
-                                uint4 b8;
-                                b8.x = __shfl_sync(0xffffffffu, bl.x, src);
-                                b8.y = __shfl_sync(0xffffffffu, bl.y, src);
-                                b8.z = __shfl_sync(0xffffffffu, bl.x, src + 1);
-                                b8.w = __shfl_sync(0xffffffffu, bl.y, src + 1);
-                                unpack_h8(b8, bv);
-                            }
-                            float rv[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-                            if constexpr (LAST >= 3) unpack_h8(ld_row(lane, 4 * g + j), rv);
-                            float o[8];
-#pragma unroll
-                            for (int e = 0; e < 8; e += 2) {
-                                const float2 r2 = apply_stages2_upto<LAST>(make_float2(v[8 * j + e], v[8 * j + e + 1]),
-                                                                           make_float2(bv[e], bv[e + 1]),
-                                                                           make_float2(rv[e], rv[e + 1]));
-                                o[e] = r2.x;
-                                o[e + 1] = r2.y;
-                            }
-                            st_row(lane, 4 * g + j, pack_h8(o));
-                        }
-                    };
-                    switch (args.epi) {
-                        case 3: finish(IntC<3>{}); break;
-                        case 2: finish(IntC<2>{}); break;
-                        case 1: finish(IntC<1>{}); break;
-                        default: finish(IntC<0>{}); break;
-                    }
-                }
-                __syncwarp();
-                {
-                    const int col = ncol0 + 8 * cj;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const int row = w.m0 + 32 * q + cr + 4 * i;
-                        const uint4 t = ld_row(cr + 4 * i, cj);
-                        if (row < args.M && col < args.N)
-                            __stcs(reinterpret_cast<uint4*>(args.Y + static_cast<int64_t>(row) * args.N + col), t);
-                    }
-                }
-                __syncwarp();
-                if (reader) {
-                    // all eight warps have read the other part's sums: clear the word for the
-                    // next call.  A split unit is the last unit of its pair and each pair gets at
-                    // most one, so part_written and part_read each complete their phase 0 once.
+                    finish_chunk(w, c1, 0, 1 - p, false, u, c0, bl);
+                    finish_chunk(w, c0, 1, 1 - p, true, nu, nc, bl);
+                    // all eight warps have read the sums: clear the word for a later call (a graph
+                    // replay reuses its epoch)
                     if (lane == 0) mbar_arrive(part_read);
-                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_read, 0, flag)) *ready_word(w, w.part) = 0;
+                    if (warp == 2 && lane == 0 && mbar_wait_bounded(part_read, 0, flag)) *full_word(w) = 0;
                     __syncwarp();
                 }
             }
@@ -542,19 +646,22 @@ int max_active_pairs() {
     return cached[dev] > 0 ? cached[dev] : sm_count() / 2;
 }
 
-// Split-K workspace: the ready words (one per split tile, CTA rank and column half, padded to
-// 1 KB), then the exchanged fp32 partial sums of the split tiles, 128 x 256 per CTA.
+// Split-K workspace: a 2 KB header (the ticket words, one per split tile and CTA rank, then the
+// full words), then the raw fp32 partial sums of the split tiles, 128 x 256 per K half and CTA.
 constexpr int kSplitMaxTiles = 64;
-constexpr int64_t kSplitHeader = 1024;
-constexpr int64_t kSplitTileBytes = 2LL * BM * BN * 4;
-static_assert(2 * 2 * kSplitMaxTiles * 4 <= kSplitHeader, "ready words fit the header");
+constexpr int64_t kSplitHeader = 2048;
+constexpr int64_t kSplitFullOffset = 8 * 2 * kSplitMaxTiles;
+constexpr int64_t kSplitTileBytes = 2LL * 2LL * BM * BN * 4;
+static_assert(kSplitFullOffset + 4 * 2 * kSplitMaxTiles <= kSplitHeader, "ticket and full words fit the header");
 
 int64_t split_ws_bytes(int tiles) {
     const int t = tiles < kSplitMaxTiles ? tiles : kSplitMaxTiles;
     return kSplitHeader + t * kSplitTileBytes;
 }
 
-// Tag of one call for the ready words: never 0, different from the tags of recent calls.
+std::atomic<long long> g_partner_window{kPartnerWindow};
+
+// Tag of one call for the ticket and full words: never 0, different from the tags of recent calls.
 int next_epoch() {
     static std::atomic<unsigned> counter{0};
     unsigned e = counter.fetch_add(1, std::memory_order_relaxed) % 0x7fffffffu;
@@ -595,9 +702,11 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     a.full_units = split ? tiles - tail : tiles;
     a.units = a.full_units + 2 * (tiles - a.full_units);
     a.nk_split = nk / 2;
-    a.ready = split ? static_cast<int*>(ws) : nullptr;
+    a.ticket = split ? static_cast<unsigned long long*>(ws) : nullptr;
+    a.full = split ? reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + kSplitFullOffset) : nullptr;
     a.part = split ? reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSplitHeader) : nullptr;
     a.epoch = split ? next_epoch() : 1;
+    a.partner_window = g_partner_window.load(std::memory_order_relaxed);
     return launch_pdl(gemm_tc_kernel, dim3(static_cast<unsigned>(2 * clusters)), dim3(kMainThreads), MAIN_SMEM, st,
                       2, mA, mB, a);
 }
@@ -630,7 +739,8 @@ int gemm_report(int i, fuse_kernel_record* out) {
             if (!main_attr_ok()) return check_launch();
             const int rc = describe_kernel((const void*)gemm_tc_kernel,
                                            "gemm_tc_kernel (2-CTA cluster, 128x256 tcgen05)",
-                                           kMainThreads, static_cast<int>(MAIN_SMEM), out);
+                                           kMainThreads, static_cast<int>(MAIN_SMEM), out,
+                                           static_cast<int>(TMEM_COLS));
             if (rc == FUSE_OK) {
                 out->cluster_size = 2;
                 out->max_active_clusters = max_active_pairs();
@@ -692,6 +802,12 @@ extern "C" int fuse_gemm_epilogue_plan(const void* A, const void* B, const void*
 extern "C" int fuse_gemm_epilogue(const void* A, const void* B, const void* bias, const void* R, void* Y,
                                   int64_t M, int64_t N, int64_t Kdim, fuse_stream_t stream) {
     return fuse_gemm_epilogue_ws(A, B, bias, R, Y, M, N, Kdim, 0u, nullptr, 0, stream);
+}
+
+extern "C" int fuse_debug_split_window(int64_t cycles) {
+    if (cycles < 0 || cycles > 2000000000LL) return FUSE_EINVAL;
+    fc::g_partner_window.store(cycles, std::memory_order_relaxed);
+    return FUSE_OK;
 }
 
 extern "C" size_t fuse_gemm_workspace_bytes(int64_t M, int64_t N, int64_t Kdim) {

@@ -281,7 +281,9 @@ template <int NM>
 int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs& a, cudaStream_t st) {
     using L = DecodeLayout<NM>;
     // all of an SM's shared memory as shared (not L1) lets two decode CTAs share an SM, so the
-    // whole grid (ceil(N/128) x 8 CTAs) is resident in one wave
+    // whole grid (ceil(N/128) x 8 CTAs) is resident in one wave (CTA start stamps: the 256 CTAs
+    // of N = 4096 start within ~1.2 us, two per SM on 148 SMs; the occupancy API, which reports
+    // one CTA per SM for kernels that allocate tensor memory, undercounts)
     static const bool attr =
         cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(L::SMEM)) == cudaSuccess &&
@@ -348,7 +350,8 @@ int decode_report(fuse_kernel_record* out) {
                                static_cast<int>(cudaSharedmemCarveoutMaxShared));
     const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
                                    "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
-                                   static_cast<int>(DecodeLayout<16>::SMEM), out);
+                                   static_cast<int>(DecodeLayout<16>::SMEM), out,
+                                   static_cast<int>(DecodeLayout<16>::TCOLS));
     if (rc == FUSE_OK) {
         out->cluster_size = DEC_SPLIT;
         out->max_active_clusters = decode_max_active_clusters<16>();

@@ -45,14 +45,20 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 // One CTA per row.  ADD: the row is h = x + res (one fp32 rounding per element), stored to h
 // before it is normalised; h may be x or res itself (each element is read before the same thread
-// writes it).
+// writes it).  Rows are whole 16-byte vectors (hidden % 4 == 0, 16-byte aligned bases).
 template <int THR, int VPT, bool ADD>
 __global__ void __launch_bounds__(THR) rmsnorm_row_kernel(const float* x, const float* res,
                                                           const float* __restrict__ w, float* h,
                                                           float* __restrict__ y, int hidden, float eps) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
-    __shared__ float red[THR / 32];
+    pdl_trigger();
     const int64_t row = blockIdx.x;
+    // the row's input on its way into L2 while the preceding kernel may still run
+    if (threadIdx.x == 0) {
+        prefetch_l2_bulk(x + row * hidden, static_cast<uint32_t>(hidden) * 4u);
+        if (ADD) prefetch_l2_bulk(res + row * hidden, static_cast<uint32_t>(hidden) * 4u);
+    }
+    pdl_wait();  // before any global-memory load or store (programmatic dependent launch)
+    __shared__ float red[THR / 32];
     const int nv = hidden / 4;
     const float4* xr = reinterpret_cast<const float4*>(x + row * hidden);
     float4 v[VPT];

@@ -108,6 +108,25 @@ typedef struct {
  */
 int fuse_chain_run(const fuse_stage* stages, int K, const void* x, void* y, int64_t n,
                    int dtype, int mode, fuse_stream_t stream);
+/* The same chain for data in host memory: the call a host-side caller makes with its own buffers.
+ * x_host is copied to the device, the chain runs there, and y comes back to y_host.  The vector
+ * is cut into `slices` (1..64) pieces of whole 32-byte vectors, and each piece's copy in, kernel(s)
+ * and copy out are ordered by events, so both copy directions overlap the kernels and each other.
+ *   x_host, y_host  host memory of n elements of `dtype` (page-locked, from cudaHostAlloc or
+ *           cudaHostRegister, for the copies to run asynchronously; pageable memory works, but its
+ *           copies wait for the host)
+ *   x_dev, y_dev    device scratch of n elements each, owned by the caller (overwritten; may be
+ *           the same buffer, may not partially overlap); the call allocates nothing
+ *   stages, K, n, dtype, mode  as fuse_chain_run()
+ * Stream order: the copies start after the work queued on `stream` before the call, the kernels
+ * run on `stream`, and `stream` continues only after the last piece is back in y_host (read
+ * y_host after synchronizing `stream`).  The copies run on two helper streams that the library
+ * creates at the first call on each device (with five events) and keeps until the process exits;
+ * calls from several host threads are serialized on them.
+ */
+int fuse_chain_run_host(const fuse_stage* stages, int K, const void* x_host, void* y_host,
+                        int64_t n, int dtype, int mode, void* x_dev, void* y_dev, int slices,
+                        fuse_stream_t stream);
 
 /* ===================================================================== RMSNorm
  * [OFCG] §3.2 and fusion_lab [A2]: RMSNorm unfused is four passes (x*x, reduce-mean, x*r, *g),
@@ -243,16 +262,27 @@ int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, cons
  * not fill a whole number of waves of the persistent kernel and the last, partial wave would leave
  * at least half of the SM pairs idle, each tile of that wave is split over K between two SM pairs,
  * which exchange fp32 partial sums through the workspace and each apply the epilogue to one half of
- * the tile's columns.  Results equal the unsplit kernel's up to fp32 summation order.
+ * the tile's columns.  A ticket in the workspace decides who finishes what, and neither pair waits
+ * for one that has not started: if the other pair is late (other work holds the SMs it would run
+ * on), the first leaves its sums and the other finishes the whole tile.  Results equal the
+ * unsplit kernel's up to fp32 summation order.
  *   workspace  device memory of at least fuse_gemm_workspace_bytes(M, N, Kdim) bytes, 256-byte
- *              aligned, zero-filled before its first use (every completed call leaves it so);
- *              not shared with a call that may run at the same time.  NULL, or smaller, or
- *              misaligned: no split (still correct).  Must not overlap any operand (FUSE_EINVAL).
+ *              aligned, zero-filled before its first use (every completed call leaves it so; after
+ *              a call that failed with FUSE_ETIMEOUT, zero it again); not shared with a call that
+ *              may run at the same time.  NULL, or smaller, or misaligned: no split (still
+ *              correct).  Must not overlap any operand (FUSE_EINVAL).
  */
 int fuse_gemm_epilogue_ws(const void* A, const void* B, const void* bias, const void* R, void* Y,
                           int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask, void* workspace,
                           size_t ws_bytes, fuse_stream_t stream);
-/* Workspace bytes for fuse_gemm_epilogue_ws (0 when no split can apply, e.g. M <= 64). */
+/* Test hook of the split tiles: how long (SM cycles, 0 <= cycles <= 2e9; default 100000) the first
+ * part of a split tile waits for the other part's ticket before it leaves the whole tile to it.
+ * 0 makes every first part leave, so the path where one part finishes a tile alone runs on every
+ * split tile; results are the same up to fp32 summation order.  Applies to calls launched after
+ * it (process-wide); FUSE_EINVAL outside the range. */
+int fuse_debug_split_window(int64_t cycles);
+/* Workspace bytes for fuse_gemm_epilogue_ws (0 when no split can apply, e.g. M <= 64): a 2 KB
+ * header and 512 KB of fp32 partial sums per split tile, for at most 64 tiles. */
 size_t fuse_gemm_workspace_bytes(int64_t M, int64_t N, int64_t Kdim);
 /* [K4] §① traffic of a plan, in bytes: 2 * (M*K + K*N + N + 2*M*N + 2*cuts*M*N). */
 int64_t fuse_gemm_bytes(int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask);
@@ -351,10 +381,20 @@ typedef struct {
     int32_t static_smem_bytes;
     int32_t dynamic_smem_bytes;       /* as launched                                            */
     int32_t block_threads;            /* as launched                                            */
-    int32_t blocks_per_sm;            /* occupancy API at that block size and smem              */
+    int32_t blocks_per_sm;            /* CTAs one SM holds at once: the least of what threads,
+                                         registers, shared memory (with the 1 KB each CTA reserves)
+                                         and tensor-memory columns allow                          */
     int32_t max_threads_per_block;
     int32_t cluster_size;             /* CTAs per thread-block cluster as launched (1 = none)    */
-    int32_t max_active_clusters;      /* clusters resident at once on the GPU (0 if no cluster)  */
+    int32_t max_active_clusters;      /* clusters resident at once per the occupancy API (0 if no
+                                         cluster); like blocks_per_sm_api, conservative for kernels
+                                         that allocate tensor memory                              */
+    int32_t blocks_per_sm_api;        /* cudaOccupancyMaxActiveBlocksPerMultiprocessor's answer.
+                                         For kernels that allocate tensor memory it is 1 whatever
+                                         their shared memory, while the hardware runs as many CTAs
+                                         as blocks_per_sm (CTA start stamps of the decode GEMM:
+                                         two per SM, its 256 CTAs in one wave on 148 SMs)         */
+    int32_t tmem_cols;                /* tensor-memory columns one CTA allocates (0: none)        */
     /* What ptxas -v printed for this kernel when the library was built (the same figures as
      * fuse_ptxas_entry(); -1 each if the build kept no record of the kernel):                   */
     int32_t ptxas_registers;

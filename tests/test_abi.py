@@ -232,10 +232,11 @@ def test_gemm_host_validation():
 
 
 def test_gemm_workspace_bytes_is_host_arithmetic():
-    """The split-K workspace size needs no GPU: a 1 KB header of ready words plus one 256 KB fp32
-    partial tile per CTA pair tile, for at most 64 tiles; none for the decode shapes."""
+    """The split-K workspace size needs no GPU: a 2 KB header of ticket and full words plus one
+    512 KB fp32 partial tile per CTA pair tile (two K halves x two CTAs x 128 x 256), for at most
+    64 tiles; none for the decode shapes."""
     assert fc.fuse_gemm_workspace_bytes(16, 4096, 4096) == 0
     assert fc.fuse_gemm_workspace_bytes(64, 4096, 4096) == 0
-    assert fc.fuse_gemm_workspace_bytes(256, 256, 64) == 1024 + 1 * 2 * 128 * 256 * 4
-    assert fc.fuse_gemm_workspace_bytes(2560, 2048, 128) == 1024 + 64 * 2 * 128 * 256 * 4
-    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 1024 + 64 * 2 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(256, 256, 64) == 2048 + 1 * 4 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(2560, 2048, 128) == 2048 + 64 * 4 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 2048 + 64 * 4 * 128 * 256 * 4

@@ -147,3 +147,58 @@ def test_fat_probe_register_report(cuda_device):
     assert fat["blocks_per_sm"] == 1
     assert fused["blocks_per_sm"] >= 6
     assert fused["local_bytes_per_thread"] == 0
+
+
+@pytest.mark.parametrize("n,slices,pinned,mode", [(1, 1, True, fc.FUSE_FUSED), (100_003, 3, True, fc.FUSE_FUSED),
+                                                  (1 << 20, 8, True, fc.FUSE_UNFUSED),
+                                                  (65_537, 64, False, fc.FUSE_FUSED),
+                                                  (4096, 5, True, fc.FUSE_FAT)])
+def test_host_buffer_entry_point(cuda_device, n, slices, pinned, mode):
+    """fuse_chain_run_host: x from host memory, y back to host memory, through the caller's
+    device scratch, in slices whose copies overlap the kernels: bit-exact with the oracle (the
+    chain is element-wise, so slicing changes nothing), for pinned and pageable host memory."""
+    import torch
+    relu, a, b = wl.chain_stages(6)
+    st = _stages(relu, a, b)
+    x = wl.chain_input(n, salt=21)
+    xh = torch.from_numpy(x)
+    yh = torch.full((n,), float("nan"))
+    if pinned:
+        xh, yh = xh.pin_memory(), yh.pin_memory()
+    xd = torch.empty(n, device="cuda")
+    yd = torch.empty(n, device="cuda")
+    s = torch.cuda.Stream()
+    fc.fuse_chain_run_host(st, xh, yh, xd, yd, mode, slices, stream=s)
+    s.synchronize()
+    assert fc.fuse_check() == fc.FUSE_OK
+    assert np.array_equal(yh.numpy().view(np.uint32), oracle.chain(relu, a, b, x).view(np.uint32))
+
+
+def test_host_buffer_entry_point_is_stream_ordered_and_in_place(cuda_device):
+    """Work queued on the stream before the call (a kernel writing the host-visible input through
+    a device copy) is finished before the copies start; x_dev may be y_dev; two calls in a row on
+    one stream give the chain applied twice."""
+    import torch
+    relu, a, b = wl.chain_stages(3)
+    st = _stages(relu, a, b)
+    n = 300_001
+    x = wl.chain_input(n, salt=22)
+    xh = torch.from_numpy(x).pin_memory()
+    mid = torch.empty(n).pin_memory()
+    out = torch.empty(n).pin_memory()
+    buf = torch.empty(n, device="cuda")
+    s = torch.cuda.Stream()
+    fc.fuse_chain_run_host(st, xh, mid, buf, buf, fc.FUSE_FUSED, 4, stream=s)
+    fc.fuse_chain_run_host(st, mid, out, buf, buf, fc.FUSE_FUSED, 7, stream=s)
+    s.synchronize()
+    once = oracle.chain(relu, a, b, x)
+    assert np.array_equal(mid.numpy().view(np.uint32), once.view(np.uint32))
+    assert np.array_equal(out.numpy().view(np.uint32), oracle.chain(relu, a, b, once).view(np.uint32))
+    lib = fc._load()
+    arr = fc._stages(st)
+    assert lib.fuse_chain_run_host(arr, 3, xh.data_ptr(), out.data_ptr(), n, fc.FUSE_F32, fc.FUSE_FUSED,
+                                   buf.data_ptr(), buf.data_ptr(), 0, s.cuda_stream) == fc.FUSE_EINVAL
+    assert lib.fuse_chain_run_host(arr, 3, xh.data_ptr(), out.data_ptr(), n, fc.FUSE_F32, fc.FUSE_FUSED,
+                                   buf.data_ptr(), buf.data_ptr() + 4, 2, s.cuda_stream) == fc.FUSE_EINVAL
+    assert lib.fuse_chain_run_host(arr, 3, None, out.data_ptr(), n, fc.FUSE_F32, fc.FUSE_FUSED,
+                                   buf.data_ptr(), buf.data_ptr(), 2, s.cuda_stream) == fc.FUSE_EINVAL

@@ -65,8 +65,8 @@ def _dev(bits, shape=None):
 
 
 def _run(A, B, bias, R, mask, ws=False, workspace=None):
-    """ws: pass a zero-filled split-K workspace (or `workspace`, reused); its ready words must be
-    zero again after the call."""
+    """ws: pass a zero-filled split-K workspace (or `workspace`, reused); its ticket and full words
+    must be zero again after the call."""
     import torch
     M, K = A.shape
     N = B.shape[1]
@@ -77,8 +77,8 @@ def _run(A, B, bias, R, mask, ws=False, workspace=None):
                           workspace=workspace if ws else False)
     torch.cuda.synchronize()
     assert fc.fuse_check() == fc.FUSE_OK
-    if ws and workspace.numel() >= 1024:
-        assert int(workspace[:1024].count_nonzero()) == 0
+    if ws and workspace.numel() >= 2048:
+        assert int(workspace[:2048].count_nonzero()) == 0
     return Y.cpu().view(torch.int16).numpy().view(np.uint16)
 
 
@@ -103,6 +103,16 @@ def test_several_tiles_and_k_blocks(cuda_device, shape):
     _check(_run(A, B, bias, R, 0), oracle.gemm_epilogue(A, B, bias, R, 0), 0, A, B)
 
 
+@pytest.mark.parametrize("shape", [(4500, 776, 136), (8192, 512, 64)])
+def test_tile_bands(cuda_device, shape):
+    """More than 16 pair rows (4096 rows): the persistent kernel walks its tiles in bands of 16 pair
+    rows; every tile is computed once (sampled rows of every band and the ragged last one)."""
+    A, B, bias, R = wl.gemm_input(*shape, salt=14, std=1.0 / 8.0)
+    rows = np.unique(np.concatenate([np.arange(0, shape[0], 97), [shape[0] - 1]]))
+    y = _run(A, B, bias, R, 0)
+    _check(y[rows], oracle.gemm_epilogue(A, B, bias, R, 0, rows=rows), 0, A[rows], B)
+
+
 @pytest.mark.parametrize("shape", [(300, 520, 200), (129, 264, 72), (65, 8, 8), (200, 136, 4104)])
 @pytest.mark.parametrize("mask", [0, 7])
 def test_ragged_shapes(cuda_device, shape, mask):
@@ -122,9 +132,36 @@ def test_last_wave_split_over_k(cuda_device, shape, mask, ws):
     _check(_run(A, B, bias, R, mask, ws=ws), oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
 
 
+@pytest.mark.parametrize("shape", [(2560, 2048, 128), (2500, 2040, 200), (4096, 4096, 4096)])
+def test_split_tile_finished_by_one_part(cuda_device, shape):
+    """With no partner window the first part of every split tile leaves its sums and the other
+    part finishes the whole tile alone (the path taken when the other pair starts late): same
+    results as the unsplit kernel up to fp32 summation order, and the workspace header is left
+    zero-filled."""
+    import torch
+    lib = fc._load()
+    A, B, bias, R = wl.gemm_input(*shape, salt=13, std=1.0 / 8.0)
+    wsb = torch.zeros(fc.fuse_gemm_workspace_bytes(*shape), dtype=torch.uint8, device="cuda")
+    assert lib.fuse_debug_split_window(0) == fc.FUSE_OK
+    try:
+        y_alone = _run(A, B, bias, R, 0, ws=True, workspace=wsb)
+    finally:
+        assert lib.fuse_debug_split_window(100000) == fc.FUSE_OK
+    assert int(wsb[:2048].count_nonzero()) == 0
+    y_norm = _run(A, B, bias, R, 0, ws=True, workspace=wsb)
+    y0 = _run(A, B, bias, R, 0).view(np.float16).astype(np.float64)
+    for y in (y_alone, y_norm):
+        y1 = y.view(np.float16).astype(np.float64)
+        diff = np.abs(y1 - y0)
+        assert np.all(diff <= _ulp16(np.maximum(np.abs(y0), np.abs(y1))) + 2.0 ** -16)
+    rows = np.arange(0, shape[0], max(1, shape[0] // 24))
+    _check(y_alone[rows], oracle.gemm_epilogue(A, B, bias, R, 0, rows=rows), 0, A[rows], B)
+    assert lib.fuse_debug_split_window(-1) == fc.FUSE_EINVAL
+
+
 def test_split_workspace_reused_across_calls(cuda_device):
-    """One workspace for consecutive calls: each call finds the ready words cleared by the one
-    before, and the results are identical."""
+    """One workspace for consecutive calls: each call finds the ticket and full words cleared by
+    the one before (the header is zero after every call), and the results are identical."""
     import torch
     A, B, bias, R = wl.gemm_input(2560, 2048, 256, salt=10, std=1.0 / 8.0)
     wsb = torch.zeros(fc.fuse_gemm_workspace_bytes(2560, 2048, 256), dtype=torch.uint8, device="cuda")
@@ -132,6 +169,7 @@ def test_split_workspace_reused_across_calls(cuda_device):
     _check(y0, oracle.gemm_epilogue(A, B, bias, R, 0), 0, A, B)
     for _ in range(3):
         assert np.array_equal(_run(A, B, bias, R, 0, ws=True, workspace=wsb), y0)
+        assert int(wsb[:2048].count_nonzero()) == 0
 
 
 @pytest.mark.parametrize("shape", [(2560, 2048, 256), (4096, 4096, 4096)])
@@ -159,7 +197,7 @@ def test_module_workspace_by_default(cuda_device):
     assert fc.fuse_check() == fc.FUSE_OK
     key = (torch.device("cuda").index or 0, torch.cuda.current_stream().cuda_stream)
     ws = [v for k, v in fc._GEMM_WS.items() if k[1] == key[1]]
-    assert ws and int(ws[0][:1024].count_nonzero()) == 0
+    assert ws and int(ws[0][:2048].count_nonzero()) == 0
     y_auto = Y.cpu().view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(y_auto, _run(A, B, bias, R, 0, ws=True))
 
@@ -167,7 +205,7 @@ def test_module_workspace_by_default(cuda_device):
 def test_workspace_size_and_overlap(cuda_device):
     import torch
     assert fc.fuse_gemm_workspace_bytes(16, 4096, 4096) == 0            # decode: no split
-    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 1024 + 64 * 2 * 128 * 256 * 4
+    assert fc.fuse_gemm_workspace_bytes(4096, 4096, 4096) == 2048 + 64 * 4 * 128 * 256 * 4
     A = torch.zeros(256, 64, dtype=torch.float16, device="cuda")
     B = torch.zeros(64, 256, dtype=torch.float16, device="cuda")
     b = torch.zeros(256, dtype=torch.float16, device="cuda")

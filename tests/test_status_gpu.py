@@ -34,8 +34,24 @@ def test_kernel_report_covers_every_variant(cuda_device):
     for i in range(n):
         r = fc.fuse_kernel_report(i)
         assert r["regs_per_thread"] > 0 and r["blocks_per_sm"] >= 1, r
+        assert r["blocks_per_sm_api"] >= 1, r
     with pytest.raises(fc.FuseError):
         fc.fuse_kernel_report(n)
+
+
+def test_decode_gemm_grid_is_resident_in_one_wave(cuda_device):
+    """The decode GEMM's 83 KB of shared memory and 32 tensor-memory columns let two CTAs share an
+    SM, so the 256 CTAs of N = 4096 (32 clusters of 8) fit the 152 SMs at once; the tcgen05 GEMM
+    and attention kernels hold one CTA per SM."""
+    recs = {fc.fuse_kernel_report(i)["name"].split(" ")[0]: fc.fuse_kernel_report(i)
+            for i in range(fc.fuse_kernel_count())}
+    dec = recs["gemm_decode_kernel<16>"]
+    assert dec["tmem_cols"] == 32 and dec["blocks_per_sm"] == 2, dec
+    import torch
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert dec["blocks_per_sm"] * sms >= 256
+    for name in ("gemm_tc_kernel", "attn_persist_kernel<D=256>"):
+        assert recs[name]["blocks_per_sm"] == 1 and recs[name]["tmem_cols"] == 512, recs[name]
 
 
 def test_kernel_report_carries_the_ptxas_figures_of_its_build(cuda_device):
