@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--K", type=int, default=8, help="chain stages for --profile")
     ap.add_argument("--tile", type=int, default=64, help="softmax skip tile for --profile")
     ap.add_argument("--mask", type=int, default=0, help="GEMM cut mask for --profile gemm")
+    ap.add_argument("--no-static-b", action="store_true",
+                    help="--profile gemm at M <= 64: leave FUSE_GEMM_STATIC_B off")
     return ap.parse_args()
 
 
@@ -402,14 +404,14 @@ def run_ours(args, rank, world, local):
                 gws = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, gN, gK)), dtype=torch.uint8, device=dev)
                 gemm_bufs[M] = (A, Bs, bias, Rr, Ys, rotating(nb), rotating(2), gws)
 
-        def gemm(M, mask):
+        def gemm(M, mask, flags=0):
             A, Bs, bias, Rr, Ys, brot, yrot, gws = gemm_bufs[M]
 
             def fn():
                 b, y = Bs[brot()], Ys[yrot()]
                 check(lib.fuse_gemm_epilogue_ws(A.data_ptr(), b.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
-                                                y.data_ptr(), M, gN, gK, mask, gws.data_ptr(), gws.numel(), sh),
-                      "fuse_gemm_epilogue_ws")
+                                                y.data_ptr(), M, gN, gK, mask | flags, gws.data_ptr(), gws.numel(),
+                                                sh), "fuse_gemm_epilogue_ws")
                 counter["launches"] += 1 + bin(mask).count("1")
             return fn
         flops = {M: 2 * M * gN * gK for M in wl.GEMM_MS}
@@ -419,10 +421,15 @@ def run_ours(args, rank, world, local):
                                 "gemm_M4096_fused" if m_ == 0 else "gemm_M4096_unfused"))
         # decode calls are ~10 us: 16 (8) back-to-back calls per group, as a decode loop issues
         # them, so the group's leading launch latency is spread over enough calls
+        # the decode loop's weights are never written by the kernels before them, so its calls
+        # carry FUSE_GEMM_STATIC_B (the first weight boxes load while the preceding call finishes);
+        # one group without it shows the plain stream-ordered call
         for p_, m_ in plans.items():
-            groups.append(Group(f"gemm_M16_{p_}", gemm(16, m_), fc.fuse_gemm_bytes(16, gN, gK, m_),
+            groups.append(Group(f"gemm_M16_{p_}", gemm(16, m_, fc.FUSE_GEMM_STATIC_B), fc.fuse_gemm_bytes(16, gN, gK, m_),
                                 16 if m_ == 0 else 8, "hbm", "gemm_decode_kernel<16>" if m_ == 0 else None,
                                 1 + bin(m_).count("1"), "gemm_M16_fused" if m_ == 0 else "gemm_M16_unfused"))
+        groups.append(Group("gemm_M16_[4]_nostatic", gemm(16, 0), fc.fuse_gemm_bytes(16, gN, gK, 0), 16, "hbm", None,
+                            1, "gemm_M16_nostatic"))
 
     def make_events():
         # per group: the untimed leading call's pair, then one pair around the timed calls
@@ -599,6 +606,8 @@ def run_ours(args, rank, world, local):
             gm[f"M{M}"] = ent
         gm["M4096"]["roofline"] = roofline_of("gemm_M4096_fused")
         gm["M16"]["roofline"] = roofline_of("gemm_M16_fused")
+        gm["M16"]["static_weight_flag"] = "FUSE_GEMM_STATIC_B on every M = 16 group but one"
+        gm["M16"]["[4]_no_static_flag_us"] = round(call_ms("gemm_M16_[4]_nostatic") * 1e3, 2)
         rows["gemm_epilogue"] = gm
         rows["launch_graph"] = launch_graph_rows(fc, lib, wl, torch, dev, gemm_bufs[16], check)
         rows["planner"] = planner_rows(fc, wl, peaks, rows["launch_graph"]["t_exec_queued_us"],
@@ -1117,12 +1126,16 @@ def run_profile(args):
     elif name == "gemm":
         M = args.size or 4096
         A, B, bias, Rr = wl.gemm_input(M, device=dev)
+        # decode shapes rotate six weight copies (192 MiB, beyond L2), as the bench does, and carry
+        # FUSE_GEMM_STATIC_B as the bench's decode loop does unless --no-static-b is given
+        Bs = [B] + [B.clone() for _ in range(5)] if M <= 64 else [B]
+        flags = fc.FUSE_GEMM_STATIC_B if M <= 64 and not args.no_static_b else 0
         Ys = [torch.empty(M, wl.GEMM_N, dtype=torch.float16, device=dev) for _ in range(2)]
         gws = torch.zeros(max(1, fc.fuse_gemm_workspace_bytes(M, wl.GEMM_N, wl.GEMM_K)), dtype=torch.uint8,
                           device=dev)
         for i in range(L):
-            rc = lib.fuse_gemm_epilogue_ws(A.data_ptr(), B.data_ptr(), bias.data_ptr(), Rr.data_ptr(),
-                                           Ys[i % 2].data_ptr(), M, wl.GEMM_N, wl.GEMM_K, args.mask,
+            rc = lib.fuse_gemm_epilogue_ws(A.data_ptr(), Bs[i % len(Bs)].data_ptr(), bias.data_ptr(), Rr.data_ptr(),
+                                           Ys[i % 2].data_ptr(), M, wl.GEMM_N, wl.GEMM_K, args.mask | flags,
                                            gws.data_ptr(), gws.numel(), stream)
             assert rc == 0, fc.fuse_strerror(rc)
         nbytes = fc.fuse_gemm_bytes(M, wl.GEMM_N, wl.GEMM_K, args.mask)

@@ -287,6 +287,7 @@ def fuse_rmsnorm_unfused_static(x, w, y, eps: float, stream=None) -> None:
 
 
 FUSE_RMSNORM_STATIC_MAX_ROWS = 65536
+FUSE_GEMM_STATIC_B = 0x100
 
 
 def fuse_causal_softmax(s, p, scale: float, skip_tile: int = 0, mode: int = FUSE_FUSED,

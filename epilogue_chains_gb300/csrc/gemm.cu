@@ -44,7 +44,7 @@ namespace fc {
 
 // the decode kernel (gemm_decode.cu)
 int launch_decode_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
-                       int64_t N, int64_t K, int epi, cudaStream_t st);
+                       int64_t N, int64_t K, int epi, bool b_static, cudaStream_t st);
 int decode_report(fuse_kernel_record* out);
 
 namespace {
@@ -671,11 +671,11 @@ int next_epoch() {
 // GEMM + the stages 1..epi, fp16 result into Y.  `ws` (ws_bytes, zero-filled before its first use)
 // lets the last, partial wave of tiles be split over K; without it that wave runs whole tiles.
 int launch_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
-                int64_t N, int64_t K, int epi, void* ws, size_t ws_bytes, cudaStream_t st) {
+                int64_t N, int64_t K, int epi, void* ws, size_t ws_bytes, bool b_static, cudaStream_t st) {
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     CUtensorMap mA, mB;
-    if (M <= 64) return launch_decode_gemm(A, B, bias, R, Y, M, N, K, epi, st);
+    if (M <= 64) return launch_decode_gemm(A, B, bias, R, Y, M, N, K, epi, b_static, st);
     if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
     if (!main_attr_ok()) return check_launch();
     MainArgs a;
@@ -759,7 +759,9 @@ extern "C" int fuse_gemm_epilogue_ws(const void* A, const void* B, const void* b
                                      int64_t M, int64_t N, int64_t Kdim, uint32_t cut_mask, void* workspace,
                                      size_t ws_bytes, fuse_stream_t stream) {
     using namespace fc;
-    if (M < 0 || N < 0 || Kdim < 0 || cut_mask > 7u) return FUSE_EINVAL;
+    if (M < 0 || N < 0 || Kdim < 0 || (cut_mask & ~(7u | FUSE_GEMM_STATIC_B)) != 0u) return FUSE_EINVAL;
+    const bool b_static = (cut_mask & FUSE_GEMM_STATIC_B) != 0u;
+    cut_mask &= 7u;
     if (M == 0 || N == 0) return FUSE_OK;
     if (Kdim == 0) return FUSE_EUNSUPPORTED;
     if (!A || !B || !bias || !R || !Y) return FUSE_EINVAL;
@@ -785,7 +787,7 @@ extern "C" int fuse_gemm_epilogue_ws(const void* A, const void* B, const void* b
     while (first < 4) {
         int last = first;
         while (last < 3 && !((cut_mask >> last) & 1u)) ++last;
-        const int rc = first == 0 ? launch_gemm(A, B, bias, R, Y, M, N, Kdim, last, workspace, ws_bytes, st)
+        const int rc = first == 0 ? launch_gemm(A, B, bias, R, Y, M, N, Kdim, last, workspace, ws_bytes, b_static, st)
                                   : launch_tail(Y, bias, R, M, N, first, last, st);
         if (rc != FUSE_OK) return rc;
         first = last + 1;

@@ -3,13 +3,18 @@
 // once bounds the time.
 //
 // GB300 design: swap A and B so the weight's N fills the 128-row MMA dimension and M becomes the
-// MMA's N (16, 32 or 64); split K over an 8-CTA cluster (256 CTAs for N = 4096, one wave); every
-// CTA streams its 128-column x K/8 slab of the weight through a 4-stage TMA ring into tcgen05 MMAs
-// (fp32 accumulator in TMEM), then sends each of the eight column slices of its partial to the CTA
-// that owns that slice (st.async into the owner's shared memory, completion on its mbarrier).  The
-// owner sums the eight partials in rank order and applies the epilogue: no global workspace, no
-// cluster barrier after the main loop.  The bias and residual values of a CTA's outputs are loaded
-// at kernel start.  Every mbarrier wait is bounded (watchdog).
+// MMA's N (16, 32 or 64); split K over an 8-CTA cluster (256 CTAs for N = 4096, one wave at two
+// CTAs per SM); every CTA streams its 128-column x K/8 slab of the weight through a 5-stage TMA
+// ring (M <= 16) into tcgen05 MMAs (fp32 accumulator in TMEM), then sends each of the eight column
+// slices of its partial to the CTA that owns that slice (st.async into the owner's shared memory,
+// completion on its mbarrier).  The owner sums the eight partials in rank order and applies the
+// epilogue: no global workspace, no cluster barrier after the main loop.  In a stream of decode
+// calls the time goes to waiting for the preceding call (its grid completing releases this one
+// ~1.7 us after its last CTA ends), the weight stream and the exchange; so nothing but the TMA
+// issue sits between the grid-dependency wait and the first load (the epilogue's bias and
+// residual loads belong to the warps idle during the main loop), and with FUSE_GEMM_STATIC_B the
+// first ring of weight boxes is already on its way before that wait.  Every mbarrier wait is
+// bounded (watchdog).
 #include <cudaTypedefs.h>
 #include <math.h>
 
@@ -38,11 +43,13 @@ struct DecodeArgs {
     const __half* R;
     __half* Y;
     int* flag;
+    int b_static;       // 1: B is not written by the work queued before this call (see below)
 };
 
 template <int NM>
 struct DecodeLayout {
-    static constexpr int STAGES = NM <= 32 ? 4 : 3;
+    // 5 x 18 KB for M <= 16 keeps two CTAs per SM (2 x 100 KB), so the whole grid is resident
+    static constexpr int STAGES = NM <= 16 ? 5 : (NM <= 32 ? 4 : 3);
     static constexpr uint32_t A_ST = NM * BK * 2;
     static constexpr uint32_t OFF_BT = 0;
     static constexpr uint32_t OFF_AS = OFF_BT + STAGES * DEC_BT_STAGE;
@@ -109,14 +116,27 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
         mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(128 * NM * 4));
         prefetch_map(&mapA);
         prefetch_map(&mapB);
-        // Start this CTA's whole weight slice on its way into L2 while the preceding kernel may
-        // still run: an L2 prefetch returns nothing to the SM, and L2 is where that kernel's
-        // writes land, so the loads after pdl_wait() read current data, only sooner.
-        for (int kb = 0; kb < nk; ++kb) {
-            const int k = (kb0 + kb) * BK;
-            tma_prefetch_2d(&mapB, n0, k);
-            tma_prefetch_2d(&mapB, n0 + 64, k);
-            tma_prefetch_2d(&mapA, k, 0);
+        if (args.b_static) {
+            // The caller vouches that nothing queued before this call writes B: the first ring of
+            // weight boxes is loaded now, while the preceding kernel may still run (A, which it may
+            // have written, follows after the grid-dependency wait; each stage's barrier expects
+            // both, so no MMA starts before A is current).
+            for (int kb = 0; kb < nk && kb < L::STAGES; ++kb) {
+                const int k = (kb0 + kb) * BK;
+                mbar_arrive_expect_tx(full_bar(kb), DEC_BT_STAGE + L::A_ST);
+                tma_load_2d(base + L::OFF_BT + kb * DEC_BT_STAGE, &mapB, n0, k, full_bar(kb));
+                tma_load_2d(base + L::OFF_BT + kb * DEC_BT_STAGE + B_BOX, &mapB, n0 + 64, k, full_bar(kb));
+            }
+        } else {
+            // Start this CTA's whole weight slice on its way into L2 while the preceding kernel
+            // may still run: an L2 prefetch returns nothing to the SM, and L2 is where that
+            // kernel's writes land, so the loads after pdl_wait() read current data, only sooner.
+            for (int kb = 0; kb < nk; ++kb) {
+                const int k = (kb0 + kb) * BK;
+                tma_prefetch_2d(&mapB, n0, k);
+                tma_prefetch_2d(&mapB, n0 + 64, k);
+                tma_prefetch_2d(&mapA, k, 0);
+            }
         }
     }
     if (warp == 1) tmem_alloc(holder, L::TCOLS);
@@ -132,38 +152,51 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     // After the K reduction CTA `rank` finishes output columns [n0 + COLS*rank, +COLS) of all NM
-    // rows, in units of one column and four consecutive rows: unit idx = threadIdx.x +
-    // kDecThreads*u is slice column idx / (NM/4), rows 4*(idx % (NM/4)) .. +3.  Each thread loads
-    // the bias and residual values of its units now, so their latency hides under the main loop.
+    // rows, in units of one column and four consecutive rows: unit idx = uthread + kDecThreads*u
+    // is slice column idx / (NM/4), rows 4*(idx % (NM/4)) .. +3.  Units go to warps 2 and 3 first
+    // (uthread = threadIdx.x ^ 64), which have nothing to do during the main loop and load the
+    // bias and residual values of their units now, so that latency hides under it; the TMA and
+    // MMA warps (0 and 1) hold units only when there are more than 64 (M > 16) and load theirs
+    // after their loops, so no global load delays the first TMA issue or the first MMA.
     constexpr int COLS = 128 / DEC_SPLIT;  // 16
     constexpr int UNITS = NM * COLS / 4;
     constexpr int UPT = (UNITS + kDecThreads - 1) / kDecThreads;
+    const int uthread = static_cast<int>(threadIdx.x) ^ 64;
     float eb[UPT], er[UPT][4];
+    auto load_units = [&]() {
 #pragma unroll
-    for (int u = 0; u < UPT; ++u) {
-        const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
-        const int n = n0 + COLS * static_cast<int>(rank) + idx / (NM / 4);
-        const int m0 = 4 * (idx % (NM / 4));
-        const bool valid = idx < UNITS && n < args.N;
-        eb[u] = valid && args.epi >= 1 ? __half2float(__ldg(args.bias + n)) : 0.0f;
+        for (int u = 0; u < UPT; ++u) {
+            const int idx = uthread + kDecThreads * u;
+            const int n = n0 + COLS * static_cast<int>(rank) + idx / (NM / 4);
+            const int m0 = 4 * (idx % (NM / 4));
+            const bool valid = idx < UNITS && n < args.N;
+            eb[u] = valid && args.epi >= 1 ? __half2float(__ldg(args.bias + n)) : 0.0f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            er[u][i] = valid && args.epi >= 3 && m0 + i < args.M
-                           ? __half2float(__ldcs(args.R + static_cast<int64_t>(m0 + i) * args.N + n))
-                           : 0.0f;
-    }
+            for (int i = 0; i < 4; ++i)
+                er[u][i] = valid && args.epi >= 3 && m0 + i < args.M
+                               ? __half2float(__ldcs(args.R + static_cast<int64_t>(m0 + i) * args.N + n))
+                               : 0.0f;
+        }
+    };
+    if (warp >= 2) load_units();
 
     if (warp == 0) {
         uint32_t inflight = 0, issue_par = 0, phase = 0;
         int stage = 0;
         for (int kb = 0; kb < nk; ++kb) {
-            if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
+            // stages whose weight boxes went out before the grid-dependency wait only need A (their
+            // barriers are fresh, so there is nothing to wait for, and the loop cannot stop before
+            // every such stage has its A: each of their barriers completes)
+            const bool early = args.b_static && kb < L::STAGES;
+            if (!early && !mbar_wait_bounded(empty_bar(stage), phase ^ 1u, flag)) { ok = false; break; }
             inflight &= ~(1u << stage);
             if (lane == 0) {
-                mbar_arrive_expect_tx(full_bar(stage), DEC_BT_STAGE + L::A_ST);
                 const int k = (kb0 + kb) * BK;
-                tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE, &mapB, n0, k, full_bar(stage));
-                tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE + B_BOX, &mapB, n0 + 64, k, full_bar(stage));
+                if (!early) {
+                    mbar_arrive_expect_tx(full_bar(stage), DEC_BT_STAGE + L::A_ST);
+                    tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE, &mapB, n0, k, full_bar(stage));
+                    tma_load_2d(base + L::OFF_BT + stage * DEC_BT_STAGE + B_BOX, &mapB, n0 + 64, k, full_bar(stage));
+                }
                 tma_load_2d(base + L::OFF_AS + stage * L::A_ST, &mapA, k, 0, full_bar(stage));
             }
             inflight |= 1u << stage;
@@ -207,6 +240,7 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
             (void)mbar_wait_drain(drain_bar, 0);
         }
     }
+    if (warp < 2) load_units();
     // All four warps: thread (warp, lane) holds output column n0 + 32*warp + lane of this CTA's
     // partial (its TMEM lane) for all NM rows and sends it to the CTA that owns that column's slice,
     // into row `rank` of that CTA's receive buffer.
@@ -243,7 +277,7 @@ __global__ void __launch_bounds__(kDecThreads) gemm_decode_kernel(
     if (received) {
 #pragma unroll
         for (int u = 0; u < UPT; ++u) {
-            const int idx = static_cast<int>(threadIdx.x) + kDecThreads * u;
+            const int idx = uthread + kDecThreads * u;
             if (idx >= UNITS) break;
             const int c = idx / (NM / 4);
             const int m0 = 4 * (idx % (NM / 4));
@@ -320,7 +354,7 @@ int decode_max_active_clusters() {
 
 // Y = stages 1..epi of the chain applied to A @ B, for M <= 64 (FUSE_OK or an error status).
 int launch_decode_gemm(const void* A, const void* B, const void* bias, const void* R, void* Y, int64_t M,
-                       int64_t N, int64_t K, int epi, cudaStream_t st) {
+                       int64_t N, int64_t K, int epi, bool b_static, cudaStream_t st) {
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     CUtensorMap mA, mB;
@@ -337,6 +371,7 @@ int launch_decode_gemm(const void* A, const void* B, const void* bias, const voi
     a.R = static_cast<const __half*>(R);
     a.Y = static_cast<__half*>(Y);
     a.flag = flag;
+    a.b_static = b_static ? 1 : 0;
     if (NM == 16) return launch_decode<16>(mA, mB, a, st);
     if (NM == 32) return launch_decode<32>(mA, mB, a, st);
     return launch_decode<64>(mA, mB, a, st);

@@ -253,6 +253,13 @@ size_t fuse_causal_softmax_workspace_bytes(int64_t batch_heads, int64_t S, int m
  * to fp16 exactly at the cuts.  No workspace is needed (fuse_gemm_epilogue_ws() takes an optional
  * one that balances the last wave of tiles).
  */
+/* Flag for the cut_mask argument of fuse_gemm_epilogue_plan/_ws (OR it in): the caller vouches
+ * that no work queued on the stream before the call writes B (a weight, as in a decode loop).
+ * The decode kernel (M <= 64) then loads its first ring of weight boxes while the preceding kernel
+ * may still run, instead of after waiting for it; A, bias and R are still read only after that
+ * wait.  Results are unchanged; if something queued before the call does write B, the call may
+ * read B's old contents.  Ignored for M > 64. */
+#define FUSE_GEMM_STATIC_B 0x100u
 int fuse_gemm_epilogue(const void* A, const void* B, const void* bias, const void* R, void* Y,
                        int64_t M, int64_t N, int64_t Kdim, fuse_stream_t stream);
 int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, const void* R, void* Y,
@@ -266,6 +273,8 @@ int fuse_gemm_epilogue_plan(const void* A, const void* B, const void* bias, cons
  * for one that has not started: if the other pair is late (other work holds the SMs it would run
  * on), the first leaves its sums and the other finishes the whole tile.  Results equal the
  * unsplit kernel's up to fp32 summation order.
+ *   cut_mask   the plan (bits 0..2, as fuse_gemm_epilogue_plan), optionally | FUSE_GEMM_STATIC_B;
+ *              any other bit: FUSE_EINVAL.
  *   workspace  device memory of at least fuse_gemm_workspace_bytes(M, N, Kdim) bytes, 256-byte
  *              aligned, zero-filled before its first use (every completed call leaves it so; after
  *              a call that failed with FUSE_ETIMEOUT, zero it again); not shared with a call that

@@ -229,6 +229,13 @@ def test_gemm_host_validation():
     assert lib.fuse_gemm_epilogue_plan(0x1008, 0x2000, 0x3000, 0x4000, 0x9000, 64, 64, 64, 0,
                                        None) == fc.FUSE_EALIGN      # A not 16-byte aligned
     assert lib.fuse_gemm_epilogue_plan(None, None, None, None, None, 0, 64, 64, 0, None) == fc.FUSE_OK
+    # the static-weight flag is the only bit accepted beside the plan's three
+    assert lib.fuse_gemm_epilogue_plan(None, None, None, None, None, 0, 64, 64,
+                                       fc.FUSE_GEMM_STATIC_B | 7, None) == fc.FUSE_OK
+    assert lib.fuse_gemm_epilogue_plan(0x1000, 0x2000, 0x3000, 0x4000, 0x9000, 16, 64, 64,
+                                       0x200, None) == fc.FUSE_EINVAL
+    hdr = open(HEADER).read()
+    assert re.search(r"#define FUSE_GEMM_STATIC_B 0x100u", hdr) and fc.FUSE_GEMM_STATIC_B == 0x100
 
 
 def test_gemm_workspace_bytes_is_host_arithmetic():

@@ -325,3 +325,43 @@ def test_accumulation_term_is_needed_by_cublas_too(cuda_device):
     _check(cub.astype(np.float16).view(np.uint16), ref.astype(np.float16).view(np.uint16), 0, A, B)
     rms = lambda d: float(np.sqrt(np.mean(d ** 2)))
     assert rms(ours - ref) <= 3 * rms(cub - ref) + 1e-6
+
+
+@pytest.mark.parametrize("shape", [(16, 4096, 4096), (1, 520, 200), (33, 264, 4104), (64, 1024, 512), (300, 520, 200)])
+@pytest.mark.parametrize("mask", [0, 7])
+def test_static_weight_flag_changes_no_result(cuda_device, shape, mask):
+    """FUSE_GEMM_STATIC_B lets the decode kernel load its first weight boxes before waiting for the
+    preceding kernel; the arithmetic is the same, so Y is bit-identical with and without it (the
+    M > 64 kernel ignores the flag)."""
+    import torch
+    A, B, bias, R = wl.gemm_input(*shape, salt=15, std=1.0 / 8.0)
+    ys = []
+    for flag in (0, fc.FUSE_GEMM_STATIC_B):
+        Y = torch.full((shape[0], shape[1]), float("nan"), dtype=torch.float16, device="cuda")
+        fc.fuse_gemm_epilogue(_dev(A), _dev(B), _dev(bias), _dev(R), Y, cut_mask=mask | flag, workspace=False)
+        torch.cuda.synchronize()
+        assert fc.fuse_check() == fc.FUSE_OK
+        ys.append(Y.cpu().view(torch.int16).numpy().view(np.uint16))
+    assert np.array_equal(ys[0], ys[1])
+    _check(ys[1], oracle.gemm_epilogue(A, B, bias, R, mask), mask, A, B)
+
+
+def test_weight_written_by_the_preceding_kernel_is_read_without_the_flag(cuda_device):
+    """Without FUSE_GEMM_STATIC_B the decode kernel reads B only after the preceding kernel on the
+    stream has finished: a weight that kernel writes (here a copy of a second weight over the
+    first) is the one used, in every call of a stream of them."""
+    import torch
+    A, B1, bias, R = wl.gemm_input(16, 4096, 4096, salt=16, std=1.0 / 8.0)
+    _, B2, _, _ = wl.gemm_input(16, 4096, 4096, salt=17, std=1.0 / 8.0)
+    Ad, bd, Rd = _dev(A), _dev(bias), _dev(R)
+    Bd, B2d = _dev(B1), _dev(B2)
+    Y = torch.empty(16, 4096, dtype=torch.float16, device="cuda")
+    want = oracle.gemm_epilogue(A, B2, bias, R, 0)
+    for _ in range(3):
+        Bd.copy_(_dev(B1))
+        torch.cuda.synchronize()
+        Bd.copy_(B2d)                     # queued on the stream right before the call
+        fc.fuse_gemm_epilogue(Ad, Bd, bd, Rd, Y, workspace=False)
+        torch.cuda.synchronize()
+        got = Y.cpu().view(torch.int16).numpy().view(np.uint16)
+        _check(got, want, 0, A, B2)
