@@ -357,16 +357,29 @@ extern "C" int fuse_chain_run_host(const fuse_stage* stages, int K, const void* 
     int rc = host_pipe_init(hp);
     if (rc != FUSE_OK) return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    // slices of whole 32-byte vectors, so each slice keeps the vector path of the whole call
-    int64_t per = (n + slices - 1) / slices;
-    per = (per + 31) / 32 * 32;
     auto ok = [&](cudaError_t err) { return err == cudaSuccess ? FUSE_OK : record_cuda_error(err); };
     // the copies start after the work already queued on `stream`
     if ((rc = ok(cudaEventRecord(hp.entry, st))) || (rc = ok(cudaStreamWaitEvent(hp.s_in, hp.entry, 0))) ||
         (rc = ok(cudaStreamWaitEvent(hp.s_out, hp.entry, 0))))
         return rc;
-    for (int64_t lo = 0; lo < n; lo += per) {
-        const int64_t cnt = n - lo < per ? n - lo : per;
+    // Slice boundaries in whole 32-byte vectors (each slice keeps the vector path of the whole
+    // call).  The first slice's copy in and the last slice's copy out overlap nothing, so with
+    // three or more slices those two are a quarter of the size of the others (weights 1, 4, ...,
+    // 4, 1): the pipeline fills and drains on small pieces.
+    const int64_t wsum = slices >= 3 ? 4 * (slices - 2) + 2 : slices;
+    auto bound = [&](int i) -> int64_t {   // first element of slice i (i = slices -> n)
+        if (i <= 0) return 0;
+        if (i >= slices) return n;
+        const int64_t w = slices >= 3 ? 1 + 4 * (i - 1) : i;
+        const int64_t e = static_cast<int64_t>(static_cast<double>(n) * static_cast<double>(w) /
+                                               static_cast<double>(wsum));
+        const int64_t a = e / 32 * 32;
+        return a < n ? a : n;
+    };
+    for (int i = 0; i < slices; ++i) {
+        const int64_t lo = bound(i), hi = bound(i + 1);
+        if (hi <= lo) continue;
+        const int64_t cnt = hi - lo;
         const size_t off = static_cast<size_t>(lo * eb), len = static_cast<size_t>(cnt * eb);
         if ((rc = ok(cudaMemcpyAsync(static_cast<char*>(x_dev) + off, static_cast<const char*>(x_host) + off, len,
                                      cudaMemcpyHostToDevice, hp.s_in))) ||
