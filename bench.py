@@ -488,7 +488,7 @@ def run_ours(args, rank, world, local):
     kernel_src = {"softmax_fused": "softmax.cu", "chain_fused": "chain.cu", "gemm_M4096_fused": "gemm.cu",
                   "chain_fat": "chain.cu", "rmsnorm_fused": "rmsnorm.cu", "gemm_M16_fused": "gemm_decode.cu",
                   "add_rmsnorm_fused": "rmsnorm.cu", "silu_mul_fused": "silu_mul.cu",
-                  "attention_fused": "attention.cu"}
+                  "attention_fused": "attention.cu", "chain26_fused": "chain.cu"}
     families = {}
     for g in groups:
         families.setdefault(g.family, []).append(g)
