@@ -171,6 +171,72 @@ __device__ __forceinline__ float2 block_exp2(const float (&s)[HK], int k0, int l
     return sum2;
 }
 
+// The same two steps for a block at or past the diagonal, where key k of the block is visible to
+// the lane's row iff k <= lim.  A warp's 32 lanes hold 32 consecutive rows, so their limits are
+// base + lane with base = lim - lane a multiple of 32, and every aligned chunk of 32 keys is, for
+// the whole warp, either visible (ks + 31 <= base), masked (ks > base + 31) or the one band where
+// key ks + e is visible for lanes e <= lane (ks == base).  Branching per chunk on those
+// warp-uniform cases keeps the per-element mask to that band and skips masked chunks (the
+// softmax is issue-bound, and the element-wise mask of block_row_max / block_exp2 with MASK
+// more than doubled a diagonal block's softmax time); maxima and sums are theirs, bit for bit
+// (masked keys contribute -inf to the maximum and +0, in the same order, to the sum).
+template <int HK>
+__device__ __forceinline__ float block_row_max_diag(const float (&s)[HK], const float (&so)[HK], int k0, int ko,
+                                                    int base, int lane) {
+    float m[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    auto chunk = [&](const float (&v)[HK], int ks, int c) {
+        if (ks + 31 <= base) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) m[e & 3] = fmaxf(m[e & 3], v[32 * c + e]);
+        } else if (ks == base) {
+#pragma unroll
+            for (int e = 0; e < 32; ++e) m[e & 3] = fmaxf(m[e & 3], e > lane ? -INFINITY : v[32 * c + e]);
+        }
+    };
+#pragma unroll
+    for (int c = 0; c < HK / 32; ++c) {
+        chunk(s, k0 + 32 * c, c);
+        chunk(so, ko + 32 * c, c);
+    }
+    return fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3]));
+}
+
+template <int HK>
+__device__ __forceinline__ float2 block_exp2_diag(const float (&s)[HK], int k0, int base, int lane, float c,
+                                                  float m, uint32_t (&pk)[HK / 2]) {
+    const float2 c2 = make_float2(c, c), nm2 = make_float2(-m, -m);
+    float2 sum2 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int cc = 0; cc < HK / 32; ++cc) {
+        const int ks = k0 + 32 * cc;
+        if (ks + 31 <= base) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const int k = 32 * cc + e;
+                const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+                const float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+                sum2 = __fadd2_rn(sum2, p);
+                pk[k / 2] = pack_bf16x2(p.x, p.y);
+            }
+        } else if (ks == base) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+                const int k = 32 * cc + e;
+                const float2 x = __ffma2_rn(make_float2(s[k], s[k + 1]), c2, nm2);
+                float2 p = make_float2(ex2f(x.x), ex2f(x.y));
+                if (e > lane) p.x = 0.0f;
+                if (e + 1 > lane) p.y = 0.0f;
+                sum2 = __fadd2_rn(sum2, p);
+                pk[k / 2] = pack_bf16x2(p.x, p.y);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) pk[(32 * cc + e) / 2] = 0u;
+        }
+    }
+    return sum2;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
     const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
@@ -356,13 +422,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
             __syncwarp();
             if (lane == 0) mbar_arrive(s_free(sb));   // the score buffer may be overwritten now
 
-            // keys with index > query index are masked (only in the blocks at the diagonal)
             // keys with index > query index are masked: only in the blocks at and past the
             // tile's diagonal (j >= qt), a condition uniform over the CTA
             const int lim = qrow - j * kAttnK;           // last visible key of this block
             const bool diag = j >= qt;
             const int k0 = HK * hh, ko = HK * (1 - hh);
-            const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
+            const float mx = (diag ? block_row_max_diag<HK>(s, so, k0, ko, lim - lane, lane)
                                    : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
             float alpha = 1.0f;
             bool rescale = false;
@@ -375,7 +440,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
             }
             // p = 2^(s c - m) for this warp's HK keys
             uint32_t pk[HK / 2];
-            const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
+            const float2 sum2 = diag ? block_exp2_diag<HK>(s, k0, lim - lane, lane, c, m_used, pk)
                                      : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
             l = l * alpha + (sum2.x + sum2.y);
 
@@ -834,7 +899,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                 const int lim = qrow - j * kAttnK;           // last visible key of this block
                 const bool diag = j >= qt;
                 const int k0 = HK * hh, ko = HK * (1 - hh);
-                const float mx = (diag ? block_row_max<HK, true>(s, so, k0, ko, lim)
+                const float mx = (diag ? block_row_max_diag<HK>(s, so, k0, ko, lim - lane, lane)
                                        : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
                 float alpha = 1.0f;
                 bool rescale = false;
@@ -846,7 +911,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                     m_used = mx;
                 }
                 uint32_t pk[HK / 2];
-                const float2 sum2 = diag ? block_exp2<HK, true>(s, k0, lim, c, m_used, pk)
+                const float2 sum2 = diag ? block_exp2_diag<HK>(s, k0, lim - lane, lane, c, m_used, pk)
                                          : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
                 l = l * alpha + (sum2.x + sum2.y);
 
