@@ -92,6 +92,12 @@ int describe_kernel(const void* kernel, const char* name, int block, int dyn_sme
     out->block_threads = block;
     out->max_threads_per_block = a.maxThreadsPerBlock;
     out->tmem_cols = tmem_cols;
+    // above the default 48 KB a launch opts in to its dynamic shared memory first; do the same so
+    // the answer does not depend on whether the kernel has been launched in this process yet
+    if (dyn_smem > a.maxDynamicSharedSizeBytes) {
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+        if (e != cudaSuccess) return record_cuda_error(e);
+    }
     int b = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kernel, block, dyn_smem);
     if (e != cudaSuccess) return record_cuda_error(e);

@@ -30,6 +30,8 @@ struct ChainParams {
                     // body in groups of 4 elements
     int K;
     int prefetch;   // 1: start this CTA's input on its way into L2 before the grid-dependency wait
+    int64_t ahead;  // with prefetch: also start the input of CTA blockIdx.x + ahead (the CTA that
+                    // takes this slot one wave later); 0 = none
     uint32_t relu_mask;
     float a[FUSE_MAX_STAGES];
     float b[FUSE_MAX_STAGES];
@@ -83,19 +85,25 @@ __device__ __forceinline__ void chain_body(const ChainParams& p) {
 }
 
 // This CTA's share of the 32-byte-aligned body on its way into L2 while the preceding kernel may
-// still run, then the grid-dependency wait (before any global-memory load or store).  Not for an
-// unfused stage after the first: its input is the intermediate the preceding stage is writing,
-// already in L2 or about to be overwritten, and fetching it from DRAM early only adds traffic
-// (measured: the K = 8 unfused chain at N = 2^24 went from 104 to 113 us with it).
+// still run, then the grid-dependency wait (before any global-memory load or store).  The share of
+// the CTA one wave later goes too: at the start of a launch the first wave then has two waves of
+// input in flight across the grid-dependency release, and in steady state every CTA finds its
+// input already on its way (measured at N = 2^24: 21.0 -> 20.1 us per call; one wave ahead only
+// for the first wave gains half of that, two waves ahead or twice the distance lose it again).
+// Not for an unfused stage after the first: its input is the intermediate the preceding stage is
+// writing, already in L2 or about to be overwritten, and fetching it from DRAM early only adds
+// traffic (measured: the K = 8 unfused chain at N = 2^24 went from 104 to 113 us with it).
 template <typename T>
 __device__ __forceinline__ void prefetch_then_wait(const ChainParams& p) {
     pdl_trigger();
     if (p.prefetch && threadIdx.x == 0) {
-        const int64_t v0 = static_cast<int64_t>(blockIdx.x) * kBlock;
-        const int64_t nv = p.nvec - v0 < kBlock ? p.nvec - v0 : kBlock;
-        if (nv > 0)
-            prefetch_l2_bulk(static_cast<const T*>(p.x) + p.head + v0 * Vec32<T>::N,
-                             static_cast<uint32_t>(nv) * 32u);
+        for (int w = 0; w < (p.ahead > 0 ? 2 : 1); ++w) {
+            const int64_t v0 = (static_cast<int64_t>(blockIdx.x) + w * p.ahead) * kBlock;
+            const int64_t nv = p.nvec - v0 < kBlock ? p.nvec - v0 : kBlock;
+            if (nv > 0)
+                prefetch_l2_bulk(static_cast<const T*>(p.x) + p.head + v0 * Vec32<T>::N,
+                                 static_cast<uint32_t>(nv) * 32u);
+        }
     }
     pdl_wait();
 }
@@ -110,6 +118,13 @@ template <typename T>
 __global__ void __launch_bounds__(kBlock) chain_stage_kernel(const __grid_constant__ ChainParams p) {
     prefetch_then_wait<T>(p);
     chain_body<T, true>(p);
+}
+
+// CTAs of the element kernels resident on the whole device at once (one wave).
+template <typename T>
+int64_t resident_ctas() {
+    static const int occ = blocks_per_sm(chain_fused_kernel<T>, kBlock);
+    return static_cast<int64_t>(sm_count()) * occ;
 }
 
 // ---------------------------------------------------------------------------------- fat probe
@@ -223,6 +238,7 @@ template <typename T>
 int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
     ChainParams p = base;
     p.prefetch = 1;
+    p.ahead = resident_ctas<T>();
     partition<T>(p, p.x, p.y);
     if (mode == FUSE_FUSED) {
         return launch_pdl(chain_fused_kernel<T>, dim3(exact_grid<T>(p)), dim3(kBlock), 0, stream, 1, p);
@@ -244,6 +260,7 @@ int launch_chain(const ChainParams& base, int mode, cudaStream_t stream) {
         q.relu_mask = (base.relu_mask >> s) & 1u;
         if (s > 0) q.x = base.y;
         q.prefetch = s == 0;
+        q.ahead = s == 0 ? resident_ctas<T>() : 0;
         partition<T>(q, q.x, q.y);
         const int rc = launch_pdl(chain_stage_kernel<T>, dim3(exact_grid<T>(q)), dim3(kBlock), 0, stream, 1, q);
         if (rc != FUSE_OK) return rc;

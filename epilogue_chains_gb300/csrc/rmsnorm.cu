@@ -46,16 +46,24 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 // One CTA per row.  ADD: the row is h = x + res (one fp32 rounding per element), stored to h
 // before it is normalised; h may be x or res itself (each element is read before the same thread
 // writes it).  Rows are whole 16-byte vectors (hidden % 4 == 0, 16-byte aligned bases).
+// Before the grid-dependency wait, the row's input, and that of row + ahead (the row this slot
+// takes one wave later; ahead = 0: none), start on their way into L2 while the preceding kernel
+// may still run.
 template <int THR, int VPT, bool ADD>
 __global__ void __launch_bounds__(THR) rmsnorm_row_kernel(const float* x, const float* res,
                                                           const float* __restrict__ w, float* h,
-                                                          float* __restrict__ y, int hidden, float eps) {
+                                                          float* __restrict__ y, int hidden, float eps,
+                                                          int ahead) {
     pdl_trigger();
     const int64_t row = blockIdx.x;
-    // the row's input on its way into L2 while the preceding kernel may still run
     if (threadIdx.x == 0) {
-        prefetch_l2_bulk(x + row * hidden, static_cast<uint32_t>(hidden) * 4u);
-        if (ADD) prefetch_l2_bulk(res + row * hidden, static_cast<uint32_t>(hidden) * 4u);
+        const uint32_t bytes = static_cast<uint32_t>(hidden) * 4u;
+        prefetch_l2_bulk(x + row * hidden, bytes);
+        if (ADD) prefetch_l2_bulk(res + row * hidden, bytes);
+        if (ahead > 0 && row + ahead < gridDim.x) {
+            prefetch_l2_bulk(x + (row + ahead) * hidden, bytes);
+            if (ADD) prefetch_l2_bulk(res + (row + ahead) * hidden, bytes);
+        }
     }
     pdl_wait();  // before any global-memory load or store (programmatic dependent launch)
     __shared__ float red[THR / 32];
@@ -236,7 +244,12 @@ __global__ void __launch_bounds__(kEwBlock) rms_weight_kernel(float* __restrict_
 template <int THR, int VPT, bool ADD>
 int launch_fused_vec(const float* x, const float* res, const float* w, float* h, float* y,
                      int64_t rows, int hidden, float eps, cudaStream_t st) {
-    return launch_pdl(rmsnorm_row_kernel<THR, VPT, ADD>, dim3(static_cast<unsigned>(rows)), dim3(THR), 0, st, 1, x, res, w, h, y, hidden, eps);
+    // The residual form reads two rows per CTA: prefetching the next wave's rows as well measured
+    // no faster (22.34 -> 22.31 us at [2048, 4096]) and read 7 % more from DRAM (lines evicted
+    // before their use), so it prefetches its own rows only.
+    static const int occ = blocks_per_sm(rmsnorm_row_kernel<THR, VPT, ADD>, THR);
+    const int ahead = ADD ? 0 : sm_count() * occ;
+    return launch_pdl(rmsnorm_row_kernel<THR, VPT, ADD>, dim3(static_cast<unsigned>(rows)), dim3(THR), 0, st, 1, x, res, w, h, y, hidden, eps, ahead);
 }
 
 template <int EPT, bool ADD>

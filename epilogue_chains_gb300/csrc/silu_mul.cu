@@ -30,6 +30,7 @@ struct SiluParams {
     int64_t rows, cols, ld;  // g and u: row stride ld elements; y: row stride cols
     int64_t vpr;             // 32-byte vectors per row (vector path)
     int64_t nvec;            // rows * vpr
+    int64_t ahead;           // vector path: CTAs one wave later, whose input is prefetched too
 };
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -58,9 +59,39 @@ __device__ __forceinline__ float apply(float gv, float uv, float yv) {
     return yv * uv;
 }
 
+// The inputs CTA `cta` reads from DRAM (g and u; u alone for the multiply step, whose y is the
+// intermediate the preceding step just wrote) on their way into L2: one contiguous range per row
+// its vectors touch, at most two (a CTA's vectors cross at most one row boundary when a row holds
+// at least a CTA's worth of them; narrower rows are left to the loads).  Ranges start on 32-byte
+// vector boundaries and are whole vectors long.
+template <typename T, int STEP>
+__device__ __forceinline__ void prefetch_share(const SiluParams& p, int64_t cta) {
+    const int64_t t0 = cta * kBlock;
+    if (t0 >= p.nvec) return;
+    const int64_t t1 = t0 + kBlock < p.nvec ? t0 + kBlock : p.nvec;
+    constexpr int E = Vec32<T>::N;
+    int64_t t = t0;
+    for (int seg = 0; seg < 2 && t < t1; ++seg) {
+        const int64_t row = t / p.vpr;
+        const int64_t end = t1 < (row + 1) * p.vpr ? t1 : (row + 1) * p.vpr;
+        const int64_t src = row * p.ld + (t - row * p.vpr) * E;
+        const uint32_t bytes = static_cast<uint32_t>(end - t) * 32u;
+        if (STEP != kMul) prefetch_l2_bulk(static_cast<const T*>(p.g) + src, bytes);
+        if (STEP != kSilu) prefetch_l2_bulk(static_cast<const T*>(p.u) + src, bytes);
+        t = end;
+    }
+}
+
+// Before the grid-dependency wait, the CTA's own inputs and those of the CTA one wave later start
+// on their way into L2 while the preceding kernel may still run (the pointwise chain's scheme).
 template <typename T, int STEP>
 __global__ void __launch_bounds__(kBlock) silu_mul_vec_kernel(const __grid_constant__ SiluParams p) {
-    pdl_begin();  // before any global-memory access (programmatic dependent launch)
+    pdl_trigger();
+    if (threadIdx.x == 0) {
+        prefetch_share<T, STEP>(p, blockIdx.x);
+        if (p.ahead > 0) prefetch_share<T, STEP>(p, static_cast<int64_t>(blockIdx.x) + p.ahead);
+    }
+    pdl_wait();  // before any global-memory load or store (programmatic dependent launch)
     using V = Vec32<T>;
     constexpr int E = V::N;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -107,7 +138,10 @@ int launch(const SiluParams& p, bool vec, cudaStream_t st) {
     if (vec) {
         const int64_t grid = ceil_div(p.nvec, kBlock);
         if (grid > 0x7fffffffLL) return FUSE_EUNSUPPORTED;
-        return launch_pdl(silu_mul_vec_kernel<T, STEP>, dim3(static_cast<unsigned>(grid)), dim3(kBlock), 0, st, 1, p);
+        static const int occ = blocks_per_sm(silu_mul_vec_kernel<T, STEP>, kBlock);
+        SiluParams q = p;
+        q.ahead = static_cast<int64_t>(sm_count()) * occ;
+        return launch_pdl(silu_mul_vec_kernel<T, STEP>, dim3(static_cast<unsigned>(grid)), dim3(kBlock), 0, st, 1, q);
     } else {
         int64_t grid = ceil_div(p.rows * p.cols, kBlock);
         const int64_t cap = static_cast<int64_t>(sm_count()) * (2048 / kBlock) * 4;
@@ -161,7 +195,7 @@ extern "C" int fuse_silu_mul(const void* g, const void* u, int64_t ld, void* y, 
     const int64_t in_bytes = ((rows - 1) * ld + cols) * eb, out_bytes = rows * cols * eb;
     if (overlaps(y, out_bytes, u, in_bytes)) return FUSE_EINVAL;
     if (overlaps(y, out_bytes, g, in_bytes) && !(y == g && ld == cols)) return FUSE_EINVAL;
-    SiluParams p{g, u, y, rows, cols, ld, 0, 0};
+    SiluParams p{g, u, y, rows, cols, ld, 0, 0, 0};
     const int64_t E = 32 / eb;
     const bool vec = cols % E == 0 && ld % E == 0 && is_aligned(g, 32) && is_aligned(u, 32) &&
                      is_aligned(y, 32);

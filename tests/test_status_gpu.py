@@ -65,3 +65,16 @@ def test_kernel_report_carries_the_ptxas_figures_of_its_build(cuda_device):
         assert r["ptxas_registers"] == t["registers"] == r["regs_per_thread"], r["name"]
         assert r["spill_store_bytes"] == 0 and r["spill_load_bytes"] == 0, r["name"]
         assert r["stack_bytes"] == 0 and r["local_bytes_per_thread"] == 0, r["name"]
+
+
+def test_kernel_report_needs_no_prior_launch():
+    """The report's occupancy figures do not depend on which kernels ran before: in a fresh
+    process, before any launch, every record already gives at least one resident block."""
+    import subprocess, sys, os
+    code = ("import epilogue_chains_gb300 as fc\n"
+            "bad = [r['name'] for r in (fc.fuse_kernel_report(i) for i in range(fc.fuse_kernel_count()))"
+            " if r['blocks_per_sm_api'] < 1 or r['blocks_per_sm'] < 1]\n"
+            "assert not bad, bad\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
