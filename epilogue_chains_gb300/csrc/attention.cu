@@ -661,6 +661,25 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
     cluster_sync();   // both CTAs' barriers exist before either signals the other
     tc_fence_after();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + L::OFF_HOLD);
+    // The cluster's first item's Q rows and first key and value blocks on their way into L2 while
+    // the preceding kernel may still run (an L2 fill changes no data, whoever writes these lines
+    // before the grid-dependency wait returns).
+    if (lane == 0 && my_items > 0 && (warp == 0 || warp == 2 || warp == 3)) {
+        int bh, u, nb;
+        item(0, bh, u, nb);
+        if (warp == 3) {
+            const int row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
+            for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, row0);
+        } else if (warp == 0) {
+            for (int j = 0; j < nb && j < kPairK; ++j)
+                for (int c = 0; c < L::QATOMS; ++c)
+                    tma_prefetch_2d(&mKh, 64 * c, bh * a.S + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2));
+        } else {
+            for (int j = 0; j < nb && j < kPairV; ++j)
+                for (int c = 0; c < L::VATOMS; ++c)
+                    tma_prefetch_2d(&mV, static_cast<int>(rank) * (D / 2) + 64 * c, bh * a.S + j * kAttnK);
+        }
+    }
     pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
     if (warp == 0 || warp == 2) {
