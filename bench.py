@@ -256,10 +256,15 @@ def run_ours(args, rank, world, local):
             counter["launches"] += K if mode == fc.FUSE_UNFUSED else 1
         return fn
 
-    groups = [Group(f"chain_fused_K{K}", chain(K, fc.FUSE_FUSED), chain_bytes, 4, "hbm",
+    # Calls of one kind run back to back between one event pair.  The first call after an event
+    # record cannot start under the preceding call's tail (measured per call for the K = 4 chain:
+    # 21.5 / 20.2 / 19.5 / 19.1 us for 2 / 4 / 8 / 16 calls; SiLU*up 28.6 / 27.4 / 26.7 / 26.3 us;
+    # RMSNorm 13.3 / 12.5 / 12.0 / 11.6 us), so calls under ~100 us are timed 8 to a group, fused
+    # and unfused alike, and longer ones 2 to 4.
+    groups = [Group(f"chain_fused_K{K}", chain(K, fc.FUSE_FUSED), chain_bytes, 8, "hbm",
                     "chain_fused_kernel<f32>", 1, "chain_fused") for K in KS]
     groups += [Group(f"chain_unfused_K{K}", chain(K, fc.FUSE_UNFUSED),
-                     fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED), 2, "hbm", None, K,
+                     fc.fuse_chain_bytes(K, N, fc.FUSE_F32, fc.FUSE_UNFUSED), 8, "hbm", None, K,
                      "chain_unfused") for K in KS]
     # The same sweep at N = 2^26 (256 MiB per operand, twice the L2): an unfused stage's 256 MiB
     # intermediate cannot stay in L2, so every stage moves its 2 N b through DRAM as the ledger
@@ -279,7 +284,7 @@ def run_ours(args, rank, world, local):
             counter["launches"] += K if mode == fc.FUSE_UNFUSED else 1
         return fn
 
-    groups += [Group(f"chain26_fused_K{K}", chain_big(K, fc.FUSE_FUSED), chain_bytes_big, 2, "hbm",
+    groups += [Group(f"chain26_fused_K{K}", chain_big(K, fc.FUSE_FUSED), chain_bytes_big, 4, "hbm",
                      "chain_fused_kernel<f32>", 1, "chain26_fused") for K in KS]
     groups += [Group(f"chain26_unfused_K{K}", chain_big(K, fc.FUSE_UNFUSED),
                      fc.fuse_chain_bytes(K, NB, fc.FUSE_F32, fc.FUSE_UNFUSED), 2, "hbm", None, K,
@@ -312,7 +317,7 @@ def run_ours(args, rank, world, local):
             # one call per x/y pair of the rotation: the group's leading launch latency is spread over
             # as many ~13 us calls as the rotation holds
             Group("rmsnorm_fused", rms(fc.FUSE_FUSED), rb[fc.FUSE_FUSED], 8, "hbm", "rmsnorm_row_kernel", 1),
-            Group("rmsnorm_unfused", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED], 4, "hbm", None, 4),
+            Group("rmsnorm_unfused", rms(fc.FUSE_UNFUSED), rb[fc.FUSE_UNFUSED], 8, "hbm", None, 4),
         ]
         # -------------------------------------------------------------- residual add + RMSNorm
         with torch.cuda.stream(stream):
@@ -350,11 +355,11 @@ def run_ours(args, rank, world, local):
             return fn
         sb = {m: fc.fuse_silu_mul_bytes(SR, SC, fc.FUSE_BF16, m) for m in (fc.FUSE_FUSED, fc.FUSE_UNFUSED)}
         groups += [
-            Group("add_rmsnorm_fused", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED], 4, "hbm",
+            Group("add_rmsnorm_fused", addrms(fc.FUSE_FUSED), ab[fc.FUSE_FUSED], 8, "hbm",
                   "rmsnorm_row_kernel<+residual>", 1),
-            Group("add_rmsnorm_unfused", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED], 4, "hbm", None, 5),
-            Group("silu_mul_fused", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED], 2, "hbm", "silu_mul_vec_kernel<bf16>", 1),
-            Group("silu_mul_unfused", silu(fc.FUSE_UNFUSED), sb[fc.FUSE_UNFUSED], 2, "hbm", None, 2),
+            Group("add_rmsnorm_unfused", addrms(fc.FUSE_UNFUSED), ab[fc.FUSE_UNFUSED], 8, "hbm", None, 5),
+            Group("silu_mul_fused", silu(fc.FUSE_FUSED), sb[fc.FUSE_FUSED], 8, "hbm", "silu_mul_vec_kernel<bf16>", 1),
+            Group("silu_mul_unfused", silu(fc.FUSE_UNFUSED), sb[fc.FUSE_UNFUSED], 8, "hbm", None, 2),
         ]
         # -------------------------------------------------------------- causal softmax
         bh, S = wl.SM_B * wl.SM_H, wl.SM_S
@@ -416,7 +421,7 @@ def run_ours(args, rank, world, local):
             return fn
         flops = {M: 2 * M * gN * gK for M in wl.GEMM_MS}
         for p_, m_ in plans.items():
-            groups.append(Group(f"gemm_M4096_{p_}", gemm(4096, m_), flops[4096], 2 if m_ == 0 else 1, "tensor",
+            groups.append(Group(f"gemm_M4096_{p_}", gemm(4096, m_), flops[4096], 4 if m_ == 0 else 2, "tensor",
                                 "gemm_tc_kernel" if m_ == 0 else None, 1 + bin(m_).count("1"),
                                 "gemm_M4096_fused" if m_ == 0 else "gemm_M4096_unfused"))
         # decode calls are ~10 us: 16 (8) back-to-back calls per group, as a decode loop issues
