@@ -271,16 +271,20 @@ def test_full_size_sampled_rows(cuda_device, plan, ws):
            rows)
 
 
-def test_full_size_256_rows_as_benchmarked(cuda_device):
-    """Plan [4] at 4096^3 with the split-K workspace, exactly as the bench runs it: a fixed random
-    subset of 256 full rows (plus both ends and the 128-row tile edges around the middle) against
-    the oracle, element by element."""
+def test_full_size_every_row_as_benchmarked(cuda_device):
+    """Plan [4] at 4096^3 with the split-K workspace, exactly as the bench runs it: every element
+    of all 4096 rows against the oracle, which runs on several host threads, 256 rows at a time."""
+    import concurrent.futures as cf
+    import os
     A, B, bias, R = wl.gemm_input(4096)
     Y = _run(A, B, bias, R, 0, ws=True)
-    g = np.random.default_rng(20261002)
-    rows = np.unique(np.concatenate([[0, 127, 128, 2047, 2048, 4095], g.choice(4096, 256, replace=False)]))
-    assert rows.size >= 256
-    _check(Y[rows], oracle.gemm_epilogue(A, B, bias, R, 0, rows=rows), 0, A, B, rows)
+    workers = max(1, min(16, (os.cpu_count() or 2) - 1))
+    with cf.ThreadPoolExecutor(workers) as ex:
+        refs = {r0: ex.submit(oracle.gemm_epilogue, A, B, bias, R, 0, np.arange(r0, r0 + 256))
+                for r0 in range(0, 4096, 256)}
+        for r0, f in refs.items():
+            rows = np.arange(r0, r0 + 256)
+            _check(Y[rows], f.result(), 0, A, B, rows)
 
 
 def test_stress_full_size_sampled_rows(cuda_device):
