@@ -3,6 +3,7 @@
 #include <string.h>
 
 #include <mutex>
+#include <vector>
 
 #include "fc_internal.cuh"
 #include "fc_tc.cuh"
@@ -56,6 +57,28 @@ int sm_count() {
         cached[dev] = n > 0 ? n : 1;
     }
     return cached[dev];
+}
+
+int opt_in_smem(const void* kernel, int bytes, bool max_shared_carveout) {
+    struct Done {
+        const void* kernel;
+        int dev, bytes;
+    };
+    static std::mutex mu;
+    static std::vector<Done> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return record_cuda_error(e);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Done& d : done)
+        if (d.kernel == kernel && d.dev == dev && d.bytes >= bytes) return FUSE_OK;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && max_shared_carveout)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e != cudaSuccess) return record_cuda_error(e);
+    done.push_back({kernel, dev, bytes});
+    return FUSE_OK;
 }
 
 // The ptxas -v table of this build (generated from the build's own ptxas output and linked in).

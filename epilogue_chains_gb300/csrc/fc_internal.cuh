@@ -76,6 +76,11 @@ int launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cud
 
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
+// Opt `kernel` into `bytes` of dynamic shared memory on the current device (and, with
+// max_shared_carveout, into the largest shared-memory carveout) once per device: a kernel
+// attribute belongs to a device's context, so every device a process launches on needs its own.
+// Returns FUSE_OK or the recorded CUDA error.
+int opt_in_smem(const void* kernel, int bytes, bool max_shared_carveout = false);
 
 // Device address of the watchdog word on the current device (nullptr on failure).  Kernels with
 // bounded waits take it as a parameter and set it when a wait runs out.

@@ -607,10 +607,8 @@ bool overlap(const void* a, int64_t abytes, const void* b, int64_t bbytes) {
     return x < y + static_cast<uintptr_t>(bbytes) && y < x + static_cast<uintptr_t>(abytes);
 }
 
-bool main_attr_ok() {
-    static const bool ok = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                static_cast<int>(MAIN_SMEM)) == cudaSuccess;
-    return ok;
+int main_attr() {
+    return opt_in_smem((const void*)gemm_tc_kernel, static_cast<int>(MAIN_SMEM));
 }
 
 // 2-CTA clusters that can be resident at once (a cluster needs both its CTAs in one GPC, so an
@@ -624,7 +622,7 @@ int max_active_pairs() {
         return sm_count() / 2;
     }
     std::lock_guard<std::mutex> lock(mu);
-    if (cached[dev] == 0 && main_attr_ok()) {
+    if (cached[dev] == 0 && main_attr() == FUSE_OK) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * static_cast<unsigned>(sm_count()));
         cfg.blockDim = dim3(kMainThreads);
@@ -677,7 +675,7 @@ int launch_gemm(const void* A, const void* B, const void* bias, const void* R, v
     CUtensorMap mA, mB;
     if (M <= 64) return launch_decode_gemm(A, B, bias, R, Y, M, N, K, epi, b_static, st);
     if (!make_map(&mA, A, M, K, 64, BM) || !make_map(&mB, B, K, N, 64, 64)) return FUSE_ECUDA;
-    if (!main_attr_ok()) return check_launch();
+    if (const int rc = main_attr(); rc != FUSE_OK) return rc;
     MainArgs a;
     a.M = static_cast<int>(M);
     a.N = static_cast<int>(N);
@@ -736,7 +734,7 @@ int gemm_report_count() { return 3; }
 int gemm_report(int i, fuse_kernel_record* out) {
     switch (i) {
         case 0: {
-            if (!main_attr_ok()) return check_launch();
+            if (const int ra = main_attr(); ra != FUSE_OK) return ra;
             const int rc = describe_kernel((const void*)gemm_tc_kernel,
                                            "gemm_tc_kernel (2-CTA cluster, 128x256 tcgen05)",
                                            kMainThreads, static_cast<int>(MAIN_SMEM), out,

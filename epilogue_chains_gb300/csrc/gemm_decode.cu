@@ -318,12 +318,8 @@ int launch_decode(const CUtensorMap& mA, const CUtensorMap& mB, const DecodeArgs
     // whole grid (ceil(N/128) x 8 CTAs) is resident in one wave (CTA start stamps: the 256 CTAs
     // of N = 4096 start within ~1.2 us, two per SM on 148 SMs; the occupancy API, which reports
     // one CTA per SM for kernels that allocate tensor memory, undercounts)
-    static const bool attr =
-        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(L::SMEM)) == cudaSuccess &&
-        cudaFuncSetAttribute(gemm_decode_kernel<NM>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             static_cast<int>(cudaSharedmemCarveoutMaxShared)) == cudaSuccess;
-    if (!attr) return check_launch();
+    const int rc = opt_in_smem((const void*)gemm_decode_kernel<NM>, static_cast<int>(L::SMEM), true);
+    if (rc != FUSE_OK) return rc;
     return launch_pdl(gemm_decode_kernel<NM>, dim3(static_cast<unsigned>(ceil_div(a.N, 128) * DEC_SPLIT)), dim3(kDecThreads), L::SMEM, st, DEC_SPLIT, mA, mB, a);
 }
 
@@ -379,10 +375,10 @@ int launch_decode_gemm(const void* A, const void* B, const void* bias, const voi
 
 // Kernel record of the M = 16 decode kernel.
 int decode_report(fuse_kernel_record* out) {
-    (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(DecodeLayout<16>::SMEM));
-    (void)cudaFuncSetAttribute(gemm_decode_kernel<16>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    // the launch configuration's attributes, as a launch sets them (shared-memory carveout included)
+    if (const int ra = opt_in_smem((const void*)gemm_decode_kernel<16>, static_cast<int>(DecodeLayout<16>::SMEM), true);
+        ra != FUSE_OK)
+        return ra;
     const int rc = describe_kernel((const void*)gemm_decode_kernel<16>,
                                    "gemm_decode_kernel<16> (swap-AB, split-K x8)", kDecThreads,
                                    static_cast<int>(DecodeLayout<16>::SMEM), out,

@@ -429,10 +429,9 @@ template <int VPL, typename OutT>
 int launch_vec(const __nv_bfloat16* s, OutT* p, int64_t rows, int S, float c, int tile,
                cudaStream_t st) {
     const size_t smem = fused_smem_bytes(S);
-    static const bool attr_ok = cudaFuncSetAttribute(softmax_fused_kernel<VPL, OutT>,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                     static_cast<int>(fused_smem_bytes(512 * VPL))) == cudaSuccess;
-    if (!attr_ok) return check_launch();
+    const int attr_rc = opt_in_smem((const void*)softmax_fused_kernel<VPL, OutT>,
+                                    static_cast<int>(fused_smem_bytes(512 * VPL)));
+    if (attr_rc != FUSE_OK) return attr_rc;
     int* flag = watchdog_flag();
     if (!flag) return FUSE_ECUDA;
     const int occ = blocks_per_sm(softmax_fused_kernel<VPL, OutT>, kSmBlock, smem);
