@@ -128,10 +128,33 @@ struct AttnSched {
     uint16_t item[kSchedItems];
 };
 
+// Per-warpgroup register budgets (the block is launched with 128 per thread).
+template <int N> __device__ __forceinline__ void setmaxnreg_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N> __device__ __forceinline__ void setmaxnreg_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+// Wait until at most one committed bulk store group still reads its shared-memory source.
+__device__ __forceinline__ void bulk_wait_read1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+
 __device__ __forceinline__ float max3f(float a, float b, float c) {
     float r;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
+}
+
+// Keys k0 + k of a block at or past the diagonal that the lane's row does not see (k0 + k > lim)
+// become -inf in place, one compare and select per key, so that the plain maximum and exponential
+// below serve every block: a masked key gives -inf to the maximum and 2^-inf = +0 as its weight,
+// the same maxima, weights and sums, bit for bit, as leaving it out.  (A separate masked copy of
+// the maximum and exponential code, run once or twice per tile pair, came back to the SM's
+// instruction cache every time and took twice as long as this.)
+template <int HK>
+__device__ __forceinline__ void mask_block(float (&v)[HK], int k0, int lim) {
+    const int th = lim - k0;   // key k0 + k is visible iff k <= th
+#pragma unroll
+    for (int k = 0; k < HK; ++k) v[k] = k > th ? -INFINITY : v[k];
 }
 
 // Row maximum over this thread's HK scores s (keys k0 + k) and its partner warp's HK scores so
@@ -537,6 +560,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1) attn_fwd_kernel(
 // Warp roles are given at the persistent kernel below, the only kernel on this layout.
 // K and V ring depths (K_j+2 is loaded once S_j has completed, V_j+2 once PV_j has).
 constexpr int kPairK = 2, kPairV = 2;
+// Warps that read out and store each item's O (one per TMEM lane quadrant).
+constexpr int kAttnReadoutWarps = 4;
 
 template <int D>
 struct PairLayout {
@@ -551,15 +576,15 @@ struct PairLayout {
     static constexpr uint32_t OFF_Q = 0;
     static constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;                 // + stage * KH_BYTES
     static constexpr uint32_t OFF_V = OFF_K + kPairK * KH_BYTES;       // + stage * VH_BYTES
-    // output staging: per softmax warp 32 rows x 64 columns of bf16 (one 128-byte-swizzled box of
-    // the O tensor map), written to global memory by a TMA store
+    // output staging: two boxes per output warp, each 32 rows x 64 columns of bf16 (one
+    // 128-byte-swizzled box of the O tensor map), written to global memory by TMA stores
     static constexpr uint32_t ST_WARP = 32 * 128;
     static constexpr uint32_t OFF_ST = OFF_V + kPairV * VH_BYTES;
-    static constexpr uint32_t OFF_LX = OFF_ST + kAttnSoftmaxWarps * ST_WARP;   // row-sum exchange, 2 x 128 fp32
+    static constexpr uint32_t OFF_LX = OFF_ST + 2 * kAttnReadoutWarps * ST_WARP;   // row sums, 2 x 128 fp32
     static constexpr uint32_t OFF_BAR = OFF_LX + 2 * kAttnQ * 4;
     // q_full, drain, l_ready, s_full, s_free, p_full[2], o_done[2], k_full[KS], k_empty[KS],
-    // v_full[VS], v_empty[VS], q_empty, o_free
-    static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV + 2;
+    // v_full[VS], v_empty[VS], q_empty, o_free, lx_free
+    static constexpr int N_BARS = 9 + 2 * kPairK + 2 * kPairV + 3;
     static constexpr uint32_t OFF_HOLD = OFF_BAR + N_BARS * 8;
     static constexpr uint32_t SMEM = OFF_HOLD + 16 + 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -582,13 +607,18 @@ struct PairLayout {
 //     the current item's last S has completed (q_empty), and the K and V rings must not wait.
 //   warp 1 of CTA 0: every MMA of the pair, per item in the order S_0, S_1, PV_0, S_2, PV_1, ...;
 //     its commits signal both CTAs' barriers.
-//   warps 4-11: softmax and output of this CTA's 128 query rows (two warps per TMEM lane
-//     quadrant, each exponentiating half of a block's keys and rescaling half of O's columns);
-//     they release S and publish P on CTA 0's barriers.
-// At an item boundary the softmax warps first turn the next item's S_0 into P_0 (so its S_1 can
-// start at once), then read out and store the previous item's O and arrive on o_free; the next
-// item's PV_0, which overwrites O (accumulate off), waits for o_free.
-constexpr int kPersistThreads = 32 * (4 + kAttnSoftmaxWarps);
+//   warps 4-11: softmax of this CTA's 128 query rows (two warps per TMEM lane quadrant, each
+//     exponentiating half of a block's keys and rescaling half of O's columns); they release S
+//     and publish P on CTA 0's barriers, and after an item's last block its row sums (l_ready).
+//   warps 12-15: the output: once an item's last PV has completed, each reads its lane
+//     quadrant's 32 rows of O from TMEM, divides them by the row sums, stores them (staged in
+//     shared memory, TMA box stores) and arrives on o_free; the next item's PV_0, which overwrites
+//     O (accumulate off), waits for it.  Meanwhile the softmax warps go on releasing the next
+//     item's S blocks, so its S MMAs fill the tensor pipe while O is read out.
+// Register budgets per warpgroup (setmaxnreg; launched at 128 per thread): producers and MMA
+// issuer 48, softmax 160, output 144 -- 48 x 128 + 160 x 256 + 144 x 128 = 65,536, all the CTA is
+// launched with.
+constexpr int kPersistThreads = 32 * (4 + kAttnSoftmaxWarps + kAttnReadoutWarps);
 
 template <int D>
 __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
@@ -614,7 +644,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
     auto k_empty = [&](int i) { return bar0 + 8u * (9 + KS + i); };
     auto v_full = [&](int i) { return bar0 + 8u * (9 + 2 * KS + i); };
     auto v_empty = [&](int i) { return bar0 + 8u * (9 + 2 * KS + VS + i); };
-    const uint32_t q_empty = bar0 + 8u * (L::N_BARS - 2), o_free = bar0 + 8u * (L::N_BARS - 1);
+    const uint32_t q_empty = bar0 + 8u * (L::N_BARS - 3), o_free = bar0 + 8u * (L::N_BARS - 2);
+    const uint32_t lx_free = bar0 + 8u * (L::N_BARS - 1);
     int* flag = a.flag;
 
     const int ntile = a.S / kAttnQ;
@@ -637,7 +668,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_empty, 1);
-        mbar_init(o_free, 2 * kAttnSoftmaxWarps);   // both CTAs' softmax warps (CTA 0's copy)
+        mbar_init(o_free, 2 * kAttnReadoutWarps);   // both CTAs' output warps (CTA 0's copy)
+        mbar_init(lx_free, kAttnReadoutWarps);      // this CTA's output warps have read the row sums
         mbar_init(drain, 1);
         mbar_init(l_ready, kAttnSoftmaxWarps);
         mbar_init(s_full, 1);
@@ -682,146 +714,162 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
     }
     pdl_wait();  // the preceding kernel has completed: global memory may be touched
 
-    if (warp == 0 || warp == 2) {
-        // ---------------------------------------------------------------- K / V producers
-        if (lane == 0) {
-            const bool is_k = warp == 0;
-            prefetch_map(is_k ? &mKh : &mV);
-            const int R = is_k ? KS : VS;
-            int g = 0;   // blocks loaded so far, over all items
-            bool ok = true;
-            for (int t = 0; ok && t < my_items; ++t) {
-                int bh, u, nb;
-                item(t, bh, u, nb);
-                const int krow0 = bh * a.S;
-                for (int j = 0; j < nb; ++j, ++g) {
-                    const int st = g % R;
-                    const uint32_t full = is_k ? k_full(st) : v_full(st);
-                    const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
-                    if (g >= R && !mbar_wait_bounded(empty, ((g - R) / R) & 1, flag)) { ok = false; break; }
-                    if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
-                    const uint32_t full_cl = mapa_shared(full, 0);
-                    if (is_k) {
-                        const int y = krow0 + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2);
-                        for (int c = 0; c < L::QATOMS; ++c)
-                            tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
-                                             full_cl);
-                    } else {
-                        const int y = krow0 + j * kAttnK;
-                        for (int c = 0; c < L::VATOMS; ++c)
-                            tma_load_2d_pair(base + L::OFF_V + st * L::VH_BYTES + c * L::V_REGION, &mV,
-                                             static_cast<int>(rank) * (D / 2) + 64 * c, y, full_cl);
+    if (warp < 4) {
+        // ================================================ warpgroup 0: producers and MMA issuer
+        setmaxnreg_dec<48>();
+        if (warp == 0 || warp == 2) {
+            // ---------------------------------------------------------------- K / V producers
+            if (lane == 0) {
+                const bool is_k = warp == 0;
+                prefetch_map(is_k ? &mKh : &mV);
+                const int R = is_k ? KS : VS;
+                int g = 0;   // blocks loaded so far, over all items
+                bool ok = true;
+                for (int t = 0; ok && t < my_items; ++t) {
+                    int bh, u, nb;
+                    item(t, bh, u, nb);
+                    const int krow0 = bh * a.S;
+                    for (int j = 0; j < nb; ++j, ++g) {
+                        const int st = g % R;
+                        const uint32_t full = is_k ? k_full(st) : v_full(st);
+                        const uint32_t empty = is_k ? k_empty(st) : v_empty(st);
+                        if (g >= R && !mbar_wait_bounded(empty, ((g - R) / R) & 1, flag)) { ok = false; break; }
+                        if (leader) mbar_arrive_expect_tx(full, 2 * (is_k ? L::KH_BYTES : L::VH_BYTES));
+                        const uint32_t full_cl = mapa_shared(full, 0);
+                        if (is_k) {
+                            const int y = krow0 + j * kAttnK + static_cast<int>(rank) * (kAttnK / 2);
+                            for (int c = 0; c < L::QATOMS; ++c)
+                                tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
+                                                 full_cl);
+                        } else {
+                            const int y = krow0 + j * kAttnK;
+                            for (int c = 0; c < L::VATOMS; ++c)
+                                tma_load_2d_pair(base + L::OFF_V + st * L::VH_BYTES + c * L::V_REGION, &mV,
+                                                 static_cast<int>(rank) * (D / 2) + 64 * c, y, full_cl);
+                        }
                     }
                 }
+                if (!ok && leader)   // both CTAs' copies in flight complete on CTA 0's barriers
+                    for (int h = g - R < 0 ? 0 : g - R; h < g; ++h)
+                        (void)mbar_wait_drain(is_k ? k_full(h % R) : v_full(h % R), (h / R) & 1);
             }
-            if (!ok && leader)   // both CTAs' copies in flight complete on CTA 0's barriers
-                for (int h = g - R < 0 ? 0 : g - R; h < g; ++h)
-                    (void)mbar_wait_drain(is_k ? k_full(h % R) : v_full(h % R), (h / R) & 1);
-        }
-        __syncwarp();
-    } else if (warp == 3) {
-        // ---------------------------------------------------------------- Q producer
-        if (lane == 0) {
-            prefetch_map(&mQ);
-            const uint32_t qf = mapa_shared(q_full, 0);
-            int t = 0;
-            for (; t < my_items; ++t) {
-                // the previous item's last S has completed in both CTAs
-                if (t >= 1 && !mbar_wait_bounded(q_empty, (t - 1) & 1, flag)) break;
-                int bh, u, nb;
-                item(t, bh, u, nb);
-                const int row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
-                if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
-                for (int c = 0; c < L::QATOMS; ++c)
-                    tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
-                // the next item's Q into L2 now, so that its load (after this item's last S) is short
-                if (t + 1 < my_items) {
-                    item(t + 1, bh, u, nb);
-                    const int row1 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
-                    for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, row1);
+            __syncwarp();
+        } else if (warp == 3) {
+            // ---------------------------------------------------------------- Q producer
+            if (lane == 0) {
+                prefetch_map(&mQ);
+                const uint32_t qf = mapa_shared(q_full, 0);
+                // Each item's rows are looked up (list and order, a few hundred cycles) one item ahead,
+                // so the load follows the q_empty wait at once.
+                int row0 = 0;
+                if (my_items > 0) {
+                    int bh, u, nb;
+                    item(0, bh, u, nb);
+                    row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
                 }
+                int t = 0;
+                for (; t < my_items; ++t) {
+                    // the previous item's last S has completed in both CTAs
+                    if (t >= 1 && !mbar_wait_bounded(q_empty, (t - 1) & 1, flag)) break;
+                    if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
+                    for (int c = 0; c < L::QATOMS; ++c)
+                        tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
+                    // the next item's Q into L2 now, so that its load (after this item's last S) is short
+                    if (t + 1 < my_items) {
+                        int bh, u, nb;
+                        item(t + 1, bh, u, nb);
+                        row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
+                        for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, row0);
+                    }
+                }
+                if (t < my_items && t >= 1 && leader) (void)mbar_wait_drain(q_full, (t - 1) & 1);
             }
-            if (t < my_items && t >= 1 && leader) (void)mbar_wait_drain(q_full, (t - 1) & 1);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ---------------------------------------------------------------- MMA issuer (CTA 0)
-        if (leader && lane == 0) {
-            constexpr uint32_t idS = idesc_f16(2 * kAttnQ, kAttnK, false, false, true);
-            constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
-            bool issued = false;
-            // S_j and PV_j of item t are global block g = (blocks of earlier items) + j
-            auto issue_s = [&](int t, int j, int g, int nb) -> bool {
-                const int st = g % KS;
-                if (j == 0 && !mbar_wait_bounded(q_full, t & 1, flag)) return false;
-                if (!mbar_wait_bounded(k_full(st), (g / KS) & 1, flag)) return false;
-                // both CTAs have read the previous S into registers
-                if (g >= 1 && !mbar_wait_bounded(s_free, (g - 1) & 1, flag)) return false;
-                tc_fence_after();
-                const uint32_t kb = base + L::OFF_K + st * L::KH_BYTES;
+            __syncwarp();
+        } else {
+            // ---------------------------------------------------------------- MMA issuer (CTA 0)
+            if (leader && lane == 0) {
+                constexpr uint32_t idS = idesc_f16(2 * kAttnQ, kAttnK, false, false, true);
+                constexpr uint32_t idO = idesc_f16(2 * kAttnQ, D, false, true, true);
+                bool issued = false;
+                // S_j and PV_j of item t are global block g = (blocks of earlier items) + j
+                auto issue_s = [&](int t, int j, int g, int nb) -> bool {
+                    const int st = g % KS;
+                    if (j == 0 && !mbar_wait_bounded(q_full, t & 1, flag)) return false;
+                    if (!mbar_wait_bounded(k_full(st), (g / KS) & 1, flag)) return false;
+                    // both CTAs have read the previous S into registers
+                    if (g >= 1 && !mbar_wait_bounded(s_free, (g - 1) & 1, flag)) return false;
+                    tc_fence_after();
+                    const uint32_t kb = base + L::OFF_K + st * L::KH_BYTES;
 #pragma unroll
-                for (int s = 0; s < D / 16; ++s)
-                    tc_mma_pair(tmem + L::S_COL,
-                                smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
-                                smem_desc_sw128(kb + (s / 4) * L::KH_REGION + (s % 4) * 32, 16, 1024), idS,
-                                s > 0 ? 1u : 0u);
-                tc_commit_pair_mc(s_full, 0x3);
-                tc_commit_pair_mc(k_empty(st), 0x3);
-                if (j == nb - 1) tc_commit_pair_mc(q_empty, 0x3);   // the item's Q is no longer read
-                issued = true;
-                return true;
-            };
-            auto issue_pv = [&](int t, int j, int g) -> bool {
-                const int st = g % VS, pb = g % 2;
-                if (!mbar_wait_bounded(p_full(pb), (g / 2) & 1, flag)) return false;
-                // the previous item's O has been read out by both CTAs
-                if (j == 0 && t >= 1 && !mbar_wait_bounded(o_free, (t - 1) & 1, flag)) return false;
-                if (!mbar_wait_bounded(v_full(st), (g / VS) & 1, flag)) return false;
-                tc_fence_after();
-                const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
+                    for (int s = 0; s < D / 16; ++s)
+                        tc_mma_pair(tmem + L::S_COL,
+                                    smem_desc_sw128(base + L::OFF_Q + (s / 4) * L::Q_REGION + (s % 4) * 32, 16, 1024),
+                                    smem_desc_sw128(kb + (s / 4) * L::KH_REGION + (s % 4) * 32, 16, 1024), idS,
+                                    s > 0 ? 1u : 0u);
+                    tc_commit_pair_mc(s_full, 0x3);
+                    tc_commit_pair_mc(k_empty(st), 0x3);
+                    if (j == nb - 1) tc_commit_pair_mc(q_empty, 0x3);   // the item's Q is no longer read
+                    issued = true;
+                    return true;
+                };
+                auto issue_pv = [&](int t, int j, int g) -> bool {
+                    const int st = g % VS, pb = g % 2;
+                    if (!mbar_wait_bounded(p_full(pb), (g / 2) & 1, flag)) return false;
+                    // the previous item's O has been read out by both CTAs
+                    if (j == 0 && t >= 1 && !mbar_wait_bounded(o_free, (t - 1) & 1, flag)) return false;
+                    if (!mbar_wait_bounded(v_full(st), (g / VS) & 1, flag)) return false;
+                    tc_fence_after();
+                    const uint32_t vb = base + L::OFF_V + st * L::VH_BYTES;
 #pragma unroll
-                for (int s = 0; s < kAttnK / 16; ++s)
-                    tc_mma_pair_ts(tmem + L::O_COL, tmem + L::P_COL + (kAttnK / 2) * pb + 8 * s,
-                                   smem_desc_sw128(vb + s * 2048, L::V_REGION, 1024), idO, (j > 0 || s > 0) ? 1u : 0u);
-                tc_commit_pair_mc(o_done(pb), 0x3);
-                tc_commit_pair_mc(v_empty(st), 0x3);
-                issued = true;
-                return true;
-            };
-            // S_0, then for every block g (over all items) S_g+1 before PV_g: the next scores are
-            // computed while the softmax warps work on the current ones, across item boundaries
-            // too (the next item's S_0 precedes the current item's last PV)
-            bool ok = my_items > 0;
-            int ts = 0, js = 0, nbs = 0, tp = 0, jp = 0, nbp = 0, bh_, u_;
-            if (ok) {
-                item(0, bh_, u_, nbs);
-                nbp = nbs;
-                ok = issue_s(0, 0, 0, nbs);
-                js = 1;
-            }
-            for (int g = 0; ok && tp < my_items; ++g) {
-                if (js == nbs && ts + 1 < my_items) {   // the S cursor moves to the next item
-                    ++ts;
-                    js = 0;
-                    item(ts, bh_, u_, nbs);
+                    for (int s = 0; s < kAttnK / 16; ++s)
+                        tc_mma_pair_ts(tmem + L::O_COL, tmem + L::P_COL + (kAttnK / 2) * pb + 8 * s,
+                                       smem_desc_sw128(vb + s * 2048, L::V_REGION, 1024), idO,
+                                       (j > 0 || s > 0) ? 1u : 0u);
+                    tc_commit_pair_mc(o_done(pb), 0x3);
+                    tc_commit_pair_mc(v_empty(st), 0x3);
+                    issued = true;
+                    return true;
+                };
+                // S_0, then for every block g (over all items) S_g+1 before PV_g: the next scores are
+                // computed while the softmax warps work on the current ones, across item boundaries
+                // too (the next item's S_0 precedes the current item's last PV)
+                // The item after the S cursor's is looked up (nb_next) once the cursor's item has
+                // issued its S_0, while the queued MMAs run; when the PV cursor moves on, the S cursor
+                // is already on that item (S runs one block ahead), so its block count is nbs.
+                bool ok = my_items > 0;
+                int ts = 0, js = 0, nbs = 0, tp = 0, jp = 0, nbp = 0, nb_next = 0, bh_, u_;
+                if (ok) {
+                    item(0, bh_, u_, nbs);
+                    nbp = nbs;
+                    ok = issue_s(0, 0, 0, nbs);
+                    js = 1;
+                    if (my_items > 1) item(1, bh_, u_, nb_next);
                 }
-                if (js < nbs) {
-                    if (!issue_s(ts, js, g + 1, nbs)) { ok = false; break; }
-                    ++js;
+                for (int g = 0; ok && tp < my_items; ++g) {
+                    if (js == nbs && ts + 1 < my_items) {   // the S cursor moves to the next item
+                        ++ts;
+                        js = 0;
+                        nbs = nb_next;
+                    }
+                    if (js < nbs) {
+                        if (!issue_s(ts, js, g + 1, nbs)) { ok = false; break; }
+                        if (++js == 1 && ts + 1 < my_items) item(ts + 1, bh_, u_, nb_next);
+                    }
+                    if (!issue_pv(tp, jp, g)) { ok = false; break; }
+                    if (++jp == nbp && ++tp < my_items) {
+                        jp = 0;
+                        nbp = nbs;
+                    }
                 }
-                if (!issue_pv(tp, jp, g)) { ok = false; break; }
-                if (++jp == nbp && ++tp < my_items) {
-                    jp = 0;
-                    item(tp, bh_, u_, nbp);
+                if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
+                    tc_commit_pair(drain);
+                    (void)mbar_wait_drain(drain, 0);
                 }
             }
-            if (!ok && issued) {  // MMAs in flight must finish before TMEM is freed
-                tc_commit_pair(drain);
-                (void)mbar_wait_drain(drain, 0);
-            }
+            __syncwarp();
         }
-        __syncwarp();
-    } else {
+    } else if (warp < 4 + kAttnSoftmaxWarps) {
+        setmaxnreg_inc<160>();
         // ---------------------------------------------------------------- softmax warps
         // Warp w serves TMEM lane quadrant w % 4 (query rows 32 (w % 4) + lane of this CTA's tile)
         // and half hh of each block's keys and of O's columns.
@@ -833,61 +881,8 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
         const uint32_t s_free0 = mapa_shared(s_free, 0);
         const uint32_t p_full_a = mapa_shared(p_full(0), 0), p_full_b = mapa_shared(p_full(1), 0);
         float* lx = reinterpret_cast<float*>(gbase + L::OFF_LX);
-        const uint32_t o_free0 = mapa_shared(o_free, 0);
-        uint8_t* stage = gbase + L::OFF_ST + (warp - 4) * L::ST_WARP;
-        const uint32_t stage_s = base + L::OFF_ST + (warp - 4) * L::ST_WARP;
-        // Read out item e's O (its last PV is global block g_last): O / l, this warp's 32 rows and
-        // half of the columns.  The row sum is the sum of the two halves' partial sums, exchanged
-        // through shared memory (a bounded mbarrier wait, not a named barrier: a warp that gave
-        // up earlier must not leave its partner blocked).  The partner cannot overwrite its slot
-        // for item e + 1 before this warp has read it: it writes that slot only after item
-        // e + 1's last PV, which follows that item's PV_0, which waits on this warp's o_free
-        // arrival at the end of this read-out.
-        auto epilogue = [&](int e, int bh_e, int qt_e, float l_e, int g_last) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(o_done(g_last % 2), (g_last / 2) & 1, flag)))
-                return false;
-            tc_fence_after();
-            lx[hh * kAttnQ + r] = l_e;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(l_ready);
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded(l_ready, e & 1, flag))) return false;
-            const float inv = 1.0f / (l_e + lx[(1 - hh) * kAttnQ + r]);
-            // 64 columns at a time: TMEM -> registers -> this warp's staging box (row = lane, 16-byte
-            // chunks in the 128-byte swizzle of the O tensor map) -> TMA store.  A store instruction
-            // per lane and row would touch 32 rows per warp instruction; the box store writes whole
-            // 128-byte lines.
-            const int orow0 = bh_e * a.S + qt_e * kAttnQ + 32 * qd;
-#pragma unroll 1
-            for (int k = 0; k < D / 128; ++k) {
-                float o[64];
-                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 64 * k, o);
-                tmem_ld32(tmem + lanes + L::O_COL + (D / 2) * hh + 64 * k + 32, o + 32);
-                tmem_ld_wait();
-                if (lane == 0) bulk_wait_read0();   // the previous box has left the staging buffer
-                __syncwarp();
-#pragma unroll
-                for (int v = 0; v < 8; ++v)
-                    *reinterpret_cast<uint4*>(stage + lane * 128 + ((v ^ (lane & 7)) * 16)) =
-                        make_uint4(pack_bf16x2(o[8 * v] * inv, o[8 * v + 1] * inv),
-                                   pack_bf16x2(o[8 * v + 2] * inv, o[8 * v + 3] * inv),
-                                   pack_bf16x2(o[8 * v + 4] * inv, o[8 * v + 5] * inv),
-                                   pack_bf16x2(o[8 * v + 6] * inv, o[8 * v + 7] * inv));
-                fence_async_smem();   // generic-proxy writes become visible to the TMA engine
-                __syncwarp();
-                if (lane == 0) {
-                    tma_store_2d(&mO, (D / 2) * hh + 64 * k, orow0, stage_s);
-                    bulk_commit();
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(o_free0);   // the next item's PV_0 may overwrite O
-            return true;
-        };
         bool ok = true;
         int g = 0;   // global block index
-        int bh_p = 0, qt_p = 0;   // the previous item, whose O is read out at the next item's block 0
-        float l_p = 0.0f;
         for (int t = 0; ok && t < my_items; ++t) {
             int bh, u, nb;
             item(t, bh, u, nb);
@@ -918,8 +913,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                 const int lim = qrow - j * kAttnK;           // last visible key of this block
                 const bool diag = j >= qt;
                 const int k0 = HK * hh, ko = HK * (1 - hh);
-                const float mx = (diag ? block_row_max_diag<HK>(s, so, k0, ko, lim - lane, lane)
-                                       : block_row_max<HK, false>(s, so, k0, ko, lim)) * c;
+                const bool past = j > qt;   // every key of the block lies past this CTA's rows
+                if (diag && !past) {
+                    mask_block<HK>(s, k0, lim);
+                    mask_block<HK>(so, ko, lim);
+                }
+                const float mx = past ? -INFINITY : block_row_max<HK, false>(s, so, k0, ko, lim) * c;
                 float alpha = 1.0f;
                 bool rescale = false;
                 if (mx > m_used + kRescaleLog2) {
@@ -930,8 +929,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                     m_used = mx;
                 }
                 uint32_t pk[HK / 2];
-                const float2 sum2 = diag ? block_exp2_diag<HK>(s, k0, lim - lane, lane, c, m_used, pk)
-                                         : block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
+                float2 sum2 = make_float2(0.0f, 0.0f);
+                if (past) {
+#pragma unroll
+                    for (int i = 0; i < HK / 2; ++i) pk[i] = 0u;
+                } else {
+                    sum2 = block_exp2<HK, false>(s, k0, lim, c, m_used, pk);
+                }
                 l = l * alpha + (sum2.x + sum2.y);
 
                 // P buffer pb was last read by PV of global block g - 2
@@ -965,17 +969,98 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(pb ? p_full_b : p_full_a);
-                // the previous item's output, now that this item's S_1 can run
-                if (j == 0 && t >= 1 && !epilogue(t - 1, bh_p, qt_p, l_p, g - 1)) {
-                    ok = false;
-                    break;
-                }
             }
-            bh_p = bh;
-            qt_p = qt;
-            l_p = l;
+            if (!ok) break;
+            // the item's row sums (this warp's half of the keys) for the output warps, once they
+            // have read the previous item's
+            if (t >= 1 && !__all_sync(0xffffffffu, mbar_wait_bounded(lx_free, (t - 1) & 1, flag))) {
+                ok = false;
+                break;
+            }
+            lx[hh * kAttnQ + r] = l;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(l_ready);
         }
-        if (ok && my_items > 0) (void)epilogue(my_items - 1, bh_p, qt_p, l_p, g - 1);
+    } else {
+        // ---------------------------------------------------------------- output warps
+        setmaxnreg_inc<144>();   // 48 x 128 + 160 x 256 + 144 x 128 = 65,536 (the launch's 512 x 128)
+        // Warp 12 + q reads TMEM lane quadrant q: rows 32 q + lane of this CTA's tile, all of O's
+        // columns, 64 at a time (chunk k), and stores them (scaled by 1 / l, bf16) through its two
+        // staging boxes (row = lane, 16-byte pieces in the 128-byte swizzle of the O tensor map)
+        // with TMA box stores; a box is written again only once the store from it two chunks
+        // earlier has read it.  O leaves TMEM as early as the registers allow: chunks 0 .. NCH - 3
+        // go straight to their boxes, chunk NCH - 2 is held packed to bf16 pairs and chunk
+        // NCH - 1 as fp32, and o_free is signalled once all of them are read, so the next item's
+        // PV_0 overwrites O while the last two chunks are staged and stored.
+        constexpr int NCH = D / 64;
+        const int ow = warp - 4 - kAttnSoftmaxWarps;
+        const int qd = warp % 4;
+        const int r = 32 * qd + lane;
+        const uint32_t lanes = static_cast<uint32_t>(32 * qd) << 16;
+        const float* lx = reinterpret_cast<const float*>(gbase + L::OFF_LX);
+        const uint32_t o_free0 = mapa_shared(o_free, 0);
+        auto stage_box = [&](int k, int orow0, const uint32_t (&w)[32]) {
+            const int box = 2 * ow + (k & 1);
+            uint8_t* stage = gbase + L::OFF_ST + box * L::ST_WARP;
+            if (lane == 0) bulk_wait_read1();   // the store from this box two chunks ago has read it
+            __syncwarp();
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+                *reinterpret_cast<uint4*>(stage + lane * 128 + ((v ^ (lane & 7)) * 16)) =
+                    make_uint4(w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+            fence_async_smem();   // generic-proxy writes become visible to the TMA engine
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_2d(&mO, 64 * k, orow0, base + L::OFF_ST + box * L::ST_WARP);
+                bulk_commit();
+            }
+        };
+        auto pack = [&](const float (&o)[64], float inv, uint32_t (&w)[32]) {
+#pragma unroll
+            for (int v = 0; v < 32; ++v) w[v] = pack_bf16x2(o[2 * v] * inv, o[2 * v + 1] * inv);
+        };
+        bool ok = true;
+        int g = 0;
+        for (int t = 0; ok && t < my_items; ++t) {
+            int bh, u, nb;
+            item(t, bh, u, nb);
+            const int qt = 2 * u + static_cast<int>(rank);
+            g += nb;
+            const int g_last = g - 1;   // the item's last PV
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(l_ready, t & 1, flag)) ||
+                !__all_sync(0xffffffffu, mbar_wait_bounded(o_done(g_last % 2), (g_last / 2) & 1, flag))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const float inv = 1.0f / (lx[r] + lx[kAttnQ + r]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(lx_free);
+            const int orow0 = bh * a.S + qt * kAttnQ + 32 * qd;
+            float o[64];
+            uint32_t w[32], held[32];
+#pragma unroll 1
+            for (int k = 0; k < NCH - 2; ++k) {
+                tmem_ld32(tmem + lanes + L::O_COL + 64 * k, o);
+                tmem_ld32(tmem + lanes + L::O_COL + 64 * k + 32, o + 32);
+                tmem_ld_wait();
+                pack(o, inv, w);
+                stage_box(k, orow0, w);
+            }
+            tmem_ld32(tmem + lanes + L::O_COL + 64 * (NCH - 2), o);
+            tmem_ld32(tmem + lanes + L::O_COL + 64 * (NCH - 2) + 32, o + 32);
+            tmem_ld_wait();
+            pack(o, inv, held);
+            tmem_ld32(tmem + lanes + L::O_COL + 64 * (NCH - 1), o);
+            tmem_ld32(tmem + lanes + L::O_COL + 64 * (NCH - 1) + 32, o + 32);
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(o_free0);   // the next item's PV_0 may overwrite O
+            stage_box(NCH - 2, orow0, held);
+            pack(o, inv, w);
+            stage_box(NCH - 1, orow0, w);
+        }
         if (lane == 0) bulk_wait0();   // the output stores have completed
         __syncwarp();
     }
