@@ -596,11 +596,10 @@ struct PairLayout {
 };
 
 // ================================================================== persistent 2-SM variant
-// The 2-SM pipeline above in a persistent kernel: each cluster stays resident and walks a list of
-// tile pairs (items c, c + C, c + 2C, ... of the order_item() order for cluster c of C), so the
-// set-up (TMEM allocation, barriers) happens once and every ring (K, V, S, P) runs on across
-// items: the next item's Q, K and V stream in while the current item finishes.  Roles (384
-// threads per CTA):
+// The 2-SM pipeline above in a persistent kernel: each cluster stays resident and walks its list
+// of tile pairs (AttnSched), so the set-up (TMEM allocation, barriers) happens once and every
+// ring (K, V, S, P) runs on across items: the next item's Q, K and V stream in while the current
+// item finishes.  Roles (512 threads per CTA):
 //   warp 0, lane 0: this CTA's half of every K block (TMA); warp 2, lane 0: its half of every V
 //     block; warp 3, lane 0: its 128 Q rows.  The bytes of both CTAs complete on CTA 0's barriers.
 //     Q gets a warp of its own because the next item's Q may only overwrite the current one once
