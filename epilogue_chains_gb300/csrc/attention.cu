@@ -1111,8 +1111,8 @@ int launch_attn(const CUtensorMap& mQ, const CUtensorMap& mK, const CUtensorMap&
 // to the cluster whose estimated finish time is earliest (the order a shared work queue would hand
 // them out in), so the clusters finish together; a plain round-robin leaves the busiest cluster
 // ~14 % above the mean at [128, 2048, 256] on 76 clusters.  Estimated cost of an item: 10 per key
-// block plus 14 for its fixed costs (the output read-out and the pipeline refill cost about 1.4
-// blocks).  Lists are cached per shape.
+// block plus 8 for its fixed costs (what an item boundary adds, the wait for the next Q and for
+// the output release, measured at 0.75 of a block).  Lists are cached per shape.
 void build_sched(int BH, int per_head, int ncl, AttnSched* out) {
     out->n = 0;
     const int64_t n = static_cast<int64_t>(BH) * per_head;
@@ -1127,7 +1127,7 @@ void build_sched(int BH, int per_head, int ncl, AttnSched* out) {
         int bh, heavy;
         order_item(i, per_head, BH, bh, heavy);
         const int nb = 2 * (per_head - 1 - heavy) + 2;
-        load[c] += 10 * nb + 14;
+        load[c] += 10 * nb + 8;
         owner[i] = static_cast<uint8_t>(c);
         ++count[c];
     }
