@@ -741,6 +741,14 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                             for (int c = 0; c < L::QATOMS; ++c)
                                 tma_load_2d_pair(base + L::OFF_K + st * L::KH_BYTES + c * L::KH_REGION, &mKh, 64 * c, y,
                                                  full_cl);
+                            // the next item's Q rows into L2 once this item's last K block is on its
+                            // way, about two blocks before the Q producer loads them
+                            if (j == nb - 1 && t + 1 < my_items) {
+                                int nbh, nu, nnb;
+                                item(t + 1, nbh, nu, nnb);
+                                const int qrow = nbh * a.S + (2 * nu + static_cast<int>(rank)) * kAttnQ;
+                                for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, qrow);
+                            }
                         } else {
                             const int y = krow0 + j * kAttnK;
                             for (int c = 0; c < L::VATOMS; ++c)
@@ -774,12 +782,12 @@ __global__ void __launch_bounds__(kPersistThreads, 1) attn_persist_kernel(
                     if (leader) mbar_arrive_expect_tx(q_full, 2 * L::Q_BYTES);
                     for (int c = 0; c < L::QATOMS; ++c)
                         tma_load_2d_pair(base + L::OFF_Q + c * L::Q_REGION, &mQ, 64 * c, row0, qf);
-                    // the next item's Q into L2 now, so that its load (after this item's last S) is short
+                    // the next item's rows (its Q reaches L2 by the K producer's prefetch, two blocks
+                    // before this item's last S frees the buffer)
                     if (t + 1 < my_items) {
                         int bh, u, nb;
                         item(t + 1, bh, u, nb);
                         row0 = bh * a.S + (2 * u + static_cast<int>(rank)) * kAttnQ;
-                        for (int c = 0; c < L::QATOMS; ++c) tma_prefetch_2d(&mQ, 64 * c, row0);
                     }
                 }
                 if (t < my_items && t >= 1 && leader) (void)mbar_wait_drain(q_full, (t - 1) & 1);
