@@ -318,8 +318,9 @@ int64_t fuse_attention_flops(int64_t bh, int64_t S, int64_t D);
  * items are pairs of adjacent 128-row query tiles: item i of bh * (S / 256) covers slice and tile
  * pair as ordered in groups of 16 slices, heaviest pair first within a group; an item with pair
  * index u reads 2u + 2 key blocks.  Items go, in that order, to the cluster with the earliest
- * estimated finish (10 per key block + 14 per item).  Cluster c runs items[first[c]] ..
- * items[first[c + 1] - 1].
+ * estimated finish (10 per key block + 8 per item); then, while it narrows their gap, the
+ * busiest cluster trades an item for a lighter one of the same 16-slice group with the idlest.
+ * Cluster c runs items[first[c]] .. items[first[c + 1] - 1], in increasing order.
  *   first   host int32 [clusters + 1];  items  host int32 [bh * S / 256]
  *   S a multiple of 256; 1 <= clusters <= 96; bh * S / 256 <= 4096 (the kernel falls back to a
  *   round-robin assignment beyond these, and so does this call: FUSE_EUNSUPPORTED).
