@@ -61,11 +61,12 @@ def test_small_shapes_every_row(cuda_device, shape):
     assert np.array_equal(o[:, 0], v[:, 0])
 
 
-@pytest.mark.parametrize("shape", [(160, 256, 128), (97, 512, 256)])
+@pytest.mark.parametrize("shape", [(160, 256, 128), (97, 512, 256), (12, 4096, 256), (24, 4096, 128)])
 def test_more_tile_pairs_than_resident_clusters(cuda_device, shape):
     """More (slice, tile pair) items than clusters fit on the GPU (~74): each cluster walks
-    several items of different lengths, and the counts per cluster are uneven.  The first, second
-    and last rows of every 128-row tile and a few random rows are checked in every slice."""
+    several items of different lengths (at S = 4096 up to 32 key blocks each), and the counts per
+    cluster are uneven.  The first, second and last rows of every 128-row tile and a few random
+    rows are checked in every slice."""
     bh, S, D = shape
     q, k, v = wl.attention_input(bh, S, D, salt=7 * S + D)
     scale = 1.0 / np.sqrt(D)
