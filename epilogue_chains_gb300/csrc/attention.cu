@@ -601,8 +601,9 @@ struct PairLayout {
 // of tile pairs (AttnSched), so the set-up (TMEM allocation, barriers) happens once and every
 // ring (K, V, S, P) runs on across items: the next item's Q, K and V stream in while the current
 // item finishes.  Roles (512 threads per CTA):
-//   warp 0, lane 0: this CTA's half of every K block (TMA); warp 2, lane 0: its half of every V
-//     block; warp 3, lane 0: its 128 Q rows.  The bytes of both CTAs complete on CTA 0's barriers.
+//   warp 0, lane 0: this CTA's half of every K block (TMA), and with an item's last K block the
+//     next item's Q rows into L2; warp 2, lane 0: its half of every V block; warp 3, lane 0: its
+//     128 Q rows.  The bytes of both CTAs complete on CTA 0's barriers.
 //     Q gets a warp of its own because the next item's Q may only overwrite the current one once
 //     the current item's last S has completed (q_empty), and the K and V rings must not wait.
 //   warp 1 of CTA 0: every MMA of the pair, per item in the order S_0, S_1, PV_0, S_2, PV_1, ...;
@@ -611,10 +612,11 @@ struct PairLayout {
 //     exponentiating half of a block's keys and rescaling half of O's columns); they release S
 //     and publish P on CTA 0's barriers, and after an item's last block its row sums (l_ready).
 //   warps 12-15: the output: once an item's last PV has completed, each reads its lane
-//     quadrant's 32 rows of O from TMEM, divides them by the row sums, stores them (staged in
-//     shared memory, TMA box stores) and arrives on o_free; the next item's PV_0, which overwrites
-//     O (accumulate off), waits for it.  Meanwhile the softmax warps go on releasing the next
-//     item's S blocks, so its S MMAs fill the tensor pipe while O is read out.
+//     quadrant's 32 rows of O from TMEM, divides them by the row sums and arrives on o_free as
+//     soon as all of them have left TMEM (the next item's PV_0, which overwrites O with
+//     accumulate off, waits for it), then stores them (staged in shared memory, TMA box stores).
+//     Meanwhile the softmax warps go on with the next item's S blocks, so its S MMAs fill the
+//     tensor pipe while O is read out.
 // Register budgets per warpgroup (setmaxnreg; launched at 128 per thread): producers and MMA
 // issuer 48, softmax 160, output 144 -- 48 x 128 + 160 x 256 + 144 x 128 = 65,536, all the CTA is
 // launched with.
