@@ -12,11 +12,10 @@
 // shared-memory reduction across the CTA's warps, then the scaled row written with 16-byte
 // streaming stores.  x (and the residual) are read from HBM exactly once; w (16 KB at hidden 4096)
 // stays in L1/L2.  An exact grid of short CTAs lets the hardware scheduler balance rows over the
-// SMs: on GB300 this matches a plain 2-in/2-out streaming copy of the same bytes for the residual
-// form (24.4 us at [2048, 4096]), where a persistent grid that prefetched the next row lost ~8 %
-// to its last, partial round of rows; for RMSNorm alone (32 MiB each way) both run at the speed of
-// a cudaMemcpy of the same 32 MiB (about 16 us), the fixed cost of filling and draining the memory
-// pipeline dominating at that size.
+// SMs: a persistent grid that prefetched the next row into registers lost ~8 % to its last,
+// partial round of rows.  Instead, before its grid-dependency wait each CTA starts its own row and
+// the row of the CTA one wave later on their way into L2 (bulk prefetches), so a launch's first
+// reads overlap the end of the launch before it.
 #include <cuda.h>
 
 #include <mutex>
