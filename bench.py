@@ -260,7 +260,8 @@ def run_ours(args, rank, world, local):
     # record cannot start under the preceding call's tail (measured per call for the K = 4 chain:
     # 21.5 / 20.2 / 19.5 / 19.1 us for 2 / 4 / 8 / 16 calls; SiLU*up 28.6 / 27.4 / 26.7 / 26.3 us;
     # RMSNorm 13.3 / 12.5 / 12.0 / 11.6 us), so calls under ~100 us are timed 8 to a group, fused
-    # and unfused alike, and longer ones 2 to 4.
+    # and unfused alike, and longer ones 2 to 4 (4 where that start, ~7 us for attention, would
+    # otherwise cost more than 1 %).
     groups = [Group(f"chain_fused_K{K}", chain(K, fc.FUSE_FUSED), chain_bytes, 8, "hbm",
                     "chain_fused_kernel<f32>", 1, "chain_fused") for K in KS]
     groups += [Group(f"chain_unfused_K{K}", chain(K, fc.FUSE_UNFUSED),
@@ -396,7 +397,7 @@ def run_ours(args, rank, world, local):
                                      ABH, AS, AD, wl.ATT_SCALE, sh), "fuse_attention")
             counter["launches"] += 1
         att_flops = fc.fuse_attention_flops(ABH, AS, AD)
-        groups += [Group("attention_fused", attn, att_flops, 2, "tensor", "attn_persist_kernel<D=256>", 1)]
+        groups += [Group("attention_fused", attn, att_flops, 4, "tensor", "attn_persist_kernel<D=256>", 1)]
         # -------------------------------------------------------------- GEMM epilogue chain
         gN, gK = wl.GEMM_N, wl.GEMM_K
         with torch.cuda.stream(stream):
